@@ -1,0 +1,199 @@
+"""ctypes front end of the CPU oracle (oracle/dsa_oracle.cpp).
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__ (build, and one
+check in smoke) and bench.py's cpu_baseline / reference leg.  The product
+package never imports it.
+
+Every array crosses as numpy; tensors are converted on the host.  fp64 out.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dsa_oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle_dsa.so")
+_lock = threading.Lock()
+_lib = None
+
+ORACLE_OK = 0
+ORACLE_ERR_ARG = 1
+ORACLE_ERR_GROUPING = 2
+ORACLE_ERR_CONTEXT = 3
+ORACLE_ERR_BLOCK_TABLE = 4
+ORACLE_ERR_BLOCK_ID = 5
+ORACLE_ERR_STRIDE = 6
+
+# the schedule rule's constants (the metadata call's tile and grouping sizes)
+TILE_TOKENS = 128
+GROUP_MAX_ROWS = 8
+BASE_WEIGHT = 4
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with g++ (plain -O2, IEEE arithmetic)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", "-fno-fast-math",
+           _SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build()
+            L = ctypes.CDLL(path)
+            P = ctypes.c_void_p
+            i32, i64, dbl, u8 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double, ctypes.c_uint8
+            L.oracle_version.restype = ctypes.c_int
+            L.oracle_set_plant.argtypes = [ctypes.c_int]
+            L.oracle_e4m3_value.argtypes = [u8]
+            L.oracle_e4m3_value.restype = dbl
+            L.oracle_e2m1_value.argtypes = [u8]
+            L.oracle_e2m1_value.restype = dbl
+            L.oracle_validate.argtypes = [P, P, P, i64, i32, i64, i32, i64]
+            L.oracle_validate.restype = ctypes.c_int
+            L.oracle_paged_mqa_logits.argtypes = [P, P, i64, i64, i32, P, P, P, i64, i32, i32,
+                                                  i32, i32, P, i32, P, P, i64, i32]
+            L.oracle_paged_mqa_logits.restype = ctypes.c_int
+            L.oracle_top_k_per_row.argtypes = [P, i64, P, P, i32, i32, P, i64, i32]
+            L.oracle_top_k_per_row.restype = ctypes.c_int
+            L.oracle_schedule.argtypes = [P, P, i32, i32, i32, i32, i32, P]
+            L.oracle_schedule.restype = ctypes.c_int
+            L.oracle_schedule_words.argtypes = [i32, i32]
+            L.oracle_schedule_words.restype = i64
+            _lib = L
+    return _lib
+
+
+def _np(x, dtype):
+    """numpy copy/view of a torch tensor or array-like, C-contiguous, given dtype."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").contiguous().numpy()
+    return np.ascontiguousarray(np.asarray(x), dtype=dtype)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"oracle {what} returned status {code}")
+        self.code = code
+
+
+def set_plant(p: int) -> None:
+    lib().oracle_set_plant(int(p))
+
+
+def e4m3_value(code: int) -> float:
+    return lib().oracle_e4m3_value(int(code) & 0xFF)
+
+
+def e2m1_value(nibble: int) -> float:
+    return lib().oracle_e2m1_value(int(nibble) & 0xF)
+
+
+def validate(context_lens, indices, block_table, num_pages, logits_stride, block_kv=64) -> int:
+    cl = _np(context_lens, np.int32)
+    ind = _np(indices, np.int32)
+    bt = _np(block_table, np.int32)
+    T = cl.shape[0]
+    bt2 = bt.reshape(T, -1) if T else bt.reshape(0, max(1, bt.size))
+    return lib().oracle_validate(_ptr(cl), _ptr(ind), _ptr(bt2), bt2.shape[1], T,
+                                 int(num_pages), int(block_kv), int(logits_stride))
+
+
+def paged_mqa_logits(q, kv_cache, page_stride, kv_format, weights, context_lens, block_table,
+                     out_cols, rows=None, with_bound=True, block_kv=64, nthreads=0):
+    """fp64 logits (and bound) of the selected rows: arrays [n_sel, out_cols]."""
+    qn = _np(q, np.uint8)
+    kv = _np(kv_cache, np.uint8)
+    w = _np(weights, np.float32)
+    cl = _np(context_lens, np.int32)
+    bt = _np(block_table, np.int32)
+    T = cl.shape[0]
+    H = w.shape[1] if w.ndim == 2 else w.size // max(T, 1)
+    D = qn.size // max(T * H, 1)
+    bt2 = bt.reshape(T, -1)
+    rws = None if rows is None else _np(rows, np.int32)
+    n_sel = T if rws is None else rws.shape[0]
+    num_pages = kv.shape[0] if kv.ndim == 2 else kv.size // page_stride
+    logits = np.empty((n_sel, out_cols), dtype=np.float64)
+    bound = np.empty((n_sel, out_cols), dtype=np.float64) if with_bound else None
+    st = lib().oracle_paged_mqa_logits(_ptr(qn), _ptr(kv), int(page_stride), int(num_pages),
+                                       int(kv_format), _ptr(w), _ptr(cl), _ptr(bt2),
+                                       bt2.shape[1], T, H, D, int(block_kv), _ptr(rws),
+                                       n_sel, _ptr(logits), _ptr(bound), int(out_cols),
+                                       int(nthreads))
+    if st != ORACLE_OK:
+        raise OracleError(st, "paged_mqa_logits")
+    return logits, bound
+
+
+def top_k_per_row(scores, row_ends, k, row_starts=None, nthreads=0):
+    """Stable per-row top-k of an fp64 score matrix [rows, stride] -> int32 [rows, k]."""
+    sc = _np(scores, np.float64)
+    if sc.ndim == 1:
+        sc = sc.reshape(1, -1)
+    ends = _np(row_ends, np.int32)
+    starts = _np(row_starts, np.int32)
+    R = ends.shape[0]
+    out = np.empty((R, k), dtype=np.int32)
+    st = lib().oracle_top_k_per_row(_ptr(sc), sc.shape[1], _ptr(starts), _ptr(ends), R, int(k),
+                                    _ptr(out), k, int(nthreads))
+    if st != ORACLE_OK:
+        raise OracleError(st, "top_k_per_row")
+    return out
+
+
+def schedule_words(num_sms: int, num_rows: int) -> int:
+    return int(lib().oracle_schedule_words(int(num_sms), int(num_rows)))
+
+
+def schedule(context_lens, indices, num_sms, tile_tokens=TILE_TOKENS,
+             group_max_rows=GROUP_MAX_ROWS, base_weight=BASE_WEIGHT):
+    """The schedule words the metadata call must produce (int32 array)."""
+    cl = _np(context_lens, np.int32)
+    ind = _np(indices, np.int32)
+    T = cl.shape[0]
+    out = np.zeros(schedule_words(num_sms, T), dtype=np.int32)
+    st = lib().oracle_schedule(_ptr(cl), _ptr(ind), T, int(num_sms), int(tile_tokens),
+                               int(group_max_rows), int(base_weight), _ptr(out))
+    if st != ORACLE_OK:
+        raise OracleError(st, "schedule")
+    return out
+
+
+def parse_schedule(words, num_sms, num_rows):
+    """Split schedule words into (header, sm_start, group_row_start, group_unit_start)."""
+    w = np.asarray(words)
+    hdr = w[:8]
+    sm = w[8: 8 + num_sms + 1]
+    grs = w[8 + num_sms + 1: 8 + num_sms + 1 + num_rows + 1]
+    gus = w[8 + num_sms + 1 + num_rows + 1: 8 + num_sms + 1 + 2 * (num_rows + 1)]
+    return hdr, sm, grs, gus
+
+
+def workload_logits(wl, rows=None, with_bound=True, nthreads=0, out_cols=None):
+    """Oracle logits of a workloads.Workload (host copies are made as needed)."""
+    return paged_mqa_logits(wl.q, wl.kv_cache, wl.page_stride, wl.kv_format, wl.weights,
+                            wl.context_lens, wl.block_table,
+                            wl.logits_stride if out_cols is None else out_cols,
+                            rows=rows, with_bound=with_bound, nthreads=nthreads)

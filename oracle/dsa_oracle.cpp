@@ -1,0 +1,424 @@
+/*
+ * CPU oracle for the DSA indexer decode path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path loads this file: it
+ * is built and called by tests/, by __graft_entry__.smoke() (one small check)
+ * and by bench.py's cpu_baseline / reference leg.  It shares no code, header,
+ * table or constant generator with the CUDA library.
+ *
+ * Everything here is the plain definition written out, in fp64, one element
+ * at a time, with no blocking, fusion or reordering:
+ *
+ *   logits[t, s] = kscale[s] * sum_h w[t, h] * max(0, sum_d q[t, h, d] * k[s, d])
+ *                  for s < L_t, and -inf for s >= L_t
+ *
+ * ("varlen paged MQA logits": PR 47469 "Route SM100 sparse-indexer decode
+ * through varlen paged MQA logits", Purpose; the per-row causal limit and the
+ * row-sliced block table follow the sparse_attn_indexer docs,
+ * _varlen_decode_rows; the head-weighted ReLU score is the indexer score named
+ * there as fp8_fp4_paged_mqa_logits.)  The key k[s, :] is read through the
+ * row's block table, page = block_table[t][s / 64], slot = s % 64, and decoded
+ * from its stored bits.
+ *
+ *   top_k_per_row: the k largest scores of columns [row_start, row_end), ties
+ *   to the lower column, returned in ascending column order, padded with -1
+ *   (sparse_attn_indexer docs: forward_cpu fills the top-k buffer with -1;
+ *   _merge_dcp_topk_global names a stable top-k and -1 padding).
+ *
+ * Each function below cites the passage it follows.  Parity pins: see
+ * tests/test_oracle_pins.py.  "parity unpinned" is stated beside any function
+ * that has no pin (none at present).
+ */
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+constexpr int kKvFp8 = 0;
+constexpr int kKvFp4 = 1;
+
+// Planted-mistake switch used only by the oracle's own pin tests, to show that
+// every pin can fail.  0 = the correct definition.
+int g_plant = 0;
+
+// --- number formats --------------------------------------------------------
+
+// OCP 8-bit floating point, E4M3 ("FN": no infinities, S.1111.111 is NaN):
+// exponent bias 7, three mantissa bits, subnormals at exponent field 0.
+double decode_e4m3(uint8_t code) {
+  const int sign = (code >> 7) & 1;
+  const int expo = (code >> 3) & 0xF;
+  const int mant = code & 0x7;
+  double mag;
+  if (expo == 0xF && mant == 0x7) {
+    return std::numeric_limits<double>::quiet_NaN();
+  } else if (expo == 0) {
+    mag = std::ldexp(static_cast<double>(mant) / 8.0, 1 - 7);
+  } else {
+    mag = std::ldexp(1.0 + static_cast<double>(mant) / 8.0, expo - 7);
+  }
+  return sign ? -mag : mag;
+}
+
+// OCP Microscaling FP4 E2M1: exponent bias 1, one mantissa bit, subnormal at
+// exponent field 0, no NaN or infinity.
+double decode_e2m1(uint8_t nibble) {
+  const int sign = (nibble >> 3) & 1;
+  const int expo = (nibble >> 1) & 0x3;
+  const int mant = nibble & 0x1;
+  double mag;
+  if (expo == 0) {
+    mag = static_cast<double>(mant) * 0.5;
+  } else {
+    mag = std::ldexp(1.0 + static_cast<double>(mant) / 2.0, expo - 1);
+  }
+  return sign ? -mag : mag;
+}
+
+float load_f32(const uint8_t* p) {
+  float f;
+  std::memcpy(&f, p, 4);
+  return f;
+}
+
+// Decode the stored key of one token into fp64 values k[0..D) (without the
+// per-token scale) and return the per-token scale.  Page layouts:
+//   FP8: values [64][D] e4m3 at 0, fp32 scale[64] after the values.
+//   FP4: packed e2m1 [64][D/2] at 0 (element 2i in the low nibble of byte i),
+//        e4m3 block scales [64][D/16] after them, fp32 token scale[64] last.
+// (Per-token payload: sparse_attn_indexer docs, _gather_workspace_shapes and
+// kv_cache_as_quant_view; the split of values and scales inside the page and
+// the two-level FP4 scale are this build's storage reading.)
+double decode_token(const uint8_t* page, int kv_format, int slot, int D, int block_kv,
+                    double* k) {
+  if (kv_format == kKvFp8) {
+    const uint8_t* v = page + static_cast<int64_t>(slot) * D;
+    for (int d = 0; d < D; ++d) k[d] = decode_e4m3(v[d]);
+    return load_f32(page + static_cast<int64_t>(block_kv) * D + 4 * slot);
+  }
+  const uint8_t* v = page + static_cast<int64_t>(slot) * (D / 2);
+  const uint8_t* bs = page + static_cast<int64_t>(block_kv) * (D / 2) +
+                      static_cast<int64_t>(slot) * (D / 16);
+  for (int d = 0; d < D; ++d) {
+    const uint8_t byte = v[d / 2];
+    const uint8_t nib = (d % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+    const int blk = (g_plant == 6) ? (d / 32) : (d / 16);
+    k[d] = decode_e2m1(nib) * decode_e4m3(bs[blk]);
+  }
+  return load_f32(page + static_cast<int64_t>(block_kv) * (D / 2 + D / 16) + 4 * slot);
+}
+
+template <typename F>
+void parallel_for(int n, int nthreads, F&& fn) {
+  if (nthreads <= 0) nthreads = static_cast<int>(std::thread::hardware_concurrency());
+  if (nthreads <= 1 || n <= 1) {
+    for (int i = 0; i < n; ++i) fn(i);
+    return;
+  }
+  nthreads = std::min(nthreads, n);
+  std::vector<std::thread> pool;
+  for (int w = 0; w < nthreads; ++w) {
+    pool.emplace_back([&, w]() {
+      for (int i = w; i < n; i += nthreads) fn(i);
+    });
+  }
+  for (auto& th : pool) th.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+// Status codes of the oracle's entry points.
+enum {
+  ORACLE_OK = 0,
+  ORACLE_ERR_ARG = 1,          // bad sizes or null pointers
+  ORACLE_ERR_GROUPING = 2,     // equal request ids not adjacent
+  ORACLE_ERR_CONTEXT = 3,      // a row's causal limit decreases inside a request, or < 0
+  ORACLE_ERR_BLOCK_TABLE = 4,  // rows of one request read different pages
+  ORACLE_ERR_BLOCK_ID = 5,     // a page id outside [0, num_pages)
+  ORACLE_ERR_STRIDE = 6,       // logits row stride below round_up(max L_t, block_kv)
+};
+
+int oracle_version(void) { return 1; }
+
+void oracle_set_plant(int p) { g_plant = p; }
+
+double oracle_e4m3_value(uint8_t code) { return decode_e4m3(code); }
+
+double oracle_e2m1_value(uint8_t nibble) { return decode_e2m1(nibble & 0xF); }
+
+// Preconditions of the varlen decode call (PR 56811 "Fix
+// fp8_fp4_paged_mqa_logits MQA kpool varlen path for speculative decode",
+// Purpose: consecutive equal request indices identify the rows of one
+// request; sparse_attn_indexer docs, _varlen_decode_rows: block table sliced
+// by row).  Rows of one request must be adjacent, see non-decreasing causal
+// limits, and read the same pages; every page a row reads must exist; the
+// logits row stride must hold round_up(L_t, block_kv) columns.
+int oracle_validate(const int32_t* context_lens, const int32_t* indices,
+                    const int32_t* block_table, int64_t bt_stride, int32_t num_rows,
+                    int64_t num_pages, int32_t block_kv, int64_t logits_stride) {
+  if (num_rows < 0 || block_kv <= 0 || (num_rows > 0 && (!context_lens || !block_table)))
+    return ORACLE_ERR_ARG;
+  int64_t max_pages_needed = 0;
+  for (int t = 0; t < num_rows; ++t) {
+    if (context_lens[t] < 0) return ORACLE_ERR_CONTEXT;
+    const int64_t pages = (static_cast<int64_t>(context_lens[t]) + block_kv - 1) / block_kv;
+    max_pages_needed = std::max(max_pages_needed, pages);
+    if (pages > bt_stride) return ORACLE_ERR_ARG;
+    for (int64_t p = 0; p < pages; ++p) {
+      const int32_t b = block_table[t * bt_stride + p];
+      if (b < 0 || b >= num_pages) return ORACLE_ERR_BLOCK_ID;
+    }
+    if (static_cast<int64_t>(context_lens[t]) > logits_stride) return ORACLE_ERR_STRIDE;
+    if ((static_cast<int64_t>(context_lens[t]) + block_kv - 1) / block_kv * block_kv >
+        logits_stride)
+      return ORACLE_ERR_STRIDE;
+  }
+  if (!indices) return ORACLE_OK;
+  // adjacency: a request id, once its run ends, never appears again
+  std::vector<int32_t> seen;
+  for (int t = 0; t < num_rows; ++t) {
+    const bool new_run = (t == 0) || indices[t] != indices[t - 1];
+    if (new_run) {
+      if (std::find(seen.begin(), seen.end(), indices[t]) != seen.end())
+        return ORACLE_ERR_GROUPING;
+      seen.push_back(indices[t]);
+    } else {
+      if (context_lens[t] < context_lens[t - 1]) return ORACLE_ERR_CONTEXT;
+      // rows of one request read identical pages over the longer row's span
+      const int64_t pages = (static_cast<int64_t>(context_lens[t]) + block_kv - 1) / block_kv;
+      int t0 = t - 1;
+      while (t0 > 0 && indices[t0 - 1] == indices[t]) --t0;
+      for (int64_t p = 0; p < pages; ++p) {
+        if (block_table[t * bt_stride + p] != block_table[t0 * bt_stride + p])
+          return ORACLE_ERR_BLOCK_TABLE;
+      }
+    }
+  }
+  (void)max_pages_needed;
+  return ORACLE_OK;
+}
+
+// Paged MQA logits in fp64 (definition in the header comment).
+//   q        [num_rows][H][D] e4m3 codes
+//   weights  [num_rows][H] fp32 (the per-token q scale is folded into them:
+//            sparse_attn_indexer docs, SparseAttnIndexer.forward_cuda)
+//   rows     which rows to evaluate (NULL: all rows, in order); output row i
+//            holds row rows[i]
+//   logits   [n_sel][out_cols] fp64; columns >= L_t are -inf
+//   bound    [n_sel][out_cols] fp64 or NULL: kscale * sum_h sum_d |w q k|, the
+//            magnitude the accuracy tolerance is stated against
+int oracle_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_cache, int64_t page_stride,
+                            int64_t num_pages, int32_t kv_format, const float* weights,
+                            const int32_t* context_lens, const int32_t* block_table,
+                            int64_t bt_stride, int32_t num_rows, int32_t H, int32_t D,
+                            int32_t block_kv, const int32_t* rows, int32_t n_sel,
+                            double* logits, double* bound, int64_t out_cols,
+                            int32_t nthreads) {
+  if (!q || !kv_cache || !weights || !context_lens || !block_table || !logits) return ORACLE_ERR_ARG;
+  if (H <= 0 || D <= 0 || D % 32 != 0 || block_kv <= 0 || num_rows < 0) return ORACLE_ERR_ARG;
+  if (kv_format != kKvFp8 && kv_format != kKvFp4) return ORACLE_ERR_ARG;
+  if (n_sel < 0) return ORACLE_ERR_ARG;
+  const int n_eval = rows ? n_sel : num_rows;
+  for (int i = 0; i < n_eval; ++i) {
+    const int t = rows ? rows[i] : i;
+    if (t < 0 || t >= num_rows) return ORACLE_ERR_ARG;
+    if (context_lens[t] < 0 || context_lens[t] > out_cols) return ORACLE_ERR_STRIDE;
+    const int64_t pages = (static_cast<int64_t>(context_lens[t]) + block_kv - 1) / block_kv;
+    for (int64_t p = 0; p < pages; ++p) {
+      const int32_t b = block_table[t * bt_stride + p];
+      if (b < 0 || b >= num_pages) return ORACLE_ERR_BLOCK_ID;
+    }
+  }
+  const double neg_inf = -std::numeric_limits<double>::infinity();
+  parallel_for(n_eval, nthreads, [&](int i) {
+    const int t = rows ? rows[i] : i;
+    const int32_t L = context_lens[t];
+    std::vector<double> qd(static_cast<size_t>(H) * D), k(D);
+    for (int64_t j = 0; j < static_cast<int64_t>(H) * D; ++j)
+      qd[j] = decode_e4m3(q[static_cast<int64_t>(t) * H * D + j]);
+    double* out = logits + static_cast<int64_t>(i) * out_cols;
+    double* bnd = bound ? bound + static_cast<int64_t>(i) * out_cols : nullptr;
+    for (int64_t s = 0; s < out_cols; ++s) {
+      if (s >= L) {
+        out[s] = neg_inf;
+        if (bnd) bnd[s] = 0.0;
+        continue;
+      }
+      const int64_t col_page = (g_plant == 3) ? (s / (2 * block_kv)) : (s / block_kv);
+      const int32_t page_id = block_table[t * bt_stride + col_page];
+      const uint8_t* page = kv_cache + static_cast<int64_t>(page_id) * page_stride;
+      const int slot = static_cast<int>(s % block_kv);
+      const double kscale = decode_token(page, kv_format, slot, D, block_kv, k.data());
+      double acc = 0.0, mag = 0.0;
+      for (int h = 0; h < H; ++h) {
+        const double w = weights[static_cast<int64_t>(t) * H + h];
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) {
+          const double qv = (g_plant == 1) ? qd[static_cast<int64_t>(d % H) * D + h % D]
+                                           : qd[static_cast<int64_t>(h) * D + d];
+          dot += qv * k[d];
+          mag += std::fabs(w * qv * k[d]);
+        }
+        if (g_plant == 2) {
+          acc += w * dot;                       // ReLU dropped
+        } else if (g_plant == 4) {
+          acc += w * std::max(-dot, 0.0);       // sign flipped inside ReLU
+        } else if (g_plant == 5) {
+          acc += std::max(dot, 0.0);            // head weight dropped
+        } else {
+          acc += w * std::max(dot, 0.0);
+        }
+      }
+      out[s] = kscale * acc;
+      if (bnd) bnd[s] = std::fabs(kscale) * mag;
+    }
+  });
+  return ORACLE_OK;
+}
+
+// Per-row top-k (sparse_attn_indexer docs: _varlen_decode_rows calls the
+// selector with the row ends = the rows' causal limits; forward_cpu pre-fills
+// -1; _merge_dcp_topk_global: stable top-k, -1 padding).  Order: score
+// descending, then column ascending (ties to the lower column); -0 equals +0;
+// NaN ranks below every number.  The chosen columns are written in ascending
+// column order, then -1 up to k.
+//   scores    [num_rows][stride] fp64 (fp32 / bf16 logits convert exactly)
+//   row_starts NULL means 0
+int oracle_top_k_per_row(const double* scores, int64_t stride, const int32_t* row_starts,
+                         const int32_t* row_ends, int32_t num_rows, int32_t k,
+                         int32_t* out_idx, int64_t out_stride, int32_t nthreads) {
+  if (!scores || !row_ends || !out_idx || k <= 0 || out_stride < k || num_rows < 0)
+    return ORACLE_ERR_ARG;
+  for (int t = 0; t < num_rows; ++t) {
+    const int64_t a = row_starts ? row_starts[t] : 0;
+    const int64_t b = row_ends[t];
+    if (a < 0 || b > stride || (b > a && a >= stride)) return ORACLE_ERR_ARG;
+  }
+  parallel_for(num_rows, nthreads, [&](int t) {
+    const int64_t a = row_starts ? row_starts[t] : 0;
+    const int64_t b = std::max<int64_t>(row_ends[t], a);
+    const double* row = scores + static_cast<int64_t>(t) * stride;
+    std::vector<int64_t> cols;
+    cols.reserve(static_cast<size_t>(b - a));
+    for (int64_t s = a; s < b; ++s) cols.push_back(s);
+    auto better = [&](int64_t x, int64_t y) {
+      const double vx = row[x], vy = row[y];
+      const bool nx = std::isnan(vx), ny = std::isnan(vy);
+      if (nx || ny) return !nx && ny;
+      if (g_plant == 7) return vx < vy;
+      return vx > vy;
+    };
+    std::stable_sort(cols.begin(), cols.end(), better);
+    const int64_t take = std::min<int64_t>(k, static_cast<int64_t>(cols.size()));
+    std::vector<int64_t> chosen(cols.begin(), cols.begin() + take);
+    std::sort(chosen.begin(), chosen.end());
+    int32_t* out = out_idx + static_cast<int64_t>(t) * out_stride;
+    for (int64_t i = 0; i < k; ++i) out[i] = i < take ? static_cast<int32_t>(chosen[i]) : -1;
+  });
+  return ORACLE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Work schedule (the metadata call: PR 47469 Purpose and Changes,
+// get_paged_mqa_logits_metadata(seq_lens, block_kv, num_sms, indices); its
+// output shape is [num_sms + 1, ...] per sparse_attn_indexer docs,
+// _varlen_decode_rows, which passes schedule.shape[0] - 1 back as num_sms).
+//
+// The pages fix the inputs and the purpose (balance (request, K-block) work
+// over the SMs, grouping consecutive equal request ids) but not the split
+// rule.  This build's rule, written out:
+//   1. runs  = maximal runs of consecutive rows with equal request id
+//              (indices == NULL: every row is its own run);
+//   2. groups = each run cut into consecutive pieces of at most
+//              group_max_rows rows;
+//   3. group g: n_g rows, Lmax_g = max causal limit of its rows (negative
+//      counts as 0), tiles_g = ceil(Lmax_g / tile_tokens), every tile weighs
+//      base_weight + n_g;
+//   4. units are the (group, tile) pairs in group-major order; P(u) = total
+//      weight of the units before u, W = P(U);
+//   5. SM i (0 <= i <= num_sms) starts at the smallest u with
+//      P(u) * num_sms >= i * W; SM i owns units [start_i, start_{i+1}).
+//
+// Layout written (int32): header[8] = {magic 0x44534131, num_rows,
+// varlen (indices != NULL), num_sms, num_groups, num_units, tile_tokens,
+// group_max_rows}, then sm_start[num_sms + 1], then
+// group_row_start[num_rows + 1] (entries past num_groups are unused and
+// written as num_rows), then group_unit_start[num_rows + 1] (entries past
+// num_groups written as num_units).
+// ---------------------------------------------------------------------------
+int oracle_schedule(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
+                    int32_t num_sms, int32_t tile_tokens, int32_t group_max_rows,
+                    int32_t base_weight, int32_t* out) {
+  if (num_rows < 0 || num_sms <= 0 || tile_tokens <= 0 || group_max_rows <= 0 ||
+      base_weight < 1 || !out || (num_rows > 0 && !context_lens))
+    return ORACLE_ERR_ARG;
+  std::vector<int32_t> group_row_start;
+  for (int t = 0; t < num_rows; ++t) {
+    const bool new_run = (t == 0) || !indices || indices[t] != indices[t - 1];
+    if (new_run) {
+      group_row_start.push_back(t);
+    } else if (t - group_row_start.back() >= group_max_rows) {
+      group_row_start.push_back(t);
+    }
+  }
+  const int G = static_cast<int>(group_row_start.size());
+  group_row_start.push_back(num_rows);
+  std::vector<int64_t> tiles(G), weight(G);
+  for (int g = 0; g < G; ++g) {
+    int64_t lmax = 0;
+    for (int t = group_row_start[g]; t < group_row_start[g + 1]; ++t)
+      lmax = std::max<int64_t>(lmax, context_lens[t]);
+    tiles[g] = (lmax + tile_tokens - 1) / tile_tokens;
+    weight[g] = base_weight + (group_row_start[g + 1] - group_row_start[g]);
+  }
+  // enumerate units one by one with their prefix weights
+  std::vector<int64_t> unit_prefix;  // P(u) for u = 0..U
+  std::vector<int32_t> group_unit_start(G + 1, 0);
+  int64_t P = 0;
+  for (int g = 0; g < G; ++g) {
+    group_unit_start[g] = static_cast<int32_t>(unit_prefix.size());
+    for (int64_t j = 0; j < tiles[g]; ++j) {
+      unit_prefix.push_back(P);
+      P += weight[g];
+    }
+  }
+  const int64_t U = static_cast<int64_t>(unit_prefix.size());
+  group_unit_start[G] = static_cast<int32_t>(U);
+  unit_prefix.push_back(P);
+  const int64_t W = P;
+  int32_t* hdr = out;
+  hdr[0] = 0x44534131;
+  hdr[1] = num_rows;
+  hdr[2] = indices ? 1 : 0;
+  hdr[3] = num_sms;
+  hdr[4] = G;
+  hdr[5] = static_cast<int32_t>(U);
+  hdr[6] = tile_tokens;
+  hdr[7] = group_max_rows;
+  int32_t* sm_start = out + 8;
+  for (int i = 0; i <= num_sms; ++i) {
+    int64_t u = 0;
+    while (u < U && unit_prefix[u] * num_sms < static_cast<int64_t>(i) * W) ++u;
+    sm_start[i] = static_cast<int32_t>(u);
+  }
+  int32_t* grs = sm_start + num_sms + 1;
+  int32_t* gus = grs + num_rows + 1;
+  for (int g = 0; g <= num_rows; ++g) {
+    grs[g] = g <= G ? group_row_start[g] : num_rows;
+    gus[g] = g <= G ? group_unit_start[g] : static_cast<int32_t>(U);
+  }
+  return ORACLE_OK;
+}
+
+int64_t oracle_schedule_words(int32_t num_sms, int32_t num_rows) {
+  return 8 + (static_cast<int64_t>(num_sms) + 1) + 2 * (static_cast<int64_t>(num_rows) + 1);
+}
+
+}  // extern "C"

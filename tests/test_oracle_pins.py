@@ -1,0 +1,428 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+* number formats: every e4m3 code against torch's float8_e4m3fn conversion and
+  the named values of the OCP FP8 spec; every e2m1 code against the OCP MX
+  spec's table (tests/golden/);
+* closed forms: a one-hot query reads a single decoded key value back;
+  logits(q) - logits(-q) and logits(q) + logits(-q) reduce the ReLU away and
+  leave a plain matrix product, checked against numpy's matmul over keys
+  decoded by torch;
+* brute force on tiny unpaged inputs (dense numpy evaluation over keys gathered
+  and decoded independently of the oracle);
+* invariants: permuting physical pages, padding the varlen batch to
+  (B, max_n), and plain decode (indices = None) against indices = arange(B);
+* top-k against a brute-force Python sort on random, tie-heavy, bf16-rounded,
+  -inf and NaN rows;
+* the schedule rule's properties;
+* planted mistakes: each deliberate error switched on inside the oracle makes
+  at least one of the pins above fail.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    out = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            a, b = line.split()
+            out.append((int(a, 16), float(b)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# independent decoding of a workload (torch float8 for e4m3, golden table for e2m1)
+# ---------------------------------------------------------------------------
+
+def _e2m1_table():
+    tab = np.zeros(16)
+    for code, val in _read_golden("e2m1_ocp_mx.txt"):
+        tab[code] = val
+    return tab
+
+
+def dense_keys(wl, t):
+    """Keys of row t, decoded without the oracle: (values [L, D] fp64, scale [L] fp64)."""
+    L = int(wl.context_lens[t])
+    kv = wl.kv_cache.numpy()
+    bt = wl.block_table.numpy()
+    s = np.arange(L)
+    page = bt[t, s // 64]
+    slot = s % 64
+    if wl.kv_format == W.KV_FP8:
+        codes = kv[page[:, None], slot[:, None] * 128 + np.arange(128)[None, :]]
+        vals = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).double().numpy()
+        sc = kv[page[:, None], 8192 + slot[:, None] * 4 + np.arange(4)[None, :]]
+        scale = sc.copy().view(np.float32).reshape(-1).astype(np.float64)
+        return vals, scale
+    tab = _e2m1_table()
+    packed = kv[page[:, None], slot[:, None] * 64 + np.arange(64)[None, :]]
+    lo = tab[packed & 0xF]
+    hi = tab[packed >> 4]
+    el = np.empty((L, 128))
+    el[:, 0::2] = lo
+    el[:, 1::2] = hi
+    bsc = kv[page[:, None], 4096 + slot[:, None] * 8 + np.arange(8)[None, :]]
+    bs = torch.from_numpy(bsc.copy()).view(torch.float8_e4m3fn).double().numpy()
+    vals = el * np.repeat(bs, 16, axis=1)
+    sc = kv[page[:, None], 4608 + slot[:, None] * 4 + np.arange(4)[None, :]]
+    scale = sc.copy().view(np.float32).reshape(-1).astype(np.float64)
+    return vals, scale
+
+
+def dense_q(wl, t):
+    return wl.q[t].view(torch.float8_e4m3fn).double().numpy()  # [H, D]
+
+
+def small_workload(seed=0, H=64, kv_format=W.KV_FP8, lens=(150, 77, 203), rows=(1, 3, 2)):
+    return W.build("pin", list(lens), list(rows), kv_format=kv_format, heads=H, seed=seed,
+                   topk=16)
+
+
+# ---------------------------------------------------------------------------
+# pin checks (plain functions so the planted-mistake test can run them too)
+# ---------------------------------------------------------------------------
+
+def check_e4m3_vs_torch():
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    mine = np.array([oracle.e4m3_value(c) for c in range(256)])
+    assert np.array_equal(np.isnan(ref), np.isnan(mine))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], mine[ok])
+    assert np.array_equal(np.signbit(ref[ok]), np.signbit(mine[ok]))
+    for code, val in _read_golden("e4m3_ocp_fp8.txt"):
+        got = oracle.e4m3_value(code)
+        if math.isnan(val):
+            assert math.isnan(got)
+        else:
+            assert got == val and math.copysign(1, got) == math.copysign(1, val)
+
+
+def check_e2m1_vs_spec():
+    for code, val in _read_golden("e2m1_ocp_mx.txt"):
+        got = oracle.e2m1_value(code)
+        assert got == val and math.copysign(1, got) == math.copysign(1, val), (code, got, val)
+
+
+def check_bruteforce(kv_format=W.KV_FP8, H=64, seed=0):
+    wl = small_workload(seed=seed, H=H, kv_format=kv_format)
+    lg, bd = oracle.workload_logits(wl)
+    for t in range(wl.num_rows):
+        L = int(wl.context_lens[t])
+        K, ks = dense_keys(wl, t)
+        Q = dense_q(wl, t)
+        w = wl.weights[t].double().numpy()
+        S = Q @ K.T                                  # [H, L]
+        ref = ks * (w @ np.maximum(S, 0.0))
+        mag = ks * (np.abs(w)[:, None] * (np.abs(Q) @ np.abs(K).T)).sum(axis=0)
+        tol = 1e-12 * (mag + 1e-300)
+        assert np.all(np.abs(lg[t, :L] - ref) <= tol), t
+        assert np.allclose(bd[t, :L], mag, rtol=1e-12, atol=0)
+        assert np.all(np.isneginf(lg[t, L:]))
+
+
+def check_one_hot_reads_key():
+    """H = 1, w = 1, q = e_d: logit[s] = kscale[s] * max(k[s, d], 0)."""
+    wl = small_workload(seed=5, H=1, lens=(130,), rows=(1,))
+    d = 37
+    q = torch.zeros_like(wl.q)
+    q[0, 0, d] = 0x38                                 # e4m3 1.0
+    wl.q = q
+    wl.weights = torch.ones_like(wl.weights)
+    lg, _ = oracle.workload_logits(wl)
+    K, ks = dense_keys(wl, 0)
+    assert np.array_equal(lg[0, :130], ks * np.maximum(K[:, d], 0.0))
+
+
+def _neg_q(wl):
+    w2 = W.Workload(**{**wl.__dict__})
+    w2.q = wl.q ^ 0x80                                # exact negation of every code
+    return w2
+
+
+def check_relu_identities(kv_format=W.KV_FP8):
+    """logits(q) - logits(-q) = ks * (w^T Q) K^T and logits(q) + logits(-q) = ks * w^T |Q K^T|."""
+    wl = small_workload(seed=7, kv_format=kv_format)
+    lp, bp = oracle.workload_logits(wl)
+    lm, _ = oracle.workload_logits(_neg_q(wl))
+    for t in range(wl.num_rows):
+        L = int(wl.context_lens[t])
+        K, ks = dense_keys(wl, t)
+        Q = dense_q(wl, t)
+        w = wl.weights[t].double().numpy()
+        lin = ks * ((w @ Q) @ K.T)
+        absr = ks * (w @ np.abs(Q @ K.T))
+        tol = 1e-12 * (bp[t, :L] + 1e-300)
+        assert np.all(np.abs((lp[t, :L] - lm[t, :L]) - lin) <= 2 * tol)
+        assert np.all(np.abs((lp[t, :L] + lm[t, :L]) - absr) <= 2 * tol)
+
+
+def check_weight_scaling():
+    wl = small_workload(seed=9)
+    a, _ = oracle.workload_logits(wl)
+    wl2 = W.Workload(**{**wl.__dict__})
+    wl2.weights = wl.weights * 4.0                    # exact power-of-two scaling
+    b, _ = oracle.workload_logits(wl2)
+    fin = np.isfinite(a)
+    assert np.array_equal(b[fin], 4.0 * a[fin])
+
+
+def check_page_permutation():
+    wl = small_workload(seed=11)
+    a, _ = oracle.workload_logits(wl)
+    g = torch.Generator().manual_seed(3)
+    perm = torch.randperm(wl.num_pages, generator=g)      # new slot of old page p = perm[p]
+    kv2 = torch.empty_like(wl.kv_cache)
+    kv2[perm] = wl.kv_cache
+    bt2 = wl.block_table.clone()
+    m = bt2 >= 0
+    bt2[m] = perm[bt2[m].long()].to(torch.int32)
+    wl2 = W.Workload(**{**wl.__dict__})
+    wl2.kv_cache, wl2.block_table = kv2, bt2
+    b, _ = oracle.workload_logits(wl2)
+    assert np.array_equal(a, b)
+
+
+def check_varlen_equals_padded():
+    wl = small_workload(seed=13, lens=(300, 129, 64, 1), rows=(2, 5, 1, 1))
+    a, _ = oracle.workload_logits(wl)
+    slot_row, max_n = W.padded_rows(wl)
+    # padded batch: every request gets max_n rows; padding rows repeat the
+    # request's last row (its q, weights, block table and causal limit)
+    src = []
+    t = 0
+    for n in wl.rows_per_request:
+        for j in range(max_n):
+            src.append(t + min(j, n - 1))
+        t += n
+    src = torch.tensor(src)
+    wl2 = W.Workload(**{**wl.__dict__})
+    wl2.q, wl2.weights = wl.q[src], wl.weights[src]
+    wl2.context_lens, wl2.block_table = wl.context_lens[src], wl.block_table[src]
+    wl2.indices = None
+    b, _ = oracle.workload_logits(wl2)
+    valid = slot_row >= 0
+    assert np.array_equal(b[valid.numpy()], a[slot_row[valid].numpy()])
+
+
+def check_topk_bruteforce(seed=0):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for kind in ("random", "ties", "bf16", "inf", "nan", "short", "empty", "start"):
+        R, C = 5, 97
+        x = rng.standard_normal((R, C))
+        if kind == "ties":
+            x = rng.integers(-3, 3, (R, C)).astype(np.float64)
+            x[0, :] = 0.0
+            x[1, ::2] = -0.0
+        elif kind == "bf16":
+            x = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+        elif kind == "inf":
+            x[:, 50:] = -np.inf
+        elif kind == "nan":
+            x[:, ::7] = np.nan
+        ends = rng.integers(0, C + 1, R).astype(np.int32)
+        starts = np.zeros(R, np.int32)
+        if kind == "short":
+            ends = np.minimum(ends, 9)
+        if kind == "empty":
+            ends[:] = 0
+        if kind == "start":
+            starts = rng.integers(0, 40, R).astype(np.int32)
+            ends = np.maximum(ends, starts)
+        cases.append((x, starts, ends))
+    for x, starts, ends in cases:
+        for k in (1, 8, 16, 100):
+            got = oracle.top_k_per_row(x, ends, k, row_starts=starts)
+            for r in range(x.shape[0]):
+                cols = range(int(starts[r]), int(ends[r]))
+                key = (lambda s: (1, 0.0, s) if np.isnan(x[r, s]) else (0, -x[r, s], s))
+                pick = sorted(sorted(cols, key=key)[:k])
+                ref = pick + [-1] * (k - len(pick))
+                assert list(got[r]) == ref, (r, k)
+
+
+def check_fp4_bruteforce():
+    check_bruteforce(kv_format=W.KV_FP4, seed=21)
+
+
+PIN_CHECKS = [
+    check_e4m3_vs_torch, check_e2m1_vs_spec, check_bruteforce, check_one_hot_reads_key,
+    check_relu_identities, check_weight_scaling, check_page_permutation,
+    check_varlen_equals_padded, check_topk_bruteforce, check_fp4_bruteforce,
+]
+
+
+# ---------------------------------------------------------------------------
+# tests
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("check", PIN_CHECKS, ids=lambda f: f.__name__)
+def test_pin(check):
+    oracle.set_plant(0)
+    check()
+
+
+def test_bruteforce_few_heads():
+    for H in (1, 2):
+        check_bruteforce(H=H, seed=H)
+
+
+def test_fp4_relu_identities():
+    check_relu_identities(kv_format=W.KV_FP4)
+
+
+def test_fp4_unit_keys_closed_form():
+    """FP4 keys all 1.0 (code 0x2, block scale 1.0, token scale 1): logit = sum_h w_h relu(sum_d q_hd)."""
+    wl = small_workload(seed=3, kv_format=W.KV_FP4, lens=(70,), rows=(1,))
+    kv = wl.kv_cache.clone()
+    for p in wl.block_table[0, :2].tolist():
+        kv[p, :4096] = 0x22
+        kv[p, 4096:4608] = 0x38
+        kv[p, 4608:4864] = torch.tensor([1.0] * 64, dtype=torch.float32).view(torch.uint8)
+    wl.kv_cache = kv
+    lg, _ = oracle.workload_logits(wl)
+    Q = dense_q(wl, 0)
+    w = wl.weights[0].double().numpy()
+    ref = float(w @ np.maximum(Q.sum(axis=1), 0.0))
+    assert np.allclose(lg[0, :70], ref, rtol=1e-13, atol=0)
+
+
+def test_plain_equals_arange():
+    wl = W.config("tiny")
+    B = wl.num_rows
+    s_none = oracle.schedule(wl.context_lens, None, 16)
+    s_ar = oracle.schedule(wl.context_lens, torch.arange(B, dtype=torch.int32), 16)
+    assert s_none[2] == 0 and s_ar[2] == 1
+    s_none[2] = 1
+    assert np.array_equal(s_none, s_ar)
+    assert oracle.validate(wl.context_lens, None, wl.block_table, wl.num_pages,
+                           wl.logits_stride) == 0
+    assert oracle.validate(wl.context_lens, torch.arange(B, dtype=torch.int32), wl.block_table,
+                           wl.num_pages, wl.logits_stride) == 0
+
+
+def test_topk_all_equal_picks_first_k():
+    x = np.zeros((1, 50))
+    assert list(oracle.top_k_per_row(x, [50], 10)[0]) == list(range(10))
+    x = np.full((1, 50), -np.inf)
+    assert list(oracle.top_k_per_row(x, [50], 3)[0]) == [0, 1, 2]
+
+
+def test_topk_short_rows_pad():
+    x = np.arange(10, dtype=np.float64)[None, :]
+    assert list(oracle.top_k_per_row(x, [4], 6)[0]) == [0, 1, 2, 3, -1, -1]
+    assert list(oracle.top_k_per_row(x, [0], 3)[0]) == [-1, -1, -1]
+
+
+def _schedule_props(lens, ids, S):
+    T = len(lens)
+    words = oracle.schedule(np.array(lens, np.int32), None if ids is None else np.array(ids, np.int32), S)
+    assert len(words) == oracle.schedule_words(S, T)
+    hdr, sm, grs, gus = oracle.parse_schedule(words, S, T)
+    G, U = int(hdr[4]), int(hdr[5])
+    assert hdr[0] == 0x44534131 and hdr[1] == T and hdr[3] == S and hdr[6] == 128 and hdr[7] == 8
+    # groups: cover every row, no longer than 8 rows, one request id each,
+    # a run continues into the next group only when the group is full
+    assert grs[0] == 0 and grs[G] == T and np.all(np.diff(grs[: G + 1]) > 0)
+    assert np.all(np.diff(grs[: G + 1]) <= 8)
+    for g in range(G):
+        rows = range(grs[g], grs[g + 1])
+        if ids is not None:
+            assert len({ids[t] for t in rows}) == 1
+        else:
+            assert len(rows) == 1
+        if g + 1 < G and ids is not None and ids[grs[g + 1]] == ids[grs[g + 1] - 1]:
+            assert grs[g + 1] - grs[g] == 8
+        lmax = max(max(lens[t] for t in rows), 0)
+        assert gus[g + 1] - gus[g] == (lmax + 127) // 128
+    assert gus[0] == 0 and gus[G] == U
+    # SM split: monotone, complete, balanced within one unit's weight
+    assert sm[0] == 0 and sm[S] == U and np.all(np.diff(sm) >= 0)
+    unit_w = []
+    for g in range(G):
+        unit_w += [4 + (grs[g + 1] - grs[g])] * int(gus[g + 1] - gus[g])
+    unit_w = np.array(unit_w, dtype=np.int64)
+    Wt = int(unit_w.sum())
+    if U:
+        mx = int(unit_w.max())
+        for i in range(S):
+            work = int(unit_w[sm[i]: sm[i + 1]].sum())
+            assert work <= Wt / S + mx and work >= Wt / S - mx
+    return words
+
+
+def test_schedule_properties():
+    rng = np.random.default_rng(0)
+    _schedule_props([300, 517], [0, 1], 8)
+    _schedule_props([300, 517], None, 148)
+    _schedule_props([], None, 4)
+    _schedule_props([0, 0, 5], [0, 1, 1], 3)
+    for trial in range(20):
+        B = int(rng.integers(1, 30))
+        n = rng.integers(1, 12, B)
+        ids, lens = [], []
+        for r in range(B):
+            L = int(rng.integers(0, 5000))
+            for j in range(n[r]):
+                ids.append(r)
+                lens.append(max(0, L - n[r] + 1 + j))
+        _schedule_props(lens, ids, int(rng.integers(1, 200)))
+
+
+def test_validate_errors():
+    wl = small_workload(seed=1)
+    ok = dict(context_lens=wl.context_lens, indices=wl.indices, block_table=wl.block_table,
+              num_pages=wl.num_pages, logits_stride=wl.logits_stride)
+    assert oracle.validate(**ok) == oracle.ORACLE_OK
+    bad = dict(ok, indices=torch.tensor([0, 1, 1, 1, 0, 2], dtype=torch.int32))
+    assert oracle.validate(**bad) == oracle.ORACLE_ERR_GROUPING
+    cl = wl.context_lens.clone()
+    cl[2] = cl[1] - 1
+    assert oracle.validate(**dict(ok, context_lens=cl)) == oracle.ORACLE_ERR_CONTEXT
+    bt = wl.block_table.clone()
+    bt[2, 0] = (bt[1, 0] + 1) % wl.num_pages
+    assert oracle.validate(**dict(ok, block_table=bt)) == oracle.ORACLE_ERR_BLOCK_TABLE
+    bt = wl.block_table.clone()
+    bt[0, 0] = wl.num_pages
+    assert oracle.validate(**dict(ok, block_table=bt)) == oracle.ORACLE_ERR_BLOCK_ID
+    assert oracle.validate(**dict(ok, logits_stride=wl.logits_stride - 64)) == oracle.ORACLE_ERR_STRIDE
+
+
+# plant id -> the mistake it switches on inside the oracle
+PLANTS = {
+    1: "query operand transposed (q[d][h] for q[h][d])",
+    2: "ReLU dropped",
+    3: "page index s / 128 for s / 64 (wrong block size)",
+    4: "sign flipped inside the ReLU",
+    5: "head weight dropped",
+    6: "FP4 block scale index d / 32 for d / 16",
+    7: "top-k order reversed",
+}
+
+
+@pytest.mark.parametrize("plant", sorted(PLANTS), ids=lambda p: PLANTS[p])
+def test_planted_mistake_is_caught(plant):
+    caught = []
+    oracle.set_plant(plant)
+    try:
+        for check in PIN_CHECKS:
+            try:
+                check()
+            except AssertionError:
+                caught.append(check.__name__)
+    finally:
+        oracle.set_plant(0)
+    assert caught, f"no pin caught plant {plant}: {PLANTS[plant]}"
