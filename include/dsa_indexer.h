@@ -1,0 +1,202 @@
+/*
+ * dsa_indexer.h - C ABI of the GB300 (sm_103a) DeepSeek-sparse-attention
+ * indexer decode path: varlen paged MQA logits followed by per-row top-k.
+ *
+ * Three calls make one indexer decode step, in stream order:
+ *
+ *   dsa_paged_mqa_logits_metadata  -> per-SM work schedule
+ *   dsa_fp8_fp4_paged_mqa_logits   -> logits[t, s] for every row t
+ *   dsa_top_k_per_row              -> the k best columns of every row
+ *
+ * Conventions shared by every call:
+ *   - Pointers marked (device) are CUDA device pointers of the current device;
+ *     the caller allocates, owns and frees every buffer.  The library never
+ *     allocates, frees or synchronises; it only enqueues kernels on `stream`
+ *     (0 = the legacy default stream).  Calls are asynchronous.
+ *   - The return value reports host-side checks and launch errors
+ *     (dsa_status_t).  Faults found on the device (a page id out of range, a
+ *     schedule built for other inputs, a pipeline wait that ran out) are
+ *     written to `*status` (device int32, may be NULL) with atomicCAS from 0,
+ *     so the first one sticks; the caller zeroes it and reads it when it
+ *     wants.  A device fault leaves the outputs unspecified but never hangs
+ *     or traps the GPU.
+ *   - Sizes: H = 64 heads, D = 128 head dim and block_kv = 64 tokens per page
+ *     are the supported shape (others return DSA_ERR_UNSUPPORTED).
+ *
+ * Sources.  The operations are the ones named by the vLLM sparse attention
+ * indexer pages:
+ *   [PR47469] "[Attention][DSA] Route SM100 sparse-indexer decode through
+ *             varlen paged MQA logits", Purpose and Changes;
+ *   [PR56811] "[Bugfix][GLM-5.3-Flash] Fix fp8_fp4_paged_mqa_logits MQA kpool
+ *             varlen path for speculative decode", Purpose;
+ *   [DOCS]    vllm.model_executor.layers.sparse_attn_indexer API docs,
+ *             sections _varlen_decode_rows, as_fp32_logits, forward_cpu,
+ *             forward_cuda, kv_cache_as_quant_view, _gather_workspace_shapes.
+ */
+#ifndef DSA_INDEXER_H_
+#define DSA_INDEXER_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsa_stream_t; /* = cudaStream_t */
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,       /* null pointer, negative size, misaligned buffer */
+  DSA_ERR_UNSUPPORTED = 2,       /* H != 64, D != 128, block_kv != 64, k > 2048, ... */
+  DSA_ERR_SCHEDULE_MISMATCH = 3, /* (device) schedule built for other rows / mode / SM count */
+  DSA_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
+  DSA_ERR_BAD_BLOCK = 5,         /* (device) page id outside [0, num_pages) or past the table */
+  DSA_ERR_TIMEOUT = 6,           /* (device) a pipeline wait ran out; the kernel returned early */
+  DSA_ERR_NO_DEVICE = 7          /* no usable sm_103 device */
+} dsa_status_t;
+
+enum { DSA_KV_FP8 = 0, DSA_KV_FP4 = 1 };
+enum { DSA_LOGITS_F32 = 0, DSA_LOGITS_BF16 = 1 };
+
+/* Tokens per page, heads and head dimension of the supported shape. */
+#define DSA_BLOCK_KV 64
+#define DSA_NUM_HEADS 64
+#define DSA_HEAD_DIM 128
+/* Bytes of one page: FP8 = 64 x 128 e4m3 codes, then 64 fp32 scales;
+   FP4 = 64 x 64 bytes of packed e2m1 (element 2i in the low nibble of byte i),
+   then 64 x 8 e4m3 block scales (one per 16 elements), then 64 fp32 token
+   scales.  The page stride may be larger (a per-layer view into a shared
+   allocation, [DOCS] forward_cpu) and must be a multiple of 16. */
+#define DSA_FP8_PAGE_BYTES 8448
+#define DSA_FP4_PAGE_BYTES 4864
+/* Largest k of dsa_top_k_per_row. */
+#define DSA_MAX_TOPK 2048
+
+/* Text of a status code (static storage). */
+const char* dsa_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dsa_version(void);
+
+/* Number of int32 words of a schedule for `num_sms` SMs and `num_rows` rows:
+   8 + (num_sms + 1) + 2 * (num_rows + 1). */
+int64_t dsa_schedule_words(int32_t num_sms, int32_t num_rows);
+
+/* SM count of the current device (what the metadata call should balance
+   over), or a negative dsa_status_t. */
+int32_t dsa_device_num_sms(void);
+
+/*
+ * dsa_paged_mqa_logits_metadata - per-SM work schedule of the logits call.
+ *
+ * [PR47469] Purpose/Changes: get_paged_mqa_logits_metadata(seq_lens,
+ * block_kv, num_sms, indices) builds the SM schedule; passing the per-row
+ * request id `indices` selects the varlen schedule.  [DOCS]
+ * _varlen_decode_rows: a slice of rows gets its own schedule, built from that
+ * slice's seq_lens and indices.
+ *
+ *   context_lens (device) int32 [num_rows]: causal limit L_t of each row
+ *                (the row sees keys 0 .. L_t - 1); non-decreasing within a
+ *                request.
+ *   indices      (device) int32 [num_rows] or NULL: request id of each row.
+ *                Rows of one request must be adjacent ([PR56811] Purpose).
+ *                NULL means every row is its own request (plain decode;
+ *                equal to indices = arange(num_rows)).
+ *   num_rows     >= 0.
+ *   block_kv     must be 64.
+ *   num_sms      >= 1 (normally dsa_device_num_sms()); the logits call must
+ *                be given the same value.
+ *   schedule     (device) int32 [dsa_schedule_words(num_sms, num_rows)], out.
+ *
+ * Rule: runs of equal ids are cut into groups of at most 8 rows; group g
+ * covers ceil(max L_t / 128) tiles of 128 keys; a tile weighs 4 + rows(g);
+ * SM i starts at the first tile whose preceding weight reaches i/num_sms of
+ * the total.  Layout: header[8] = {0x44534131, num_rows, varlen flag,
+ * num_sms, num_groups, num_tiles, 128, 8}, sm_start[num_sms + 1],
+ * group_row_start[num_rows + 1], group_tile_start[num_rows + 1].
+ */
+int dsa_paged_mqa_logits_metadata(const int32_t* context_lens, const int32_t* indices,
+                                  int32_t num_rows, int32_t block_kv, int32_t num_sms,
+                                  int32_t* schedule, dsa_stream_t stream);
+
+/*
+ * dsa_fp8_fp4_paged_mqa_logits - varlen paged MQA logits.
+ *
+ * [PR47469] Purpose and [PR56811] Purpose: rows that share a request id are
+ * processed together, so one K page serves all of a request's rows and heads
+ * with no padding to (B, max_decode_len).  [DOCS] _varlen_decode_rows: the
+ * call takes q, weights, the key cache, seq_lens, the row-sliced block table,
+ * the schedule and indices; [DOCS] forward_cuda: the FP8 q's per-token scale
+ * is folded into the weights.
+ *
+ *   logits[t, s] = kscale[s] * sum_h weights[t, h] * max(0, sum_d q[t,h,d] * k[s,d])
+ *                  for s < L_t;  -inf for L_t <= s < round_up(L_t, 64).
+ *   FP8 keys: k[s, d] = e4m3 code; kscale[s] = the page's fp32 scale.
+ *   FP4 keys: k[s, d] = e2m1 * e4m3 block scale of d / 16; kscale[s] = the
+ *             page's fp32 token scale.
+ *   Columns at or past round_up(L_t, 64) are not written.
+ *
+ *   q            (device) e4m3 [num_rows][64][128], 16-byte aligned.
+ *   kv_cache     (device) page pool, 16-byte aligned; page p at
+ *                kv_cache + p * page_stride_bytes.
+ *   page_stride_bytes >= page bytes of kv_format, multiple of 16.
+ *   num_pages    pages in the pool, >= 1.
+ *   kv_format    DSA_KV_FP8 or DSA_KV_FP4.
+ *   weights      (device) fp32 [num_rows][64], 16-byte aligned.
+ *   context_lens (device) int32 [num_rows] (as for the metadata call).
+ *   block_table  (device) int32 [num_rows][block_table_stride]: page ids of
+ *                each row's keys.  Rows of one request must hold the same
+ *                page ids; the kernel reads them from the last row of each
+ *                group (the row with the largest causal limit).  Entries
+ *                read must lie in [0, num_pages) and below the stride;
+ *                others are reported as DSA_ERR_BAD_BLOCK.
+ *   indices      (device) int32 [num_rows] or NULL; must be NULL exactly when
+ *                the schedule was built with NULL (else
+ *                DSA_ERR_SCHEDULE_MISMATCH, the kpool fault of [PR56811]).
+ *   schedule     (device) output of the metadata call for these rows.
+ *   num_sms      the num_sms the schedule was built for; one CTA per SM.
+ *   logits       (device) fp32 or bf16 [num_rows][logits_stride], 16-byte
+ *                aligned; logits_stride >= round_up(max L_t, 64) elements and
+ *                a multiple of 8.
+ *   logits_dtype DSA_LOGITS_F32 or DSA_LOGITS_BF16 (round to nearest even).
+ *   num_heads, head_dim, block_kv: must be 64, 128, 64.
+ */
+int dsa_fp8_fp4_paged_mqa_logits(const void* q, const void* kv_cache, int64_t page_stride_bytes,
+                                 int64_t num_pages, int32_t kv_format, const float* weights,
+                                 const int32_t* context_lens, const int32_t* block_table,
+                                 int64_t block_table_stride, const int32_t* indices,
+                                 const int32_t* schedule, int32_t num_sms, void* logits,
+                                 int32_t logits_dtype, int64_t logits_stride, int32_t num_rows,
+                                 int32_t num_heads, int32_t head_dim, int32_t block_kv,
+                                 int32_t* status, dsa_stream_t stream);
+
+/*
+ * dsa_top_k_per_row - the k largest logits of each row.
+ *
+ * [DOCS] _varlen_decode_rows: selector(logits, seq_lens, ..., out, k) with the
+ * rows' causal limits as row ends; [DOCS] forward_cpu: the output is pre-filled
+ * with -1, which pads rows shorter than k; [DOCS] as_fp32_logits: BF16 logits
+ * are upcast to fp32 for the selection, only below the row end (here the
+ * upcast is exact and done while reading).
+ *
+ *   logits       (device) fp32 or bf16 [num_rows][logits_stride].
+ *   row_starts   (device) int32 [num_rows] or NULL (= 0).
+ *   row_ends     (device) int32 [num_rows]; columns [row_start, row_end) compete;
+ *                row_end <= logits_stride.
+ *   k            1 .. DSA_MAX_TOPK.
+ *   out_idx      (device) int32 [num_rows][out_stride], out_stride >= k:
+ *                the chosen columns in ascending order, then -1 up to k.
+ * Order: larger logit first; equal logits go to the lower column; -0 == +0;
+ * NaN ranks below every number.
+ */
+int dsa_top_k_per_row(const void* logits, int32_t logits_dtype, int64_t logits_stride,
+                      const int32_t* row_starts, const int32_t* row_ends, int32_t num_rows,
+                      int32_t k, int32_t* out_idx, int64_t out_stride, int32_t* status,
+                      dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_INDEXER_H_ */

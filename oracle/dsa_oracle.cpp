@@ -237,7 +237,15 @@ int oracle_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_cache, int64_t p
     }
   }
   const double neg_inf = -std::numeric_limits<double>::infinity();
-  parallel_for(n_eval, nthreads, [&](int i) {
+  // Work items are (selected row, block of kColBlock columns); each output
+  // element is computed on its own, so the split changes no arithmetic.
+  constexpr int64_t kColBlock = 2048;
+  const int64_t blocks_per_row = (out_cols + kColBlock - 1) / kColBlock;
+  const int64_t n_items = static_cast<int64_t>(n_eval) * std::max<int64_t>(blocks_per_row, 1);
+  parallel_for(static_cast<int>(n_items), nthreads, [&](int item) {
+    const int i = static_cast<int>(item / std::max<int64_t>(blocks_per_row, 1));
+    const int64_t c0 = (item % std::max<int64_t>(blocks_per_row, 1)) * kColBlock;
+    const int64_t c1 = std::min<int64_t>(c0 + kColBlock, out_cols);
     const int t = rows ? rows[i] : i;
     const int32_t L = context_lens[t];
     std::vector<double> qd(static_cast<size_t>(H) * D), k(D);
@@ -245,7 +253,7 @@ int oracle_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_cache, int64_t p
       qd[j] = decode_e4m3(q[static_cast<int64_t>(t) * H * D + j]);
     double* out = logits + static_cast<int64_t>(i) * out_cols;
     double* bnd = bound ? bound + static_cast<int64_t>(i) * out_cols : nullptr;
-    for (int64_t s = 0; s < out_cols; ++s) {
+    for (int64_t s = c0; s < c1; ++s) {
       if (s >= L) {
         out[s] = neg_inf;
         if (bnd) bnd[s] = 0.0;

@@ -1,0 +1,200 @@
+"""Python binding of libdsa_indexer (the GB300 DSA indexer decode path).
+
+Thin ctypes layer over the C ABI of ``include/dsa_indexer.h``: it only turns
+torch tensors into pointers, sizes and the current CUDA stream, and allocates
+outputs the caller did not pass (torch is used for device memory and streams
+only).  Every step of the path runs in the library's kernels; there is no
+fallback.  If the library has not been built, every call raises.
+
+    sched  = paged_mqa_logits_metadata(context_lens, indices, num_sms)
+    logits = fp8_fp4_paged_mqa_logits(q, kv_cache, weights, context_lens,
+                                      block_table, sched, indices=indices)
+    idx    = top_k_per_row(logits, None, context_lens, k)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB_PATH, build  # noqa: F401
+
+DSA_OK = 0
+DSA_ERR_INVALID_ARG = 1
+DSA_ERR_UNSUPPORTED = 2
+DSA_ERR_SCHEDULE_MISMATCH = 3
+DSA_ERR_CUDA = 4
+DSA_ERR_BAD_BLOCK = 5
+DSA_ERR_TIMEOUT = 6
+DSA_ERR_NO_DEVICE = 7
+
+KV_FP8 = 0
+KV_FP4 = 1
+LOGITS_F32 = 0
+LOGITS_BF16 = 1
+
+BLOCK_KV = 64
+NUM_HEADS = 64
+HEAD_DIM = 128
+FP8_PAGE_BYTES = 8448
+FP4_PAGE_BYTES = 4864
+MAX_TOPK = 2048
+
+# C entry points and their argument types
+_P, _I32, _I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+_SIGS = {
+    "dsa_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "dsa_version": ([], ctypes.c_int),
+    "dsa_schedule_words": ([_I32, _I32], _I64),
+    "dsa_device_num_sms": ([], _I32),
+    "dsa_paged_mqa_logits_metadata": ([_P, _P, _I32, _I32, _I32, _P, _P], ctypes.c_int),
+    "dsa_fp8_fp4_paged_mqa_logits": ([_P, _P, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _P, _I32,
+                                      _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P],
+                                     ctypes.c_int),
+    "dsa_top_k_per_row": ([_P, _I32, _I64, _P, _P, _I32, _I32, _P, _I64, _P, _P], ctypes.c_int),
+}
+EXPORTED = tuple(_SIGS)
+
+_lib = None
+
+
+class DsaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        msg = lib().dsa_status_string(code).decode() if _lib is not None else str(code)
+        super().__init__(f"{what}: {msg} (status {code})")
+        self.code = code
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libdsa_indexer is not built ({LIB_PATH}); "
+                               "run __graft_entry__.build() or "
+                               "sparse_attention_indexer_paged_gb300.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(code: int, what: str):
+    if code != DSA_OK:
+        raise DsaError(code, what)
+
+
+def _dev_i32(x, device):
+    if x is None:
+        return None
+    if not torch.is_tensor(x):
+        x = torch.as_tensor(x)
+    return x.to(device=device, dtype=torch.int32).contiguous()
+
+
+def status_string(code: int) -> str:
+    return lib().dsa_status_string(int(code)).decode()
+
+
+def device_num_sms() -> int:
+    n = lib().dsa_device_num_sms()
+    if n < 0:
+        raise DsaError(-n, "dsa_device_num_sms")
+    return int(n)
+
+
+def schedule_words(num_sms: int, num_rows: int) -> int:
+    return int(lib().dsa_schedule_words(int(num_sms), int(num_rows)))
+
+
+def paged_mqa_logits_metadata(context_lens, indices=None, num_sms=None, block_kv=BLOCK_KV,
+                              out=None):
+    """Per-SM work schedule (int32 device tensor) for the logits call."""
+    ctx = context_lens
+    device = ctx.device
+    T = int(ctx.shape[0])
+    if num_sms is None:
+        num_sms = device_num_sms()
+    words = schedule_words(num_sms, T)
+    if out is None:
+        out = torch.empty(words, dtype=torch.int32, device=device)
+    assert out.dtype == torch.int32 and out.is_contiguous() and out.numel() >= words
+    ctx = _dev_i32(ctx, device)
+    ind = _dev_i32(indices, device)
+    _check(lib().dsa_paged_mqa_logits_metadata(_ptr(ctx), _ptr(ind), T, int(block_kv),
+                                               int(num_sms), _ptr(out), _stream(device)),
+           "paged_mqa_logits_metadata")
+    return out
+
+
+def fp8_fp4_paged_mqa_logits(q, kv_cache, weights, context_lens, block_table, schedule,
+                             indices=None, kv_format=KV_FP8, logits_dtype=LOGITS_F32,
+                             logits_stride=None, num_sms=None, out=None, status=None,
+                             page_stride=None):
+    """Varlen paged MQA logits [num_rows, logits_stride] (fp32 or bf16).
+
+    q [T, 64, 128] e4m3 codes (uint8 or float8_e4m3fn); kv_cache [num_pages,
+    page_stride] uint8 pages; weights [T, 64] fp32; context_lens [T];
+    block_table [T, max_pages] int32; schedule from paged_mqa_logits_metadata.
+    Columns >= round_up(L_t, 64) of a row are not specified.
+    """
+    device = q.device
+    T = int(q.shape[0])
+    if num_sms is None:
+        num_sms = device_num_sms()
+    ctx = _dev_i32(context_lens, device)
+    bt = _dev_i32(block_table, device)
+    if bt.dim() == 1:
+        bt = bt.view(max(T, 1), -1)
+    ind = _dev_i32(indices, device)
+    if logits_stride is None:
+        mx = int(ctx.max().item()) if T else 0
+        logits_stride = max(BLOCK_KV, (mx + BLOCK_KV - 1) // BLOCK_KV * BLOCK_KV)
+    dt = torch.float32 if logits_dtype == LOGITS_F32 else torch.bfloat16
+    if out is None:
+        out = torch.empty((T, logits_stride), dtype=dt, device=device)
+    assert out.dtype == dt and out.stride(-1) == 1 and out.stride(0) == logits_stride
+    qq = q.view(torch.uint8) if q.dtype != torch.uint8 else q
+    assert qq.is_contiguous() and weights.is_contiguous() and weights.dtype == torch.float32
+    assert kv_cache.dim() == 2 and kv_cache.stride(1) == 1
+    pstride = kv_cache.stride(0) if page_stride is None else int(page_stride)
+    _check(lib().dsa_fp8_fp4_paged_mqa_logits(
+        _ptr(qq), _ptr(kv_cache), pstride, int(kv_cache.shape[0]), int(kv_format), _ptr(weights),
+        _ptr(ctx), _ptr(bt), int(bt.stride(0)), _ptr(ind), _ptr(schedule), int(num_sms),
+        _ptr(out), int(logits_dtype), int(logits_stride), T, NUM_HEADS, HEAD_DIM, BLOCK_KV,
+        _ptr(status), _stream(device)), "fp8_fp4_paged_mqa_logits")
+    return out
+
+
+def top_k_per_row(logits, row_starts, row_ends, k, out=None, status=None):
+    """Top-k columns of each row in [row_start, row_end): int32 [rows, k], ascending, -1 padded."""
+    device = logits.device
+    R = int(logits.shape[0])
+    if logits.dtype == torch.float32:
+        dt = LOGITS_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = LOGITS_BF16
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    assert logits.stride(-1) == 1
+    if out is None:
+        out = torch.empty((R, k), dtype=torch.int32, device=device)
+    assert out.dtype == torch.int32 and out.stride(-1) == 1
+    starts = _dev_i32(row_starts, device)
+    ends = _dev_i32(row_ends, device)
+    _check(lib().dsa_top_k_per_row(_ptr(logits), dt, int(logits.stride(0)), _ptr(starts),
+                                   _ptr(ends), R, int(k), _ptr(out), int(out.stride(0)),
+                                   _ptr(status), _stream(device)), "top_k_per_row")
+    return out

@@ -1,0 +1,196 @@
+// C ABI of the indexer library: argument checks, tensor maps, launches.
+// Every entry point is stream-ordered; nothing here allocates, frees or
+// synchronises.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace dsa {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void resolve_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device check, cached per device: sm_103 is the only compiled target.
+std::atomic<int> g_dev_ok[64];
+
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return DSA_ERR_NO_DEVICE;
+  if (dev < 64) {
+    const int cached = g_dev_ok[dev].load(std::memory_order_relaxed);
+    if (cached == 1) return DSA_OK;
+    if (cached == 2) return DSA_ERR_NO_DEVICE;
+  }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return DSA_ERR_NO_DEVICE;
+  const bool ok = major == 10 && minor == 3;
+  if (dev < 64) g_dev_ok[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
+  return ok ? DSA_OK : DSA_ERR_NO_DEVICE;
+}
+
+int launch_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+}  // namespace
+
+bool encode_tensor_map_u8(void* tmap_out, int rank, void* base, const uint64_t* dims,
+                          const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128) {
+  std::call_once(g_encode_once, resolve_encode);
+  if (g_encode == nullptr) return false;
+  cuuint64_t gd[5];
+  cuuint64_t gs[4];
+  cuuint32_t bx[5];
+  cuuint32_t es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) gs[i] = strides_bytes[i];
+  }
+  const CUresult r = g_encode(static_cast<CUtensorMap*>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                              static_cast<cuuint32_t>(rank), base, gd, gs, bx, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+const char* dsa_status_string(int status) {
+  switch (status) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_INVALID_ARG: return "invalid argument";
+    case DSA_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case DSA_ERR_SCHEDULE_MISMATCH: return "schedule was built for other rows, mode or SM count";
+    case DSA_ERR_CUDA: return "CUDA runtime or launch error";
+    case DSA_ERR_BAD_BLOCK: return "page id outside the pool or past the block table";
+    case DSA_ERR_TIMEOUT: return "a pipeline wait ran out; the kernel returned early";
+    case DSA_ERR_NO_DEVICE: return "no sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+int dsa_version(void) { return 100; }
+
+int64_t dsa_schedule_words(int32_t num_sms, int32_t num_rows) {
+  if (num_sms < 1 || num_rows < 0) return -1;
+  return kScheduleHeaderWords + (static_cast<int64_t>(num_sms) + 1) +
+         2 * (static_cast<int64_t>(num_rows) + 1);
+}
+
+int32_t dsa_device_num_sms(void) {
+  const int st = check_device();
+  if (st != DSA_OK) return -st;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -DSA_ERR_CUDA;
+  return n;
+}
+
+int dsa_paged_mqa_logits_metadata(const int32_t* context_lens, const int32_t* indices,
+                                  int32_t num_rows, int32_t block_kv, int32_t num_sms,
+                                  int32_t* schedule, dsa_stream_t stream) {
+  if (num_rows < 0 || num_sms < 1 || schedule == nullptr) return DSA_ERR_INVALID_ARG;
+  if (num_rows > 0 && context_lens == nullptr) return DSA_ERR_INVALID_ARG;
+  if (num_sms > 1023) return DSA_ERR_UNSUPPORTED;
+  if (block_kv != kPageTokens) return DSA_ERR_UNSUPPORTED;
+  const int dev = check_device();
+  if (dev != DSA_OK) return dev;
+  return launch_status(launch_metadata(context_lens, indices, num_rows, num_sms, schedule,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dsa_fp8_fp4_paged_mqa_logits(const void* q, const void* kv_cache, int64_t page_stride_bytes,
+                                 int64_t num_pages, int32_t kv_format, const float* weights,
+                                 const int32_t* context_lens, const int32_t* block_table,
+                                 int64_t block_table_stride, const int32_t* indices,
+                                 const int32_t* schedule, int32_t num_sms, void* logits,
+                                 int32_t logits_dtype, int64_t logits_stride, int32_t num_rows,
+                                 int32_t num_heads, int32_t head_dim, int32_t block_kv,
+                                 int32_t* status, dsa_stream_t stream) {
+  if (num_heads != kHeads || head_dim != kHeadDim || block_kv != kPageTokens)
+    return DSA_ERR_UNSUPPORTED;
+  if (kv_format != DSA_KV_FP8 && kv_format != DSA_KV_FP4) return DSA_ERR_UNSUPPORTED;
+  if (logits_dtype != DSA_LOGITS_F32 && logits_dtype != DSA_LOGITS_BF16) return DSA_ERR_UNSUPPORTED;
+  if (num_rows < 0 || num_sms < 1 || num_sms > 1023) return DSA_ERR_INVALID_ARG;
+  if (num_rows == 0) return DSA_OK;
+  if (!q || !kv_cache || !weights || !context_lens || !block_table || !schedule || !logits)
+    return DSA_ERR_INVALID_ARG;
+  const int64_t page_bytes = kv_format == DSA_KV_FP8 ? DSA_FP8_PAGE_BYTES : DSA_FP4_PAGE_BYTES;
+  if (page_stride_bytes < page_bytes || page_stride_bytes % 16 != 0) return DSA_ERR_INVALID_ARG;
+  if (num_pages < 1 || num_pages > INT32_MAX) return DSA_ERR_INVALID_ARG;
+  if (block_table_stride < 1 || logits_stride < 1 || logits_stride % 8 != 0) return DSA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_rows) * kHeads >= (static_cast<int64_t>(1) << 31))
+    return DSA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(weights, 16) || !aligned(logits, 16))
+    return DSA_ERR_INVALID_ARG;
+  const int dev = check_device();
+  if (dev != DSA_OK) return dev;
+  LogitsArgs a;
+  a.q = static_cast<const uint8_t*>(q);
+  a.kv_cache = static_cast<const uint8_t*>(kv_cache);
+  a.page_stride = page_stride_bytes;
+  a.num_pages = num_pages;
+  a.kv_format = kv_format;
+  a.weights = weights;
+  a.context_lens = context_lens;
+  a.block_table = block_table;
+  a.bt_stride = block_table_stride;
+  a.indices = indices;
+  a.schedule = schedule;
+  a.num_sms = num_sms;
+  a.logits = logits;
+  a.logits_dtype = logits_dtype;
+  a.logits_stride = logits_stride;
+  a.num_rows = num_rows;
+  a.status = status;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = kv_format == DSA_KV_FP8 ? launch_logits_fp8(a, st) : launch_logits_fp4(a, st);
+  if (e == cudaErrorInvalidValue) return DSA_ERR_INVALID_ARG;
+  if (e == cudaErrorNotSupported) return DSA_ERR_UNSUPPORTED;
+  return launch_status(e);
+}
+
+int dsa_top_k_per_row(const void* logits, int32_t logits_dtype, int64_t logits_stride,
+                      const int32_t* row_starts, const int32_t* row_ends, int32_t num_rows,
+                      int32_t k, int32_t* out_idx, int64_t out_stride, int32_t* status,
+                      dsa_stream_t stream) {
+  if (logits_dtype != DSA_LOGITS_F32 && logits_dtype != DSA_LOGITS_BF16) return DSA_ERR_UNSUPPORTED;
+  if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (num_rows < 0 || out_stride < k) return DSA_ERR_INVALID_ARG;
+  if (num_rows == 0) return DSA_OK;
+  if (!logits || !row_ends || !out_idx) return DSA_ERR_INVALID_ARG;
+  if (logits_stride < 1 || logits_stride % 4 != 0 || logits_stride >= INT32_MAX) return DSA_ERR_INVALID_ARG;
+  if (!aligned(logits, 16)) return DSA_ERR_INVALID_ARG;
+  const int dev = check_device();
+  if (dev != DSA_OK) return dev;
+  return launch_status(launch_top_k(logits, logits_dtype, logits_stride, row_starts, row_ends,
+                                    num_rows, k, out_idx, out_stride, status,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

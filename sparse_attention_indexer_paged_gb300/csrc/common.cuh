@@ -1,0 +1,76 @@
+// Shared constants and host-side launch declarations of the indexer library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "dsa_indexer.h"
+
+namespace dsa {
+
+// Supported shape.
+constexpr int kHeads = DSA_NUM_HEADS;       // 64
+constexpr int kHeadDim = DSA_HEAD_DIM;      // 128
+constexpr int kPageTokens = DSA_BLOCK_KV;   // 64 tokens per page
+
+// Schedule rule: a tile is two pages (128 keys, the M of one MMA); runs of
+// equal request ids are cut into groups of at most kGroupMaxRows rows; every
+// tile of group g weighs kBaseWeight + rows(g).
+constexpr int kTileTokens = 128;
+constexpr int kGroupMaxRows = 8;
+constexpr int kBaseWeight = 4;
+constexpr int32_t kScheduleMagic = 0x44534131;
+constexpr int kScheduleHeaderWords = 8;
+
+// Device status codes (same values as dsa_status_t).
+constexpr int kErrScheduleMismatch = DSA_ERR_SCHEDULE_MISMATCH;
+constexpr int kErrBadBlock = DSA_ERR_BAD_BLOCK;
+constexpr int kErrTimeout = DSA_ERR_TIMEOUT;
+constexpr int kErrInvalid = DSA_ERR_INVALID_ARG;
+
+// A pipeline wait that sees no progress for this long gives up (the kernel
+// then records DSA_ERR_TIMEOUT and returns).  Draining in-flight copies before
+// exit is bounded separately.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s
+constexpr uint64_t kDrainTimeoutNs = 200000000ull;   // 0.2 s
+
+// ----------------------------------------------------------------- launchers
+// (defined in the kernel translation units, called by api.cu after the
+// arguments have been checked)
+
+cudaError_t launch_metadata(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
+                            int32_t num_sms, int32_t* schedule, cudaStream_t stream);
+
+struct LogitsArgs {
+  const uint8_t* q;
+  const uint8_t* kv_cache;
+  int64_t page_stride;
+  int64_t num_pages;
+  int32_t kv_format;
+  const float* weights;
+  const int32_t* context_lens;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* indices;
+  const int32_t* schedule;
+  int32_t num_sms;
+  void* logits;
+  int32_t logits_dtype;
+  int64_t logits_stride;
+  int32_t num_rows;
+  int32_t* status;
+};
+
+cudaError_t launch_logits_fp8(const LogitsArgs& a, cudaStream_t stream);
+cudaError_t launch_logits_fp4(const LogitsArgs& a, cudaStream_t stream);
+
+cudaError_t launch_top_k(const void* logits, int32_t logits_dtype, int64_t logits_stride,
+                         const int32_t* row_starts, const int32_t* row_ends, int32_t num_rows,
+                         int32_t k, int32_t* out_idx, int64_t out_stride, int32_t* status,
+                         cudaStream_t stream);
+
+// Tensor-map encoding through the driver entry point (no libcuda link).
+bool encode_tensor_map_u8(void* tmap_out, int rank, void* base, const uint64_t* dims,
+                          const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);
+
+}  // namespace dsa

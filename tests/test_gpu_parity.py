@@ -1,0 +1,222 @@
+"""GPU parity of the indexer decode path against the CPU oracle, through the
+C ABI (binding -> libdsa_indexer.so), on seeded synthetic inputs.
+
+Small cases run the oracle on every row (several tiles, ragged tails, groups
+longer than 8 rows, empty rows); the full-size decode workloads compare
+sampled rows element by element and every row's top-k against the oracle's
+top-k of the GPU logits."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_indexer_paged_gb300 as dsa
+import workloads as W
+from gpu_helpers import (check_logits, check_topk_exact, check_topk_tie_band, run_path,
+                         sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+MIXED = dict(request_lens=[1, 63, 64, 65, 127, 128, 129, 300, 1000, 2500],
+             rows_per_request=[1, 2, 1, 3, 1, 6, 8, 2, 4, 11])
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    dsa.build()
+    dsa.lib()
+
+
+def _full_check(wl, num_sms=None, use_indices=True):
+    out = run_path(wl, num_sms=num_sms, use_indices=use_indices)
+    assert int(out["status"].item()) == 0, dsa.status_string(int(out["status"].item()))
+    ref, bound, worst = check_logits(wl, out["logits"])
+    check_topk_exact(out["logits"], out["idx"], wl.context_lens, wl.topk)
+    check_topk_tie_band(out["idx"], ref, bound, wl.context_lens, wl.topk, list(range(wl.num_rows)))
+    return out, worst
+
+
+# ---------------------------------------------------------------- metadata
+
+@pytest.mark.parametrize("name", ["tiny", "plain", "mtp", "varlen"])
+def test_metadata_matches_oracle(name):
+    ctx, ind = W.config_rows(name)
+    for S in (1, 7, 148, dsa.device_num_sms(), 1023):
+        for use_ind in (True, False):
+            ids = ind if use_ind else None
+            got = dsa.paged_mqa_logits_metadata(ctx.cuda(), None if ids is None else ids.cuda(), S)
+            ref = oracle.schedule(ctx, ids, S)
+            assert np.array_equal(got.cpu().numpy(), ref), (name, S, use_ind)
+
+
+def test_metadata_ragged_groups():
+    wl = W.build("mixed", **MIXED, topk=64)
+    for S in (1, 3, 5, 64, 152):
+        got = dsa.paged_mqa_logits_metadata(wl.context_lens.cuda(), wl.indices.cuda(), S)
+        assert np.array_equal(got.cpu().numpy(), oracle.schedule(wl.context_lens, wl.indices, S))
+
+
+def test_metadata_long_batch():
+    """More rows than one CTA pass (chunked scans), random run lengths and zero-length rows."""
+    rng = np.random.default_rng(5)
+    ctx, ids = [], []
+    for r in range(900):
+        n = int(rng.integers(1, 14))
+        L = int(rng.integers(0, 3000))
+        for j in range(n):
+            ctx.append(max(0, L - n + 1 + j))
+            ids.append(r)
+    ctx = torch.tensor(ctx, dtype=torch.int32)
+    ids = torch.tensor(ids, dtype=torch.int32)
+    for S in (1, 148, 1023):
+        got = dsa.paged_mqa_logits_metadata(ctx.cuda(), ids.cuda(), S)
+        assert np.array_equal(got.cpu().numpy(), oracle.schedule(ctx, ids, S)), S
+
+
+# ---------------------------------------------------------------- logits + top-k, small
+
+def test_tiny_config():
+    _full_check(W.config("tiny"))
+
+
+def test_mixed_ragged():
+    _full_check(W.build("mixed", **MIXED, topk=64, seed=1))
+
+
+@pytest.mark.parametrize("S", [1, 5, 37])
+def test_mixed_any_sm_split(S):
+    _full_check(W.build("mixed", **MIXED, topk=256, seed=2), num_sms=S)
+
+
+def test_plain_decode_equals_arange():
+    kw = dict(request_lens=[700, 1, 130, 4097, 64], rows_per_request=[1] * 5, topk=128, seed=3)
+    a = run_path(W.build("arange", **kw))
+    b = run_path(W.build("plain", plain_indices=True, **kw), use_indices=False)
+    for t, L in enumerate(kw["request_lens"]):      # the specified span of each row
+        end = (L + 63) // 64 * 64
+        assert torch.equal(a["logits"][t, :end], b["logits"][t, :end]), t
+    assert torch.equal(a["idx"], b["idx"])
+    check_logits(W.build("plain", plain_indices=True, **kw), b["logits"])
+
+
+def test_varlen_equals_padded():
+    """Varlen rows give the logits of a (B, max_n) padded batch on its valid rows."""
+    wl = W.build("v", request_lens=[900, 333, 1500], rows_per_request=[3, 1, 5], topk=64, seed=4)
+    slot_row, max_n = W.padded_rows(wl)
+    src = []
+    t = 0
+    for n in wl.rows_per_request:
+        for j in range(max_n):
+            src.append(t + min(j, n - 1))
+        t += n
+    src = torch.tensor(src)
+    pad = W.Workload(**{**wl.__dict__})
+    pad.q, pad.weights = wl.q[src], wl.weights[src]
+    pad.context_lens, pad.block_table = wl.context_lens[src], wl.block_table[src]
+    pad.indices = None
+    a = run_path(wl)
+    b = run_path(pad, use_indices=False)
+    valid = (slot_row >= 0).nonzero().flatten()
+    la = a["logits"][slot_row[valid]]
+    lb = b["logits"][valid]
+    check_logits(wl, a["logits"])
+    check_logits(pad, b["logits"])
+    fin = torch.isfinite(la)
+    assert torch.equal(fin, torch.isfinite(lb))
+    assert torch.allclose(la[fin], lb[fin], rtol=1e-5, atol=1e-5)
+
+
+def test_padded_page_stride():
+    _full_check(W.build("stride", request_lens=[777, 2048], rows_per_request=[2, 3], topk=100,
+                        page_stride=8704, seed=5))
+
+
+def test_bf16_logits_fp8_keys():
+    _full_check(W.build("bf16", **MIXED, topk=64, logits_dtype=W.LOGITS_BF16, seed=6))
+
+
+def test_zero_length_and_short_rows():
+    wl = W.build("short", request_lens=[0, 5, 64, 0], rows_per_request=[1, 1, 1, 1], topk=16,
+                 seed=7)
+    out = run_path(wl)
+    assert int(out["status"].item()) == 0
+    check_logits(wl, out["logits"])
+    idx = out["idx"].cpu()
+    assert torch.equal(idx[0], torch.full((16,), -1, dtype=torch.int32))
+    assert idx[1, :5].tolist() == [0, 1, 2, 3, 4] and torch.all(idx[1, 5:] == -1)
+    check_topk_exact(out["logits"], out["idx"], wl.context_lens, 16)
+
+
+def test_empty_batch():
+    dev = torch.device("cuda")
+    ctx = torch.zeros(0, dtype=torch.int32, device=dev)
+    sched = dsa.paged_mqa_logits_metadata(ctx, None, 8)
+    assert sched.cpu()[:8].tolist() == [0x44534131, 0, 0, 8, 0, 0, 128, 8]
+    lg = torch.empty((0, 64), device=dev)
+    out = dsa.top_k_per_row(lg, None, ctx, 8)
+    assert out.shape == (0, 8)
+
+
+# ---------------------------------------------------------------- device faults (reported, never hang)
+
+def test_bad_block_id_reported():
+    wl = W.build("bad", request_lens=[300], rows_per_request=[1], topk=8, seed=8)
+    wl.block_table[0, 2] = wl.num_pages + 5
+    out = run_path(wl)
+    assert int(out["status"].item()) == dsa.DSA_ERR_BAD_BLOCK
+
+
+def test_schedule_mode_mismatch_reported():
+    """A varlen schedule used by a plain call: the kpool fault class, caught."""
+    wl = W.build("mm", request_lens=[300, 200], rows_per_request=[2, 1], topk=8, seed=9).to("cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    S = dsa.device_num_sms()
+    sched = dsa.paged_mqa_logits_metadata(wl.context_lens, wl.indices, S)
+    dsa.fp8_fp4_paged_mqa_logits(wl.q, wl.kv_cache, wl.weights, wl.context_lens, wl.block_table,
+                                 sched, indices=None, logits_stride=wl.logits_stride, num_sms=S,
+                                 status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == dsa.DSA_ERR_SCHEDULE_MISMATCH
+    st.zero_()
+    dsa.fp8_fp4_paged_mqa_logits(wl.q, wl.kv_cache, wl.weights, wl.context_lens, wl.block_table,
+                                 sched, indices=wl.indices, logits_stride=wl.logits_stride,
+                                 num_sms=S - 1, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == dsa.DSA_ERR_SCHEDULE_MISMATCH
+
+
+# ---------------------------------------------------------------- top-k on its own
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_topk_standalone(dtype):
+    g = torch.Generator().manual_seed(11)
+    R, C = 12, 40000
+    x = torch.randn((R, C), generator=g)
+    x[1] = torch.round(x[1] * 2)           # heavy ties
+    x[2, 5000:] = float("-inf")
+    x[3, ::9] = float("nan")
+    x[4] = 0.0
+    x[4, ::2] = -0.0
+    x[5, :] = torch.arange(C, dtype=torch.float32)   # strictly increasing
+    x = x.to(dtype).cuda()
+    ends = torch.tensor([C, C, C, C, C, C, 1, 0, 2047, 2049, 30001, 17], dtype=torch.int32)
+    starts = torch.tensor([0, 3, 0, 7, 0, 1000, 0, 0, 0, 0, 5, 0], dtype=torch.int32)
+    for k in (1, 7, 256, 2048):
+        got = dsa.top_k_per_row(x, starts.cuda(), ends.cuda(), k).cpu().numpy()
+        ref = oracle.top_k_per_row(x.float().cpu().double().numpy(), ends, k, row_starts=starts)
+        assert np.array_equal(got, ref), k
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled
+
+@pytest.mark.parametrize("name", ["plain", "mtp", "varlen"])
+def test_full_size_sampled(name):
+    wl = W.config(name, device="cuda")
+    out = run_path(wl)
+    assert int(out["status"].item()) == 0, dsa.status_string(int(out["status"].item()))
+    host = wl.to("cpu")
+    rows = sample_rows(wl.num_rows, 4, seed=len(name))
+    ref, bound, _ = check_logits(host, out["logits"], rows=rows)
+    check_topk_exact(out["logits"], out["idx"], host.context_lens, wl.topk)
+    check_topk_tie_band(out["idx"], ref, bound, host.context_lens, wl.topk, rows)

@@ -306,8 +306,8 @@ def _uniform_ints(gen, lo, hi, n):
     return [int(v) for v in torch.randint(lo, hi + 1, (n,), generator=gen)]
 
 
-def config(name: str, device="cpu", **overrides) -> Workload:
-    """Named decode workloads.
+def config_spec(name: str) -> dict:
+    """Keyword arguments of build() for a named decode workload.
 
     tiny        B=2, L=[300, 517], one row each, k=256, seed 0
     plain       B=64, L ~ U{4096..32768}, one row each (indices=arange), k=2048, seed 1
@@ -317,16 +317,16 @@ def config(name: str, device="cpu", **overrides) -> Workload:
     """
     g = torch.Generator()
     if name == "tiny":
-        kw = dict(request_lens=[300, 517], rows_per_request=[1, 1], topk=256, seed=0)
-    elif name == "plain":
+        return dict(request_lens=[300, 517], rows_per_request=[1, 1], topk=256, seed=0)
+    if name == "plain":
         g.manual_seed(1)
-        kw = dict(request_lens=_uniform_ints(g, 4096, 32768, 64), rows_per_request=[1] * 64,
-                  topk=2048, seed=1)
-    elif name == "mtp":
+        return dict(request_lens=_uniform_ints(g, 4096, 32768, 64), rows_per_request=[1] * 64,
+                    topk=2048, seed=1)
+    if name == "mtp":
         g.manual_seed(2)
-        kw = dict(request_lens=_uniform_ints(g, 8192, 65536, 128), rows_per_request=[2] * 128,
-                  topk=2048, seed=2)
-    elif name in ("varlen", "fp4_varlen"):
+        return dict(request_lens=_uniform_ints(g, 8192, 65536, 128),
+                    rows_per_request=[2] * 128, topk=2048, seed=2)
+    if name in ("varlen", "fp4_varlen"):
         seed = 3 if name == "varlen" else 4
         g.manual_seed(seed)
         lens = [120000 + d for d in _uniform_ints(g, -2048, 2048, 40)]
@@ -334,10 +334,27 @@ def config(name: str, device="cpu", **overrides) -> Workload:
         kw = dict(request_lens=lens, rows_per_request=rows, topk=2048, seed=seed)
         if name == "fp4_varlen":
             kw.update(kv_format=KV_FP4, logits_dtype=LOGITS_BF16)
-    else:
-        raise ValueError(f"unknown workload {name!r}")
+        return kw
+    raise ValueError(f"unknown workload {name!r}")
+
+
+def config(name: str, device="cpu", **overrides) -> Workload:
+    """Build a named decode workload (see config_spec)."""
+    kw = config_spec(name)
     kw.update(overrides)
     return build(name, device=device, **kw)
+
+
+def config_rows(name: str, plain_indices: bool = False):
+    """(context_lens, indices) of a named workload, without building its key pool."""
+    kw = config_spec(name)
+    ctx, ids = [], []
+    for r, (L, n) in enumerate(zip(kw["request_lens"], kw["rows_per_request"])):
+        for j in range(n):
+            ctx.append(L - n + 1 + j)
+            ids.append(r)
+    ctx = torch.tensor(ctx, dtype=torch.int32)
+    return ctx, (None if plain_indices else torch.tensor(ids, dtype=torch.int32))
 
 
 CONFIG_NAMES = ("tiny", "plain", "mtp", "varlen", "fp4_varlen")
