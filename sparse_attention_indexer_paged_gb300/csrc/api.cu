@@ -143,7 +143,8 @@ int dsa_fp8_fp4_paged_mqa_logits(const void* q, const void* kv_cache, int64_t pa
   const int64_t page_bytes = kv_format == DSA_KV_FP8 ? DSA_FP8_PAGE_BYTES : DSA_FP4_PAGE_BYTES;
   if (page_stride_bytes < page_bytes || page_stride_bytes % 16 != 0) return DSA_ERR_INVALID_ARG;
   if (num_pages < 1 || num_pages > INT32_MAX) return DSA_ERR_INVALID_ARG;
-  if (block_table_stride < 1 || logits_stride < 1 || logits_stride % 8 != 0) return DSA_ERR_INVALID_ARG;
+  if (block_table_stride < 1 || logits_stride < 1 || logits_stride % 8 != 0 || logits_stride >= INT32_MAX)
+    return DSA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(num_rows) * kHeads >= (static_cast<int64_t>(1) << 31))
     return DSA_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(weights, 16) || !aligned(logits, 16))

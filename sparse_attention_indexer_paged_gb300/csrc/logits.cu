@@ -10,25 +10,34 @@
 // keys (two 64-token pages).  Every K tile is read from HBM once per group
 // and serves all of the group's rows and heads.
 //
-// The contraction is laid out with the keys as M: for each tile and each
-// row r of the group, D[token, h] = sum_d K[token, d] * Q[r, h, d] is one
-// 128 x 64 block of a tcgen05 MMA (A = the K tile, B = the group's Q rows,
-// N = 64 per row, up to 4 rows per instruction).  TMEM lane = token, so the
-// head-weighted ReLU reduction of a (token, row) runs inside one thread with
-// no cross-lane traffic, and a warp's 32 logits are 32 consecutive columns.
+// The contraction is laid out with the keys as M: for a tile and one row r
+// of the group, D[token, h] = sum_d K[token, d] * Q[r, h, d] is a 128 x 64
+// tcgen05 MMA (A = the K tile, B = Q row r, K = 128 in four steps).  TMEM
+// lane = token, so the head-weighted ReLU reduction of a (tile, row) pair
+// runs inside one thread with no cross-lane traffic, and a warp's 32 logits
+// are 32 consecutive columns.
 //
-// Warp roles (384 threads):
-//   warp 0      TMA producer: the group's Q rows and weights, then the K
-//               pages (3-D tensor map over the pool, page id from the block
-//               table) and their scales, into a kStages-deep ring.
-//   warp 1      MMA issuer and TMEM owner (512 columns = 8 slots of 64).
-//   warps 2-3   idle (FP8) / key dequantisation (FP4).
-//   warps 4-11  two epilogue warpgroups: tcgen05.ld of a (tile, row) slot,
-//               relu, packed-fp32 FMA with the head weights, key scale,
-//               causal mask, store.  Warpgroup g drains the TMEM slots of
-//               parity g, so every slot barrier has a single consumer that
-//               sees each of its phases in order (a parity wait cannot then
-//               pass on a phase that belongs to another consumer).
+// The CTA's (tile, row) pairs form one stream.  TMEM holds two buffers of
+// four pairs (2 x 256 columns); the MMA issuer fills one buffer while the
+// epilogue drains the other, with one full/empty handshake per buffer.
+// Epilogue warpgroup w takes pair w of every buffer, so every warp waits on
+// every phase of the buffer barriers in order.
+//
+// Rings: K values (kStages tiles, released by the MMA commit) and key scales
+// (kScaleStages tiles, released by the epilogue, loaded by their own warp)
+// are separate, so the HBM prefetch depth does not depend on how far behind
+// the epilogue runs.
+//
+// Warp roles (640 threads):
+//   warp 0      TMA producer: the group's Q rows, then per tile the K pages
+//               (3-D tensor map over the pool, page id from the block table).
+//   warp 1      MMA issuer and TMEM owner (512 columns).
+//   warp 2      head weights and causal limits of each group (double buffered).
+//   warp 3      key scales, up to kScaleStages tiles ahead.
+//   warps 4-19  four epilogue warpgroups: tcgen05.ld of a pair, relu,
+//               packed-fp32 FMA with the head weights, key scale, causal
+//               mask, store.  Each warpgroup's first warp waits on the
+//               mbarriers; the other three meet it at a named barrier.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -36,32 +45,39 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kStages = 6;
+constexpr int kThreads = 640;
+constexpr int kEpiWarpgroups = 4;  // warps 4..19
+constexpr int kEpiWarps = 4 * kEpiWarpgroups;
+constexpr int kStages = 8;         // K value ring, one 128-token tile per stage
+constexpr int kScaleStages = 16;   // key scale ring
 constexpr int kTmemCols = 512;
-constexpr int kSlots = 8;
-constexpr int kSlotCols = 64;
-constexpr int kMaxRowsPerMma = 4;  // N = 256
+constexpr int kBufPairs = 4;       // (tile, row) pairs per TMEM buffer
+constexpr int kPairCols = 64;      // 64 heads of one pair
+constexpr int kBufCols = kBufPairs * kPairCols;
+constexpr int kWBufFloats = kGroupMaxRows * kHeads;       // 512
 
 constexpr int kPageValBytesFp8 = kPageTokens * kHeadDim;  // 8192
 constexpr int kKvStageBytes = 2 * kPageValBytesFp8;       // 16384: one 128 x 128 e4m3 tile
 constexpr int kQRowBytes = kHeads * kHeadDim;             // 8192: 64 heads x 128 e4m3
 constexpr int kScaleStageFloats = kTileTokens;            // 128 key scales per tile
-constexpr int kWBufFloats = kGroupMaxRows * kHeads;       // 512
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffKv = 0;
 constexpr int kOffQ = kOffKv + kStages * kKvStageBytes;
 constexpr int kOffScale = kOffQ + kGroupMaxRows * kQRowBytes;
-constexpr int kOffW = kOffScale + kStages * kScaleStageFloats * 4;
-constexpr int kOffBar = kOffW + 2 * kWBufFloats * 4;
-// barriers: kv_full[S], kv_empty[S], q_full, q_empty, w_full[2], w_empty[2],
-// tmem_full[8], tmem_empty[8], mma_done
-constexpr int kNumBars = 2 * kStages + 2 + 4 + 2 * kSlots + 1;
+constexpr int kOffW = kOffScale + kScaleStages * kScaleStageFloats * 4;
+constexpr int kOffCtx = kOffW + 2 * kWBufFloats * 4;  // causal limits of the group's rows
+constexpr int kOffDec = kOffCtx + 2 * kGroupMaxRows * 4;  // per-warpgroup wait verdicts
+constexpr int kOffBar = kOffDec + 2 * kEpiWarpgroups * 4;
+// barriers: kv_full[S], kv_empty[S], sc_full[SS], sc_empty[SS], q_full,
+// q_empty, w_full[2], w_empty[2], tm_full[2], tm_empty[2], mma_done
+constexpr int kNumBars = 2 * kStages + 2 * kScaleStages + 2 + 4 + 4 + 1;
 constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemAddr + 4;
 constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
 static_assert(kOffQ % 1024 == 0 && kOffKv % 1024 == 0, "MMA tiles need 1024-byte alignment");
+static_assert((kStages & (kStages - 1)) == 0 && (kBufPairs & (kBufPairs - 1)) == 0, "powers of two");
+static_assert(kOffBar % 8 == 0 && kOffW % 16 == 0, "alignment");
 static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
 
 struct Params {
@@ -83,13 +99,16 @@ struct Params {
 };
 
 struct Bars {
-  uint32_t kv_full, kv_empty, q_full, q_empty, w_full, w_empty, tmem_full, tmem_empty, mma_done;
+  uint32_t kv_full, kv_empty, sc_full, sc_empty, q_full, q_empty, w_full, w_empty, tm_full,
+      tm_empty, mma_done;
   __device__ uint32_t kvf(int s) const { return kv_full + 8 * s; }
   __device__ uint32_t kve(int s) const { return kv_empty + 8 * s; }
+  __device__ uint32_t scf(int s) const { return sc_full + 8 * s; }
+  __device__ uint32_t sce(int s) const { return sc_empty + 8 * s; }
   __device__ uint32_t wf(int b) const { return w_full + 8 * b; }
   __device__ uint32_t we(int b) const { return w_empty + 8 * b; }
-  __device__ uint32_t tf(int s) const { return tmem_full + 8 * s; }
-  __device__ uint32_t te(int s) const { return tmem_empty + 8 * s; }
+  __device__ uint32_t tf(int b) const { return tm_full + 8 * b; }
+  __device__ uint32_t te(int b) const { return tm_empty + 8 * b; }
 };
 
 // The CTA's walk over its units: groups in order, and the tiles [j0, j1) of
@@ -138,19 +157,29 @@ struct Walk {
   }
 };
 
-// Warp-uniform wait: lane 0 waits (bounded), the verdict is broadcast, and
-// every lane then observes the completed phase itself (it cannot move on
-// before this warp arrives on the matching "empty" barrier).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag,
-                                          int32_t* status) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, abort_flag, status) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) {
-    for (int i = 0; i < (1 << 20) && !mbar_try_wait(bar, parity); ++i) {
-    }
+// Warpgroup-wide wait: the leader lane waits on the mbarrier(s) (its
+// acquire makes the completed phase's data visible), then the warpgroup's
+// four warps meet at a hardware named barrier, which orders memory among
+// them and costs no issue slots while waiting.  The leader publishes its
+// verdict in decision[n & 1] before the barrier (n counts this warpgroup's
+// waits), so all four warps take the same branch: no warp can be left alone
+// at a named barrier, which has no timeout.  Up to three barriers are waited
+// in order (a zero address is skipped).  Returns false on timeout or abort.
+__device__ __forceinline__ bool wg_wait(uint32_t bar0, uint32_t par0, uint32_t bar1, uint32_t par1,
+                                        uint32_t bar2, uint32_t par2, bool leader,
+                                        uint32_t named_id, volatile int32_t* decision, int& n,
+                                        volatile int32_t* abort_flag, int32_t* status) {
+  const int slot = n & 1;
+  ++n;
+  if (leader) {
+    bool ok = true;
+    if (ok && bar0) ok = wait_or_abort(bar0, par0, abort_flag, status);
+    if (ok && bar1) ok = wait_or_abort(bar1, par1, abort_flag, status);
+    if (ok && bar2) ok = wait_or_abort(bar2, par2, abort_flag, status);
+    decision[slot] = ok ? 1 : 0;
   }
-  return ok != 0;
+  named_bar_sync(named_id, 128);
+  return decision[slot] != 0;
 }
 
 __device__ __forceinline__ float relu_f(uint32_t bits) { return fmaxf(__uint_as_float(bits), 0.0f); }
@@ -186,33 +215,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (u0 >= u1 || G == 0) return;  // no work: the whole CTA leaves before any set-up
 
   Bars bars;
-  const uint32_t bar0 = sbase + kOffBar;
-  bars.kv_full = bar0;
+  bars.kv_full = sbase + kOffBar;
   bars.kv_empty = bars.kv_full + 8 * kStages;
-  bars.q_full = bars.kv_empty + 8 * kStages;
+  bars.sc_full = bars.kv_empty + 8 * kStages;
+  bars.sc_empty = bars.sc_full + 8 * kScaleStages;
+  bars.q_full = bars.sc_empty + 8 * kScaleStages;
   bars.q_empty = bars.q_full + 8;
   bars.w_full = bars.q_empty + 8;
   bars.w_empty = bars.w_full + 16;
-  bars.tmem_full = bars.w_empty + 16;
-  bars.tmem_empty = bars.tmem_full + 8 * kSlots;
-  bars.mma_done = bars.tmem_empty + 8 * kSlots;
+  bars.tm_full = bars.w_empty + 16;
+  bars.tm_empty = bars.tm_full + 16;
+  bars.mma_done = bars.tm_empty + 16;
   uint32_t* tmem_addr_smem = reinterpret_cast<uint32_t*>(smem + kOffTmemAddr);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kOffAbort);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bars.kvf(s), 1);
-      mbar_init(bars.kve(s), 1 + 8);  // MMA commit + every epilogue warp (key scales read)
+      mbar_init(bars.kve(s), 1);  // the MMA commit of the tile
+    }
+    for (int s = 0; s < kScaleStages; ++s) {
+      mbar_init(bars.scf(s), 1);
+      mbar_init(bars.sce(s), kEpiWarps);  // every epilogue warp has read the tile's scales
     }
     mbar_init(bars.q_full, 1);
     mbar_init(bars.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.wf(b), 1);
-      mbar_init(bars.we(b), 8);  // every epilogue warp
-    }
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(bars.tf(s), 1);
-      mbar_init(bars.te(s), 4);
+      mbar_init(bars.we(b), kEpiWarps);
+      mbar_init(bars.tf(b), 1);
+      mbar_init(bars.te(b), kEpiWarps);
     }
     mbar_init(bars.mma_done, 1);
     *abort_flag = 0;
@@ -233,105 +265,188 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_w = sbase + kOffW;
   const float* scale_sm = reinterpret_cast<const float*>(smem + kOffScale);
   const float* w_sm = reinterpret_cast<const float*>(smem + kOffW);
+  int32_t* ctx_sm = reinterpret_cast<int32_t*>(smem + kOffCtx);
 
   Walk walk;
   walk.start(grs, gus, p.ctx, G, T, u0, u1);
 
   if (warp == 0) {
-    // =================================================== TMA producer
+    // =================================================== TMA producer (K values, Q)
+    // The whole warp walks the work: block ids are fetched 32 at a time with
+    // one coalesced load and handed out by shuffle; lane 0 waits and issues.
     if (lane == 0) {
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_kv);
-      const uint64_t pol_stream = policy_evict_first();  // K pages are read once
-      const uint64_t pol_keep = policy_evict_last();      // q and weights
-      int it = 0, nq = 0, nw = 0;  // K tiles, Q groups and weight groups issued
+    }
+    const uint64_t pol_stream = policy_evict_first();  // K pages are read once
+    const uint64_t pol_keep = policy_evict_last();      // q
+    int it = 0, nq = 0;  // tiles and Q groups issued
+    bool ok = true;
+    while (ok && walk.next()) {
+      const int r0 = walk.r0, n = walk.n;
+      if (lane == 0) {
+        ok = wait_or_abort(bars.q_empty, (nq & 1) ^ 1, abort_flag, p.status);
+        if (ok) {
+          mbar_arrive_expect_tx(bars.q_full, static_cast<uint32_t>(n * kQRowBytes));
+          for (int r = 0; r < n; ++r)
+            tma_load_2d(s_q + r * kQRowBytes, &tm_q, 0, (r0 + r) * kHeads, bars.q_full, pol_keep);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      ++nq;
+      const int32_t* bt_row = p.block_table + static_cast<int64_t>(r0 + n - 1) * p.bt_stride;
+      int32_t lane_blk = -1;  // block id of page (pg_base + lane)
+      int pg_base = -32;
+      for (int j = walk.j0; j < walk.j1; ++j, ++it) {
+        if (2 * j >= pg_base + 32) {
+          pg_base = 2 * j;
+          const int pg = pg_base + lane;
+          lane_blk = -1;
+          if (pg < walk.npages) {
+            int32_t b = (pg < p.bt_stride) ? __ldg(bt_row + pg) : -1;
+            if (b < 0 || b >= p.num_pages) {
+              report(p.status, kErrBadBlock);
+              b = 0;
+            }
+            lane_blk = b;
+          }
+        }
+        const int32_t blk0 = __shfl_sync(0xffffffffu, lane_blk, 2 * j - pg_base);
+        const int32_t blk1 = __shfl_sync(0xffffffffu, lane_blk, 2 * j + 1 - pg_base);
+        if (lane == 0) {
+          const int st = it % kStages;
+          ok = wait_or_abort(bars.kve(st), ((it / kStages) & 1) ^ 1, abort_flag, p.status);
+          if (ok) {
+            const int npg = (blk0 >= 0 ? 1 : 0) + (blk1 >= 0 ? 1 : 0);
+            mbar_arrive_expect_tx(bars.kvf(st), static_cast<uint32_t>(npg * kPageValBytesFp8));
+            if (blk0 >= 0)
+              tma_load_3d(s_kv + st * kKvStageBytes, &tm_kv, 0, 0, blk0, bars.kvf(st), pol_stream);
+            if (blk1 >= 0)
+              tma_load_3d(s_kv + st * kKvStageBytes + kPageValBytesFp8, &tm_kv, 0, 0, blk1,
+                          bars.kvf(st), pol_stream);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+    }
+    // Drain: every copy this CTA issued has landed before it may exit (a
+    // phase that already completed returns at once).
+    if (lane == 0) {
+      for (int i = max(0, it - kStages); i < it; ++i) wait_drain(bars.kvf(i % kStages), (i / kStages) & 1);
+      if (nq > 0) wait_drain(bars.q_full, (nq - 1) & 1);
+    }
+  } else if (warp == 3) {
+    // =================================================== key scales
+    // Runs ahead of the K pipeline by up to kScaleStages tiles, gated only
+    // by the epilogue.  Block ids come 32 at a time as in the K producer.
+    const uint64_t pol_stream = policy_evict_first();
+    int it = 0;
+    bool ok = true;
+    while (ok && walk.next()) {
+      const int32_t* bt_row = p.block_table + static_cast<int64_t>(walk.r0 + walk.n - 1) * p.bt_stride;
+      int32_t lane_blk = -1;
+      int pg_base = -32;
+      for (int j = walk.j0; j < walk.j1; ++j, ++it) {
+        if (2 * j >= pg_base + 32) {
+          pg_base = 2 * j;
+          const int pg = pg_base + lane;
+          lane_blk = -1;
+          if (pg < walk.npages) {
+            int32_t b = (pg < p.bt_stride) ? __ldg(bt_row + pg) : -1;
+            lane_blk = (b < 0 || b >= p.num_pages) ? 0 : b;  // reported by the K producer
+          }
+        }
+        const int32_t blk0 = __shfl_sync(0xffffffffu, lane_blk, 2 * j - pg_base);
+        const int32_t blk1 = __shfl_sync(0xffffffffu, lane_blk, 2 * j + 1 - pg_base);
+        if (lane == 0) {
+          const int ss = it % kScaleStages;
+          ok = wait_or_abort(bars.sce(ss), ((it / kScaleStages) & 1) ^ 1, abort_flag, p.status);
+          if (ok) {
+            const int npg = (blk0 >= 0 ? 1 : 0) + (blk1 >= 0 ? 1 : 0);
+            mbar_arrive_expect_tx(bars.scf(ss), static_cast<uint32_t>(npg * kPageTokens * 4));
+            if (blk0 >= 0)
+              bulk_load(s_scale + ss * kScaleStageFloats * 4,
+                        p.kv_cache + static_cast<int64_t>(blk0) * p.page_stride + kPageValBytesFp8,
+                        kPageTokens * 4, bars.scf(ss), pol_stream);
+            if (blk1 >= 0)
+              bulk_load(s_scale + (ss * kScaleStageFloats + kPageTokens) * 4,
+                        p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride + kPageValBytesFp8,
+                        kPageTokens * 4, bars.scf(ss), pol_stream);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+    }
+    if (lane == 0)
+      for (int i = max(0, it - kScaleStages); i < it; ++i)
+        wait_drain(bars.scf(i % kScaleStages), (i / kScaleStages) & 1);
+  } else if (warp == 2) {
+    // =================================================== weights + causal limits
+    // A separate producer: the epilogue may hold a group's weights until TMEM
+    // buffers that also carry later groups' pairs complete, so these loads
+    // must never sit in front of the K and Q loads.
+    if (lane == 0) {
+      const uint64_t pol_keep = policy_evict_last();
+      int nw = 0;
       bool ok = true;
       while (ok && walk.next()) {
         const int r0 = walk.r0, n = walk.n;
-        ok = wait_or_abort(bars.q_empty, (nq & 1) ^ 1, abort_flag, p.status);
-        if (!ok) break;
-        mbar_arrive_expect_tx(bars.q_full, static_cast<uint32_t>(n * kQRowBytes));
-        for (int r = 0; r < n; ++r)
-          tma_load_2d(s_q + r * kQRowBytes, &tm_q, 0, (r0 + r) * kHeads, bars.q_full, pol_keep);
-        ++nq;
         const int wb = nw & 1;
         ok = wait_or_abort(bars.we(wb), ((nw >> 1) & 1) ^ 1, abort_flag, p.status);
         if (!ok) break;
+        for (int r = 0; r < n; ++r) ctx_sm[wb * kGroupMaxRows + r] = p.ctx[r0 + r];
         mbar_arrive_expect_tx(bars.wf(wb), static_cast<uint32_t>(n * kHeads * 4));
         bulk_load(s_w + wb * kWBufFloats * 4, p.weights + static_cast<int64_t>(r0) * kHeads,
                   n * kHeads * 4, bars.wf(wb), pol_keep);
         ++nw;
-        const int32_t* bt_row = p.block_table + static_cast<int64_t>(r0 + n - 1) * p.bt_stride;
-        for (int j = walk.j0; j < walk.j1; ++j, ++it) {
-          const int st = it % kStages;
-          ok = wait_or_abort(bars.kve(st), ((it / kStages) & 1) ^ 1, abort_flag, p.status);
-          if (!ok) break;
-          int32_t blk[2];
-          uint32_t bytes = 0;
-          for (int h = 0; h < 2; ++h) {
-            const int pg = 2 * j + h;
-            blk[h] = -1;
-            if (pg < walk.npages) {
-              int32_t b = (pg < p.bt_stride) ? bt_row[pg] : -1;
-              if (b < 0 || b >= p.num_pages) {
-                report(p.status, kErrBadBlock);
-                b = 0;
-              }
-              blk[h] = b;
-              bytes += kPageValBytesFp8 + kPageTokens * 4;
-            }
-          }
-          mbar_arrive_expect_tx(bars.kvf(st), bytes);
-          for (int h = 0; h < 2; ++h) {
-            if (blk[h] < 0) continue;
-            tma_load_3d(s_kv + st * kKvStageBytes + h * kPageValBytesFp8, &tm_kv, 0, 0, blk[h],
-                        bars.kvf(st), pol_stream);
-            bulk_load(s_scale + (st * kScaleStageFloats + h * kPageTokens) * 4,
-                      p.kv_cache + static_cast<int64_t>(blk[h]) * p.page_stride + kPageValBytesFp8,
-                      kPageTokens * 4, bars.kvf(st), pol_stream);
-          }
-        }
       }
-      // Drain: every copy this CTA issued has landed before it may exit (a
-      // phase that already completed returns at once).
-      for (int i = max(0, it - kStages); i < it; ++i) wait_drain(bars.kvf(i % kStages), (i / kStages) & 1);
-      if (nq > 0) wait_drain(bars.q_full, (nq - 1) & 1);
       if (nw > 0) wait_drain(bars.wf((nw - 1) & 1), ((nw - 1) >> 1) & 1);
     }
   } else if (warp == 1) {
     // =================================================== MMA issuer
     if (lane == 0) {
-      int it = 0, gi = 0, sc = 0;
+      // idesc for N = 64, 128, 192, 256 (1..4 pairs of one tile)
+      const uint32_t id1 = idesc(kFmtE4M3, kFmtE4M3, 128, 64), id2 = idesc(kFmtE4M3, kFmtE4M3, 128, 128);
+      const uint32_t id3 = idesc(kFmtE4M3, kFmtE4M3, 128, 192), id4 = idesc(kFmtE4M3, kFmtE4M3, 128, 256);
+      const uint32_t a_lo0 = sdesc_lo(s_kv), q_lo0 = sdesc_lo(s_q);
+      constexpr uint32_t kStageLo = kKvStageBytes >> 4, kRowLo = kQRowBytes >> 4;
+      uint32_t it = 0, gi = 0, pos = 0;  // tiles, groups, pairs issued
       bool ok = true;
       while (ok && walk.next()) {
         const int n = walk.n;
         ok = wait_or_abort(bars.q_full, gi & 1, abort_flag, p.status);
         if (!ok) break;
-        for (int j = walk.j0; j < walk.j1 && ok; ++j, ++it) {
-          const int st = it % kStages;
+        for (int j = walk.j0; j < walk.j1; ++j, ++it) {
+          const uint32_t st = it & (kStages - 1);
           ok = wait_or_abort(bars.kvf(st), (it / kStages) & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t a_tile = s_kv + st * kKvStageBytes;
+          const uint32_t a_lo = a_lo0 + st * kStageLo;
           int r = 0;
           while (r < n) {
-            const int c = sc % kSlots;
-            const int len = min(min(n - r, kMaxRowsPerMma), kSlots - c);
-            for (int i = 0; i < len && ok; ++i)
-              ok = wait_or_abort(bars.te(c + i), (((sc + i) / kSlots) & 1) ^ 1, abort_flag, p.status);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t d_tmem = tmem + static_cast<uint32_t>(c * kSlotCols);
-            const uint32_t id = idesc(kFmtE4M3, kFmtE4M3, 128, static_cast<uint32_t>(kSlotCols * len));
-#pragma unroll
-            for (int kk = 0; kk < kHeadDim / 32; ++kk) {
-              const uint64_t ad = sdesc_k_sw128(a_tile + kk * 32);
-              const uint64_t bd = sdesc_k_sw128(s_q + r * kQRowBytes + kk * 32);
-              mma_f8f6f4(d_tmem, ad, bd, id, kk > 0 ? 1u : 0u);
+            const uint32_t c = pos & (kBufPairs - 1);
+            const uint32_t k = pos / kBufPairs;
+            const uint32_t b = k & 1;
+            if (c == 0) {
+              ok = wait_or_abort(bars.te(b), ((k >> 1) & 1) ^ 1, abort_flag, p.status);
+              if (!ok) break;
+              tc_fence_after();
             }
-            for (int i = 0; i < len; ++i) mma_commit(bars.tf(c + i));
+            const int len = min(n - r, static_cast<int>(kBufPairs - c));
+            const uint32_t d_tmem = tmem + b * kBufCols + c * kPairCols;
+            const uint32_t id = len == 1 ? id1 : (len == 2 ? id2 : (len == 3 ? id3 : id4));
+            const uint32_t b_lo = q_lo0 + static_cast<uint32_t>(r) * kRowLo;
+            // K = 128 in four steps of 32 bytes inside the swizzled row (+2 in the address field)
+            mma_f8f6f4_w<false>(d_tmem, a_lo, kSdescHi, b_lo, kSdescHi, id);
+            mma_f8f6f4_w<true>(d_tmem, a_lo + 2, kSdescHi, b_lo + 2, kSdescHi, id);
+            mma_f8f6f4_w<true>(d_tmem, a_lo + 4, kSdescHi, b_lo + 4, kSdescHi, id);
+            mma_f8f6f4_w<true>(d_tmem, a_lo + 6, kSdescHi, b_lo + 6, kSdescHi, id);
             r += len;
-            sc += len;
+            pos += len;
+            if ((pos & (kBufPairs - 1)) == 0) mma_commit(bars.tf(b));
           }
           if (!ok) break;
           mma_commit(bars.kve(st));
@@ -340,63 +455,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bars.q_empty);
         ++gi;
       }
+      if (ok && (pos & (kBufPairs - 1)) != 0) mma_commit(bars.tf((pos / kBufPairs) & 1));  // last, partial buffer
       // No MMA may still be writing TMEM when it is freed.
       mma_commit(bars.mma_done);
       wait_drain(bars.mma_done, 0);
     }
   } else if (warp >= 4) {
     // =================================================== epilogue
-    const int wg = (warp - 4) >> 2;  // warpgroup 0 drains even TMEM slots, 1 odd slots
+    const int wg = (warp - 4) >> 2;  // takes pair wg of every TMEM buffer
     const int quarter = warp & 3;    // TMEM lanes this warp may read
     const int tok = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const bool leader = ((warp - 4) & 3) == 0 && lane == 0;
+    const uint32_t named_id = 1 + wg;  // named barrier of this warpgroup
+    volatile int32_t* decision = reinterpret_cast<volatile int32_t*>(smem + kOffDec) + 2 * wg;
+    int nwait = 0;
     float* out_f = static_cast<float*>(p.logits);
     __nv_bfloat16* out_h = static_cast<__nv_bfloat16*>(p.logits);
-    int it = 0, gi = 0, sc = 0;
+    int it = 0, gi = 0, pos = 0;
     bool ok = true;
     while (ok && walk.next()) {
       const int r0 = walk.r0, n = walk.n;
       const int wb = gi & 1;
-      ok = warp_wait(bars.wf(wb), (gi >> 1) & 1, abort_flag, p.status);
+      ok = wg_wait(bars.wf(wb), (gi >> 1) & 1, 0, 0, 0, 0, leader, named_id, decision, nwait,
+                   abort_flag, p.status);
       if (!ok) break;
-      const int64_t store_lim = min(static_cast<int64_t>(walk.npages) * kPageTokens, p.logits_stride);
-      for (int j = walk.j0; j < walk.j1; ++j, ++it, sc += n) {
-        const int st = it % kStages;
-        ok = warp_wait(bars.kvf(st), (it / kStages) & 1, abort_flag, p.status);
+      const int lim = static_cast<int>(min(static_cast<int64_t>(walk.npages) * kPageTokens, p.logits_stride));
+      for (int j = walk.j0; j < walk.j1; ++j, ++it) {
+        const int ss = it % kScaleStages;
+        ok = wg_wait(bars.scf(ss), (it / kScaleStages) & 1, 0, 0, 0, 0, leader, named_id, decision,
+                     nwait, abort_flag, p.status);
         if (!ok) break;
-        const float kscale = scale_sm[st * kScaleStageFloats + tok];
+        const float kscale = scale_sm[ss * kScaleStageFloats + tok];
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars.kve(st));
-        const int64_t s = static_cast<int64_t>(j) * kTileTokens + tok;
-        for (int r = 0; r < n; ++r) {
-          const int slot_abs = sc + r;
-          if ((slot_abs & 1) != wg) continue;  // each TMEM slot always drains to one warpgroup
-          const int slot = slot_abs % kSlots;
-          ok = warp_wait(bars.tf(slot), (slot_abs / kSlots) & 1, abort_flag, p.status);
+        if (lane == 0) mbar_arrive(bars.sce(ss));
+        const int scol = j * kTileTokens + tok;
+        for (int r = 0; r < n; ++r, ++pos) {
+          if ((pos % kBufPairs) != wg) continue;
+          const int k = pos / kBufPairs;
+          const int b = k & 1;
+          ok = wg_wait(bars.tf(b), (k >> 1) & 1, 0, 0, 0, 0, leader, named_id, decision, nwait,
+                       abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
           uint32_t v[64];
-          tmem_ld_x64(t_lane + static_cast<uint32_t>(slot * kSlotCols), v);
+          tmem_ld_x64(t_lane + static_cast<uint32_t>(b * kBufCols + wg * kPairCols), v);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bars.te(slot));
-          const float* wr = w_sm + wb * kWBufFloats + r * kHeads;
-          float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f, a2 = 0.f, b2 = 0.f, a3 = 0.f, b3 = 0.f;
+          if (lane == 0) mbar_arrive(bars.te(b));
+          const float4* wr = reinterpret_cast<const float4*>(w_sm + wb * kWBufFloats + r * kHeads);
+          float2 c0 = make_float2(0.f, 0.f), c1 = c0, c2 = c0, c3 = c0;
 #pragma unroll
           for (int h = 0; h < kHeads; h += 8) {
-            const float4 wa = *reinterpret_cast<const float4*>(wr + h);
-            const float4 wc = *reinterpret_cast<const float4*>(wr + h + 4);
-            ffma2(a0, b0, relu_f(v[h + 0]), relu_f(v[h + 1]), wa.x, wa.y);
-            ffma2(a1, b1, relu_f(v[h + 2]), relu_f(v[h + 3]), wa.z, wa.w);
-            ffma2(a2, b2, relu_f(v[h + 4]), relu_f(v[h + 5]), wc.x, wc.y);
-            ffma2(a3, b3, relu_f(v[h + 6]), relu_f(v[h + 7]), wc.z, wc.w);
+            const float4 wa = wr[h / 4];
+            c0 = __ffma2_rn(make_float2(relu_f(v[h + 0]), relu_f(v[h + 1])), make_float2(wa.x, wa.y), c0);
+            c1 = __ffma2_rn(make_float2(relu_f(v[h + 2]), relu_f(v[h + 3])), make_float2(wa.z, wa.w), c1);
+            const float4 wc = wr[h / 4 + 1];
+            c2 = __ffma2_rn(make_float2(relu_f(v[h + 4]), relu_f(v[h + 5])), make_float2(wc.x, wc.y), c2);
+            c3 = __ffma2_rn(make_float2(relu_f(v[h + 6]), relu_f(v[h + 7])), make_float2(wc.z, wc.w), c3);
           }
-          const float acc = ((a0 + b0) + (a1 + b1)) + ((a2 + b2) + (a3 + b3));
-          const int L = p.ctx[r0 + r];
-          const float logit = (s < L) ? kscale * acc : -INFINITY;
-          if (s < store_lim) {
-            const int64_t off = static_cast<int64_t>(r0 + r) * p.logits_stride + s;
+          const float acc = ((c0.x + c0.y) + (c1.x + c1.y)) + ((c2.x + c2.y) + (c3.x + c3.y));
+          const int L = ctx_sm[wb * kGroupMaxRows + r];
+          const float logit = (scol < L) ? kscale * acc : -INFINITY;
+          if (scol < lim) {
+            const int64_t off = static_cast<int64_t>(r0 + r) * p.logits_stride + scol;
             if (p.logits_bf16) out_h[off] = __float2bfloat16_rn(logit);
             else out_f[off] = logit;
           }

@@ -55,23 +55,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete may be
+// suspended (not spinning, so it takes no issue slots) until the phase
+// completes or kSuspendHintNs passes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase of `bar` with the given parity has completed.  Returns
 // false (without waiting further) once the CTA's abort flag is set, or after
 // kWaitTimeoutNs, in which case it records DSA_ERR_TIMEOUT and sets the flag
 // so that every other role of the CTA stops too.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile int32_t* abort_flag, int32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_sleep(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-        *abort_flag = 1;
-        report(status, kErrTimeout);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      *abort_flag = 1;
+      report(status, kErrTimeout);
+      return false;
     }
   }
 }
@@ -80,10 +93,29 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 // are already in flight before the CTA exits.
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity)) {
     if (global_timer_ns() - t0 > kDrainTimeoutNs) return false;
   }
   return true;
+}
+
+// Named barrier over `nthreads` threads (a multiple of 32); hardware wait,
+// no polling, with CTA-scope memory ordering among the participants.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// 16-byte asynchronous global -> shared copy (completes in the background;
+// the issuing thread waits for it with cp_async_wait).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most `n` of this thread's committed copy groups are pending.
+template <int n>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA / bulk copies
@@ -191,6 +223,26 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint
       : "memory");
 }
 
+// As mma_f8f6f4 with each descriptor given as its two 32-bit halves (the
+// pair is assembled inside the asm, so no 64-bit arithmetic is needed), and
+// the accumulate flag fixed at compile time.
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_f8f6f4_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                             uint32_t b_lo, uint32_t b_hi, uint32_t idesc_v) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc_v), "n"(kAccumulate ? 1 : 0)
+      : "memory");
+}
+
+// High and low 32-bit words of sdesc_k_sw128(saddr).
+constexpr uint32_t kSdescHi = (1024 >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr) { return ((saddr >> 4) & 0x3FFFu) | (1u << 16); }
+
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                         uint32_t idesc_v, uint32_t accumulate) {
   asm volatile(
@@ -235,21 +287,6 @@ __device__ __forceinline__ void tmem_ld_x64(uint32_t taddr, uint32_t (&r)[64]) {
 
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// ---------------------------------------------------------------- packed fp32
-
-// acc.{x,y} += x.{0,1} * w.{0,1}, one packed fp32 FMA (round to nearest).
-__device__ __forceinline__ void ffma2(float& ax, float& ay, float x0, float x1, float w0,
-                                      float w1) {
-  asm("{\n\t.reg .b64 a, x, w;\n\t"
-      "mov.b64 a, {%0, %1};\n\t"
-      "mov.b64 x, {%2, %3};\n\t"
-      "mov.b64 w, {%4, %5};\n\t"
-      "fma.rn.f32x2 a, x, w, a;\n\t"
-      "mov.b64 {%0, %1}, a;\n\t}"
-      : "+f"(ax), "+f"(ay)
-      : "f"(x0), "f"(x1), "f"(w0), "f"(w1));
 }
 
 }  // namespace dsa

@@ -4,10 +4,20 @@
 // logits are read as their exact fp32 values).
 //
 // One CTA per row.  Scores map to order-preserving 32-bit keys (NaN lowest,
-// -0 == +0).  Three histogram passes over the row (11, 11 and 10 key bits)
-// find the k-th largest key tau and how many keys equal to tau are kept
-// (the lowest columns among them).  A final ordered pass writes the chosen
-// columns in ascending order with block-wide prefix sums.
+// -0 == +0); the k-th largest key tau and the number of keys equal to tau
+// that are kept (the lowest columns among them) are found by radix select.
+//
+// Fast path (rows up to kFastMaxCols columns whose threshold bin holds at
+// most kCandCap keys), two reads of the row:
+//   pass 1  histogram of the top 11 key bits;
+//   pass 2  columns above the threshold bin set their bit in a shared-memory
+//           bitmap; the threshold bin's (key, column) pairs go to a
+//           shared-memory candidate list;
+//   then    the low 21 bits are resolved on the candidates alone, the kept
+//           candidates set their bits, and one block-wide scan over the
+//           bitmaps writes the chosen columns in ascending order.
+// Other rows take the general path: three histogram passes over the row
+// (11, 11 and 10 key bits) and an ordered compaction pass.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -18,7 +28,20 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
-constexpr int kPerThread = 8;  // elements per thread per chunk of the ordered pass
+constexpr int kPerThread = 8;          // elements per thread per chunk of the ordered pass
+constexpr int kFastMaxCols = 1 << 18;  // columns the two shared-memory bitmaps cover
+constexpr int kBitmapWords = kFastMaxCols / 32;
+constexpr int kCandCap = 16384;        // (key, column) candidates held in shared memory
+constexpr int kLoadsInFlight = 4;      // 16-byte loads per thread per iteration
+
+// dynamic shared memory map
+constexpr int kOffHist = 0;                                   // uint32 [kBins]
+constexpr int kOffSel = kOffHist + kBins * 4;                 // uint32 [kBitmapWords]
+constexpr int kOffTie = kOffSel + kBitmapWords * 4;           // uint32 [kBitmapWords]
+constexpr int kOffCandKey = kOffTie + kBitmapWords * 4;       // uint32 [kCandCap]
+constexpr int kOffCandCol = kOffCandKey + kCandCap * 4;       // int32  [kCandCap]
+constexpr int kSmemBytes = kOffCandCol + kCandCap * 4;
+static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   uint32_t u = __float_as_uint(x);
@@ -38,26 +61,32 @@ __device__ __forceinline__ float load_score<__nv_bfloat16>(const __nv_bfloat16* 
   return __bfloat162float(row[i]);
 }
 
-// Keys of 4 consecutive columns starting at a multiple of 4.
-template <typename LT>
-__device__ __forceinline__ void load4_keys(const LT* row, int64_t i, uint32_t (&k)[4]);
-template <>
-__device__ __forceinline__ void load4_keys<float>(const float* row, int64_t i, uint32_t (&k)[4]) {
-  const float4 v = *reinterpret_cast<const float4*>(row + i);
-  k[0] = order_key(v.x);
-  k[1] = order_key(v.y);
-  k[2] = order_key(v.z);
-  k[3] = order_key(v.w);
-}
-template <>
-__device__ __forceinline__ void load4_keys<__nv_bfloat16>(const __nv_bfloat16* row, int64_t i,
-                                                          uint32_t (&k)[4]) {
-  const uint2 v = *reinterpret_cast<const uint2*>(row + i);
-  k[0] = order_key(__uint_as_float(v.x << 16));
-  k[1] = order_key(__uint_as_float(v.x & 0xffff0000u));
-  k[2] = order_key(__uint_as_float(v.y << 16));
-  k[3] = order_key(__uint_as_float(v.y & 0xffff0000u));
-}
+// Four consecutive scores starting at a multiple of 4, as a raw vector.
+template <typename LT> struct Vec4;
+template <> struct Vec4<float> {
+  using T = float4;
+  __device__ static T load(const float* row, int64_t i) {
+    return __ldg(reinterpret_cast<const float4*>(row + i));
+  }
+  __device__ static void keys(const T& v, uint32_t (&k)[4]) {
+    k[0] = order_key(v.x);
+    k[1] = order_key(v.y);
+    k[2] = order_key(v.z);
+    k[3] = order_key(v.w);
+  }
+};
+template <> struct Vec4<__nv_bfloat16> {
+  using T = uint2;
+  __device__ static T load(const __nv_bfloat16* row, int64_t i) {
+    return __ldg(reinterpret_cast<const uint2*>(row + i));
+  }
+  __device__ static void keys(const T& v, uint32_t (&k)[4]) {
+    k[0] = order_key(__uint_as_float(v.x << 16));
+    k[1] = order_key(__uint_as_float(v.x & 0xffff0000u));
+    k[2] = order_key(__uint_as_float(v.y << 16));
+    k[3] = order_key(__uint_as_float(v.y & 0xffff0000u));
+  }
+};
 
 __device__ __forceinline__ uint32_t warp_incl_sum(uint32_t x) {
   const int lane = threadIdx.x & 31;
@@ -83,14 +112,89 @@ __device__ __forceinline__ uint32_t block_excl_sum(uint32_t v, uint32_t* buf, ui
   return before + inc - v;
 }
 
+// Walk the row [a, b) in 4-column groups with kLoadsInFlight loads per thread
+// in flight; fn(first column, keys[4], valid mask) for every group.
+template <typename LT, typename F>
+__device__ __forceinline__ void for_each_quad(const LT* rp, int64_t a, int64_t b, F&& fn) {
+  const int64_t a4 = a & ~static_cast<int64_t>(3);
+  constexpr int64_t kStep = 4 * static_cast<int64_t>(kThreads) * kLoadsInFlight;
+  for (int64_t base = a4; base < b; base += kStep) {
+    typename Vec4<LT>::T v[kLoadsInFlight];
+#pragma unroll
+    for (int u = 0; u < kLoadsInFlight; ++u) {
+      const int64_t i = base + 4 * (threadIdx.x + static_cast<int64_t>(u) * kThreads);
+      if (i + 3 < b && i >= a) v[u] = Vec4<LT>::load(rp, i);
+    }
+#pragma unroll
+    for (int u = 0; u < kLoadsInFlight; ++u) {
+      const int64_t i = base + 4 * (threadIdx.x + static_cast<int64_t>(u) * kThreads);
+      if (i >= b) continue;
+      uint32_t k[4];
+      uint32_t valid = 0xfu;
+      if (i + 3 < b && i >= a) {
+        Vec4<LT>::keys(v[u], k);
+      } else {
+        valid = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int64_t c = i + e;
+          k[e] = 0;
+          if (c >= a && c < b) {
+            k[e] = order_key(load_score<LT>(rp, c));
+            valid |= 1u << e;
+          }
+        }
+      }
+      fn(i, k, valid);
+    }
+  }
+}
+
+// Finds the bin holding the `remaining`-th largest key among the histogram's
+// nbins bins (thread t owns bins nbins-1-2t and nbins-2-2t).  Returns the bin
+// and, in *above, the number of keys in higher bins.
+__device__ __forceinline__ uint32_t find_bin(const uint32_t* hist, uint32_t nbins,
+                                             uint32_t remaining, uint32_t* scan_buf,
+                                             uint32_t* s_bin, uint32_t* s_above,
+                                             uint32_t* above) {
+  const int tid = threadIdx.x;
+  uint32_t h_hi = 0, h_lo = 0;
+  const int hi = static_cast<int>(nbins) - 1 - 2 * tid;
+  if (hi >= 1) {
+    h_hi = hist[hi];
+    h_lo = hist[hi - 1];
+  }
+  uint32_t tot;
+  const uint32_t ab = block_excl_sum(h_hi + h_lo, scan_buf, &tot);
+  if (hi >= 1) {
+    if (ab < remaining && ab + h_hi >= remaining) {
+      *s_bin = static_cast<uint32_t>(hi);
+      *s_above = ab;
+    } else if (ab + h_hi < remaining && ab + h_hi + h_lo >= remaining) {
+      *s_bin = static_cast<uint32_t>(hi - 1);
+      *s_above = ab + h_hi;
+    }
+  }
+  __syncthreads();
+  const uint32_t bin = *s_bin;
+  *above = *s_above;
+  __syncthreads();
+  return bin;
+}
+
 template <typename LT>
 __global__ void __launch_bounds__(kThreads, 1)
     topk_kernel(const LT* __restrict__ logits, int64_t stride, const int32_t* __restrict__ starts,
                 const int32_t* __restrict__ ends, int32_t k, int32_t* __restrict__ out,
                 int64_t out_stride) {
-  __shared__ uint32_t hist[kBins];
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
+  uint32_t* sel = reinterpret_cast<uint32_t*>(smem + kOffSel);
+  uint32_t* tie = reinterpret_cast<uint32_t*>(smem + kOffTie);
+  uint32_t* cand_key = reinterpret_cast<uint32_t*>(smem + kOffCandKey);
+  int32_t* cand_col = reinterpret_cast<int32_t*>(smem + kOffCandCol);
   __shared__ uint32_t scan_buf[kWarps];
-  __shared__ uint32_t s_bin, s_above;
+  __shared__ uint32_t s_bin, s_above, s_ncand;
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
@@ -105,62 +209,132 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  // ---- radix select of the k-th largest key
-  uint32_t prefix = 0, prefix_mask = 0;
-  uint32_t remaining = static_cast<uint32_t>(k);
-  const int64_t a4 = a & ~static_cast<int64_t>(3);
-#pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const uint32_t nbins = pass == 2 ? 1024u : 2048u;
-    for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    for (int64_t i = a4 + 4 * static_cast<int64_t>(tid); i < b; i += 4 * kThreads) {
-      uint32_t kk[4];
-      if (i + 3 < b && i >= a) {
-        load4_keys<LT>(rp, i, kk);
+  // ---- pass 1: top 11 key bits
+  for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  for_each_quad<LT>(rp, a, b, [&](int64_t, const uint32_t (&kq)[4], uint32_t valid) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if ((kk[e] & prefix_mask) == prefix) atomicAdd(&hist[(kk[e] >> shift) & (nbins - 1)], 1u);
-      } else {
-        for (int e = 0; e < 4; ++e) {
-          const int64_t c = i + e;
-          if (c < a || c >= b) continue;
-          const uint32_t key = order_key(load_score<LT>(rp, c));
-          if ((key & prefix_mask) == prefix) atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
+    for (int e = 0; e < 4; ++e)
+      if ((valid >> e) & 1u) atomicAdd(&hist[kq[e] >> 21], 1u);
+  });
+  __syncthreads();
+  uint32_t above;
+  const uint32_t b1 = find_bin(hist, 2048, static_cast<uint32_t>(k), scan_buf, &s_bin, &s_above, &above);
+  uint32_t remaining = static_cast<uint32_t>(k) - above;
+  const uint32_t c1 = hist[b1];
+  __syncthreads();
+
+  const int64_t wa = a & ~static_cast<int64_t>(31);
+  const bool fast = (b - wa) <= kFastMaxCols && c1 <= static_cast<uint32_t>(kCandCap);
+  if (fast) {
+    const int nwords = static_cast<int>((b - wa + 31) >> 5);
+    for (int i = tid; i < nwords; i += kThreads) {
+      sel[i] = 0;
+      tie[i] = 0;
+    }
+    if (tid == 0) s_ncand = 0;
+    __syncthreads();
+    // ---- pass 2: mark keys above the bin, collect the bin's candidates
+    for_each_quad<LT>(rp, a, b, [&](int64_t i, const uint32_t (&kq)[4], uint32_t valid) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (!((valid >> e) & 1u)) continue;
+        const uint32_t d = kq[e] >> 21;
+        const int64_t off = i + e - wa;
+        if (d > b1) {
+          atomicOr(&sel[off >> 5], 1u << (off & 31));
+        } else if (d == b1) {
+          const uint32_t slot = atomicAdd(&s_ncand, 1u);
+          if (slot < static_cast<uint32_t>(kCandCap)) {  // always: the bin holds c1 <= kCandCap keys
+            cand_key[slot] = kq[e];
+            cand_col[slot] = static_cast<int32_t>(i + e);
+          }
         }
       }
+    });
+    __syncthreads();
+    const int nc = min(static_cast<int>(s_ncand), kCandCap);
+    // ---- low bits on the candidates: 11 then 10 bits
+    uint32_t prefix = b1 << 21, prefix_mask = 0x7ffu << 21;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+      const int shift = pass == 0 ? 10 : 0;
+      const uint32_t nbins = pass == 0 ? 2048u : 1024u;
+      for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < nc; i += kThreads) {
+        const uint32_t key = cand_key[i];
+        if ((key & prefix_mask) == prefix) atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
+      }
+      __syncthreads();
+      const uint32_t bin = find_bin(hist, nbins, remaining, scan_buf, &s_bin, &s_above, &above);
+      prefix |= bin << shift;
+      prefix_mask |= (nbins - 1) << shift;
+      remaining -= above;
+    }
+    const uint32_t tau = prefix;
+    const uint32_t take_eq = remaining;
+    for (int i = tid; i < nc; i += kThreads) {
+      const uint32_t key = cand_key[i];
+      const int64_t off = cand_col[i] - wa;
+      if (key > tau) atomicOr(&sel[off >> 5], 1u << (off & 31));
+      else if (key == tau) atomicOr(&tie[off >> 5], 1u << (off & 31));
     }
     __syncthreads();
-    // Thread t owns bins hi = nbins-1-2t and lo = hi-1 (threads past nbins/2
-    // own none); an exclusive scan gives the count of keys in higher bins.
-    uint32_t h_hi = 0, h_lo = 0;
-    const int hi = static_cast<int>(nbins) - 1 - 2 * tid;
-    if (hi >= 1) {
-      h_hi = hist[hi];
-      h_lo = hist[hi - 1];
+    // ---- ordered output from the bitmaps
+    const int per = (nwords + kThreads - 1) / kThreads;
+    const int w0 = tid * per, w1 = min(nwords, w0 + per);
+    uint32_t nsel = 0, ntie = 0;
+    for (int w = w0; w < w1; ++w) {
+      nsel += __popc(sel[w]);
+      ntie += __popc(tie[w]);
     }
     uint32_t tot;
-    const uint32_t above = block_excl_sum(h_hi + h_lo, scan_buf, &tot);
-    if (hi >= 1) {
-      if (above < remaining && above + h_hi >= remaining) {
-        s_bin = static_cast<uint32_t>(hi);
-        s_above = above;
-      } else if (above + h_hi < remaining && above + h_hi + h_lo >= remaining) {
-        s_bin = static_cast<uint32_t>(hi - 1);
-        s_above = above + h_hi;
+    const uint32_t ex = block_excl_sum(nsel | (ntie << 16), scan_buf, &tot);
+    uint32_t sel_before = ex & 0xffffu, tie_before = ex >> 16;
+    for (int w = w0; w < w1; ++w) {
+      uint32_t ms = sel[w], mt = tie[w];
+      while (ms | mt) {
+        const uint32_t m = ms | mt;
+        const int bit = __ffs(m) - 1;
+        const int32_t col = static_cast<int32_t>(wa + 32 * static_cast<int64_t>(w) + bit);
+        if ((ms >> bit) & 1u) {
+          op[sel_before + min(tie_before, take_eq)] = col;
+          ++sel_before;
+        } else {
+          if (tie_before < take_eq) op[sel_before + tie_before] = col;
+          ++tie_before;
+        }
+        ms &= ~(1u << bit);
+        mt &= ~(1u << bit);
       }
     }
-    __syncthreads();
-    prefix |= s_bin << shift;
-    prefix_mask |= (nbins - 1) << shift;
-    remaining -= s_above;
-    __syncthreads();
+    return;
   }
-  const uint32_t tau = prefix;       // k-th largest key
-  const uint32_t take_eq = remaining; // keys equal to tau that are kept (lowest columns)
 
-  // ---- ordered compaction: column order, keys > tau, then the first take_eq ties
+  // ---- general path: remaining two digits over the whole row, then an
+  // ordered compaction of the row.
+  uint32_t prefix = b1 << 21, prefix_mask = 0x7ffu << 21;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = pass == 0 ? 10 : 0;
+    const uint32_t nbins = pass == 0 ? 2048u : 1024u;
+    for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    for_each_quad<LT>(rp, a, b, [&](int64_t, const uint32_t (&kq)[4], uint32_t valid) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (((valid >> e) & 1u) && (kq[e] & prefix_mask) == prefix)
+          atomicAdd(&hist[(kq[e] >> shift) & (nbins - 1)], 1u);
+    });
+    __syncthreads();
+    const uint32_t bin = find_bin(hist, nbins, remaining, scan_buf, &s_bin, &s_above, &above);
+    prefix |= bin << shift;
+    prefix_mask |= (nbins - 1) << shift;
+    remaining -= above;
+  }
+  const uint32_t tau = prefix;
+  const uint32_t take_eq = remaining;
   uint32_t gt_run = 0, eq_run = 0;
   for (int64_t base = a; base < b; base += static_cast<int64_t>(kThreads) * kPerThread) {
     const int64_t c0 = base + static_cast<int64_t>(tid) * kPerThread;
@@ -174,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         eq_bits |= (key == tau ? 1u : 0u) << e;
       }
     }
-    const uint32_t packed = static_cast<uint32_t>(__popc(gt_bits)) | (static_cast<uint32_t>(__popc(eq_bits)) << 16);
+    const uint32_t packed =
+        static_cast<uint32_t>(__popc(gt_bits)) | (static_cast<uint32_t>(__popc(eq_bits)) << 16);
     uint32_t tot;
     const uint32_t ex = block_excl_sum(packed, scan_buf, &tot);
     uint32_t gt_before = gt_run + (ex & 0xffffu);
@@ -201,14 +376,21 @@ cudaError_t launch_top_k(const void* logits, int32_t logits_dtype, int64_t logit
                          int32_t k, int32_t* out_idx, int64_t out_stride, int32_t* status,
                          cudaStream_t stream) {
   (void)status;
+  cudaError_t e;
   if (logits_dtype == DSA_LOGITS_BF16) {
-    topk_kernel<__nv_bfloat16><<<num_rows, kThreads, 0, stream>>>(
+    e = cudaFuncSetAttribute(topk_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
+    topk_kernel<__nv_bfloat16><<<num_rows, kThreads, kSmemBytes, stream>>>(
         static_cast<const __nv_bfloat16*>(logits), logits_stride, row_starts, row_ends, k, out_idx,
         out_stride);
   } else {
-    topk_kernel<float><<<num_rows, kThreads, 0, stream>>>(static_cast<const float*>(logits),
-                                                          logits_stride, row_starts, row_ends, k,
-                                                          out_idx, out_stride);
+    e = cudaFuncSetAttribute(topk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
+    topk_kernel<float><<<num_rows, kThreads, kSmemBytes, stream>>>(static_cast<const float*>(logits),
+                                                                    logits_stride, row_starts,
+                                                                    row_ends, k, out_idx, out_stride);
   }
   return cudaGetLastError();
 }

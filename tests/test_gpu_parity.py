@@ -122,9 +122,12 @@ def test_varlen_equals_padded():
     lb = b["logits"][valid]
     check_logits(wl, a["logits"])
     check_logits(pad, b["logits"])
-    fin = torch.isfinite(la)
-    assert torch.equal(fin, torch.isfinite(lb))
-    assert torch.allclose(la[fin], lb[fin], rtol=1e-5, atol=1e-5)
+    ctx = wl.context_lens[slot_row[valid]]
+    for i in range(la.shape[0]):                    # the specified span of each row
+        end = (int(ctx[i]) + 63) // 64 * 64
+        fin = torch.isfinite(la[i, :end])
+        assert torch.equal(fin, torch.isfinite(lb[i, :end]))
+        assert torch.allclose(la[i, :end][fin], lb[i, :end][fin], rtol=1e-5, atol=1e-5)
 
 
 def test_padded_page_stride():
@@ -220,3 +223,17 @@ def test_full_size_sampled(name):
     ref, bound, _ = check_logits(host, out["logits"], rows=rows)
     check_topk_exact(out["logits"], out["idx"], host.context_lens, wl.topk)
     check_topk_tie_band(out["idx"], ref, bound, host.context_lens, wl.topk, rows)
+
+
+def test_topk_long_row_general_path():
+    """A row longer than the shared-memory bitmaps takes the general path."""
+    g = torch.Generator().manual_seed(12)
+    x = torch.randn((2, 300032), generator=g)
+    x[1, 100000:] = torch.round(x[1, 100000:])
+    x = x.cuda()
+    ends = torch.tensor([300032, 290001], dtype=torch.int32)
+    starts = torch.tensor([0, 17], dtype=torch.int32)
+    for k in (5, 2048):
+        got = dsa.top_k_per_row(x, starts.cuda(), ends.cuda(), k).cpu().numpy()
+        ref = oracle.top_k_per_row(x.cpu().double().numpy(), ends, k, row_starts=starts)
+        assert np.array_equal(got, ref), k
