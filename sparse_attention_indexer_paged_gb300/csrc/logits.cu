@@ -48,39 +48,69 @@ namespace {
 constexpr int kThreads = 640;
 constexpr int kEpiWarpgroups = 4;  // warps 4..19
 constexpr int kEpiWarps = 4 * kEpiWarpgroups;
-constexpr int kStages = 8;         // K value ring, one 128-token tile per stage
 constexpr int kScaleStages = 16;   // key scale ring
 constexpr int kTmemCols = 512;
 constexpr int kBufPairs = 4;       // (tile, row) pairs per TMEM buffer
 constexpr int kPairCols = 64;      // 64 heads of one pair
 constexpr int kBufCols = kBufPairs * kPairCols;
 constexpr int kWBufFloats = kGroupMaxRows * kHeads;       // 512
-
 constexpr int kPageValBytesFp8 = kPageTokens * kHeadDim;  // 8192
-constexpr int kKvStageBytes = 2 * kPageValBytesFp8;       // 16384: one 128 x 128 e4m3 tile
-constexpr int kQRowBytes = kHeads * kHeadDim;             // 8192: 64 heads x 128 e4m3
+constexpr int kFp4PageBytes = DSA_FP4_PAGE_BYTES;         // 4864: values, block scales, token scales
+constexpr int kFp4GScaleOffset = kPageTokens * (kHeadDim / 2 + kHeadDim / 16);  // 4608
 constexpr int kScaleStageFloats = kTileTokens;            // 128 key scales per tile
+constexpr int kMaxKStages = 8;
+constexpr int kMaxRawStages = 2;
 
-// shared memory map (offsets from a 1024-aligned base)
-constexpr int kOffKv = 0;
-constexpr int kOffQ = kOffKv + kStages * kKvStageBytes;
-constexpr int kOffScale = kOffQ + kGroupMaxRows * kQRowBytes;
-constexpr int kOffW = kOffScale + kScaleStages * kScaleStageFloats * 4;
-constexpr int kOffCtx = kOffW + 2 * kWBufFloats * 4;  // causal limits of the group's rows
-constexpr int kOffDec = kOffCtx + 2 * kGroupMaxRows * 4;  // per-warpgroup wait verdicts
-constexpr int kOffBar = kOffDec + 2 * kEpiWarpgroups * 4;
-// barriers: kv_full[S], kv_empty[S], sc_full[SS], sc_empty[SS], q_full,
-// q_empty, w_full[2], w_empty[2], tm_full[2], tm_empty[2], mma_done
-constexpr int kNumBars = 2 * kStages + 2 * kScaleStages + 2 + 4 + 4 + 1;
-constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
-constexpr int kOffAbort = kOffTmemAddr + 4;
-constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
-static_assert(kOffQ % 1024 == 0 && kOffKv % 1024 == 0, "MMA tiles need 1024-byte alignment");
-static_assert((kStages & (kStages - 1)) == 0 && (kBufPairs & (kBufPairs - 1)) == 0, "powers of two");
-static_assert(kOffBar % 8 == 0 && kOffW % 16 == 0, "alignment");
-static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
+// Shared memory layouts (offsets from a 1024-aligned base).
+//   FP8: K ring of e4m3 tiles [128 tokens][128 B] filled by TMA, Q rows e4m3.
+//   FP4: raw page pairs (bulk copies of whole pages), dequantised f16 K tiles
+//        [2 k-halves][128 tokens][128 B], Q rows in f16 [2 k-halves][512][128 B];
+//        all MMA operands K-major with the 128-byte swizzle.
+template <int kFmt> struct Lay;
+template <> struct Lay<DSA_KV_FP8> {
+  static constexpr int kKStages = 8;
+  static constexpr int kKStageBytes = 2 * kPageValBytesFp8;  // 16384
+  static constexpr int kRawStages = 0;
+  static constexpr int kRawStageBytes = 0;
+  static constexpr int kQRowBytes = kHeads * kHeadDim;        // 8192
+  static constexpr int kOffKv = 0;
+  static constexpr int kOffQ = kOffKv + kKStages * kKStageBytes;
+  static constexpr int kOffRaw = kOffQ + kGroupMaxRows * kQRowBytes;
+};
+template <> struct Lay<DSA_KV_FP4> {
+  static constexpr int kKStages = 2;
+  static constexpr int kKStageBytes = 2 * kTileTokens * 128;  // 32768
+  static constexpr int kRawStages = 2;
+  static constexpr int kRawStageBytes = 2 * kFp4PageBytes;    // 9728
+  static constexpr int kQHalfBytes = kGroupMaxRows * kHeads * 128;  // 65536
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKv = kOffQ + 2 * kQHalfBytes;
+  static constexpr int kOffRaw = kOffKv + kKStages * kKStageBytes;
+};
+template <int kFmt> struct Smem : Lay<kFmt> {
+  using B = Lay<kFmt>;
+  static constexpr int kOffScale = B::kOffRaw + B::kRawStages * B::kRawStageBytes;
+  static constexpr int kOffW = kOffScale + kScaleStages * kScaleStageFloats * 4;
+  static constexpr int kOffCtx = kOffW + 2 * kWBufFloats * 4;  // causal limits of the group's rows
+  static constexpr int kOffDec = kOffCtx + 2 * kGroupMaxRows * 4;  // per-warpgroup wait verdicts
+  static constexpr int kOffBar = kOffDec + 2 * kEpiWarpgroups * 4;
+  // barriers: kv_full[8], kv_empty[8], raw_full[2], raw_empty[2], sc_full[SS],
+  // sc_empty[SS], q_full, q_empty, w_full[2], w_empty[2], tm_full[2], tm_empty[2], mma_done
+  static constexpr int kNumBars = 2 * kMaxKStages + 2 * kMaxRawStages + 2 * kScaleStages + 2 + 4 + 4 + 1;
+  static constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmemAddr + 4;
+  static constexpr int kBytes = kOffAbort + 4 + 1024;  // + alignment slack
+  static_assert(B::kOffQ % 1024 == 0 && B::kOffKv % 1024 == 0 && B::kKStageBytes % 1024 == 0,
+                "MMA tiles need 1024-byte alignment");
+  static_assert(B::kOffRaw % 16 == 0 && B::kRawStageBytes % 16 == 0, "bulk copies need 16 bytes");
+  static_assert((B::kKStages & (B::kKStages - 1)) == 0 && B::kKStages <= kMaxKStages, "K ring");
+  static_assert(kOffBar % 8 == 0, "mbarriers need 8-byte alignment");
+  static_assert(kBytes <= 232448, "over the per-CTA shared memory limit");
+};
+static_assert((kBufPairs & (kBufPairs - 1)) == 0, "power of two");
 
 struct Params {
+  const uint8_t* q;
   const uint8_t* kv_cache;
   int64_t page_stride;
   int64_t num_pages;
@@ -99,10 +129,12 @@ struct Params {
 };
 
 struct Bars {
-  uint32_t kv_full, kv_empty, sc_full, sc_empty, q_full, q_empty, w_full, w_empty, tm_full,
-      tm_empty, mma_done;
+  uint32_t kv_full, kv_empty, raw_full, raw_empty, sc_full, sc_empty, q_full, q_empty, w_full,
+      w_empty, tm_full, tm_empty, mma_done;
   __device__ uint32_t kvf(int s) const { return kv_full + 8 * s; }
   __device__ uint32_t kve(int s) const { return kv_empty + 8 * s; }
+  __device__ uint32_t rwf(int s) const { return raw_full + 8 * s; }
+  __device__ uint32_t rwe(int s) const { return raw_empty + 8 * s; }
   __device__ uint32_t scf(int s) const { return sc_full + 8 * s; }
   __device__ uint32_t sce(int s) const { return sc_empty + 8 * s; }
   __device__ uint32_t wf(int b) const { return w_full + 8 * b; }
@@ -188,6 +220,9 @@ template <int kFmt>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                   const Params p) {
+  using L = Smem<kFmt>;
+  constexpr bool kFp4 = kFmt == DSA_KV_FP4;
+  constexpr int kStages = L::kKStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -215,9 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (u0 >= u1 || G == 0) return;  // no work: the whole CTA leaves before any set-up
 
   Bars bars;
-  bars.kv_full = sbase + kOffBar;
-  bars.kv_empty = bars.kv_full + 8 * kStages;
-  bars.sc_full = bars.kv_empty + 8 * kStages;
+  bars.kv_full = sbase + L::kOffBar;
+  bars.kv_empty = bars.kv_full + 8 * kMaxKStages;
+  bars.raw_full = bars.kv_empty + 8 * kMaxKStages;
+  bars.raw_empty = bars.raw_full + 8 * kMaxRawStages;
+  bars.sc_full = bars.raw_empty + 8 * kMaxRawStages;
   bars.sc_empty = bars.sc_full + 8 * kScaleStages;
   bars.q_full = bars.sc_empty + 8 * kScaleStages;
   bars.q_empty = bars.q_full + 8;
@@ -226,13 +263,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   bars.tm_full = bars.w_empty + 16;
   bars.tm_empty = bars.tm_full + 16;
   bars.mma_done = bars.tm_empty + 16;
-  uint32_t* tmem_addr_smem = reinterpret_cast<uint32_t*>(smem + kOffTmemAddr);
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kOffAbort);
+  uint32_t* tmem_addr_smem = reinterpret_cast<uint32_t*>(smem + L::kOffTmemAddr);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kOffAbort);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bars.kvf(s), 1);
+      mbar_init(bars.kvf(s), 1);  // TMA (FP8) or the dequantising warp (FP4)
       mbar_init(bars.kve(s), 1);  // the MMA commit of the tile
+    }
+    for (int s = 0; s < L::kRawStages; ++s) {
+      mbar_init(bars.rwf(s), 1);
+      mbar_init(bars.rwe(s), 1);  // the dequantising warp
     }
     for (int s = 0; s < kScaleStages; ++s) {
       mbar_init(bars.scf(s), 1);
@@ -259,42 +300,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_addr_smem;
 
-  const uint32_t s_kv = sbase + kOffKv;
-  const uint32_t s_q = sbase + kOffQ;
-  const uint32_t s_scale = sbase + kOffScale;
-  const uint32_t s_w = sbase + kOffW;
-  const float* scale_sm = reinterpret_cast<const float*>(smem + kOffScale);
-  const float* w_sm = reinterpret_cast<const float*>(smem + kOffW);
-  int32_t* ctx_sm = reinterpret_cast<int32_t*>(smem + kOffCtx);
+  const uint32_t s_kv = sbase + L::kOffKv;
+  const uint32_t s_q = sbase + L::kOffQ;
+  const uint32_t s_scale = sbase + L::kOffScale;
+  const uint32_t s_w = sbase + L::kOffW;
+  float* scale_sm = reinterpret_cast<float*>(smem + L::kOffScale);
+  const float* w_sm = reinterpret_cast<const float*>(smem + L::kOffW);
+  int32_t* ctx_sm = reinterpret_cast<int32_t*>(smem + L::kOffCtx);
 
   Walk walk;
   walk.start(grs, gus, p.ctx, G, T, u0, u1);
 
   if (warp == 0) {
-    // =================================================== TMA producer (K values, Q)
+    // =================================================== producer: K pages (and FP8 Q)
     // The whole warp walks the work: block ids are fetched 32 at a time with
     // one coalesced load and handed out by shuffle; lane 0 waits and issues.
-    if (lane == 0) {
-      prefetch_tensormap(&tm_q);
-      prefetch_tensormap(&tm_kv);
+    if constexpr (!kFp4) {
+      if (lane == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_kv);
+      }
     }
     const uint64_t pol_stream = policy_evict_first();  // K pages are read once
     const uint64_t pol_keep = policy_evict_last();      // q
+    constexpr int kRing = kFp4 ? L::kRawStages : kStages;
     int it = 0, nq = 0;  // tiles and Q groups issued
     bool ok = true;
     while (ok && walk.next()) {
       const int r0 = walk.r0, n = walk.n;
-      if (lane == 0) {
-        ok = wait_or_abort(bars.q_empty, (nq & 1) ^ 1, abort_flag, p.status);
-        if (ok) {
-          mbar_arrive_expect_tx(bars.q_full, static_cast<uint32_t>(n * kQRowBytes));
-          for (int r = 0; r < n; ++r)
-            tma_load_2d(s_q + r * kQRowBytes, &tm_q, 0, (r0 + r) * kHeads, bars.q_full, pol_keep);
+      if constexpr (!kFp4) {
+        if (lane == 0) {
+          ok = wait_or_abort(bars.q_empty, (nq & 1) ^ 1, abort_flag, p.status);
+          if (ok) {
+            mbar_arrive_expect_tx(bars.q_full, static_cast<uint32_t>(n * L::kQRowBytes));
+            for (int r = 0; r < n; ++r)
+              tma_load_2d(s_q + r * L::kQRowBytes, &tm_q, 0, (r0 + r) * kHeads, bars.q_full, pol_keep);
+          }
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        ++nq;
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      ++nq;
       const int32_t* bt_row = p.block_table + static_cast<int64_t>(r0 + n - 1) * p.bt_stride;
       int32_t lane_blk = -1;  // block id of page (pg_base + lane)
       int pg_base = -32;
@@ -315,16 +361,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t blk0 = __shfl_sync(0xffffffffu, lane_blk, 2 * j - pg_base);
         const int32_t blk1 = __shfl_sync(0xffffffffu, lane_blk, 2 * j + 1 - pg_base);
         if (lane == 0) {
-          const int st = it % kStages;
-          ok = wait_or_abort(bars.kve(st), ((it / kStages) & 1) ^ 1, abort_flag, p.status);
+          const int st = it % kRing;
+          const uint32_t empty_bar = kFp4 ? bars.rwe(st) : bars.kve(st);
+          const uint32_t full_bar = kFp4 ? bars.rwf(st) : bars.kvf(st);
+          ok = wait_or_abort(empty_bar, ((it / kRing) & 1) ^ 1, abort_flag, p.status);
           if (ok) {
             const int npg = (blk0 >= 0 ? 1 : 0) + (blk1 >= 0 ? 1 : 0);
-            mbar_arrive_expect_tx(bars.kvf(st), static_cast<uint32_t>(npg * kPageValBytesFp8));
-            if (blk0 >= 0)
-              tma_load_3d(s_kv + st * kKvStageBytes, &tm_kv, 0, 0, blk0, bars.kvf(st), pol_stream);
-            if (blk1 >= 0)
-              tma_load_3d(s_kv + st * kKvStageBytes + kPageValBytesFp8, &tm_kv, 0, 0, blk1,
-                          bars.kvf(st), pol_stream);
+            if constexpr (kFp4) {
+              // whole pages: packed values, block scales and token scales
+              mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(npg * kFp4PageBytes));
+              const uint32_t dst = sbase + L::kOffRaw + st * L::kRawStageBytes;
+              if (blk0 >= 0)
+                bulk_load(dst, p.kv_cache + static_cast<int64_t>(blk0) * p.page_stride, kFp4PageBytes,
+                          full_bar, pol_stream);
+              if (blk1 >= 0)
+                bulk_load(dst + kFp4PageBytes, p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride,
+                          kFp4PageBytes, full_bar, pol_stream);
+            } else {
+              mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(npg * kPageValBytesFp8));
+              if (blk0 >= 0)
+                tma_load_3d(s_kv + st * L::kKStageBytes, &tm_kv, 0, 0, blk0, full_bar, pol_stream);
+              if (blk1 >= 0)
+                tma_load_3d(s_kv + st * L::kKStageBytes + kPageValBytesFp8, &tm_kv, 0, 0, blk1,
+                            full_bar, pol_stream);
+            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -334,55 +394,162 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Drain: every copy this CTA issued has landed before it may exit (a
     // phase that already completed returns at once).
     if (lane == 0) {
-      for (int i = max(0, it - kStages); i < it; ++i) wait_drain(bars.kvf(i % kStages), (i / kStages) & 1);
+      for (int i = max(0, it - kRing); i < it; ++i)
+        wait_drain(kFp4 ? bars.rwf(i % kRing) : bars.kvf(i % kRing), (i / kRing) & 1);
       if (nq > 0) wait_drain(bars.q_full, (nq - 1) & 1);
     }
   } else if (warp == 3) {
-    // =================================================== key scales
-    // Runs ahead of the K pipeline by up to kScaleStages tiles, gated only
-    // by the epilogue.  Block ids come 32 at a time as in the K producer.
-    const uint64_t pol_stream = policy_evict_first();
-    int it = 0;
-    bool ok = true;
-    while (ok && walk.next()) {
-      const int32_t* bt_row = p.block_table + static_cast<int64_t>(walk.r0 + walk.n - 1) * p.bt_stride;
-      int32_t lane_blk = -1;
-      int pg_base = -32;
-      for (int j = walk.j0; j < walk.j1; ++j, ++it) {
-        if (2 * j >= pg_base + 32) {
-          pg_base = 2 * j;
-          const int pg = pg_base + lane;
-          lane_blk = -1;
-          if (pg < walk.npages) {
-            int32_t b = (pg < p.bt_stride) ? __ldg(bt_row + pg) : -1;
-            lane_blk = (b < 0 || b >= p.num_pages) ? 0 : b;  // reported by the K producer
+    if constexpr (!kFp4) {
+      // =================================================== key scales (FP8)
+      // Runs ahead of the K pipeline by up to kScaleStages tiles, gated only
+      // by the epilogue.  Block ids come 32 at a time as in the K producer.
+      const uint64_t pol_stream = policy_evict_first();
+      int it = 0;
+      bool ok = true;
+      while (ok && walk.next()) {
+        const int32_t* bt_row = p.block_table + static_cast<int64_t>(walk.r0 + walk.n - 1) * p.bt_stride;
+        int32_t lane_blk = -1;
+        int pg_base = -32;
+        for (int j = walk.j0; j < walk.j1; ++j, ++it) {
+          if (2 * j >= pg_base + 32) {
+            pg_base = 2 * j;
+            const int pg = pg_base + lane;
+            lane_blk = -1;
+            if (pg < walk.npages) {
+              int32_t b = (pg < p.bt_stride) ? __ldg(bt_row + pg) : -1;
+              lane_blk = (b < 0 || b >= p.num_pages) ? 0 : b;  // reported by the K producer
+            }
           }
-        }
-        const int32_t blk0 = __shfl_sync(0xffffffffu, lane_blk, 2 * j - pg_base);
-        const int32_t blk1 = __shfl_sync(0xffffffffu, lane_blk, 2 * j + 1 - pg_base);
-        if (lane == 0) {
-          const int ss = it % kScaleStages;
-          ok = wait_or_abort(bars.sce(ss), ((it / kScaleStages) & 1) ^ 1, abort_flag, p.status);
-          if (ok) {
-            const int npg = (blk0 >= 0 ? 1 : 0) + (blk1 >= 0 ? 1 : 0);
-            mbar_arrive_expect_tx(bars.scf(ss), static_cast<uint32_t>(npg * kPageTokens * 4));
-            if (blk0 >= 0)
-              bulk_load(s_scale + ss * kScaleStageFloats * 4,
-                        p.kv_cache + static_cast<int64_t>(blk0) * p.page_stride + kPageValBytesFp8,
-                        kPageTokens * 4, bars.scf(ss), pol_stream);
-            if (blk1 >= 0)
-              bulk_load(s_scale + (ss * kScaleStageFloats + kPageTokens) * 4,
-                        p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride + kPageValBytesFp8,
-                        kPageTokens * 4, bars.scf(ss), pol_stream);
+          const int32_t blk0 = __shfl_sync(0xffffffffu, lane_blk, 2 * j - pg_base);
+          const int32_t blk1 = __shfl_sync(0xffffffffu, lane_blk, 2 * j + 1 - pg_base);
+          if (lane == 0) {
+            const int ss = it % kScaleStages;
+            ok = wait_or_abort(bars.sce(ss), ((it / kScaleStages) & 1) ^ 1, abort_flag, p.status);
+            if (ok) {
+              const int npg = (blk0 >= 0 ? 1 : 0) + (blk1 >= 0 ? 1 : 0);
+              mbar_arrive_expect_tx(bars.scf(ss), static_cast<uint32_t>(npg * kPageTokens * 4));
+              if (blk0 >= 0)
+                bulk_load(s_scale + ss * kScaleStageFloats * 4,
+                          p.kv_cache + static_cast<int64_t>(blk0) * p.page_stride + kPageValBytesFp8,
+                          kPageTokens * 4, bars.scf(ss), pol_stream);
+              if (blk1 >= 0)
+                bulk_load(s_scale + (ss * kScaleStageFloats + kPageTokens) * 4,
+                          p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride + kPageValBytesFp8,
+                          kPageTokens * 4, bars.scf(ss), pol_stream);
+            }
           }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      }
+      if (lane == 0)
+        for (int i = max(0, it - kScaleStages); i < it; ++i)
+          wait_drain(bars.scf(i % kScaleStages), (i / kScaleStages) & 1);
+    } else {
+      // =================================================== FP4 dequantisation
+      // Per group: the group's q rows, e4m3 -> f16 (exact), into the swizzled
+      // B-operand layout.  Per tile: the raw pages' e2m1 values times their
+      // e4m3 block scales -> f16 (exact: at most 6 significant bits) into the
+      // swizzled A-operand layout, and the token scales into the scale ring.
+      int it = 0, nq = 0;
+      bool ok = true;
+      const uint32_t q_half = static_cast<uint32_t>(Lay<DSA_KV_FP4>::kQHalfBytes);
+      while (ok && walk.next()) {
+        const int r0 = walk.r0, n = walk.n;
+        int okq = 1;
+        if (lane == 0) okq = wait_or_abort(bars.q_empty, (nq & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, okq, 0) != 0;
         if (!ok) break;
+        {
+          // 8 e4m3 codes per step, consecutive lanes on consecutive bytes
+          const uint2* qsrc = reinterpret_cast<const uint2*>(p.q + static_cast<int64_t>(r0) * kHeads * kHeadDim);
+          const int nchunks = n * kHeads * (kHeadDim / 8);
+          for (int i = lane; i < nchunks; i += 32) {
+            const uint2 c = __ldg(qsrc + i);
+            const int R = i >> 4;      // q row (row * 64 + head) within the group
+            const int c16 = i & 15;    // 8-element chunk along d
+            uint4 o;
+            o.x = e4m3x2_to_f16x2(c.x & 0xffffu);
+            o.y = e4m3x2_to_f16x2(c.x >> 16);
+            o.z = e4m3x2_to_f16x2(c.y & 0xffffu);
+            o.w = e4m3x2_to_f16x2(c.y >> 16);
+            const uint32_t off = static_cast<uint32_t>(c16 >> 3) * q_half + static_cast<uint32_t>(R >> 3) * 1024u +
+                                 static_cast<uint32_t>(R & 7) * 128u + (static_cast<uint32_t>((c16 & 7) ^ (R & 7)) << 4);
+            *reinterpret_cast<uint4*>(smem + L::kOffQ + off) = o;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.q_full);
+        ++nq;
+        for (int j = walk.j0; j < walk.j1; ++j, ++it) {
+          const int rs = it % L::kRawStages;
+          const int st = it % kStages;
+          const int ss = it % kScaleStages;
+          int okt = 1;
+          if (lane == 0)
+            okt = (wait_or_abort(bars.rwf(rs), (it / L::kRawStages) & 1, abort_flag, p.status) &&
+                   wait_or_abort(bars.kve(st), ((it / kStages) & 1) ^ 1, abort_flag, p.status) &&
+                   wait_or_abort(bars.sce(ss), ((it / kScaleStages) & 1) ^ 1, abort_flag, p.status))
+                      ? 1 : 0;
+          ok = __shfl_sync(0xffffffffu, okt, 0) != 0;
+          if (!ok) break;
+          const uint8_t* rawp = smem + L::kOffRaw + rs * L::kRawStageBytes;
+          // token scales of both pages -> scale ring (4 per lane)
+          {
+            const int t4 = lane * 4;  // tokens t4 .. t4+3
+            const float4 g = *reinterpret_cast<const float4*>(rawp + (t4 >> 6) * kFp4PageBytes +
+                                                              kFp4GScaleOffset + (t4 & 63) * 4);
+            *reinterpret_cast<float4*>(scale_sm + ss * kScaleStageFloats + t4) = g;
+          }
+          uint8_t* tile = smem + L::kOffKv + st * L::kKStageBytes;
+#pragma unroll 1
+          for (int tk = lane; tk < kTileTokens; tk += 32) {
+            const uint8_t* tokp = rawp + (tk >> 6) * kFp4PageBytes;
+            const int slot = tk & 63;
+            const uint4* vals = reinterpret_cast<const uint4*>(tokp + slot * (kHeadDim / 2));
+            const uint2 bsc = *reinterpret_cast<const uint2*>(tokp + kPageTokens * (kHeadDim / 2) + slot * 8);
+            uint32_t sc[8];  // f16x2 {s_b, s_b} for block b
+            {
+              const uint32_t s01 = e4m3x2_to_f16x2(bsc.x & 0xffffu), s23 = e4m3x2_to_f16x2(bsc.x >> 16);
+              const uint32_t s45 = e4m3x2_to_f16x2(bsc.y & 0xffffu), s67 = e4m3x2_to_f16x2(bsc.y >> 16);
+              sc[0] = __byte_perm(s01, 0, 0x1010); sc[1] = __byte_perm(s01, 0, 0x3232);
+              sc[2] = __byte_perm(s23, 0, 0x1010); sc[3] = __byte_perm(s23, 0, 0x3232);
+              sc[4] = __byte_perm(s45, 0, 0x1010); sc[5] = __byte_perm(s45, 0, 0x3232);
+              sc[6] = __byte_perm(s67, 0, 0x1010); sc[7] = __byte_perm(s67, 0, 0x3232);
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {  // 16-byte pieces of the packed row: 32 elements each
+              const uint4 pv = vals[q4];
+              const uint32_t words[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+              for (int wv = 0; wv < 4; ++wv) {  // 8 elements per word
+                const int c16 = q4 * 4 + wv;     // chunk of elements 8*c16 .. 8*c16+7
+                uint32_t h[4];
+                e2m1x8_to_f16x2(words[wv], h);
+                const uint32_t sb = sc[c16 >> 1];
+                uint4 o;
+                o.x = hmul2_u32(h[0], sb);
+                o.y = hmul2_u32(h[1], sb);
+                o.z = hmul2_u32(h[2], sb);
+                o.w = hmul2_u32(h[3], sb);
+                const uint32_t off = static_cast<uint32_t>(c16 >> 3) * (kTileTokens * 128u) +
+                                     static_cast<uint32_t>(tk >> 3) * 1024u + static_cast<uint32_t>(tk & 7) * 128u +
+                                     (static_cast<uint32_t>((c16 & 7) ^ (tk & 7)) << 4);
+                *reinterpret_cast<uint4*>(tile + off) = o;
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bars.rwe(rs));
+            mbar_arrive(bars.kvf(st));
+            mbar_arrive(bars.scf(ss));
+          }
+        }
       }
     }
-    if (lane == 0)
-      for (int i = max(0, it - kScaleStages); i < it; ++i)
-        wait_drain(bars.scf(i % kScaleStages), (i / kScaleStages) & 1);
   } else if (warp == 2) {
     // =================================================== weights + causal limits
     // A separate producer: the epilogue may hold a group's weights until TMEM
@@ -408,11 +575,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // =================================================== MMA issuer
     if (lane == 0) {
-      // idesc for N = 64, 128, 192, 256 (1..4 pairs of one tile)
-      const uint32_t id1 = idesc(kFmtE4M3, kFmtE4M3, 128, 64), id2 = idesc(kFmtE4M3, kFmtE4M3, 128, 128);
-      const uint32_t id3 = idesc(kFmtE4M3, kFmtE4M3, 128, 192), id4 = idesc(kFmtE4M3, kFmtE4M3, 128, 256);
+      // idesc for N = 64, 128, 192, 256 (1..4 pairs of one tile); the A/B
+      // format code 0 is e4m3 for kind::f8f6f4 and f16 for kind::f16
+      const uint32_t id1 = idesc(0, 0, 128, 64), id2 = idesc(0, 0, 128, 128);
+      const uint32_t id3 = idesc(0, 0, 128, 192), id4 = idesc(0, 0, 128, 256);
       const uint32_t a_lo0 = sdesc_lo(s_kv), q_lo0 = sdesc_lo(s_q);
-      constexpr uint32_t kStageLo = kKvStageBytes >> 4, kRowLo = kQRowBytes >> 4;
+      constexpr uint32_t kStageLo = L::kKStageBytes >> 4;
       uint32_t it = 0, gi = 0, pos = 0;  // tiles, groups, pairs issued
       bool ok = true;
       while (ok && walk.next()) {
@@ -438,12 +606,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int len = min(n - r, static_cast<int>(kBufPairs - c));
             const uint32_t d_tmem = tmem + b * kBufCols + c * kPairCols;
             const uint32_t id = len == 1 ? id1 : (len == 2 ? id2 : (len == 3 ? id3 : id4));
-            const uint32_t b_lo = q_lo0 + static_cast<uint32_t>(r) * kRowLo;
-            // K = 128 in four steps of 32 bytes inside the swizzled row (+2 in the address field)
-            mma_f8f6f4_w<false>(d_tmem, a_lo, kSdescHi, b_lo, kSdescHi, id);
-            mma_f8f6f4_w<true>(d_tmem, a_lo + 2, kSdescHi, b_lo + 2, kSdescHi, id);
-            mma_f8f6f4_w<true>(d_tmem, a_lo + 4, kSdescHi, b_lo + 4, kSdescHi, id);
-            mma_f8f6f4_w<true>(d_tmem, a_lo + 6, kSdescHi, b_lo + 6, kSdescHi, id);
+            if constexpr (!kFp4) {
+              // K = 128 e4m3 in four 32-byte steps inside the swizzled row (+2 in the address field)
+              const uint32_t b_lo = q_lo0 + static_cast<uint32_t>(r) * (L::kQRowBytes >> 4);
+              mma_f8f6f4_w<false>(d_tmem, a_lo, kSdescHi, b_lo, kSdescHi, id);
+              mma_f8f6f4_w<true>(d_tmem, a_lo + 2, kSdescHi, b_lo + 2, kSdescHi, id);
+              mma_f8f6f4_w<true>(d_tmem, a_lo + 4, kSdescHi, b_lo + 4, kSdescHi, id);
+              mma_f8f6f4_w<true>(d_tmem, a_lo + 6, kSdescHi, b_lo + 6, kSdescHi, id);
+            } else {
+              // K = 128 f16 in eight 16-element steps: two 64-element halves
+              // (separate swizzled blocks), four 32-byte steps inside each
+              constexpr uint32_t kAHalfLo = (kTileTokens * 128) >> 4;
+              constexpr uint32_t kBHalfLo = Lay<DSA_KV_FP4>::kQHalfBytes >> 4;
+              const uint32_t b_lo = q_lo0 + static_cast<uint32_t>(r) * ((kHeads * 128) >> 4);
+              mma_f16_w<false>(d_tmem, a_lo, kSdescHi, b_lo, kSdescHi, id);
+#pragma unroll
+              for (int kk = 1; kk < 8; ++kk) {
+                const uint32_t ao = (kk >> 2) * kAHalfLo + (kk & 3) * 2;
+                const uint32_t bo = (kk >> 2) * kBHalfLo + (kk & 3) * 2;
+                mma_f16_w<true>(d_tmem, a_lo + ao, kSdescHi, b_lo + bo, kSdescHi, id);
+              }
+            }
             r += len;
             pos += len;
             if ((pos & (kBufPairs - 1)) == 0) mma_commit(bars.tf(b));
@@ -468,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const bool leader = ((warp - 4) & 3) == 0 && lane == 0;
     const uint32_t named_id = 1 + wg;  // named barrier of this warpgroup
-    volatile int32_t* decision = reinterpret_cast<volatile int32_t*>(smem + kOffDec) + 2 * wg;
+    volatile int32_t* decision = reinterpret_cast<volatile int32_t*>(smem + L::kOffDec) + 2 * wg;
     int nwait = 0;
     float* out_f = static_cast<float*>(p.logits);
     __nv_bfloat16* out_h = static_cast<__nv_bfloat16*>(p.logits);
@@ -543,21 +726,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_logits_fp8(const LogitsArgs& a, cudaStream_t stream) {
-  alignas(64) CUtensorMap tm_q, tm_kv;
-  const uint64_t qdims[2] = {static_cast<uint64_t>(kHeadDim),
-                             static_cast<uint64_t>(a.num_rows) * kHeads};
-  const uint64_t qstrides[1] = {static_cast<uint64_t>(kHeadDim)};
-  const uint32_t qbox[2] = {static_cast<uint32_t>(kHeadDim), static_cast<uint32_t>(kHeads)};
-  if (!encode_tensor_map_u8(&tm_q, 2, const_cast<uint8_t*>(a.q), qdims, qstrides, qbox, true))
-    return cudaErrorInvalidValue;
-  const uint64_t kdims[3] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(kPageTokens),
-                             static_cast<uint64_t>(a.num_pages)};
-  const uint64_t kstrides[2] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(a.page_stride)};
-  const uint32_t kbox[3] = {static_cast<uint32_t>(kHeadDim), static_cast<uint32_t>(kPageTokens), 1};
-  if (!encode_tensor_map_u8(&tm_kv, 3, const_cast<uint8_t*>(a.kv_cache), kdims, kstrides, kbox, true))
-    return cudaErrorInvalidValue;
+namespace {
+
+Params make_params(const LogitsArgs& a) {
   Params p;
+  p.q = a.q;
   p.kv_cache = a.kv_cache;
   p.page_stride = a.page_stride;
   p.num_pages = a.num_pages;
@@ -573,16 +746,45 @@ cudaError_t launch_logits_fp8(const LogitsArgs& a, cudaStream_t stream) {
   p.logits_stride = a.logits_stride;
   p.num_rows = a.num_rows;
   p.status = a.status;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_logits_fp8(const LogitsArgs& a, cudaStream_t stream) {
+  alignas(64) CUtensorMap tm_q, tm_kv;
+  const uint64_t qdims[2] = {static_cast<uint64_t>(kHeadDim),
+                             static_cast<uint64_t>(a.num_rows) * kHeads};
+  const uint64_t qstrides[1] = {static_cast<uint64_t>(kHeadDim)};
+  const uint32_t qbox[2] = {static_cast<uint32_t>(kHeadDim), static_cast<uint32_t>(kHeads)};
+  if (!encode_tensor_map_u8(&tm_q, 2, const_cast<uint8_t*>(a.q), qdims, qstrides, qbox, true))
+    return cudaErrorInvalidValue;
+  const uint64_t kdims[3] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(kPageTokens),
+                             static_cast<uint64_t>(a.num_pages)};
+  const uint64_t kstrides[2] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(a.page_stride)};
+  const uint32_t kbox[3] = {static_cast<uint32_t>(kHeadDim), static_cast<uint32_t>(kPageTokens), 1};
+  if (!encode_tensor_map_u8(&tm_kv, 3, const_cast<uint8_t*>(a.kv_cache), kdims, kstrides, kbox, true))
+    return cudaErrorInvalidValue;
+  const Params p = make_params(a);
+  constexpr int kBytes = Smem<DSA_KV_FP8>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(logits_kernel<DSA_KV_FP8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
   if (e != cudaSuccess) return e;
-  logits_kernel<DSA_KV_FP8><<<a.num_sms, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, p);
+  logits_kernel<DSA_KV_FP8><<<a.num_sms, kThreads, kBytes, stream>>>(tm_q, tm_kv, p);
   return cudaGetLastError();
 }
 
-}  // namespace dsa
+cudaError_t launch_logits_fp4(const LogitsArgs& a, cudaStream_t stream) {
+  // The FP4 variant reads its pages with plain bulk copies and converts q
+  // itself; the tensor-map parameters are unused.
+  alignas(64) CUtensorMap unused{};
+  const Params p = make_params(a);
+  constexpr int kBytes = Smem<DSA_KV_FP4>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(logits_kernel<DSA_KV_FP4>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
+  if (e != cudaSuccess) return e;
+  logits_kernel<DSA_KV_FP4><<<a.num_sms, kThreads, kBytes, stream>>>(unused, unused, p);
+  return cudaGetLastError();
+}
 
-namespace dsa {
-// FP4-key variant: not built yet.
-cudaError_t launch_logits_fp4(const LogitsArgs&, cudaStream_t) { return cudaErrorNotSupported; }
 }  // namespace dsa

@@ -237,3 +237,33 @@ def test_topk_long_row_general_path():
         got = dsa.top_k_per_row(x, starts.cuda(), ends.cuda(), k).cpu().numpy()
         ref = oracle.top_k_per_row(x.cpu().double().numpy(), ends, k, row_starts=starts)
         assert np.array_equal(got, ref), k
+
+
+# ---------------------------------------------------------------- FP4 keys (e2m1 + e4m3/16 + fp32/token)
+
+@pytest.mark.parametrize("logits_dtype", [W.LOGITS_F32, W.LOGITS_BF16])
+def test_fp4_mixed_ragged(logits_dtype):
+    _full_check(W.build("fp4", **MIXED, topk=64, kv_format=W.KV_FP4, logits_dtype=logits_dtype,
+                        seed=13))
+
+
+@pytest.mark.parametrize("S", [1, 7])
+def test_fp4_any_sm_split(S):
+    _full_check(W.build("fp4s", request_lens=[700, 129, 1500], rows_per_request=[3, 8, 5], topk=128,
+                        kv_format=W.KV_FP4, seed=14), num_sms=S)
+
+
+def test_fp4_padded_page_stride():
+    _full_check(W.build("fp4p", request_lens=[333, 1024], rows_per_request=[2, 4], topk=100,
+                        kv_format=W.KV_FP4, page_stride=4864 + 16 * 9, seed=15))
+
+
+def test_fp4_full_size_sampled():
+    wl = W.config("fp4_varlen", device="cuda")
+    out = run_path(wl)
+    assert int(out["status"].item()) == 0, dsa.status_string(int(out["status"].item()))
+    host = wl.to("cpu")
+    rows = sample_rows(wl.num_rows, 4, seed=5)
+    ref, bound, _ = check_logits(host, out["logits"], rows=rows)
+    check_topk_exact(out["logits"], out["idx"], host.context_lens, wl.topk)
+    check_topk_tie_band(out["idx"], ref, bound, host.context_lens, wl.topk, rows)
