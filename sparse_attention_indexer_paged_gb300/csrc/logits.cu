@@ -21,7 +21,8 @@
 // four pairs (2 x 256 columns); the MMA issuer fills one buffer while the
 // epilogue drains the other, with one full/empty handshake per buffer.
 // Epilogue warpgroup w takes pair w of every buffer, so every warp waits on
-// every phase of the buffer barriers in order.
+// every phase of the buffer barriers in order (only the last buffer of the
+// stream may be partial, and no wait follows it).
 //
 // Rings: K values (kStages tiles, released by the MMA commit) and key scales
 // (kScaleStages tiles, released by the epilogue, loaded by their own warp)
@@ -31,13 +32,15 @@
 // Warp roles (640 threads):
 //   warp 0      TMA producer: the group's Q rows, then per tile the K pages
 //               (3-D tensor map over the pool, page id from the block table).
-//   warp 1      MMA issuer and TMEM owner (512 columns).
+//   warp 1      MMA issuer and TMEM owner (512 columns): the whole warp walks
+//               the work with warp-uniform values; one elected lane issues.
 //   warp 2      head weights and causal limits of each group (double buffered).
 //   warp 3      key scales, up to kScaleStages tiles ahead.
 //   warps 4-19  four epilogue warpgroups: tcgen05.ld of a pair, relu,
 //               packed-fp32 FMA with the head weights, key scale, causal
-//               mask, store.  Each warpgroup's first warp waits on the
-//               mbarriers; the other three meet it at a named barrier.
+//               mask, store.  Each warp visits only its own pairs and waits
+//               on the mbarriers itself (all lanes, so every lane's reads
+//               are ordered after the completed phase).
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -92,8 +95,7 @@ template <int kFmt> struct Smem : Lay<kFmt> {
   static constexpr int kOffScale = B::kOffRaw + B::kRawStages * B::kRawStageBytes;
   static constexpr int kOffW = kOffScale + kScaleStages * kScaleStageFloats * 4;
   static constexpr int kOffCtx = kOffW + 2 * kWBufFloats * 4;  // causal limits of the group's rows
-  static constexpr int kOffDec = kOffCtx + 2 * kGroupMaxRows * 4;  // per-warpgroup wait verdicts
-  static constexpr int kOffBar = kOffDec + 2 * kEpiWarpgroups * 4;
+  static constexpr int kOffBar = kOffCtx + 2 * kGroupMaxRows * 4;
   // barriers: kv_full[8], kv_empty[8], raw_full[2], raw_empty[2], sc_full[SS],
   // sc_empty[SS], q_full, q_empty, w_full[2], w_empty[2], tm_full[2], tm_empty[2], mma_done
   static constexpr int kNumBars = 2 * kMaxKStages + 2 * kMaxRawStages + 2 * kScaleStages + 2 + 4 + 4 + 1;
@@ -189,29 +191,12 @@ struct Walk {
   }
 };
 
-// Warpgroup-wide wait: the leader lane waits on the mbarrier(s) (its
-// acquire makes the completed phase's data visible), then the warpgroup's
-// four warps meet at a hardware named barrier, which orders memory among
-// them and costs no issue slots while waiting.  The leader publishes its
-// verdict in decision[n & 1] before the barrier (n counts this warpgroup's
-// waits), so all four warps take the same branch: no warp can be left alone
-// at a named barrier, which has no timeout.  Up to three barriers are waited
-// in order (a zero address is skipped).  Returns false on timeout or abort.
-__device__ __forceinline__ bool wg_wait(uint32_t bar0, uint32_t par0, uint32_t bar1, uint32_t par1,
-                                        uint32_t bar2, uint32_t par2, bool leader,
-                                        uint32_t named_id, volatile int32_t* decision, int& n,
-                                        volatile int32_t* abort_flag, int32_t* status) {
-  const int slot = n & 1;
-  ++n;
-  if (leader) {
-    bool ok = true;
-    if (ok && bar0) ok = wait_or_abort(bar0, par0, abort_flag, status);
-    if (ok && bar1) ok = wait_or_abort(bar1, par1, abort_flag, status);
-    if (ok && bar2) ok = wait_or_abort(bar2, par2, abort_flag, status);
-    decision[slot] = ok ? 1 : 0;
-  }
-  named_bar_sync(named_id, 128);
-  return decision[slot] != 0;
+// Wait by every lane of a warp: each lane's own acquire orders its later
+// reads after the completed phase; the vote keeps the warp's control flow
+// uniform (false on timeout or abort).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag,
+                                          int32_t* status) {
+  return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag, status));
 }
 
 __device__ __forceinline__ float relu_f(uint32_t bits) { return fmaxf(__uint_as_float(bits), 0.0f); }
@@ -574,51 +559,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // =================================================== MMA issuer
-    if (lane == 0) {
-      // idesc for N = 64, 128, 192, 256 (1..4 pairs of one tile); the A/B
-      // format code 0 is e4m3 for kind::f8f6f4 and f16 for kind::f16
-      const uint32_t id1 = idesc(0, 0, 128, 64), id2 = idesc(0, 0, 128, 128);
-      const uint32_t id3 = idesc(0, 0, 128, 192), id4 = idesc(0, 0, 128, 256);
-      const uint32_t a_lo0 = sdesc_lo(s_kv), q_lo0 = sdesc_lo(s_q);
-      constexpr uint32_t kStageLo = L::kKStageBytes >> 4;
-      uint32_t it = 0, gi = 0, pos = 0;  // tiles, groups, pairs issued
-      bool ok = true;
-      while (ok && walk.next()) {
-        const int n = walk.n;
-        ok = wait_or_abort(bars.q_full, gi & 1, abort_flag, p.status);
+    // The whole warp walks the work, so every value feeding an MMA is
+    // warp-uniform; one elected lane issues the MMAs and commits.  Each MMA
+    // occupies the tensor unit for at least ~48 cycles whatever its N, so a
+    // tile's rows go out as few wide MMAs as the TMEM buffers allow.
+    const uint32_t id1 = idesc(0, 0, 128, 64), id2 = idesc(0, 0, 128, 128);
+    const uint32_t id3 = idesc(0, 0, 128, 192), id4 = idesc(0, 0, 128, 256);
+    // (format code 0 is e4m3 for kind::f8f6f4 and f16 for kind::f16)
+    const uint32_t a_lo0 = sdesc_lo(s_kv), q_lo0 = sdesc_lo(s_q);
+    constexpr uint32_t kStageLo = L::kKStageBytes >> 4;
+    const bool leader = elect_one();
+    uint32_t it = 0, gi = 0, pos = 0;  // tiles, groups, pairs issued
+    bool ok = true;
+    while (ok && walk.next()) {
+      const uint32_t n = static_cast<uint32_t>(walk.n);
+      ok = warp_wait(bars.q_full, gi & 1, abort_flag, p.status);
+      if (!ok) break;
+      for (int j = walk.j0; j < walk.j1; ++j, ++it) {
+        const uint32_t st = it & (kStages - 1);
+        ok = warp_wait(bars.kvf(st), (it / kStages) & 1, abort_flag, p.status);
         if (!ok) break;
-        for (int j = walk.j0; j < walk.j1; ++j, ++it) {
-          const uint32_t st = it & (kStages - 1);
-          ok = wait_or_abort(bars.kvf(st), (it / kStages) & 1, abort_flag, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t a_lo = a_lo0 + st * kStageLo;
-          int r = 0;
-          while (r < n) {
-            const uint32_t c = pos & (kBufPairs - 1);
-            const uint32_t k = pos / kBufPairs;
-            const uint32_t b = k & 1;
-            if (c == 0) {
-              ok = wait_or_abort(bars.te(b), ((k >> 1) & 1) ^ 1, abort_flag, p.status);
-              if (!ok) break;
-              tc_fence_after();
-            }
-            const int len = min(n - r, static_cast<int>(kBufPairs - c));
-            const uint32_t d_tmem = tmem + b * kBufCols + c * kPairCols;
-            const uint32_t id = len == 1 ? id1 : (len == 2 ? id2 : (len == 3 ? id3 : id4));
-            if constexpr (!kFp4) {
-              // K = 128 e4m3 in four 32-byte steps inside the swizzled row (+2 in the address field)
-              const uint32_t b_lo = q_lo0 + static_cast<uint32_t>(r) * (L::kQRowBytes >> 4);
+        tc_fence_after();
+        const uint32_t a_lo = a_lo0 + st * kStageLo;
+        uint32_t r = 0;
+        while (r < n) {
+          const uint32_t c = pos & (kBufPairs - 1);
+          const uint32_t k = pos / kBufPairs;
+          const uint32_t b = k & 1;
+          if (c == 0) {
+            ok = warp_wait(bars.te(b), ((k >> 1) & 1) ^ 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          const uint32_t len = min(n - r, kBufPairs - c);
+          const uint32_t d_tmem = tmem + b * kBufCols + c * kPairCols;
+          const uint32_t id = len == 1 ? id1 : (len == 2 ? id2 : (len == 3 ? id3 : id4));
+          if constexpr (!kFp4) {
+            // K = 128 e4m3 in four 32-byte steps inside the swizzled row (+2 in the address field)
+            const uint32_t b_lo = q_lo0 + r * (L::kQRowBytes >> 4);
+            if (leader) {
               mma_f8f6f4_w<false>(d_tmem, a_lo, kSdescHi, b_lo, kSdescHi, id);
               mma_f8f6f4_w<true>(d_tmem, a_lo + 2, kSdescHi, b_lo + 2, kSdescHi, id);
               mma_f8f6f4_w<true>(d_tmem, a_lo + 4, kSdescHi, b_lo + 4, kSdescHi, id);
               mma_f8f6f4_w<true>(d_tmem, a_lo + 6, kSdescHi, b_lo + 6, kSdescHi, id);
-            } else {
-              // K = 128 f16 in eight 16-element steps: two 64-element halves
-              // (separate swizzled blocks), four 32-byte steps inside each
-              constexpr uint32_t kAHalfLo = (kTileTokens * 128) >> 4;
-              constexpr uint32_t kBHalfLo = Lay<DSA_KV_FP4>::kQHalfBytes >> 4;
-              const uint32_t b_lo = q_lo0 + static_cast<uint32_t>(r) * ((kHeads * 128) >> 4);
+            }
+          } else {
+            // K = 128 f16 in eight 16-element steps: two 64-element halves
+            // (separate swizzled blocks), four 32-byte steps inside each
+            constexpr uint32_t kAHalfLo = (kTileTokens * 128) >> 4;
+            constexpr uint32_t kBHalfLo = Lay<DSA_KV_FP4>::kQHalfBytes >> 4;
+            const uint32_t b_lo = q_lo0 + r * ((kHeads * 128) >> 4);
+            if (leader) {
               mma_f16_w<false>(d_tmem, a_lo, kSdescHi, b_lo, kSdescHi, id);
 #pragma unroll
               for (int kk = 1; kk < 8; ++kk) {
@@ -627,67 +618,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_f16_w<true>(d_tmem, a_lo + ao, kSdescHi, b_lo + bo, kSdescHi, id);
               }
             }
-            r += len;
-            pos += len;
-            if ((pos & (kBufPairs - 1)) == 0) mma_commit(bars.tf(b));
           }
-          if (!ok) break;
-          mma_commit(bars.kve(st));
+          r += len;
+          pos += len;
+          if ((pos & (kBufPairs - 1)) == 0 && leader) mma_commit(bars.tf(b));
         }
         if (!ok) break;
-        mma_commit(bars.q_empty);
-        ++gi;
+        if (leader) mma_commit(bars.kve(st));
       }
+      if (!ok) break;
+      if (leader) mma_commit(bars.q_empty);
+      ++gi;
+    }
+    if (leader) {
       if (ok && (pos & (kBufPairs - 1)) != 0) mma_commit(bars.tf((pos / kBufPairs) & 1));  // last, partial buffer
       // No MMA may still be writing TMEM when it is freed.
       mma_commit(bars.mma_done);
       wait_drain(bars.mma_done, 0);
     }
+    __syncwarp();
   } else if (warp >= 4) {
     // =================================================== epilogue
-    const int wg = (warp - 4) >> 2;  // takes pair wg of every TMEM buffer
+    // Pair position pos + r belongs to warpgroup (pos + r) mod 4, so this
+    // warp visits r = (wg - pos) mod 4, +4, ... of each tile.
+    const uint32_t wg = static_cast<uint32_t>(warp - 4) >> 2;
     const int quarter = warp & 3;    // TMEM lanes this warp may read
     const int tok = quarter * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const bool leader = ((warp - 4) & 3) == 0 && lane == 0;
-    const uint32_t named_id = 1 + wg;  // named barrier of this warpgroup
-    volatile int32_t* decision = reinterpret_cast<volatile int32_t*>(smem + L::kOffDec) + 2 * wg;
-    int nwait = 0;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + wg * kPairCols;
     float* out_f = static_cast<float*>(p.logits);
     __nv_bfloat16* out_h = static_cast<__nv_bfloat16*>(p.logits);
-    int it = 0, gi = 0, pos = 0;
+    uint32_t it = 0, gi = 0, pos = 0;  // tiles, groups, pairs seen
     bool ok = true;
     while (ok && walk.next()) {
       const int r0 = walk.r0, n = walk.n;
-      const int wb = gi & 1;
-      ok = wg_wait(bars.wf(wb), (gi >> 1) & 1, 0, 0, 0, 0, leader, named_id, decision, nwait,
-                   abort_flag, p.status);
+      const uint32_t wb = gi & 1;
+      ok = warp_wait(bars.wf(wb), (gi >> 1) & 1, abort_flag, p.status);
       if (!ok) break;
       const int lim = static_cast<int>(min(static_cast<int64_t>(walk.npages) * kPageTokens, p.logits_stride));
+      const float* w_grp = w_sm + wb * kWBufFloats;
+      const int32_t* ctx_grp = ctx_sm + wb * kGroupMaxRows;
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
-        const int ss = it % kScaleStages;
-        ok = wg_wait(bars.scf(ss), (it / kScaleStages) & 1, 0, 0, 0, 0, leader, named_id, decision,
-                     nwait, abort_flag, p.status);
+        const uint32_t ss = it & (kScaleStages - 1);
+        ok = warp_wait(bars.scf(ss), (it / kScaleStages) & 1, abort_flag, p.status);
         if (!ok) break;
         const float kscale = scale_sm[ss * kScaleStageFloats + tok];
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.sce(ss));
         const int scol = j * kTileTokens + tok;
-        for (int r = 0; r < n; ++r, ++pos) {
-          if ((pos % kBufPairs) != wg) continue;
-          const int k = pos / kBufPairs;
-          const int b = k & 1;
-          ok = wg_wait(bars.tf(b), (k >> 1) & 1, 0, 0, 0, 0, leader, named_id, decision, nwait,
-                       abort_flag, p.status);
+        for (uint32_t r = (wg - pos) & (kBufPairs - 1); r < static_cast<uint32_t>(n); r += kBufPairs) {
+          const uint32_t k = (pos + r) / kBufPairs;
+          const uint32_t b = k & 1;
+          ok = warp_wait(bars.tf(b), (k >> 1) & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
           uint32_t v[64];
-          tmem_ld_x64(t_lane + static_cast<uint32_t>(b * kBufCols + wg * kPairCols), v);
+          tmem_ld_x64(t_lane + b * kBufCols, v);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bars.te(b));
-          const float4* wr = reinterpret_cast<const float4*>(w_sm + wb * kWBufFloats + r * kHeads);
+          const float4* wr = reinterpret_cast<const float4*>(w_grp + r * kHeads);
           float2 c0 = make_float2(0.f, 0.f), c1 = c0, c2 = c0, c3 = c0;
 #pragma unroll
           for (int h = 0; h < kHeads; h += 8) {
@@ -699,15 +689,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             c3 = __ffma2_rn(make_float2(relu_f(v[h + 6]), relu_f(v[h + 7])), make_float2(wc.z, wc.w), c3);
           }
           const float acc = ((c0.x + c0.y) + (c1.x + c1.y)) + ((c2.x + c2.y) + (c3.x + c3.y));
-          const int L = ctx_sm[wb * kGroupMaxRows + r];
+          const int L = ctx_grp[r];
           const float logit = (scol < L) ? kscale * acc : -INFINITY;
           if (scol < lim) {
-            const int64_t off = static_cast<int64_t>(r0 + r) * p.logits_stride + scol;
+            const int64_t off = static_cast<int64_t>(r0 + static_cast<int>(r)) * p.logits_stride + scol;
             if (p.logits_bf16) out_h[off] = __float2bfloat16_rn(logit);
             else out_f[off] = logit;
           }
         }
         if (!ok) break;
+        pos += static_cast<uint32_t>(n);
       }
       if (!ok) break;
       __syncwarp();

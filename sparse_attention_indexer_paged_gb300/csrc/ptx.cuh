@@ -99,10 +99,15 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-// Named barrier over `nthreads` threads (a multiple of 32); hardware wait,
-// no polling, with CTA-scope memory ordering among the participants.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+// One lane of the (fully converged) warp is chosen; true on that lane only.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // 16-byte asynchronous global -> shared copy (completes in the background;
