@@ -33,7 +33,8 @@ ORACLE_ERR_STRIDE = 6
 # the schedule rule's constants (the metadata call's tile and grouping sizes)
 TILE_TOKENS = 128
 GROUP_MAX_ROWS = 8
-BASE_WEIGHT = 4
+TILE_WEIGHT = 6
+ROW_WEIGHT = 5
 
 
 def build(force: bool = False) -> str:
@@ -71,7 +72,7 @@ def lib():
             L.oracle_paged_mqa_logits.restype = ctypes.c_int
             L.oracle_top_k_per_row.argtypes = [P, i64, P, P, i32, i32, P, i64, i32]
             L.oracle_top_k_per_row.restype = ctypes.c_int
-            L.oracle_schedule.argtypes = [P, P, i32, i32, i32, i32, i32, P]
+            L.oracle_schedule.argtypes = [P, P, i32, i32, i32, i32, i32, i32, P]
             L.oracle_schedule.restype = ctypes.c_int
             L.oracle_schedule_words.argtypes = [i32, i32]
             L.oracle_schedule_words.restype = i64
@@ -168,14 +169,14 @@ def schedule_words(num_sms: int, num_rows: int) -> int:
 
 
 def schedule(context_lens, indices, num_sms, tile_tokens=TILE_TOKENS,
-             group_max_rows=GROUP_MAX_ROWS, base_weight=BASE_WEIGHT):
+             group_max_rows=GROUP_MAX_ROWS, tile_weight=TILE_WEIGHT, row_weight=ROW_WEIGHT):
     """The schedule words the metadata call must produce (int32 array)."""
     cl = _np(context_lens, np.int32)
     ind = _np(indices, np.int32)
     T = cl.shape[0]
     out = np.zeros(schedule_words(num_sms, T), dtype=np.int32)
     st = lib().oracle_schedule(_ptr(cl), _ptr(ind), T, int(num_sms), int(tile_tokens),
-                               int(group_max_rows), int(base_weight), _ptr(out))
+                               int(group_max_rows), int(tile_weight), int(row_weight), _ptr(out))
     if st != ORACLE_OK:
         raise OracleError(st, "schedule")
     return out

@@ -348,7 +348,7 @@ int oracle_top_k_per_row(const double* scores, int64_t stride, const int32_t* ro
 //              group_max_rows rows;
 //   3. group g: n_g rows, Lmax_g = max causal limit of its rows (negative
 //      counts as 0), tiles_g = ceil(Lmax_g / tile_tokens), every tile weighs
-//      base_weight + n_g;
+//      tile_weight + row_weight * n_g;
 //   4. units are the (group, tile) pairs in group-major order; P(u) = total
 //      weight of the units before u, W = P(U);
 //   5. SM i (0 <= i <= num_sms) starts at the smallest u with
@@ -363,9 +363,10 @@ int oracle_top_k_per_row(const double* scores, int64_t stride, const int32_t* ro
 // ---------------------------------------------------------------------------
 int oracle_schedule(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
                     int32_t num_sms, int32_t tile_tokens, int32_t group_max_rows,
-                    int32_t base_weight, int32_t* out) {
+                    int32_t tile_weight, int32_t row_weight, int32_t* out) {
   if (num_rows < 0 || num_sms <= 0 || tile_tokens <= 0 || group_max_rows <= 0 ||
-      base_weight < 1 || !out || (num_rows > 0 && !context_lens))
+      tile_weight < 0 || row_weight < 0 || tile_weight + row_weight < 1 || !out ||
+      (num_rows > 0 && !context_lens))
     return ORACLE_ERR_ARG;
   std::vector<int32_t> group_row_start;
   for (int t = 0; t < num_rows; ++t) {
@@ -384,7 +385,7 @@ int oracle_schedule(const int32_t* context_lens, const int32_t* indices, int32_t
     for (int t = group_row_start[g]; t < group_row_start[g + 1]; ++t)
       lmax = std::max<int64_t>(lmax, context_lens[t]);
     tiles[g] = (lmax + tile_tokens - 1) / tile_tokens;
-    weight[g] = base_weight + (group_row_start[g + 1] - group_row_start[g]);
+    weight[g] = tile_weight + static_cast<int64_t>(row_weight) * (group_row_start[g + 1] - group_row_start[g]);
   }
   // enumerate units one by one with their prefix weights
   std::vector<int64_t> unit_prefix;  // P(u) for u = 0..U

@@ -15,10 +15,13 @@ constexpr int kPageTokens = DSA_BLOCK_KV;   // 64 tokens per page
 
 // Schedule rule: a tile is two pages (128 keys, the M of one MMA); runs of
 // equal request ids are cut into groups of at most kGroupMaxRows rows; every
-// tile of group g weighs kBaseWeight + rows(g).
+// tile of group g weighs kTileWeight + kRowWeight * rows(g), the measured
+// ratio of a tile's fixed cost (K stream, MMA issue) to the cost of each
+// (tile, row) pair it carries (MMA columns, epilogue).
 constexpr int kTileTokens = 128;
 constexpr int kGroupMaxRows = 8;
-constexpr int kBaseWeight = 4;
+constexpr int kTileWeight = 6;
+constexpr int kRowWeight = 5;
 constexpr int32_t kScheduleMagic = 0x44534131;
 constexpr int kScheduleHeaderWords = 8;
 

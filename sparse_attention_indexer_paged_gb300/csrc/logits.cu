@@ -30,11 +30,13 @@
 // the epilogue runs.
 //
 // Warp roles (640 threads):
-//   warp 0      TMA producer: the group's Q rows, then per tile the K pages
-//               (3-D tensor map over the pool, page id from the block table).
+//   warp 0      K producer: per tile the two K pages (3-D tensor map over the
+//               pool, page id from the block table); runs ahead across groups.
 //   warp 1      MMA issuer and TMEM owner (512 columns): the whole warp walks
 //               the work with warp-uniform values; one elected lane issues.
-//   warp 2      head weights and causal limits of each group (double buffered).
+//               For FP8 keys it also loads each group's Q rows once the
+//               previous group's MMAs have completed.
+//   warp 2      per group: head weights and causal limits (double buffered).
 //   warp 3      key scales, up to kScaleStages tiles ahead.
 //   warps 4-19  four epilogue warpgroups: tcgen05.ld of a pair, relu,
 //               packed-fp32 FMA with the head weights, key scale, causal
@@ -110,6 +112,8 @@ template <int kFmt> struct Smem : Lay<kFmt> {
   static_assert(kBytes <= 232448, "over the per-CTA shared memory limit");
 };
 static_assert((kBufPairs & (kBufPairs - 1)) == 0, "power of two");
+static_assert(kFp4AHalfLo == (kTileTokens * 128) >> 4 && kFp4BHalfLo == Lay<DSA_KV_FP4>::kQHalfBytes >> 4,
+              "f16 operand halves as laid out by the dequantising warp");
 
 struct Params {
   const uint8_t* q;
@@ -146,7 +150,10 @@ struct Bars {
 };
 
 // The CTA's walk over its units: groups in order, and the tiles [j0, j1) of
-// each group that belong to this CTA.  Every role runs the same walk.
+// each group that belong to this CTA.  Every role runs the same walk with all
+// 32 lanes of its warp: the lanes search the group table 32 entries at a
+// time and read a group's causal limits in parallel, so a warp reaches its
+// first unit after a few dependent loads instead of a serial search.
 struct Walk {
   const int32_t* grs;
   const int32_t* gus;
@@ -154,9 +161,10 @@ struct Walk {
   int G, T, u, u_end, g;
   // current group
   int r0, n, npages, j0, j1;
+  int32_t lane_ctx;  // causal limit of row r0 + lane (lanes below n)
 
   __device__ void start(const int32_t* grs_, const int32_t* gus_, const int32_t* ctx_, int G_,
-                        int T_, int u0, int u1) {
+                        int T_, int u0, int u1, int lane) {
     T = T_;
     grs = grs_;
     gus = gus_;
@@ -164,28 +172,36 @@ struct Walk {
     G = G_;
     u = u0;
     u_end = u1;
-    // largest g with gus[g] <= u
-    int lo = 0, hi = G - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (gus[mid] <= u) lo = mid; else hi = mid - 1;
+    // largest g in [0, G) with gus[g] <= u (gus is non-decreasing, gus[0] = 0):
+    // each round narrows [lo, hi) 32-fold, keeping gus[lo] <= u
+    int lo = 0, hi = G;
+    while (hi - lo > 1) {
+      const int step = (hi - lo + 31) >> 5;
+      const int idx = lo + lane * step;
+      const bool le = idx < hi && __ldg(gus + idx) <= u;
+      const uint32_t m = __ballot_sync(0xffffffffu, le);
+      lo += (31 - __clz(m | 1u)) * step;
+      hi = min(hi, lo + step);
     }
     g = lo;
   }
 
   // Loads the next group that holds units of this CTA; false when done.
-  __device__ bool next() {
-    while (u < u_end && g < G && gus[g + 1] <= u) ++g;
+  __device__ bool next(int lane) {
+    while (u < u_end && g < G && __ldg(gus + g + 1) <= u) ++g;
     if (u >= u_end || g >= G) return false;
-    const int gu0 = gus[g];
-    r0 = grs[g];
-    n = grs[g + 1] - r0;
+    const int gu0 = __ldg(gus + g), gu1 = __ldg(gus + g + 1);
+    r0 = __ldg(grs + g);
+    n = __ldg(grs + g + 1) - r0;
     if (r0 < 0 || n <= 0 || n > kGroupMaxRows || r0 + n > T) return false;
-    int lmax = 0;
-    for (int t = r0; t < r0 + n; ++t) lmax = max(lmax, ctx[t]);
+    lane_ctx = lane < n ? __ldg(ctx + r0 + lane) : 0;
+    int lmax = lane_ctx;
+#pragma unroll
+    for (int o = 4; o; o >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));  // lanes 0..7
+    lmax = __shfl_sync(0xffffffffu, lmax, 0);
     npages = (lmax + kPageTokens - 1) / kPageTokens;
     j0 = u - gu0;
-    j1 = min(gus[g + 1], u_end) - gu0;
+    j1 = min(gu1, u_end) - gu0;
     u = gu0 + j1;
     return true;
   }
@@ -294,38 +310,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* ctx_sm = reinterpret_cast<int32_t*>(smem + L::kOffCtx);
 
   Walk walk;
-  walk.start(grs, gus, p.ctx, G, T, u0, u1);
+  walk.start(grs, gus, p.ctx, G, T, u0, u1, lane);
 
   if (warp == 0) {
-    // =================================================== producer: K pages (and FP8 Q)
+    // =================================================== producer: K pages
     // The whole warp walks the work: block ids are fetched 32 at a time with
     // one coalesced load and handed out by shuffle; lane 0 waits and issues.
+    // Nothing here waits on a group boundary, so the ring runs ahead across
+    // groups.
     if constexpr (!kFp4) {
-      if (lane == 0) {
-        prefetch_tensormap(&tm_q);
-        prefetch_tensormap(&tm_kv);
-      }
+      if (lane == 0) prefetch_tensormap(&tm_kv);
     }
     const uint64_t pol_stream = policy_evict_first();  // K pages are read once
-    const uint64_t pol_keep = policy_evict_last();      // q
     constexpr int kRing = kFp4 ? L::kRawStages : kStages;
-    int it = 0, nq = 0;  // tiles and Q groups issued
+    int it = 0;  // tiles issued
     bool ok = true;
-    while (ok && walk.next()) {
+    while (ok && walk.next(lane)) {
       const int r0 = walk.r0, n = walk.n;
-      if constexpr (!kFp4) {
-        if (lane == 0) {
-          ok = wait_or_abort(bars.q_empty, (nq & 1) ^ 1, abort_flag, p.status);
-          if (ok) {
-            mbar_arrive_expect_tx(bars.q_full, static_cast<uint32_t>(n * L::kQRowBytes));
-            for (int r = 0; r < n; ++r)
-              tma_load_2d(s_q + r * L::kQRowBytes, &tm_q, 0, (r0 + r) * kHeads, bars.q_full, pol_keep);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        ++nq;
-      }
       const int32_t* bt_row = p.block_table + static_cast<int64_t>(r0 + n - 1) * p.bt_stride;
       int32_t lane_blk = -1;  // block id of page (pg_base + lane)
       int pg_base = -32;
@@ -381,7 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int i = max(0, it - kRing); i < it; ++i)
         wait_drain(kFp4 ? bars.rwf(i % kRing) : bars.kvf(i % kRing), (i / kRing) & 1);
-      if (nq > 0) wait_drain(bars.q_full, (nq - 1) & 1);
     }
   } else if (warp == 3) {
     if constexpr (!kFp4) {
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_stream = policy_evict_first();
       int it = 0;
       bool ok = true;
-      while (ok && walk.next()) {
+      while (ok && walk.next(lane)) {
         const int32_t* bt_row = p.block_table + static_cast<int64_t>(walk.r0 + walk.n - 1) * p.bt_stride;
         int32_t lane_blk = -1;
         int pg_base = -32;
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0, nq = 0;
       bool ok = true;
       const uint32_t q_half = static_cast<uint32_t>(Lay<DSA_KV_FP4>::kQHalfBytes);
-      while (ok && walk.next()) {
+      while (ok && walk.next(lane)) {
         const int r0 = walk.r0, n = walk.n;
         int okq = 1;
         if (lane == 0) okq = wait_or_abort(bars.q_empty, (nq & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
@@ -536,43 +536,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 2) {
-    // =================================================== weights + causal limits
+    // =================================================== per group: weights and causal limits
     // A separate producer: the epilogue may hold a group's weights until TMEM
     // buffers that also carry later groups' pairs complete, so these loads
-    // must never sit in front of the K and Q loads.
-    if (lane == 0) {
-      const uint64_t pol_keep = policy_evict_last();
-      int nw = 0;
-      bool ok = true;
-      while (ok && walk.next()) {
-        const int r0 = walk.r0, n = walk.n;
-        const int wb = nw & 1;
-        ok = wait_or_abort(bars.we(wb), ((nw >> 1) & 1) ^ 1, abort_flag, p.status);
-        if (!ok) break;
-        for (int r = 0; r < n; ++r) ctx_sm[wb * kGroupMaxRows + r] = p.ctx[r0 + r];
+    // must never sit in front of the Q and K loads.
+    const uint64_t pol_keep = policy_evict_last();
+    int nw = 0;
+    bool ok = true;
+    while (ok && walk.next(lane)) {
+      const int r0 = walk.r0, n = walk.n;
+      const int wb = nw & 1;
+      ok = warp_wait(bars.we(wb), ((nw >> 1) & 1) ^ 1, abort_flag, p.status);
+      if (!ok) break;
+      // lanes below n write their row's causal limit; the fence and the warp
+      // barrier order those writes before lane 0's release on wf
+      if (lane < n) ctx_sm[wb * kGroupMaxRows + lane] = walk.lane_ctx;
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) {
         mbar_arrive_expect_tx(bars.wf(wb), static_cast<uint32_t>(n * kHeads * 4));
         bulk_load(s_w + wb * kWBufFloats * 4, p.weights + static_cast<int64_t>(r0) * kHeads,
                   n * kHeads * 4, bars.wf(wb), pol_keep);
-        ++nw;
       }
-      if (nw > 0) wait_drain(bars.wf((nw - 1) & 1), ((nw - 1) >> 1) & 1);
+      ++nw;
     }
+    if (lane == 0 && nw > 0) wait_drain(bars.wf((nw - 1) & 1), ((nw - 1) >> 1) & 1);
   } else if (warp == 1) {
     // =================================================== MMA issuer
     // The whole warp walks the work, so every value feeding an MMA is
     // warp-uniform; one elected lane issues the MMAs and commits.  Each MMA
     // occupies the tensor unit for at least ~48 cycles whatever its N, so a
     // tile's rows go out as few wide MMAs as the TMEM buffers allow.
-    const uint32_t id1 = idesc(0, 0, 128, 64), id2 = idesc(0, 0, 128, 128);
-    const uint32_t id3 = idesc(0, 0, 128, 192), id4 = idesc(0, 0, 128, 256);
-    // (format code 0 is e4m3 for kind::f8f6f4 and f16 for kind::f16)
+    // instruction descriptor for N = 64 * len: the N field (N >> 3 at bit
+    // 17) grows by len << 20; format code 0 is e4m3 for kind::f8f6f4 and f16
+    // for kind::f16
+    const uint32_t id_base = idesc(0, 0, 128, 0);
     const uint32_t a_lo0 = sdesc_lo(s_kv), q_lo0 = sdesc_lo(s_q);
     constexpr uint32_t kStageLo = L::kKStageBytes >> 4;
-    const bool leader = elect_one();
-    uint32_t it = 0, gi = 0, pos = 0;  // tiles, groups, pairs issued
+    constexpr uint32_t kQRowLo = (kFp4 ? kHeads * 128 : kHeads * kHeadDim) >> 4;  // one q row (64 heads) of B
+    const uint32_t issue = elect_one() ? 1u : 0u;
+    const bool leader = issue != 0;
+    if constexpr (!kFp4) {
+      if (leader) prefetch_tensormap(&tm_q);
+    }
+    const uint64_t pol_keep = policy_evict_last();  // q
+    uint32_t it = 0, gi = 0, pos = 0, nq = 0;  // tiles, groups, pairs, Q loads issued
     bool ok = true;
-    while (ok && walk.next()) {
+    while (ok && walk.next(lane)) {
       const uint32_t n = static_cast<uint32_t>(walk.n);
+      if constexpr (!kFp4) {
+        // Q buffer free once the previous group's MMAs have completed
+        ok = warp_wait(bars.q_empty, (gi & 1) ^ 1, abort_flag, p.status);
+        if (!ok) break;
+        if (leader) {
+          mbar_arrive_expect_tx(bars.q_full, n * static_cast<uint32_t>(L::kQRowBytes));
+          for (uint32_t r = 0; r < n; ++r)
+            tma_load_2d(s_q + r * L::kQRowBytes, &tm_q, 0, (walk.r0 + static_cast<int>(r)) * kHeads,
+                        bars.q_full, pol_keep);
+        }
+        ++nq;
+      }
       ok = warp_wait(bars.q_full, gi & 1, abort_flag, p.status);
       if (!ok) break;
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
@@ -581,8 +604,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t a_lo = a_lo0 + st * kStageLo;
-        uint32_t r = 0;
-        while (r < n) {
+        uint32_t b_lo = q_lo0;
+        uint32_t left = n;
+        do {  // the tile's rows, cut where a TMEM buffer ends
           const uint32_t c = pos & (kBufPairs - 1);
           const uint32_t k = pos / kBufPairs;
           const uint32_t b = k & 1;
@@ -591,47 +615,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
           }
-          const uint32_t len = min(n - r, kBufPairs - c);
+          const uint32_t len = min(left, kBufPairs - c);
           const uint32_t d_tmem = tmem + b * kBufCols + c * kPairCols;
-          const uint32_t id = len == 1 ? id1 : (len == 2 ? id2 : (len == 3 ? id3 : id4));
-          if constexpr (!kFp4) {
-            // K = 128 e4m3 in four 32-byte steps inside the swizzled row (+2 in the address field)
-            const uint32_t b_lo = q_lo0 + r * (L::kQRowBytes >> 4);
-            if (leader) {
-              mma_f8f6f4_w<false>(d_tmem, a_lo, kSdescHi, b_lo, kSdescHi, id);
-              mma_f8f6f4_w<true>(d_tmem, a_lo + 2, kSdescHi, b_lo + 2, kSdescHi, id);
-              mma_f8f6f4_w<true>(d_tmem, a_lo + 4, kSdescHi, b_lo + 4, kSdescHi, id);
-              mma_f8f6f4_w<true>(d_tmem, a_lo + 6, kSdescHi, b_lo + 6, kSdescHi, id);
-            }
-          } else {
-            // K = 128 f16 in eight 16-element steps: two 64-element halves
-            // (separate swizzled blocks), four 32-byte steps inside each
-            constexpr uint32_t kAHalfLo = (kTileTokens * 128) >> 4;
-            constexpr uint32_t kBHalfLo = Lay<DSA_KV_FP4>::kQHalfBytes >> 4;
-            const uint32_t b_lo = q_lo0 + r * ((kHeads * 128) >> 4);
-            if (leader) {
-              mma_f16_w<false>(d_tmem, a_lo, kSdescHi, b_lo, kSdescHi, id);
-#pragma unroll
-              for (int kk = 1; kk < 8; ++kk) {
-                const uint32_t ao = (kk >> 2) * kAHalfLo + (kk & 3) * 2;
-                const uint32_t bo = (kk >> 2) * kBHalfLo + (kk & 3) * 2;
-                mma_f16_w<true>(d_tmem, a_lo + ao, kSdescHi, b_lo + bo, kSdescHi, id);
-              }
-            }
-          }
-          r += len;
+          if constexpr (!kFp4) mma_fp8_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20));
+          else mma_f16_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20));
+          left -= len;
           pos += len;
-          if ((pos & (kBufPairs - 1)) == 0 && leader) mma_commit(bars.tf(b));
-        }
+          b_lo += len * kQRowLo;
+          if ((pos & (kBufPairs - 1)) == 0) mma_commit_if(issue, bars.tf(b));
+        } while (left != 0);
         if (!ok) break;
-        if (leader) mma_commit(bars.kve(st));
+        mma_commit_if(issue, bars.kve(st));
       }
       if (!ok) break;
-      if (leader) mma_commit(bars.q_empty);
+      mma_commit_if(issue, bars.q_empty);
       ++gi;
     }
     if (leader) {
       if (ok && (pos & (kBufPairs - 1)) != 0) mma_commit(bars.tf((pos / kBufPairs) & 1));  // last, partial buffer
+      // every Q copy has landed before the CTA may exit
+      if (nq > 0) wait_drain(bars.q_full, (nq - 1) & 1);
       // No MMA may still be writing TMEM when it is freed.
       mma_commit(bars.mma_done);
       wait_drain(bars.mma_done, 0);
@@ -649,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __nv_bfloat16* out_h = static_cast<__nv_bfloat16*>(p.logits);
     uint32_t it = 0, gi = 0, pos = 0;  // tiles, groups, pairs seen
     bool ok = true;
-    while (ok && walk.next()) {
+    while (ok && walk.next(lane)) {
       const int r0 = walk.r0, n = walk.n;
       const uint32_t wb = gi & 1;
       ok = warp_wait(bars.wf(wb), (gi >> 1) & 1, abort_flag, p.status);

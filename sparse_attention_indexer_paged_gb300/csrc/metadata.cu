@@ -11,7 +11,7 @@
 //           request ids, or when kGroupMaxRows rows of its run precede it in
 //           the current group;
 //   pass 2  tiles per group = ceil(max L_t / 128) and their prefix sums;
-//   pass 3  prefix weights (tile weight = kBaseWeight + rows) and, for every
+//   pass 3  prefix weights (tile weight = kTileWeight + kRowWeight * rows) and, for every
 //           SM i, the first tile u with P(u) * num_sms >= i * W (exact
 //           integer arithmetic).
 #include "common.cuh"
@@ -87,7 +87,7 @@ __device__ __forceinline__ GroupInfo group_info(const int32_t* ctx, const int32_
   for (int t = r0; t < r1; ++t) lmax = max(lmax, ctx[t]);
   GroupInfo gi;
   gi.tiles = (lmax + kTileTokens - 1) / kTileTokens;
-  gi.weight = kBaseWeight + (r1 - r0);
+  gi.weight = kTileWeight + kRowWeight * (r1 - r0);
   return gi;
 }
 

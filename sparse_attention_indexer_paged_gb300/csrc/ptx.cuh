@@ -257,6 +257,82 @@ __device__ __forceinline__ void mma_f16_w(uint32_t d_tmem, uint32_t a_lo, uint32
       : "memory");
 }
 
+// A 128-deep contraction as one block of MMAs into d_tmem (the first step
+// overwrites, the rest accumulate); only threads with `issue` set issue it
+// (one elected lane of the MMA warp).  K-major operands with the 128-byte
+// swizzle: inside a 128-byte row a 32-byte K step is +2 in the descriptor's
+// address field.
+//   e4m3 (kind::f8f6f4): four K = 32 steps inside one 128-byte row.
+__device__ __forceinline__ void mma_fp8_k128(uint32_t issue, uint32_t d_tmem, uint32_t a_lo,
+                                             uint32_t b_lo, uint32_t hi, uint32_t idesc_v) {
+  asm volatile(
+      "{\n\t.reg .pred p, f, t;\n\t.reg .b64 da, db;\n\t.reg .b32 al, bl;\n\t"
+      "setp.ne.b32 p, %0, 0;\n\t"
+      "setp.ne.b32 f, %4, %4;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "mov.b64 da, {%2, %4};\n\tmov.b64 db, {%3, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%1], da, db, %5, f;\n\t"
+      "add.u32 al, %2, 2;\n\tadd.u32 bl, %3, 2;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%1], da, db, %5, t;\n\t"
+      "add.u32 al, %2, 4;\n\tadd.u32 bl, %3, 4;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%1], da, db, %5, t;\n\t"
+      "add.u32 al, %2, 6;\n\tadd.u32 bl, %3, 6;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%1], da, db, %5, t;\n\t}" ::"r"(issue),
+      "r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc_v)
+      : "memory");
+}
+
+//   f16 (kind::f16): eight K = 16 steps; elements 0-63 and 64-127 sit in two
+//   separate swizzled blocks (the A block of a 128-token tile is 16 KB, the B
+//   block of the Q rows is kFp4QHalfBytes), four steps inside each.
+constexpr uint32_t kFp4AHalfLo = (128 * 128) >> 4;
+constexpr uint32_t kFp4BHalfLo = (8 * 64 * 128) >> 4;
+__device__ __forceinline__ void mma_f16_k128(uint32_t issue, uint32_t d_tmem, uint32_t a_lo,
+                                             uint32_t b_lo, uint32_t hi, uint32_t idesc_v) {
+  const uint32_t a2 = a_lo + kFp4AHalfLo, b2 = b_lo + kFp4BHalfLo;
+  asm volatile(
+      "{\n\t.reg .pred p, f, t;\n\t.reg .b64 da, db;\n\t.reg .b32 al, bl;\n\t"
+      "setp.ne.b32 p, %0, 0;\n\t"
+      "setp.ne.b32 f, %4, %4;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "mov.b64 da, {%2, %4};\n\tmov.b64 db, {%3, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %5, f;\n\t"
+      "add.u32 al, %2, 2;\n\tadd.u32 bl, %3, 2;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %5, t;\n\t"
+      "add.u32 al, %2, 4;\n\tadd.u32 bl, %3, 4;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %5, t;\n\t"
+      "add.u32 al, %2, 6;\n\tadd.u32 bl, %3, 6;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %5, t;\n\t"
+      "mov.b64 da, {%6, %4};\n\tmov.b64 db, {%7, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %5, t;\n\t"
+      "add.u32 al, %6, 2;\n\tadd.u32 bl, %7, 2;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %5, t;\n\t"
+      "add.u32 al, %6, 4;\n\tadd.u32 bl, %7, 4;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %5, t;\n\t"
+      "add.u32 al, %6, 6;\n\tadd.u32 bl, %7, 6;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], da, db, %5, t;\n\t}" ::"r"(issue),
+      "r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc_v), "r"(a2), "r"(b2)
+      : "memory");
+}
+
+// tcgen05.commit by the threads with `issue` set.
+__device__ __forceinline__ void mma_commit_if(uint32_t issue, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::"r"(issue),
+      "r"(bar)
+      : "memory");
+}
+
 // Orders this thread's shared-memory writes before later async-proxy reads
 // (tcgen05.mma operands) that are ordered after it by an mbarrier.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -353,7 +353,7 @@ def _schedule_props(lens, ids, S):
     assert sm[0] == 0 and sm[S] == U and np.all(np.diff(sm) >= 0)
     unit_w = []
     for g in range(G):
-        unit_w += [4 + (grs[g + 1] - grs[g])] * int(gus[g + 1] - gus[g])
+        unit_w += [oracle.TILE_WEIGHT + oracle.ROW_WEIGHT * (grs[g + 1] - grs[g])] * int(gus[g + 1] - gus[g])
     unit_w = np.array(unit_w, dtype=np.int64)
     Wt = int(unit_w.sum())
     if U:
