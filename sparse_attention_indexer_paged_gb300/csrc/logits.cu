@@ -128,7 +128,6 @@ struct Params {
   const int32_t* schedule;
   int32_t num_sms;
   void* logits;
-  int32_t logits_bf16;
   int64_t logits_stride;
   int32_t num_rows;
   int32_t* status;
@@ -217,7 +216,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 __device__ __forceinline__ float relu_f(uint32_t bits) { return fmaxf(__uint_as_float(bits), 0.0f); }
 
-template <int kFmt>
+__device__ __forceinline__ void store_logit(float* dst, float v) { *dst = v; }
+__device__ __forceinline__ void store_logit(__nv_bfloat16* dst, float v) { *dst = __float2bfloat16_rn(v); }
+
+template <int kFmt, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                   const Params p) {
@@ -643,23 +645,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4) {
     // =================================================== epilogue
     // Pair position pos + r belongs to warpgroup (pos + r) mod 4, so this
-    // warp visits r = (wg - pos) mod 4, +4, ... of each tile.
+    // warp visits r = (wg - pos) mod 4, +4, ... of each tile, and its m-th
+    // pair is the one it takes from fill m of the TMEM buffers: buffer m & 1,
+    // phase m >> 1.
+    //   sum_h w_h relu(x_h) = (sum_h w_h x_h + sum_h w_h |x_h|) / 2
+    // so the head reduction is 64 packed FMAs (the |x| is an operand
+    // modifier) instead of 64 max plus 32 packed FMAs.
     const uint32_t wg = static_cast<uint32_t>(warp - 4) >> 2;
     const int quarter = warp & 3;    // TMEM lanes this warp may read
     const int tok = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + wg * kPairCols;
-    float* out_f = static_cast<float*>(p.logits);
-    __nv_bfloat16* out_h = static_cast<__nv_bfloat16*>(p.logits);
-    uint32_t it = 0, gi = 0, pos = 0;  // tiles, groups, pairs seen
+    OutT* const out = static_cast<OutT*>(p.logits);
+    uint32_t it = 0, gi = 0, pos = 0, m = 0;  // tiles, groups, pairs seen; own pairs taken
     bool ok = true;
     while (ok && walk.next(lane)) {
-      const int r0 = walk.r0, n = walk.n;
+      const int n = walk.n;
       const uint32_t wb = gi & 1;
       ok = warp_wait(bars.wf(wb), (gi >> 1) & 1, abort_flag, p.status);
       if (!ok) break;
       const int lim = static_cast<int>(min(static_cast<int64_t>(walk.npages) * kPageTokens, p.logits_stride));
       const float* w_grp = w_sm + wb * kWBufFloats;
       const int32_t* ctx_grp = ctx_sm + wb * kGroupMaxRows;
+      OutT* const out_grp = out + static_cast<int64_t>(walk.r0) * p.logits_stride;
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
         const uint32_t ss = it & (kScaleStages - 1);
         ok = warp_wait(bars.scf(ss), (it / kScaleStages) & 1, abort_flag, p.status);
@@ -668,10 +675,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.sce(ss));
         const int scol = j * kTileTokens + tok;
-        for (uint32_t r = (wg - pos) & (kBufPairs - 1); r < static_cast<uint32_t>(n); r += kBufPairs) {
-          const uint32_t k = (pos + r) / kBufPairs;
-          const uint32_t b = k & 1;
-          ok = warp_wait(bars.tf(b), (k >> 1) & 1, abort_flag, p.status);
+        const bool in_span = scol < lim;
+        for (uint32_t r = (wg - pos) & (kBufPairs - 1); r < static_cast<uint32_t>(n); r += kBufPairs, ++m) {
+          const uint32_t b = m & 1;
+          ok = warp_wait(bars.tf(b), (m >> 1) & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
           uint32_t v[64];
@@ -681,24 +688,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bars.te(b));
           const float4* wr = reinterpret_cast<const float4*>(w_grp + r * kHeads);
-          float2 c0 = make_float2(0.f, 0.f), c1 = c0, c2 = c0, c3 = c0;
+          float2 cx = make_float2(0.f, 0.f), ca = cx;
 #pragma unroll
-          for (int h = 0; h < kHeads; h += 8) {
-            const float4 wa = wr[h / 4];
-            c0 = __ffma2_rn(make_float2(relu_f(v[h + 0]), relu_f(v[h + 1])), make_float2(wa.x, wa.y), c0);
-            c1 = __ffma2_rn(make_float2(relu_f(v[h + 2]), relu_f(v[h + 3])), make_float2(wa.z, wa.w), c1);
-            const float4 wc = wr[h / 4 + 1];
-            c2 = __ffma2_rn(make_float2(relu_f(v[h + 4]), relu_f(v[h + 5])), make_float2(wc.x, wc.y), c2);
-            c3 = __ffma2_rn(make_float2(relu_f(v[h + 6]), relu_f(v[h + 7])), make_float2(wc.z, wc.w), c3);
+          for (int h = 0; h < kHeads; h += 4) {
+            const float4 w4 = wr[h / 4];
+            const float2 x01 = make_float2(__uint_as_float(v[h + 0]), __uint_as_float(v[h + 1]));
+            const float2 x23 = make_float2(__uint_as_float(v[h + 2]), __uint_as_float(v[h + 3]));
+            cx = __ffma2_rn(x01, make_float2(w4.x, w4.y), cx);
+            ca = __ffma2_rn(make_float2(fabsf(x01.x), fabsf(x01.y)), make_float2(w4.x, w4.y), ca);
+            cx = __ffma2_rn(x23, make_float2(w4.z, w4.w), cx);
+            ca = __ffma2_rn(make_float2(fabsf(x23.x), fabsf(x23.y)), make_float2(w4.z, w4.w), ca);
           }
-          const float acc = ((c0.x + c0.y) + (c1.x + c1.y)) + ((c2.x + c2.y) + (c3.x + c3.y));
-          const int L = ctx_grp[r];
-          const float logit = (scol < L) ? kscale * acc : -INFINITY;
-          if (scol < lim) {
-            const int64_t off = static_cast<int64_t>(r0 + static_cast<int>(r)) * p.logits_stride + scol;
-            if (p.logits_bf16) out_h[off] = __float2bfloat16_rn(logit);
-            else out_f[off] = logit;
-          }
+          const float acc = 0.5f * ((cx.x + cx.y) + (ca.x + ca.y));
+          const float logit = (scol < ctx_grp[r]) ? kscale * acc : -INFINITY;
+          if (in_span) store_logit(out_grp + static_cast<int64_t>(r) * p.logits_stride + scol, logit);
         }
         if (!ok) break;
         pos += static_cast<uint32_t>(n);
@@ -736,11 +739,27 @@ Params make_params(const LogitsArgs& a) {
   p.schedule = a.schedule;
   p.num_sms = a.num_sms;
   p.logits = a.logits;
-  p.logits_bf16 = a.logits_dtype == DSA_LOGITS_BF16 ? 1 : 0;
   p.logits_stride = a.logits_stride;
   p.num_rows = a.num_rows;
   p.status = a.status;
   return p;
+}
+
+template <int kFmt, typename OutT>
+cudaError_t launch_as(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const Params& p, int grid,
+                      cudaStream_t stream) {
+  constexpr int kBytes = Smem<kFmt>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(logits_kernel<kFmt, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
+  if (e != cudaSuccess) return e;
+  logits_kernel<kFmt, OutT><<<grid, kThreads, kBytes, stream>>>(tm_q, tm_kv, p);
+  return cudaGetLastError();
+}
+
+template <int kFmt>
+cudaError_t launch(const LogitsArgs& a, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const Params& p,
+                   cudaStream_t stream) {
+  if (a.logits_dtype == DSA_LOGITS_BF16) return launch_as<kFmt, __nv_bfloat16>(tm_q, tm_kv, p, a.num_sms, stream);
+  return launch_as<kFmt, float>(tm_q, tm_kv, p, a.num_sms, stream);
 }
 
 }  // namespace
@@ -760,12 +779,7 @@ cudaError_t launch_logits_fp8(const LogitsArgs& a, cudaStream_t stream) {
   if (!encode_tensor_map_u8(&tm_kv, 3, const_cast<uint8_t*>(a.kv_cache), kdims, kstrides, kbox, true))
     return cudaErrorInvalidValue;
   const Params p = make_params(a);
-  constexpr int kBytes = Smem<DSA_KV_FP8>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(logits_kernel<DSA_KV_FP8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
-  if (e != cudaSuccess) return e;
-  logits_kernel<DSA_KV_FP8><<<a.num_sms, kThreads, kBytes, stream>>>(tm_q, tm_kv, p);
-  return cudaGetLastError();
+  return launch<DSA_KV_FP8>(a, tm_q, tm_kv, p, stream);
 }
 
 cudaError_t launch_logits_fp4(const LogitsArgs& a, cudaStream_t stream) {
@@ -773,12 +787,7 @@ cudaError_t launch_logits_fp4(const LogitsArgs& a, cudaStream_t stream) {
   // itself; the tensor-map parameters are unused.
   alignas(64) CUtensorMap unused{};
   const Params p = make_params(a);
-  constexpr int kBytes = Smem<DSA_KV_FP4>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(logits_kernel<DSA_KV_FP4>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
-  if (e != cudaSuccess) return e;
-  logits_kernel<DSA_KV_FP4><<<a.num_sms, kThreads, kBytes, stream>>>(unused, unused, p);
-  return cudaGetLastError();
+  return launch<DSA_KV_FP4>(a, unused, unused, p, stream);
 }
 
 }  // namespace dsa
