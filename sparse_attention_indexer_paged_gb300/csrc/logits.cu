@@ -17,12 +17,14 @@
 // runs inside one thread with no cross-lane traffic, and a warp's 32 logits
 // are 32 consecutive columns.
 //
-// The CTA's (tile, row) pairs form one stream.  TMEM holds two buffers of
-// four pairs (2 x 256 columns); the MMA issuer fills one buffer while the
-// epilogue drains the other, with one full/empty handshake per buffer.
-// Epilogue warpgroup w takes pair w of every buffer, so every warp waits on
-// every phase of the buffer barriers in order (only the last buffer of the
-// stream may be partial, and no wait follows it).
+// The CTA's (tile, row) pairs form one stream: pair p goes to TMEM slot
+// (buffer (p / 4) mod 2, column block p mod 4) and is drained by epilogue
+// warpgroup p mod 4, so each warpgroup owns two 64-column slots and uses them
+// alternately.  Every slot has its own full/empty barrier pair: the MMA
+// waits only for the warpgroup whose slot it is about to overwrite, and one
+// slow warpgroup does not hold up the others.  A tile's consecutive pairs
+// within a buffer still go out as one MMA of N = 64 x pairs, followed by one
+// commit per slot.
 //
 // Rings: K values (kStages tiles, released by the MMA commit) and key scales
 // (kScaleStages tiles, released by the epilogue, loaded by their own warp)
@@ -50,7 +52,12 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 640;
+// 20 warps: 4 role warps + 16 epilogue warps.  The FP4 variant adds warps
+// 20-23, so that six warps (3, 2, 20-23) share the dequantisation; with six
+// warps on a sub-partition a thread gets at most 80 registers, so its
+// epilogue reads a pair from TMEM in two 32-column halves.
+template <int kFmt> constexpr int kThreadsOf = kFmt == DSA_KV_FP4 ? 768 : 640;
+constexpr int kFp4Converters = 6;
 constexpr int kEpiWarpgroups = 4;  // warps 4..19
 constexpr int kEpiWarps = 4 * kEpiWarpgroups;
 constexpr int kScaleStages = 16;   // key scale ring
@@ -64,7 +71,8 @@ constexpr int kFp4PageBytes = DSA_FP4_PAGE_BYTES;         // 4864: values, block
 constexpr int kFp4GScaleOffset = kPageTokens * (kHeadDim / 2 + kHeadDim / 16);  // 4608
 constexpr int kScaleStageFloats = kTileTokens;            // 128 key scales per tile
 constexpr int kMaxKStages = 8;
-constexpr int kMaxRawStages = 2;
+constexpr int kMaxRawStages = 8;
+constexpr int kFp4PassRows = 4;  // q rows per MMA pass over a tile, FP4 keys
 
 // Shared memory layouts (offsets from a 1024-aligned base).
 //   FP8: K ring of e4m3 tiles [128 tokens][128 B] filled by TMA, Q rows e4m3.
@@ -85,9 +93,9 @@ template <> struct Lay<DSA_KV_FP8> {
 template <> struct Lay<DSA_KV_FP4> {
   static constexpr int kKStages = 2;
   static constexpr int kKStageBytes = 2 * kTileTokens * 128;  // 32768
-  static constexpr int kRawStages = 2;
+  static constexpr int kRawStages = 8;
   static constexpr int kRawStageBytes = 2 * kFp4PageBytes;    // 9728
-  static constexpr int kQHalfBytes = kGroupMaxRows * kHeads * 128;  // 65536
+  static constexpr int kQHalfBytes = kFp4PassRows * kHeads * 128;  // 32768
   static constexpr int kOffQ = 0;
   static constexpr int kOffKv = kOffQ + 2 * kQHalfBytes;
   static constexpr int kOffRaw = kOffKv + kKStages * kKStageBytes;
@@ -99,8 +107,8 @@ template <int kFmt> struct Smem : Lay<kFmt> {
   static constexpr int kOffCtx = kOffW + 2 * kWBufFloats * 4;  // causal limits of the group's rows
   static constexpr int kOffBar = kOffCtx + 2 * kGroupMaxRows * 4;
   // barriers: kv_full[8], kv_empty[8], raw_full[2], raw_empty[2], sc_full[SS],
-  // sc_empty[SS], q_full, q_empty, w_full[2], w_empty[2], tm_full[2], tm_empty[2], mma_done
-  static constexpr int kNumBars = 2 * kMaxKStages + 2 * kMaxRawStages + 2 * kScaleStages + 2 + 4 + 4 + 1;
+  // sc_empty[SS], q_full, q_empty, w_full[2], w_empty[2], tm_full[2][4], tm_empty[2][4], mma_done
+  static constexpr int kNumBars = 2 * kMaxKStages + 2 * kMaxRawStages + 2 * kScaleStages + 2 + 4 + 16 + 1;
   static constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemAddr + 4;
   static constexpr int kBytes = kOffAbort + 4 + 1024;  // + alignment slack
@@ -144,21 +152,26 @@ struct Bars {
   __device__ uint32_t sce(int s) const { return sc_empty + 8 * s; }
   __device__ uint32_t wf(int b) const { return w_full + 8 * b; }
   __device__ uint32_t we(int b) const { return w_empty + 8 * b; }
-  __device__ uint32_t tf(int b) const { return tm_full + 8 * b; }
-  __device__ uint32_t te(int b) const { return tm_empty + 8 * b; }
+  // TMEM slot (buffer b, warpgroup w): filled by the MMA, drained by warpgroup w
+  __device__ uint32_t tf(uint32_t b, uint32_t w) const { return tm_full + 8 * (b * kBufPairs + w); }
+  __device__ uint32_t te(uint32_t b, uint32_t w) const { return tm_empty + 8 * (b * kBufPairs + w); }
 };
 
 // The CTA's walk over its units: groups in order, and the tiles [j0, j1) of
-// each group that belong to this CTA.  Every role runs the same walk with all
-// 32 lanes of its warp: the lanes search the group table 32 entries at a
-// time and read a group's causal limits in parallel, so a warp reaches its
-// first unit after a few dependent loads instead of a serial search.
+// each group that belong to this CTA.  A group of n rows is walked as
+// ceil(n / kPassRows) row passes over the same tiles (one pass when
+// kPassRows = 8; the FP4 path uses passes of 4 rows so that its f16 copy of
+// the q rows fits next to a deep page ring).  Every role runs the same walk
+// with all 32 lanes of its warp: the lanes search the group table 32
+// entries at a time and read a group's causal limits in parallel.
+template <int kPassRows>
 struct Walk {
   const int32_t* grs;
   const int32_t* gus;
   const int32_t* ctx;
   int G, T, u, u_end, g;
-  // current group
+  int g_r0, g_n, pass, npass;  // current group and row pass
+  // current pass: rows [r0, r0 + n) of the group's tiles [j0, j1)
   int r0, n, npages, j0, j1;
   int32_t lane_ctx;  // causal limit of row r0 + lane (lanes below n)
 
@@ -171,6 +184,7 @@ struct Walk {
     G = G_;
     u = u0;
     u_end = u1;
+    pass = npass = 0;
     // largest g in [0, G) with gus[g] <= u (gus is non-decreasing, gus[0] = 0):
     // each round narrows [lo, hi) 32-fold, keeping gus[lo] <= u
     int lo = 0, hi = G;
@@ -185,23 +199,31 @@ struct Walk {
     g = lo;
   }
 
-  // Loads the next group that holds units of this CTA; false when done.
+  // Loads the next row pass that holds units of this CTA; false when done.
   __device__ bool next(int lane) {
-    while (u < u_end && g < G && __ldg(gus + g + 1) <= u) ++g;
-    if (u >= u_end || g >= G) return false;
-    const int gu0 = __ldg(gus + g), gu1 = __ldg(gus + g + 1);
-    r0 = __ldg(grs + g);
-    n = __ldg(grs + g + 1) - r0;
-    if (r0 < 0 || n <= 0 || n > kGroupMaxRows || r0 + n > T) return false;
-    lane_ctx = lane < n ? __ldg(ctx + r0 + lane) : 0;
-    int lmax = lane_ctx;
+    if (pass + 1 < npass) {
+      ++pass;  // same group and tiles, next rows
+    } else {
+      while (u < u_end && g < G && __ldg(gus + g + 1) <= u) ++g;
+      if (u >= u_end || g >= G) return false;
+      const int gu0 = __ldg(gus + g), gu1 = __ldg(gus + g + 1);
+      g_r0 = __ldg(grs + g);
+      g_n = __ldg(grs + g + 1) - g_r0;
+      if (g_r0 < 0 || g_n <= 0 || g_n > kGroupMaxRows || g_r0 + g_n > T) return false;
+      int lmax = lane < g_n ? __ldg(ctx + g_r0 + lane) : 0;
 #pragma unroll
-    for (int o = 4; o; o >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));  // lanes 0..7
-    lmax = __shfl_sync(0xffffffffu, lmax, 0);
-    npages = (lmax + kPageTokens - 1) / kPageTokens;
-    j0 = u - gu0;
-    j1 = min(gu1, u_end) - gu0;
-    u = gu0 + j1;
+      for (int o = 4; o; o >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));  // lanes 0..7
+      lmax = __shfl_sync(0xffffffffu, lmax, 0);
+      npages = (lmax + kPageTokens - 1) / kPageTokens;  // of the whole group: every pass writes its columns
+      j0 = u - gu0;
+      j1 = min(gu1, u_end) - gu0;
+      u = gu0 + j1;
+      pass = 0;
+      npass = (g_n + kPassRows - 1) / kPassRows;
+    }
+    r0 = g_r0 + pass * kPassRows;
+    n = min(g_n - pass * kPassRows, kPassRows);
+    lane_ctx = lane < n ? __ldg(ctx + r0 + lane) : 0;
     return true;
   }
 };
@@ -220,7 +242,7 @@ __device__ __forceinline__ void store_logit(float* dst, float v) { *dst = v; }
 __device__ __forceinline__ void store_logit(__nv_bfloat16* dst, float v) { *dst = __float2bfloat16_rn(v); }
 
 template <int kFmt, typename OutT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                   const Params p) {
   using L = Smem<kFmt>;
@@ -264,31 +286,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   bars.w_full = bars.q_empty + 8;
   bars.w_empty = bars.w_full + 16;
   bars.tm_full = bars.w_empty + 16;
-  bars.tm_empty = bars.tm_full + 16;
-  bars.mma_done = bars.tm_empty + 16;
+  bars.tm_empty = bars.tm_full + 8 * 2 * kBufPairs;
+  bars.mma_done = bars.tm_empty + 8 * 2 * kBufPairs;
   uint32_t* tmem_addr_smem = reinterpret_cast<uint32_t*>(smem + L::kOffTmemAddr);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kOffAbort);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bars.kvf(s), 1);  // TMA (FP8) or the dequantising warp (FP4)
+      mbar_init(bars.kvf(s), kFp4 ? kFp4Converters : 1);  // TMA (FP8) or the three dequantising warps (FP4)
       mbar_init(bars.kve(s), 1);  // the MMA commit of the tile
     }
     for (int s = 0; s < L::kRawStages; ++s) {
       mbar_init(bars.rwf(s), 1);
-      mbar_init(bars.rwe(s), 1);  // the dequantising warp
+      mbar_init(bars.rwe(s), kFp4Converters);  // the dequantising warps
     }
     for (int s = 0; s < kScaleStages; ++s) {
-      mbar_init(bars.scf(s), 1);
+      mbar_init(bars.scf(s), kFp4 ? kFp4Converters : 1);  // bulk copy (FP8) or the three dequantising warps (FP4)
       mbar_init(bars.sce(s), kEpiWarps);  // every epilogue warp has read the tile's scales
     }
-    mbar_init(bars.q_full, 1);
+    mbar_init(bars.q_full, kFp4 ? kFp4Converters : 1);  // the MMA warp's TMA (FP8) or the three converting warps (FP4)
     mbar_init(bars.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.wf(b), 1);
       mbar_init(bars.we(b), kEpiWarps);
-      mbar_init(bars.tf(b), 1);
-      mbar_init(bars.te(b), kEpiWarps);
+      for (uint32_t w = 0; w < kBufPairs; ++w) {
+        mbar_init(bars.tf(b, w), 1);  // the MMA commit of the slot's pair
+        mbar_init(bars.te(b, w), 4);  // the four warps of warpgroup w have read it
+      }
     }
     mbar_init(bars.mma_done, 1);
     *abort_flag = 0;
@@ -311,8 +335,118 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* w_sm = reinterpret_cast<const float*>(smem + L::kOffW);
   int32_t* ctx_sm = reinterpret_cast<int32_t*>(smem + L::kOffCtx);
 
-  Walk walk;
+  Walk<kFp4 ? kFp4PassRows : kGroupMaxRows> walk;
   walk.start(grs, gus, p.ctx, G, T, u0, u1, lane);
+
+  // =================================================== FP4 dequantisation (warps 3, 2, 20-23)
+  // The six warps share every tile: work item k (0..511) is 32 elements
+  // (one 16-byte piece) of token k / 4, and warp `part` takes the items
+  // k = 32 * part + lane (mod 192).  e2m1 values times their e4m3 block scale
+  // -> f16 (exact: at most 6 significant bits) into the swizzled A-operand
+  // tile; token scales into the scale ring.  The warps also share the
+  // conversion of every pass's q rows (e4m3 -> f16, exact) into the swizzled
+  // B-operand layout.  Warp 2 first loads the pass's head weights and causal
+  // limits (double buffered).
+  auto fp4_worker = [&]() {
+    using LF = Lay<DSA_KV_FP4>;
+    constexpr int kStride = 32 * kFp4Converters;
+    const int part = warp == 3 ? 0 : (warp == 2 ? 1 : warp - (4 + kEpiWarps) + 2);
+    const uint64_t pol_keep = policy_evict_last();
+    const uint32_t q_half = static_cast<uint32_t>(LF::kQHalfBytes);
+    int it = 0, nq = 0, nw = 0;
+    bool ok = true;
+    while (ok && walk.next(lane)) {
+      const int r0 = walk.r0, n = walk.n;
+      if (part == 1) {
+        const int wb = nw & 1;
+        ok = warp_wait(bars.we(wb), ((nw >> 1) & 1) ^ 1, abort_flag, p.status);
+        if (!ok) break;
+        if (lane < n) ctx_sm[wb * kGroupMaxRows + lane] = walk.lane_ctx;
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bars.wf(wb), static_cast<uint32_t>(n * kHeads * 4));
+          bulk_load(s_w + wb * kWBufFloats * 4, p.weights + static_cast<int64_t>(r0) * kHeads,
+                    n * kHeads * 4, bars.wf(wb), pol_keep);
+        }
+        ++nw;
+      }
+      // q rows of the pass, once the previous pass's MMAs have completed
+      ok = warp_wait(bars.q_empty, (nq & 1) ^ 1, abort_flag, p.status);
+      if (!ok) break;
+      {
+        // 8 e4m3 codes per step; the warps take interleaved 32-chunk blocks
+        const uint2* qsrc = reinterpret_cast<const uint2*>(p.q + static_cast<int64_t>(r0) * kHeads * kHeadDim);
+        const int nchunks = n * kHeads * (kHeadDim / 8);
+        for (int i = part * 32 + lane; i < nchunks; i += kStride) {
+          const uint2 c = __ldg(qsrc + i);
+          const int R = i >> 4;      // q row (row * 64 + head) within the pass
+          const int c16 = i & 15;    // 8-element chunk along d
+          uint4 o;
+          o.x = e4m3x2_to_f16x2(c.x & 0xffffu);
+          o.y = e4m3x2_to_f16x2(c.x >> 16);
+          o.z = e4m3x2_to_f16x2(c.y & 0xffffu);
+          o.w = e4m3x2_to_f16x2(c.y >> 16);
+          const uint32_t off = static_cast<uint32_t>(c16 >> 3) * q_half + static_cast<uint32_t>(R >> 3) * 1024u +
+                               static_cast<uint32_t>(R & 7) * 128u + (static_cast<uint32_t>((c16 & 7) ^ (R & 7)) << 4);
+          *reinterpret_cast<uint4*>(smem + LF::kOffQ + off) = o;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.q_full);
+      ++nq;
+      for (int j = walk.j0; j < walk.j1; ++j, ++it) {
+        const int rs = it % LF::kRawStages;
+        const int st = it % LF::kKStages;
+        const int ss = it % kScaleStages;
+        ok = warp_wait(bars.rwf(rs), (it / LF::kRawStages) & 1, abort_flag, p.status) &&
+             warp_wait(bars.kve(st), ((it / LF::kKStages) & 1) ^ 1, abort_flag, p.status) &&
+             warp_wait(bars.sce(ss), ((it / kScaleStages) & 1) ^ 1, abort_flag, p.status);
+        if (!ok) break;
+        const uint8_t* raw = smem + LF::kOffRaw + rs * LF::kRawStageBytes;
+        for (int t = part * 32 + lane; t < kTileTokens; t += kStride)  // token scales -> scale ring
+          scale_sm[ss * kScaleStageFloats + t] =
+              *reinterpret_cast<const float*>(raw + (t >> 6) * kFp4PageBytes + kFp4GScaleOffset + (t & 63) * 4);
+        uint8_t* tile = smem + LF::kOffKv + st * LF::kKStageBytes;
+#pragma unroll 1
+        for (int k = part * 32 + lane; k < kTileTokens * 4; k += kStride) {
+          const int tk = k >> 2, q4 = k & 3;  // token within the tile, 32-element piece
+          const uint8_t* tokp = raw + (tk >> 6) * kFp4PageBytes;
+          const int slot = tk & 63;
+          const uint4 pv = *reinterpret_cast<const uint4*>(tokp + slot * (kHeadDim / 2) + q4 * 16);
+          // block scales of the piece's two 16-element blocks
+          const uint32_t s2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(tokp + kPageTokens * (kHeadDim / 2) + slot * 8 + q4 * 2));
+          const uint32_t sb[2] = {__byte_perm(s2, 0, 0x1010), __byte_perm(s2, 0, 0x3232)};
+          const uint32_t words[4] = {pv.x, pv.y, pv.z, pv.w};
+          const uint32_t row = static_cast<uint32_t>(tk >> 3) * 1024u + static_cast<uint32_t>(tk & 7) * 128u;
+#pragma unroll
+          for (int wv = 0; wv < 4; ++wv) {  // 8 elements per word
+            const int c16 = q4 * 4 + wv;     // chunk of elements 8*c16 .. 8*c16+7
+            uint32_t h[4];
+            e2m1x8_to_f16x2(words[wv], h);
+            const uint32_t sc = sb[wv >> 1];
+            uint4 o;
+            o.x = hmul2_u32(h[0], sc);
+            o.y = hmul2_u32(h[1], sc);
+            o.z = hmul2_u32(h[2], sc);
+            o.w = hmul2_u32(h[3], sc);
+            const uint32_t off = static_cast<uint32_t>(c16 >> 3) * (kTileTokens * 128u) + row +
+                                 (static_cast<uint32_t>((c16 & 7) ^ (tk & 7)) << 4);
+            *reinterpret_cast<uint4*>(tile + off) = o;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bars.rwe(rs));
+          mbar_arrive(bars.kvf(st));
+          mbar_arrive(bars.scf(ss));
+        }
+      }
+    }
+    if (part == 1 && lane == 0 && nw > 0) wait_drain(bars.wf((nw - 1) & 1), ((nw - 1) >> 1) & 1);
+  };
 
   if (warp == 0) {
     // =================================================== producer: K pages
@@ -385,184 +519,84 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = max(0, it - kRing); i < it; ++i)
         wait_drain(kFp4 ? bars.rwf(i % kRing) : bars.kvf(i % kRing), (i / kRing) & 1);
     }
-  } else if (warp == 3) {
+  } else if (warp == 2 || warp == 3 || warp >= 4 + kEpiWarps) {
     if constexpr (!kFp4) {
-      // =================================================== key scales (FP8)
-      // Runs ahead of the K pipeline by up to kScaleStages tiles, gated only
-      // by the epilogue.  Block ids come 32 at a time as in the K producer.
-      const uint64_t pol_stream = policy_evict_first();
-      int it = 0;
-      bool ok = true;
-      while (ok && walk.next(lane)) {
-        const int32_t* bt_row = p.block_table + static_cast<int64_t>(walk.r0 + walk.n - 1) * p.bt_stride;
-        int32_t lane_blk = -1;
-        int pg_base = -32;
-        for (int j = walk.j0; j < walk.j1; ++j, ++it) {
-          if (2 * j >= pg_base + 32) {
-            pg_base = 2 * j;
-            const int pg = pg_base + lane;
-            lane_blk = -1;
-            if (pg < walk.npages) {
-              int32_t b = (pg < p.bt_stride) ? __ldg(bt_row + pg) : -1;
-              lane_blk = (b < 0 || b >= p.num_pages) ? 0 : b;  // reported by the K producer
-            }
-          }
-          const int32_t blk0 = __shfl_sync(0xffffffffu, lane_blk, 2 * j - pg_base);
-          const int32_t blk1 = __shfl_sync(0xffffffffu, lane_blk, 2 * j + 1 - pg_base);
-          if (lane == 0) {
-            const int ss = it % kScaleStages;
-            ok = wait_or_abort(bars.sce(ss), ((it / kScaleStages) & 1) ^ 1, abort_flag, p.status);
-            if (ok) {
-              const int npg = (blk0 >= 0 ? 1 : 0) + (blk1 >= 0 ? 1 : 0);
-              mbar_arrive_expect_tx(bars.scf(ss), static_cast<uint32_t>(npg * kPageTokens * 4));
-              if (blk0 >= 0)
-                bulk_load(s_scale + ss * kScaleStageFloats * 4,
-                          p.kv_cache + static_cast<int64_t>(blk0) * p.page_stride + kPageValBytesFp8,
-                          kPageTokens * 4, bars.scf(ss), pol_stream);
-              if (blk1 >= 0)
-                bulk_load(s_scale + (ss * kScaleStageFloats + kPageTokens) * 4,
-                          p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride + kPageValBytesFp8,
-                          kPageTokens * 4, bars.scf(ss), pol_stream);
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-        }
-      }
-      if (lane == 0)
-        for (int i = max(0, it - kScaleStages); i < it; ++i)
-          wait_drain(bars.scf(i % kScaleStages), (i / kScaleStages) & 1);
-    } else {
-      // =================================================== FP4 dequantisation
-      // Per group: the group's q rows, e4m3 -> f16 (exact), into the swizzled
-      // B-operand layout.  Per tile: the raw pages' e2m1 values times their
-      // e4m3 block scales -> f16 (exact: at most 6 significant bits) into the
-      // swizzled A-operand layout, and the token scales into the scale ring.
-      int it = 0, nq = 0;
-      bool ok = true;
-      const uint32_t q_half = static_cast<uint32_t>(Lay<DSA_KV_FP4>::kQHalfBytes);
-      while (ok && walk.next(lane)) {
-        const int r0 = walk.r0, n = walk.n;
-        int okq = 1;
-        if (lane == 0) okq = wait_or_abort(bars.q_empty, (nq & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
-        ok = __shfl_sync(0xffffffffu, okq, 0) != 0;
-        if (!ok) break;
-        {
-          // 8 e4m3 codes per step, consecutive lanes on consecutive bytes
-          const uint2* qsrc = reinterpret_cast<const uint2*>(p.q + static_cast<int64_t>(r0) * kHeads * kHeadDim);
-          const int nchunks = n * kHeads * (kHeadDim / 8);
-          for (int i = lane; i < nchunks; i += 32) {
-            const uint2 c = __ldg(qsrc + i);
-            const int R = i >> 4;      // q row (row * 64 + head) within the group
-            const int c16 = i & 15;    // 8-element chunk along d
-            uint4 o;
-            o.x = e4m3x2_to_f16x2(c.x & 0xffffu);
-            o.y = e4m3x2_to_f16x2(c.x >> 16);
-            o.z = e4m3x2_to_f16x2(c.y & 0xffffu);
-            o.w = e4m3x2_to_f16x2(c.y >> 16);
-            const uint32_t off = static_cast<uint32_t>(c16 >> 3) * q_half + static_cast<uint32_t>(R >> 3) * 1024u +
-                                 static_cast<uint32_t>(R & 7) * 128u + (static_cast<uint32_t>((c16 & 7) ^ (R & 7)) << 4);
-            *reinterpret_cast<uint4*>(smem + L::kOffQ + off) = o;
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.q_full);
-        ++nq;
-        for (int j = walk.j0; j < walk.j1; ++j, ++it) {
-          const int rs = it % L::kRawStages;
-          const int st = it % kStages;
-          const int ss = it % kScaleStages;
-          int okt = 1;
-          if (lane == 0)
-            okt = (wait_or_abort(bars.rwf(rs), (it / L::kRawStages) & 1, abort_flag, p.status) &&
-                   wait_or_abort(bars.kve(st), ((it / kStages) & 1) ^ 1, abort_flag, p.status) &&
-                   wait_or_abort(bars.sce(ss), ((it / kScaleStages) & 1) ^ 1, abort_flag, p.status))
-                      ? 1 : 0;
-          ok = __shfl_sync(0xffffffffu, okt, 0) != 0;
-          if (!ok) break;
-          const uint8_t* rawp = smem + L::kOffRaw + rs * L::kRawStageBytes;
-          // token scales of both pages -> scale ring (4 per lane)
-          {
-            const int t4 = lane * 4;  // tokens t4 .. t4+3
-            const float4 g = *reinterpret_cast<const float4*>(rawp + (t4 >> 6) * kFp4PageBytes +
-                                                              kFp4GScaleOffset + (t4 & 63) * 4);
-            *reinterpret_cast<float4*>(scale_sm + ss * kScaleStageFloats + t4) = g;
-          }
-          uint8_t* tile = smem + L::kOffKv + st * L::kKStageBytes;
-#pragma unroll 1
-          for (int tk = lane; tk < kTileTokens; tk += 32) {
-            const uint8_t* tokp = rawp + (tk >> 6) * kFp4PageBytes;
-            const int slot = tk & 63;
-            const uint4* vals = reinterpret_cast<const uint4*>(tokp + slot * (kHeadDim / 2));
-            const uint2 bsc = *reinterpret_cast<const uint2*>(tokp + kPageTokens * (kHeadDim / 2) + slot * 8);
-            uint32_t sc[8];  // f16x2 {s_b, s_b} for block b
-            {
-              const uint32_t s01 = e4m3x2_to_f16x2(bsc.x & 0xffffu), s23 = e4m3x2_to_f16x2(bsc.x >> 16);
-              const uint32_t s45 = e4m3x2_to_f16x2(bsc.y & 0xffffu), s67 = e4m3x2_to_f16x2(bsc.y >> 16);
-              sc[0] = __byte_perm(s01, 0, 0x1010); sc[1] = __byte_perm(s01, 0, 0x3232);
-              sc[2] = __byte_perm(s23, 0, 0x1010); sc[3] = __byte_perm(s23, 0, 0x3232);
-              sc[4] = __byte_perm(s45, 0, 0x1010); sc[5] = __byte_perm(s45, 0, 0x3232);
-              sc[6] = __byte_perm(s67, 0, 0x1010); sc[7] = __byte_perm(s67, 0, 0x3232);
-            }
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {  // 16-byte pieces of the packed row: 32 elements each
-              const uint4 pv = vals[q4];
-              const uint32_t words[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-              for (int wv = 0; wv < 4; ++wv) {  // 8 elements per word
-                const int c16 = q4 * 4 + wv;     // chunk of elements 8*c16 .. 8*c16+7
-                uint32_t h[4];
-                e2m1x8_to_f16x2(words[wv], h);
-                const uint32_t sb = sc[c16 >> 1];
-                uint4 o;
-                o.x = hmul2_u32(h[0], sb);
-                o.y = hmul2_u32(h[1], sb);
-                o.z = hmul2_u32(h[2], sb);
-                o.w = hmul2_u32(h[3], sb);
-                const uint32_t off = static_cast<uint32_t>(c16 >> 3) * (kTileTokens * 128u) +
-                                     static_cast<uint32_t>(tk >> 3) * 1024u + static_cast<uint32_t>(tk & 7) * 128u +
-                                     (static_cast<uint32_t>((c16 & 7) ^ (tk & 7)) << 4);
-                *reinterpret_cast<uint4*>(tile + off) = o;
+      if (warp == 3) {
+        // =================================================== key scales (FP8)
+        // Runs ahead of the K pipeline by up to kScaleStages tiles, gated only
+        // by the epilogue.  Block ids come 32 at a time as in the K producer.
+        const uint64_t pol_stream = policy_evict_first();
+        int it = 0;
+        bool ok = true;
+        while (ok && walk.next(lane)) {
+          const int32_t* bt_row = p.block_table + static_cast<int64_t>(walk.r0 + walk.n - 1) * p.bt_stride;
+          int32_t lane_blk = -1;
+          int pg_base = -32;
+          for (int j = walk.j0; j < walk.j1; ++j, ++it) {
+            if (2 * j >= pg_base + 32) {
+              pg_base = 2 * j;
+              const int pg = pg_base + lane;
+              lane_blk = -1;
+              if (pg < walk.npages) {
+                int32_t b = (pg < p.bt_stride) ? __ldg(bt_row + pg) : -1;
+                lane_blk = (b < 0 || b >= p.num_pages) ? 0 : b;  // reported by the K producer
               }
             }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(bars.rwe(rs));
-            mbar_arrive(bars.kvf(st));
-            mbar_arrive(bars.scf(ss));
+            const int32_t blk0 = __shfl_sync(0xffffffffu, lane_blk, 2 * j - pg_base);
+            const int32_t blk1 = __shfl_sync(0xffffffffu, lane_blk, 2 * j + 1 - pg_base);
+            if (lane == 0) {
+              const int ss = it % kScaleStages;
+              ok = wait_or_abort(bars.sce(ss), ((it / kScaleStages) & 1) ^ 1, abort_flag, p.status);
+              if (ok) {
+                const int npg = (blk0 >= 0 ? 1 : 0) + (blk1 >= 0 ? 1 : 0);
+                mbar_arrive_expect_tx(bars.scf(ss), static_cast<uint32_t>(npg * kPageTokens * 4));
+                if (blk0 >= 0)
+                  bulk_load(s_scale + ss * kScaleStageFloats * 4,
+                            p.kv_cache + static_cast<int64_t>(blk0) * p.page_stride + kPageValBytesFp8,
+                            kPageTokens * 4, bars.scf(ss), pol_stream);
+                if (blk1 >= 0)
+                  bulk_load(s_scale + (ss * kScaleStageFloats + kPageTokens) * 4,
+                            p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride + kPageValBytesFp8,
+                            kPageTokens * 4, bars.scf(ss), pol_stream);
+              }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
           }
         }
+        if (lane == 0)
+          for (int i = max(0, it - kScaleStages); i < it; ++i)
+            wait_drain(bars.scf(i % kScaleStages), (i / kScaleStages) & 1);
+      } else {
+        // =================================================== per group: weights and causal limits
+        // A separate producer: the epilogue may hold a group's weights until TMEM
+        // buffers that also carry later groups' pairs complete, so these loads
+        // must never sit in front of the Q and K loads.
+        const uint64_t pol_keep = policy_evict_last();
+        int nw = 0;
+        bool ok = true;
+        while (ok && walk.next(lane)) {
+          const int r0 = walk.r0, n = walk.n;
+          const int wb = nw & 1;
+          ok = warp_wait(bars.we(wb), ((nw >> 1) & 1) ^ 1, abort_flag, p.status);
+          if (!ok) break;
+          // lanes below n write their row's causal limit; the fence and the warp
+          // barrier order those writes before lane 0's release on wf
+          if (lane < n) ctx_sm[wb * kGroupMaxRows + lane] = walk.lane_ctx;
+          __threadfence_block();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bars.wf(wb), static_cast<uint32_t>(n * kHeads * 4));
+            bulk_load(s_w + wb * kWBufFloats * 4, p.weights + static_cast<int64_t>(r0) * kHeads,
+                      n * kHeads * 4, bars.wf(wb), pol_keep);
+          }
+          ++nw;
+        }
+        if (lane == 0 && nw > 0) wait_drain(bars.wf((nw - 1) & 1), ((nw - 1) >> 1) & 1);
       }
+    } else {
+      fp4_worker();
     }
-  } else if (warp == 2) {
-    // =================================================== per group: weights and causal limits
-    // A separate producer: the epilogue may hold a group's weights until TMEM
-    // buffers that also carry later groups' pairs complete, so these loads
-    // must never sit in front of the Q and K loads.
-    const uint64_t pol_keep = policy_evict_last();
-    int nw = 0;
-    bool ok = true;
-    while (ok && walk.next(lane)) {
-      const int r0 = walk.r0, n = walk.n;
-      const int wb = nw & 1;
-      ok = warp_wait(bars.we(wb), ((nw >> 1) & 1) ^ 1, abort_flag, p.status);
-      if (!ok) break;
-      // lanes below n write their row's causal limit; the fence and the warp
-      // barrier order those writes before lane 0's release on wf
-      if (lane < n) ctx_sm[wb * kGroupMaxRows + lane] = walk.lane_ctx;
-      __threadfence_block();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bars.wf(wb), static_cast<uint32_t>(n * kHeads * 4));
-        bulk_load(s_w + wb * kWBufFloats * 4, p.weights + static_cast<int64_t>(r0) * kHeads,
-                  n * kHeads * 4, bars.wf(wb), pol_keep);
-      }
-      ++nw;
-    }
-    if (lane == 0 && nw > 0) wait_drain(bars.wf((nw - 1) & 1), ((nw - 1) >> 1) & 1);
   } else if (warp == 1) {
     // =================================================== MMA issuer
     // The whole warp walks the work, so every value feeding an MMA is
@@ -610,21 +644,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t left = n;
         do {  // the tile's rows, cut where a TMEM buffer ends
           const uint32_t c = pos & (kBufPairs - 1);
-          const uint32_t k = pos / kBufPairs;
-          const uint32_t b = k & 1;
-          if (c == 0) {
-            ok = warp_wait(bars.te(b), ((k >> 1) & 1) ^ 1, abort_flag, p.status);
-            if (!ok) break;
-            tc_fence_after();
-          }
+          const uint32_t b = (pos / kBufPairs) & 1;
           const uint32_t len = min(left, kBufPairs - c);
+          // pair pos + i goes to slot (b, c + i), whose previous use (by the
+          // pair 8 positions earlier) its warpgroup must have read
+          for (uint32_t i = 0; i < len && ok; ++i)
+            ok = warp_wait(bars.te(b, c + i), (((pos + i) >> 3) & 1) ^ 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
           const uint32_t d_tmem = tmem + b * kBufCols + c * kPairCols;
           if constexpr (!kFp4) mma_fp8_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20));
           else mma_f16_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20));
           left -= len;
           pos += len;
           b_lo += len * kQRowLo;
-          if ((pos & (kBufPairs - 1)) == 0) mma_commit_if(issue, bars.tf(b));
+          for (uint32_t i = 0; i < len; ++i) mma_commit_if(issue, bars.tf(b, c + i));
         } while (left != 0);
         if (!ok) break;
         mma_commit_if(issue, bars.kve(st));
@@ -634,7 +668,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++gi;
     }
     if (leader) {
-      if (ok && (pos & (kBufPairs - 1)) != 0) mma_commit(bars.tf((pos / kBufPairs) & 1));  // last, partial buffer
       // every Q copy has landed before the CTA may exit
       if (nq > 0) wait_drain(bars.q_full, (nq - 1) & 1);
       // No MMA may still be writing TMEM when it is freed.
@@ -642,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_drain(bars.mma_done, 0);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 4 + kEpiWarps) {
     // =================================================== epilogue
     // Pair position pos + r belongs to warpgroup (pos + r) mod 4, so this
     // warp visits r = (wg - pos) mod 4, +4, ... of each tile, and its m-th
@@ -678,28 +711,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool in_span = scol < lim;
         for (uint32_t r = (wg - pos) & (kBufPairs - 1); r < static_cast<uint32_t>(n); r += kBufPairs, ++m) {
           const uint32_t b = m & 1;
-          ok = warp_wait(bars.tf(b), (m >> 1) & 1, abort_flag, p.status);
+          ok = warp_wait(bars.tf(b, wg), (m >> 1) & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          uint32_t v[64];
-          tmem_ld_x64(t_lane + b * kBufCols, v);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bars.te(b));
-          const float4* wr = reinterpret_cast<const float4*>(w_grp + r * kHeads);
-          float2 cx = make_float2(0.f, 0.f), ca = cx;
+          float acc;
+          if constexpr (!kFp4) {
+            uint32_t v[64];
+            tmem_ld_x64(t_lane + b * kBufCols, v);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.te(b, wg));
+            const float4* wr = reinterpret_cast<const float4*>(w_grp + r * kHeads);
+            float2 cx = make_float2(0.f, 0.f), ca = cx;
+  #pragma unroll
+            for (int h = 0; h < kHeads; h += 4) {
+              const float4 w4 = wr[h / 4];
+              const float2 x01 = make_float2(__uint_as_float(v[h + 0]), __uint_as_float(v[h + 1]));
+              const float2 x23 = make_float2(__uint_as_float(v[h + 2]), __uint_as_float(v[h + 3]));
+              cx = __ffma2_rn(x01, make_float2(w4.x, w4.y), cx);
+              ca = __ffma2_rn(make_float2(fabsf(x01.x), fabsf(x01.y)), make_float2(w4.x, w4.y), ca);
+              cx = __ffma2_rn(x23, make_float2(w4.z, w4.w), cx);
+              ca = __ffma2_rn(make_float2(fabsf(x23.x), fabsf(x23.y)), make_float2(w4.z, w4.w), ca);
+            }
+            acc = 0.5f * ((cx.x + cx.y) + (ca.x + ca.y));
+          } else {
+            // two 32-column halves, one at a time (80-register budget)
+            const float4* wr = reinterpret_cast<const float4*>(w_grp + r * kHeads);
+            float2 cx = make_float2(0.f, 0.f), ca = cx;
 #pragma unroll
-          for (int h = 0; h < kHeads; h += 4) {
-            const float4 w4 = wr[h / 4];
-            const float2 x01 = make_float2(__uint_as_float(v[h + 0]), __uint_as_float(v[h + 1]));
-            const float2 x23 = make_float2(__uint_as_float(v[h + 2]), __uint_as_float(v[h + 3]));
-            cx = __ffma2_rn(x01, make_float2(w4.x, w4.y), cx);
-            ca = __ffma2_rn(make_float2(fabsf(x01.x), fabsf(x01.y)), make_float2(w4.x, w4.y), ca);
-            cx = __ffma2_rn(x23, make_float2(w4.z, w4.w), cx);
-            ca = __ffma2_rn(make_float2(fabsf(x23.x), fabsf(x23.y)), make_float2(w4.z, w4.w), ca);
+            for (int half = 0; half < 2; ++half) {
+              uint32_t v[32];
+              tmem_ld_x32(t_lane + b * kBufCols + half * 32, v);
+              tmem_ld_wait();
+              if (half == 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.te(b, wg));
+              }
+#pragma unroll
+              for (int h = 0; h < 32; h += 4) {
+                const float4 w4 = wr[half * 8 + h / 4];
+                const float2 x01 = make_float2(__uint_as_float(v[h + 0]), __uint_as_float(v[h + 1]));
+                const float2 x23 = make_float2(__uint_as_float(v[h + 2]), __uint_as_float(v[h + 3]));
+                cx = __ffma2_rn(x01, make_float2(w4.x, w4.y), cx);
+                ca = __ffma2_rn(make_float2(fabsf(x01.x), fabsf(x01.y)), make_float2(w4.x, w4.y), ca);
+                cx = __ffma2_rn(x23, make_float2(w4.z, w4.w), cx);
+                ca = __ffma2_rn(make_float2(fabsf(x23.x), fabsf(x23.y)), make_float2(w4.z, w4.w), ca);
+              }
+            }
+            acc = 0.5f * ((cx.x + cx.y) + (ca.x + ca.y));
           }
-          const float acc = 0.5f * ((cx.x + cx.y) + (ca.x + ca.y));
           const float logit = (scol < ctx_grp[r]) ? kscale * acc : -INFINITY;
           if (in_span) store_logit(out_grp + static_cast<int64_t>(r) * p.logits_stride + scol, logit);
         }
@@ -751,7 +813,7 @@ cudaError_t launch_as(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const P
   constexpr int kBytes = Smem<kFmt>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(logits_kernel<kFmt, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
   if (e != cudaSuccess) return e;
-  logits_kernel<kFmt, OutT><<<grid, kThreads, kBytes, stream>>>(tm_q, tm_kv, p);
+  logits_kernel<kFmt, OutT><<<grid, kThreadsOf<kFmt>, kBytes, stream>>>(tm_q, tm_kv, p);
   return cudaGetLastError();
 }
 

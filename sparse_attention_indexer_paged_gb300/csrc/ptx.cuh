@@ -289,7 +289,7 @@ __device__ __forceinline__ void mma_fp8_k128(uint32_t issue, uint32_t d_tmem, ui
 //   separate swizzled blocks (the A block of a 128-token tile is 16 KB, the B
 //   block of the Q rows is kFp4QHalfBytes), four steps inside each.
 constexpr uint32_t kFp4AHalfLo = (128 * 128) >> 4;
-constexpr uint32_t kFp4BHalfLo = (8 * 64 * 128) >> 4;
+constexpr uint32_t kFp4BHalfLo = (4 * 64 * 128) >> 4;  // four q rows of 64 heads
 __device__ __forceinline__ void mma_f16_k128(uint32_t issue, uint32_t d_tmem, uint32_t a_lo,
                                              uint32_t b_lo, uint32_t hi, uint32_t idesc_v) {
   const uint32_t a2 = a_lo + kFp4AHalfLo, b2 = b_lo + kFp4BHalfLo;
@@ -409,6 +409,19 @@ __device__ __forceinline__ void tmem_ld_x64(uint32_t taddr, uint32_t (&r)[64]) {
         "=r"(r[62]), "=r"(r[63])
       : "r"(taddr)
       : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit TMEM words (as tmem_ld_x64, half the columns).
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
