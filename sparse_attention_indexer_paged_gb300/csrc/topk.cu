@@ -7,17 +7,21 @@
 // -0 == +0); the k-th largest key tau and the number of keys equal to tau
 // that are kept (the lowest columns among them) are found by radix select.
 //
-// Fast path (rows up to kFastMaxCols columns whose threshold bin holds at
-// most kCandCap keys), two reads of the row:
-//   pass 1  histogram of the top 11 key bits;
-//   pass 2  columns above the threshold bin set their bit in a shared-memory
-//           bitmap; the threshold bin's (key, column) pairs go to a
-//           shared-memory candidate list;
-//   then    the low 21 bits are resolved on the candidates alone, the kept
-//           candidates set their bits, and one block-wide scan over the
-//           bitmaps writes the chosen columns in ascending order.
-// Other rows take the general path: three histogram passes over the row
-// (11, 11 and 10 key bits) and an ordered compaction pass.
+// Sampled path (rows up to kFastMaxCols columns), one full read of the row:
+//   sample  every sv-th 4-column group (at most kSampleQuads groups); the
+//           sample's ks-th largest key (ks ~ 1.25 k / sv, two radix rounds),
+//           cut to its top 22 bits, is a threshold t;
+//   pass    keys >= t go to per-warp candidate slices (one shared counter per
+//           warp), packed afterwards;
+//   then    if at least k and at most kCandCap keys reached t, tau is found
+//           on the candidates alone (all keys >= tau are among them), the
+//           kept candidates set their bits in two shared-memory bitmaps and
+//           one block-wide scan over the bitmaps writes the chosen columns in
+//           ascending order.
+// Otherwise (the sample missed, or the row is longer) the exact passes run:
+// a histogram of the top 11 key bits, then either the bitmap/candidate pass
+// above on that bin's keys, or two more histogram passes and an ordered
+// compaction of the row.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -31,8 +35,10 @@ constexpr int kBins = 2048;
 constexpr int kPerThread = 8;          // elements per thread per chunk of the ordered pass
 constexpr int kFastMaxCols = 1 << 18;  // columns the two shared-memory bitmaps cover
 constexpr int kBitmapWords = kFastMaxCols / 32;
-constexpr int kCandCap = 16384;        // (key, column) candidates held in shared memory
+constexpr int kCandCap = 8192;         // (key, column) candidates held in shared memory
 constexpr int kLoadsInFlight = 4;      // 16-byte loads per thread per iteration
+constexpr int kStageBytes = 65536;     // threshold sample keys, then the warps' candidate columns
+constexpr int kSampleQuads = kStageBytes / 16;  // 4-column groups in the threshold sample
 
 // dynamic shared memory map
 constexpr int kOffHist = 0;                                   // uint32 [kBins]
@@ -40,7 +46,8 @@ constexpr int kOffSel = kOffHist + kBins * 4;                 // uint32 [kBitmap
 constexpr int kOffTie = kOffSel + kBitmapWords * 4;           // uint32 [kBitmapWords]
 constexpr int kOffCandKey = kOffTie + kBitmapWords * 4;       // uint32 [kCandCap]
 constexpr int kOffCandCol = kOffCandKey + kCandCap * 4;       // int32  [kCandCap]
-constexpr int kSmemBytes = kOffCandCol + kCandCap * 4;
+constexpr int kOffStage = kOffCandCol + kCandCap * 4;
+constexpr int kSmemBytes = kOffStage + kStageBytes;
 static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
 
 __device__ __forceinline__ uint32_t order_key(float x) {
@@ -182,11 +189,79 @@ __device__ __forceinline__ uint32_t find_bin(const uint32_t* hist, uint32_t nbin
   return bin;
 }
 
+// Exact selection among the shared-memory candidates (every key of the row
+// that can be in its top-k is among them), then the ordered output: keys
+// above tau set their column's bit in `sel`, the first take_eq keys equal to
+// tau (lowest columns) come from `tie`, and a block-wide scan over the
+// bitmaps writes the columns in ascending order.  `prefix`/`prefix_mask`
+// hold key bits already fixed by earlier rounds (starting at `round`: 0 for
+// none, 1 for the top 11 bits) and `remaining` the rank still to find below
+// them.  sel/tie must be zero for the words [0, nwords).
+__device__ __forceinline__ void select_candidates_and_write(
+    const uint32_t* cand_key, const int32_t* cand_col, int nc, uint32_t* sel, uint32_t* tie,
+    int nwords, int64_t wa, uint32_t prefix, uint32_t prefix_mask, uint32_t remaining, int round,
+    uint32_t* hist, uint32_t* scan_buf, uint32_t* s_bin, uint32_t* s_above, int32_t* op) {
+  const int tid = threadIdx.x;
+  uint32_t above;
+#pragma unroll 1
+  for (; round < 3; ++round) {
+    const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
+    const uint32_t nbins = round == 2 ? 1024u : 2048u;
+    for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < nc; i += kThreads) {
+      const uint32_t key = cand_key[i];
+      if ((key & prefix_mask) == prefix) atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
+    }
+    __syncthreads();
+    const uint32_t bin = find_bin(hist, nbins, remaining, scan_buf, s_bin, s_above, &above);
+    prefix |= bin << shift;
+    prefix_mask |= (nbins - 1) << shift;
+    remaining -= above;
+  }
+  const uint32_t tau = prefix;
+  const uint32_t take_eq = remaining;
+  for (int i = tid; i < nc; i += kThreads) {
+    const uint32_t key = cand_key[i];
+    const int64_t off = cand_col[i] - wa;
+    if (key > tau) atomicOr(&sel[off >> 5], 1u << (off & 31));
+    else if (key == tau) atomicOr(&tie[off >> 5], 1u << (off & 31));
+  }
+  __syncthreads();
+  const int per = (nwords + kThreads - 1) / kThreads;
+  const int w0 = tid * per, w1 = min(nwords, w0 + per);
+  uint32_t nsel = 0, ntie = 0;
+  for (int w = w0; w < w1; ++w) {
+    nsel += __popc(sel[w]);
+    ntie += __popc(tie[w]);
+  }
+  uint32_t tot;
+  const uint32_t ex = block_excl_sum(nsel | (ntie << 16), scan_buf, &tot);
+  uint32_t sel_before = ex & 0xffffu, tie_before = ex >> 16;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t ms = sel[w], mt = tie[w];
+    while (ms | mt) {
+      const uint32_t m = ms | mt;
+      const int bit = __ffs(m) - 1;
+      const int32_t col = static_cast<int32_t>(wa + 32 * static_cast<int64_t>(w) + bit);
+      if ((ms >> bit) & 1u) {
+        op[sel_before + min(tie_before, take_eq)] = col;
+        ++sel_before;
+      } else {
+        if (tie_before < take_eq) op[sel_before + tie_before] = col;
+        ++tie_before;
+      }
+      ms &= ~(1u << bit);
+      mt &= ~(1u << bit);
+    }
+  }
+}
+
 template <typename LT>
 __global__ void __launch_bounds__(kThreads, 1)
     topk_kernel(const LT* __restrict__ logits, int64_t stride, const int32_t* __restrict__ starts,
                 const int32_t* __restrict__ ends, int32_t k, int32_t* __restrict__ out,
-                int64_t out_stride) {
+                int64_t out_stride, int32_t* status) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
   uint32_t* sel = reinterpret_cast<uint32_t*>(smem + kOffSel);
@@ -195,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* cand_col = reinterpret_cast<int32_t*>(smem + kOffCandCol);
   __shared__ uint32_t scan_buf[kWarps];
   __shared__ uint32_t s_bin, s_above, s_ncand;
+  __shared__ uint32_t s_wcount[kWarps];
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
@@ -209,6 +285,143 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
+  const int64_t wa = a & ~static_cast<int64_t>(31);
+  const int nwords = static_cast<int>((b - wa + 31) >> 5);
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t above;
+  // the sampled path streams the row with 16-byte bulk copies: rows must
+  // start on 16 bytes and the rounded-up end stay inside the row stride
+  if (b - wa <= kFastMaxCols && stride % (16 / static_cast<int64_t>(sizeof(LT))) == 0) {
+    // ---- sampled threshold: every sv-th 4-column group, at most kSampleQuads
+    // groups; the sample's ks-th largest key, rounded down to its top 22
+    // bits, is a threshold t that about 1.25 k keys of the row reach
+    const int64_t a4 = a & ~static_cast<int64_t>(3);
+    const int64_t nquads = (b - a4 + 3) >> 2;
+    const int64_t sv = (nquads + kSampleQuads - 1) / kSampleQuads;
+    const int nsq = static_cast<int>((nquads + sv - 1) / sv);
+    uint32_t* skey = reinterpret_cast<uint32_t*>(smem + kOffStage);
+    for (int q = tid; q < nsq; q += kThreads) {
+      const int64_t i = a4 + 4 * (static_cast<int64_t>(q) * sv);
+      uint32_t kq[4];
+      if (i >= a && i + 3 < b) {
+        Vec4<LT>::keys(Vec4<LT>::load(rp, i), kq);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) kq[e] = (i + e >= a && i + e < b) ? order_key(load_score<LT>(rp, i + e)) : 0u;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) skey[4 * q + e] = kq[e];  // out-of-row columns: key 0, the lowest
+    }
+    for (int i = tid; i < nwords; i += kThreads) {
+      sel[i] = 0;
+      tie[i] = 0;
+    }
+    if (tid < kWarps) s_wcount[tid] = 0;
+    const int ns = 4 * nsq;
+    const int64_t want = sv == 1 ? k : (5 * static_cast<int64_t>(k)) / (4 * sv) + 16;
+    uint32_t t = 0;
+    if (want < ns) {
+      uint32_t prefix = 0, prefix_mask = 0, remaining = static_cast<uint32_t>(want);
+#pragma unroll 1
+      for (int round = 0; round < 2; ++round) {
+        const int shift = round == 0 ? 21 : 10;
+        for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < ns; i += kThreads) {
+          const uint32_t key = skey[i];
+          if ((key & prefix_mask) == prefix) atomicAdd(&hist[(key >> shift) & 2047u], 1u);
+        }
+        __syncthreads();
+        const uint32_t bin = find_bin(hist, 2048, remaining, scan_buf, &s_bin, &s_above, &above);
+        prefix |= bin << shift;
+        prefix_mask |= 2047u << shift;
+        remaining -= above;
+      }
+      t = prefix;
+    }
+    __syncthreads();
+    // ---- one pass over the row: keys >= t become candidates.  Each warp
+    // appends to its own slice of the candidate arrays (its own counter, so
+    // only lanes of one warp ever contend); the slices are packed afterwards.
+    constexpr int kWarpCap = kCandCap / kWarps;
+    uint32_t* wkey = cand_key + warp * kWarpCap;  // this warp's slice, packed later
+    int32_t* wcol = reinterpret_cast<int32_t*>(smem + kOffStage) + warp * kWarpCap;
+    constexpr int64_t kStep = 4 * static_cast<int64_t>(kThreads) * kLoadsInFlight;
+    for (int64_t base = a4; base < b; base += kStep) {
+      typename Vec4<LT>::T v[kLoadsInFlight];
+#pragma unroll
+      for (int u = 0; u < kLoadsInFlight; ++u) {
+        const int64_t i = base + 4 * (tid + static_cast<int64_t>(u) * kThreads);
+        if (i + 3 < b && i >= a) v[u] = Vec4<LT>::load(rp, i);
+      }
+#pragma unroll
+      for (int u = 0; u < kLoadsInFlight; ++u) {
+        const int64_t i = base + 4 * (tid + static_cast<int64_t>(u) * kThreads);
+        if (i >= b) continue;
+        uint32_t kq[4];
+        if (i + 3 < b && i >= a) {
+          Vec4<LT>::keys(v[u], kq);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) kq[e] = (i + e >= a && i + e < b) ? order_key(load_score<LT>(rp, i + e)) : 0u;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (kq[e] >= t && i + e >= a && i + e < b) {
+            const uint32_t slot = atomicAdd(&s_wcount[warp], 1u);
+            if (slot < static_cast<uint32_t>(kWarpCap)) {
+              wkey[slot] = kq[e];
+              wcol[slot] = static_cast<int32_t>(i + e);
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+    // pack the slices: cand_key in place (slices only move down), columns
+    // from the ring area into cand_col
+    {
+      const uint32_t cnt = lane < kWarps ? min(s_wcount[lane], static_cast<uint32_t>(kWarpCap)) : 0u;
+      bool over = false;
+      uint32_t before = 0, total = 0;
+      // every warp computes the exclusive prefix of the 32 slice counts
+      const uint32_t inc = warp_incl_sum(cnt);
+      before = inc - cnt;
+      total = __shfl_sync(0xffffffffu, inc, 31);
+      over = __any_sync(0xffffffffu, lane < kWarps && s_wcount[lane] > static_cast<uint32_t>(kWarpCap));
+      const uint32_t my_before = __shfl_sync(0xffffffffu, before, warp);
+      const uint32_t my_cnt = __shfl_sync(0xffffffffu, cnt, warp);
+      uint32_t keys_tmp[kWarpCap / 32];
+      int32_t cols_tmp[kWarpCap / 32];
+#pragma unroll
+      for (int r = 0; r < kWarpCap / 32; ++r) {
+        const uint32_t j = static_cast<uint32_t>(r * 32 + lane);
+        if (j < my_cnt) {
+          keys_tmp[r] = wkey[j];
+          cols_tmp[r] = wcol[j];
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < kWarpCap / 32; ++r) {
+        const uint32_t j = static_cast<uint32_t>(r * 32 + lane);
+        if (j < my_cnt) {
+          cand_key[my_before + j] = keys_tmp[r];
+          cand_col[my_before + j] = cols_tmp[r];
+        }
+      }
+      if (tid == 0) s_ncand = over ? 0xffffffffu : total;
+    }
+    __syncthreads();
+    const uint32_t nc = s_ncand;
+    if (nc >= static_cast<uint32_t>(k) && nc <= static_cast<uint32_t>(kCandCap)) {
+      select_candidates_and_write(cand_key, cand_col, static_cast<int>(nc), sel, tie, nwords, wa, 0u, 0u,
+                                  static_cast<uint32_t>(k), 0, hist, scan_buf, &s_bin, &s_above, op);
+      return;
+    }
+    __syncthreads();  // the sample missed (rare): exact passes below
+  }
+
   // ---- pass 1: top 11 key bits
   for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
   __syncthreads();
@@ -218,16 +431,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((valid >> e) & 1u) atomicAdd(&hist[kq[e] >> 21], 1u);
   });
   __syncthreads();
-  uint32_t above;
   const uint32_t b1 = find_bin(hist, 2048, static_cast<uint32_t>(k), scan_buf, &s_bin, &s_above, &above);
   uint32_t remaining = static_cast<uint32_t>(k) - above;
   const uint32_t c1 = hist[b1];
   __syncthreads();
 
-  const int64_t wa = a & ~static_cast<int64_t>(31);
   const bool fast = (b - wa) <= kFastMaxCols && c1 <= static_cast<uint32_t>(kCandCap);
   if (fast) {
-    const int nwords = static_cast<int>((b - wa + 31) >> 5);
     for (int i = tid; i < nwords; i += kThreads) {
       sel[i] = 0;
       tie[i] = 0;
@@ -254,61 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     });
     __syncthreads();
     const int nc = min(static_cast<int>(s_ncand), kCandCap);
-    // ---- low bits on the candidates: 11 then 10 bits
-    uint32_t prefix = b1 << 21, prefix_mask = 0x7ffu << 21;
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-      const int shift = pass == 0 ? 10 : 0;
-      const uint32_t nbins = pass == 0 ? 2048u : 1024u;
-      for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
-      __syncthreads();
-      for (int i = tid; i < nc; i += kThreads) {
-        const uint32_t key = cand_key[i];
-        if ((key & prefix_mask) == prefix) atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
-      }
-      __syncthreads();
-      const uint32_t bin = find_bin(hist, nbins, remaining, scan_buf, &s_bin, &s_above, &above);
-      prefix |= bin << shift;
-      prefix_mask |= (nbins - 1) << shift;
-      remaining -= above;
-    }
-    const uint32_t tau = prefix;
-    const uint32_t take_eq = remaining;
-    for (int i = tid; i < nc; i += kThreads) {
-      const uint32_t key = cand_key[i];
-      const int64_t off = cand_col[i] - wa;
-      if (key > tau) atomicOr(&sel[off >> 5], 1u << (off & 31));
-      else if (key == tau) atomicOr(&tie[off >> 5], 1u << (off & 31));
-    }
-    __syncthreads();
-    // ---- ordered output from the bitmaps
-    const int per = (nwords + kThreads - 1) / kThreads;
-    const int w0 = tid * per, w1 = min(nwords, w0 + per);
-    uint32_t nsel = 0, ntie = 0;
-    for (int w = w0; w < w1; ++w) {
-      nsel += __popc(sel[w]);
-      ntie += __popc(tie[w]);
-    }
-    uint32_t tot;
-    const uint32_t ex = block_excl_sum(nsel | (ntie << 16), scan_buf, &tot);
-    uint32_t sel_before = ex & 0xffffu, tie_before = ex >> 16;
-    for (int w = w0; w < w1; ++w) {
-      uint32_t ms = sel[w], mt = tie[w];
-      while (ms | mt) {
-        const uint32_t m = ms | mt;
-        const int bit = __ffs(m) - 1;
-        const int32_t col = static_cast<int32_t>(wa + 32 * static_cast<int64_t>(w) + bit);
-        if ((ms >> bit) & 1u) {
-          op[sel_before + min(tie_before, take_eq)] = col;
-          ++sel_before;
-        } else {
-          if (tie_before < take_eq) op[sel_before + tie_before] = col;
-          ++tie_before;
-        }
-        ms &= ~(1u << bit);
-        mt &= ~(1u << bit);
-      }
-    }
+    select_candidates_and_write(cand_key, cand_col, nc, sel, tie, nwords, wa, b1 << 21, 0x7ffu << 21,
+                                remaining, 1, hist, scan_buf, &s_bin, &s_above, op);
     return;
   }
 
@@ -375,7 +532,6 @@ cudaError_t launch_top_k(const void* logits, int32_t logits_dtype, int64_t logit
                          const int32_t* row_starts, const int32_t* row_ends, int32_t num_rows,
                          int32_t k, int32_t* out_idx, int64_t out_stride, int32_t* status,
                          cudaStream_t stream) {
-  (void)status;
   cudaError_t e;
   if (logits_dtype == DSA_LOGITS_BF16) {
     e = cudaFuncSetAttribute(topk_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -383,14 +539,14 @@ cudaError_t launch_top_k(const void* logits, int32_t logits_dtype, int64_t logit
     if (e != cudaSuccess) return e;
     topk_kernel<__nv_bfloat16><<<num_rows, kThreads, kSmemBytes, stream>>>(
         static_cast<const __nv_bfloat16*>(logits), logits_stride, row_starts, row_ends, k, out_idx,
-        out_stride);
+        out_stride, status);
   } else {
     e = cudaFuncSetAttribute(topk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes);
     if (e != cudaSuccess) return e;
     topk_kernel<float><<<num_rows, kThreads, kSmemBytes, stream>>>(static_cast<const float*>(logits),
                                                                     logits_stride, row_starts,
-                                                                    row_ends, k, out_idx, out_stride);
+                                                                    row_ends, k, out_idx, out_stride, status);
   }
   return cudaGetLastError();
 }
