@@ -52,19 +52,19 @@
 namespace dsa {
 namespace {
 
-// 20 warps: 4 role warps + 16 epilogue warps.  The FP4 variant adds warps
-// 20-23, so that six warps (3, 2, 20-23) share the dequantisation; with six
-// warps on a sub-partition a thread gets at most 80 registers, so its
-// epilogue reads a pair from TMEM in two 32-column halves.
+// Warps 0-3 have the producer, MMA and loader roles; warps 4-19 are four
+// epilogue warpgroups.  FP8: 20 warps, 96 registers a thread, a pair read
+// from TMEM in one 64-column load.  FP4: plus warps 20-23 so that six warps
+// (3, 2, 20-23) share the dequantisation; 24 warps leave 80 registers, so
+// the pair is read in two 32-column pieces.
+template <int kFmt> constexpr int kEpiWgOf = 4;
 template <int kFmt> constexpr int kThreadsOf = kFmt == DSA_KV_FP4 ? 768 : 640;
+template <int kFmt> constexpr int kPieceCols = kFmt == DSA_KV_FP4 ? 32 : 64;
 constexpr int kFp4Converters = 6;
-constexpr int kEpiWarpgroups = 4;  // warps 4..19
-constexpr int kEpiWarps = 4 * kEpiWarpgroups;
+constexpr int kSlots = 8;  // 64-column TMEM slots; pair p of the CTA's stream uses slot p mod 8
 constexpr int kScaleStages = 16;   // key scale ring
 constexpr int kTmemCols = 512;
-constexpr int kBufPairs = 4;       // (tile, row) pairs per TMEM buffer
 constexpr int kPairCols = 64;      // 64 heads of one pair
-constexpr int kBufCols = kBufPairs * kPairCols;
 constexpr int kWBufFloats = kGroupMaxRows * kHeads;       // 512
 constexpr int kPageValBytesFp8 = kPageTokens * kHeadDim;  // 8192
 constexpr int kFp4PageBytes = DSA_FP4_PAGE_BYTES;         // 4864: values, block scales, token scales
@@ -119,7 +119,7 @@ template <int kFmt> struct Smem : Lay<kFmt> {
   static_assert(kOffBar % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(kBytes <= 232448, "over the per-CTA shared memory limit");
 };
-static_assert((kBufPairs & (kBufPairs - 1)) == 0, "power of two");
+static_assert(kSlots * kPairCols == kTmemCols, "TMEM slots");
 static_assert(kFp4AHalfLo == (kTileTokens * 128) >> 4 && kFp4BHalfLo == Lay<DSA_KV_FP4>::kQHalfBytes >> 4,
               "f16 operand halves as laid out by the dequantising warp");
 
@@ -152,9 +152,9 @@ struct Bars {
   __device__ uint32_t sce(int s) const { return sc_empty + 8 * s; }
   __device__ uint32_t wf(int b) const { return w_full + 8 * b; }
   __device__ uint32_t we(int b) const { return w_empty + 8 * b; }
-  // TMEM slot (buffer b, warpgroup w): filled by the MMA, drained by warpgroup w
-  __device__ uint32_t tf(uint32_t b, uint32_t w) const { return tm_full + 8 * (b * kBufPairs + w); }
-  __device__ uint32_t te(uint32_t b, uint32_t w) const { return tm_empty + 8 * (b * kBufPairs + w); }
+  // TMEM slot s: filled by the MMA, drained by the warpgroup of the pair in it
+  __device__ uint32_t tf(uint32_t s) const { return tm_full + 8 * s; }
+  __device__ uint32_t te(uint32_t s) const { return tm_empty + 8 * s; }
 };
 
 // The CTA's walk over its units: groups in order, and the tiles [j0, j1) of
@@ -247,6 +247,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
                   const Params p) {
   using L = Smem<kFmt>;
   constexpr bool kFp4 = kFmt == DSA_KV_FP4;
+  constexpr int kEpiWg = kEpiWgOf<kFmt>;
+  constexpr int kEpiWarps = 4 * kEpiWg;
   constexpr int kStages = L::kKStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -286,8 +288,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   bars.w_full = bars.q_empty + 8;
   bars.w_empty = bars.w_full + 16;
   bars.tm_full = bars.w_empty + 16;
-  bars.tm_empty = bars.tm_full + 8 * 2 * kBufPairs;
-  bars.mma_done = bars.tm_empty + 8 * 2 * kBufPairs;
+  bars.tm_empty = bars.tm_full + 8 * kSlots;
+  bars.mma_done = bars.tm_empty + 8 * kSlots;
   uint32_t* tmem_addr_smem = reinterpret_cast<uint32_t*>(smem + L::kOffTmemAddr);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kOffAbort);
 
@@ -309,10 +311,10 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.wf(b), 1);
       mbar_init(bars.we(b), kEpiWarps);
-      for (uint32_t w = 0; w < kBufPairs; ++w) {
-        mbar_init(bars.tf(b, w), 1);  // the MMA commit of the slot's pair
-        mbar_init(bars.te(b, w), 4);  // the four warps of warpgroup w have read it
-      }
+    }
+    for (uint32_t sl = 0; sl < kSlots; ++sl) {
+      mbar_init(bars.tf(sl), 1);  // the MMA commit of the slot's pair
+      mbar_init(bars.te(sl), 4);  // the four warps of the pair's warpgroup have read it
     }
     mbar_init(bars.mma_done, 1);
     *abort_flag = 0;
@@ -643,22 +645,21 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         uint32_t b_lo = q_lo0;
         uint32_t left = n;
         do {  // the tile's rows, cut where a TMEM buffer ends
-          const uint32_t c = pos & (kBufPairs - 1);
-          const uint32_t b = (pos / kBufPairs) & 1;
-          const uint32_t len = min(left, kBufPairs - c);
+          const uint32_t c = pos & (kSlots - 1);
+          const uint32_t len = min(min(left, kSlots - c), 4u);  // contiguous slots, N <= 256
           // pair pos + i goes to slot (b, c + i), whose previous use (by the
           // pair 8 positions earlier) its warpgroup must have read
           for (uint32_t i = 0; i < len && ok; ++i)
-            ok = warp_wait(bars.te(b, c + i), (((pos + i) >> 3) & 1) ^ 1, abort_flag, p.status);
+            ok = warp_wait(bars.te(c + i), (((pos + i) / kSlots) & 1) ^ 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t d_tmem = tmem + b * kBufCols + c * kPairCols;
+          const uint32_t d_tmem = tmem + c * kPairCols;
           if constexpr (!kFp4) mma_fp8_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20));
           else mma_f16_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20));
           left -= len;
           pos += len;
           b_lo += len * kQRowLo;
-          for (uint32_t i = 0; i < len; ++i) mma_commit_if(issue, bars.tf(b, c + i));
+          for (uint32_t i = 0; i < len; ++i) mma_commit_if(issue, bars.tf(c + i));
         } while (left != 0);
         if (!ok) break;
         mma_commit_if(issue, bars.kve(st));
@@ -677,19 +678,22 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     __syncwarp();
   } else if (warp >= 4 && warp < 4 + kEpiWarps) {
     // =================================================== epilogue
-    // Pair position pos + r belongs to warpgroup (pos + r) mod 4, so this
-    // warp visits r = (wg - pos) mod 4, +4, ... of each tile, and its m-th
-    // pair is the one it takes from fill m of the TMEM buffers: buffer m & 1,
-    // phase m >> 1.
+    // Pair p of the CTA's stream (tile's first pair position pos, row r:
+    // p = pos + r) sits in TMEM slot p mod 8 and belongs to warpgroup
+    // p mod kEpiWg, so this warp visits r = (wg - pos) mod kEpiWg, + kEpiWg,
+    // ... of each tile; the slot's fill index is p / 8.
     //   sum_h w_h relu(x_h) = (sum_h w_h x_h + sum_h w_h |x_h|) / 2
     // so the head reduction is 64 packed FMAs (the |x| is an operand
-    // modifier) instead of 64 max plus 32 packed FMAs.
+    // modifier) instead of 64 max plus 32 packed FMAs.  The 64 columns come
+    // in pieces of kPiece (register budget); the slot is released after the
+    // last piece is read.
+    constexpr int kPiece = kPieceCols<kFmt>;
     const uint32_t wg = static_cast<uint32_t>(warp - 4) >> 2;
     const int quarter = warp & 3;    // TMEM lanes this warp may read
     const int tok = quarter * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + wg * kPairCols;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     OutT* const out = static_cast<OutT*>(p.logits);
-    uint32_t it = 0, gi = 0, pos = 0, m = 0;  // tiles, groups, pairs seen; own pairs taken
+    uint32_t it = 0, gi = 0, pos = 0;  // tiles, groups, pairs seen
     bool ok = true;
     while (ok && walk.next(lane)) {
       const int n = walk.n;
@@ -709,24 +713,27 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         if (lane == 0) mbar_arrive(bars.sce(ss));
         const int scol = j * kTileTokens + tok;
         const bool in_span = scol < lim;
-        for (uint32_t r = (wg - pos) & (kBufPairs - 1); r < static_cast<uint32_t>(n); r += kBufPairs, ++m) {
-          const uint32_t b = m & 1;
-          ok = warp_wait(bars.tf(b, wg), (m >> 1) & 1, abort_flag, p.status);
+        for (uint32_t r = (wg - pos) & (kEpiWg - 1); r < static_cast<uint32_t>(n); r += kEpiWg) {
+          const uint32_t pp = pos + r;
+          const uint32_t sl = pp & (kSlots - 1);
+          ok = warp_wait(bars.tf(sl), (pp / kSlots) & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          float acc;
-          if constexpr (!kFp4) {
-            uint32_t v[64];
-            tmem_ld_x64(t_lane + b * kBufCols, v);
+          const float4* wr = reinterpret_cast<const float4*>(w_grp + r * kHeads);
+          float2 cx = make_float2(0.f, 0.f), ca = cx;
+#pragma unroll
+          for (int pc = 0; pc < kHeads / kPiece; ++pc) {
+            uint32_t v[kPiece];
+            tmem_ld_cols(t_lane + sl * kPairCols + pc * kPiece, v);
             tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.te(b, wg));
-            const float4* wr = reinterpret_cast<const float4*>(w_grp + r * kHeads);
-            float2 cx = make_float2(0.f, 0.f), ca = cx;
-  #pragma unroll
-            for (int h = 0; h < kHeads; h += 4) {
-              const float4 w4 = wr[h / 4];
+            if (pc == kHeads / kPiece - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bars.te(sl));
+            }
+#pragma unroll
+            for (int h = 0; h < kPiece; h += 4) {
+              const float4 w4 = wr[(pc * kPiece + h) / 4];
               const float2 x01 = make_float2(__uint_as_float(v[h + 0]), __uint_as_float(v[h + 1]));
               const float2 x23 = make_float2(__uint_as_float(v[h + 2]), __uint_as_float(v[h + 3]));
               cx = __ffma2_rn(x01, make_float2(w4.x, w4.y), cx);
@@ -734,34 +741,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
               cx = __ffma2_rn(x23, make_float2(w4.z, w4.w), cx);
               ca = __ffma2_rn(make_float2(fabsf(x23.x), fabsf(x23.y)), make_float2(w4.z, w4.w), ca);
             }
-            acc = 0.5f * ((cx.x + cx.y) + (ca.x + ca.y));
-          } else {
-            // two 32-column halves, one at a time (80-register budget)
-            const float4* wr = reinterpret_cast<const float4*>(w_grp + r * kHeads);
-            float2 cx = make_float2(0.f, 0.f), ca = cx;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              uint32_t v[32];
-              tmem_ld_x32(t_lane + b * kBufCols + half * 32, v);
-              tmem_ld_wait();
-              if (half == 1) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars.te(b, wg));
-              }
-#pragma unroll
-              for (int h = 0; h < 32; h += 4) {
-                const float4 w4 = wr[half * 8 + h / 4];
-                const float2 x01 = make_float2(__uint_as_float(v[h + 0]), __uint_as_float(v[h + 1]));
-                const float2 x23 = make_float2(__uint_as_float(v[h + 2]), __uint_as_float(v[h + 3]));
-                cx = __ffma2_rn(x01, make_float2(w4.x, w4.y), cx);
-                ca = __ffma2_rn(make_float2(fabsf(x01.x), fabsf(x01.y)), make_float2(w4.x, w4.y), ca);
-                cx = __ffma2_rn(x23, make_float2(w4.z, w4.w), cx);
-                ca = __ffma2_rn(make_float2(fabsf(x23.x), fabsf(x23.y)), make_float2(w4.z, w4.w), ca);
-              }
-            }
-            acc = 0.5f * ((cx.x + cx.y) + (ca.x + ca.y));
           }
+          const float acc = 0.5f * ((cx.x + cx.y) + (ca.x + ca.y));
           const float logit = (scol < ctx_grp[r]) ? kscale * acc : -INFINITY;
           if (in_span) store_logit(out_grp + static_cast<int64_t>(r) * p.logits_stride + scol, logit);
         }
