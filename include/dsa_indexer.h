@@ -195,6 +195,26 @@ int dsa_top_k_per_row(const void* logits, int32_t logits_dtype, int64_t logits_s
                       int32_t k, int32_t* out_idx, int64_t out_stride, int32_t* status,
                       dsa_stream_t stream);
 
+/*
+ * dsa_selftest_wait_timeout - exercises the failure path of the library's
+ * kernels on the GPU without a fault.  The pages have no counterpart: this is
+ * part of the library's own failure detection.
+ *
+ * Every pipeline wait in the kernels is bounded: a wait that sees no progress
+ * for its time limit (2 s in the production kernels) records
+ * DSA_ERR_TIMEOUT in the caller's status word, tells the other roles of its
+ * CTA to stop, drains what it issued and returns, so the context stays
+ * usable.  This call launches one small kernel that waits, with that same
+ * code and a time limit of timeout_ns, on an mbarrier nothing arrives on.
+ *
+ *   timeout_ns  1e3 .. 1e9 (else DSA_ERR_INVALID_ARG).
+ *   status      (device) int32; receives DSA_ERR_TIMEOUT (first error wins,
+ *               as for the other calls).
+ * Returns DSA_OK once launched; the status is valid after the stream
+ * synchronises.
+ */
+int dsa_selftest_wait_timeout(int64_t timeout_ns, int32_t* status, dsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -53,6 +53,7 @@ _SIGS = {
                                       _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P],
                                      ctypes.c_int),
     "dsa_top_k_per_row": ([_P, _I32, _I64, _P, _P, _I32, _I32, _P, _I64, _P, _P], ctypes.c_int),
+    "dsa_selftest_wait_timeout": ([_I64, _P, _P], ctypes.c_int),
 }
 EXPORTED = tuple(_SIGS)
 
@@ -198,3 +199,10 @@ def top_k_per_row(logits, row_starts, row_ends, k, out=None, status=None):
                                    _ptr(ends), R, int(k), _ptr(out), int(out.stride(0)),
                                    _ptr(status), _stream(device)), "top_k_per_row")
     return out
+
+
+def selftest_wait_timeout(timeout_ns, status):
+    """Launch the bounded-wait self-test: a wait nothing satisfies runs out
+    after timeout_ns and records DSA_ERR_TIMEOUT in `status` (device int32)."""
+    _check(lib().dsa_selftest_wait_timeout(int(timeout_ns), _ptr(status), _stream(status.device)),
+           "selftest_wait_timeout")

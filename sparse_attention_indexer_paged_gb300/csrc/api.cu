@@ -194,4 +194,12 @@ int dsa_top_k_per_row(const void* logits, int32_t logits_dtype, int64_t logits_s
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int dsa_selftest_wait_timeout(int64_t timeout_ns, int32_t* status, dsa_stream_t stream) {
+  if (timeout_ns < 1000 || timeout_ns > 1000000000 || status == nullptr) return DSA_ERR_INVALID_ARG;
+  const int dev = check_device();
+  if (dev != DSA_OK) return dev;
+  return launch_status(launch_selftest_wait(static_cast<uint64_t>(timeout_ns), status,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

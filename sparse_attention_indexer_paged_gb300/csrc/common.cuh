@@ -75,6 +75,8 @@ cudaError_t launch_top_k(const void* logits, int32_t logits_dtype, int64_t logit
                          int32_t k, int32_t* out_idx, int64_t out_stride, int32_t* status,
                          cudaStream_t stream);
 
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, int32_t* status, cudaStream_t stream);
+
 // Tensor-map encoding through the driver entry point (no libcuda link).
 bool encode_tensor_map_u8(void* tmap_out, int rank, void* base, const uint64_t* dims,
                           const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);

@@ -74,19 +74,25 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 // false (without waiting further) once the CTA's abort flag is set, or after
 // kWaitTimeoutNs, in which case it records DSA_ERR_TIMEOUT and sets the flag
 // so that every other role of the CTA stops too.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile int32_t* abort_flag, int32_t* status) {
+__device__ __forceinline__ bool wait_or_abort_for(uint32_t bar, uint32_t parity,
+                                                  volatile int32_t* abort_flag, int32_t* status,
+                                                  uint64_t timeout_ns) {
   if (mbar_try_wait_sleep(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+    if (global_timer_ns() - t0 > timeout_ns) {
       *abort_flag = 1;
       report(status, kErrTimeout);
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int32_t* abort_flag, int32_t* status) {
+  return wait_or_abort_for(bar, parity, abort_flag, status, kWaitTimeoutNs);
 }
 
 // Bounded wait that ignores the abort flag: used while draining copies that

@@ -109,6 +109,13 @@ def test_host_checks_metadata_and_topk(lib):
         dsa.DSA_OK
 
 
+def test_host_checks_selftest(lib):
+    st = P(256)
+    assert lib.dsa_selftest_wait_timeout(999, st, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_selftest_wait_timeout(2_000_000_000, st, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_selftest_wait_timeout(1_000_000, None, None) == dsa.DSA_ERR_INVALID_ARG
+
+
 def test_product_path_has_no_fallback():
     """The package imports nothing from the oracle and has no CPU compute path."""
     pkg = os.path.dirname(dsa.__file__)
