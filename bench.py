@@ -261,50 +261,94 @@ def run_ours(args, rank, world, local):
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         ms_step = float(tt.item())
 
-    # ---- end to end through the C ABI from pinned host buffers
+    # ---- end to end through the C ABI from pinned host buffers.  Every step
+    # copies its inputs host -> device and reads its result back; a serving
+    # loop overlaps step i's kernels with step i+1's input copy and step
+    # i-1's result copy, so device inputs and outputs are double buffered
+    # and three streams are ordered by events.
     hq = wl.q.cpu().pin_memory()
     hw = wl.weights.cpu().pin_memory()
     hctx = wl.context_lens.cpu().pin_memory()
     hind = None if wl.indices is None else wl.indices.cpu().pin_memory()
     hbt = wl.block_table.cpu().pin_memory()
-    hidx = torch.empty((T, wl.topk), dtype=torch.int32).pin_memory()
-    dq, dw, dctx = torch.empty_like(wl.q), torch.empty_like(wl.weights), torch.empty_like(wl.context_lens)
-    dind = None if hind is None else torch.empty_like(wl.indices)
-    dbt = torch.empty_like(wl.block_table)
-    didx = torch.empty_like(idx)
-    meta2, lg2, tk2 = make_calls(dq, dw, dctx, dind, dbt, didx)
-    h2d = [(dq, hq), (dw, hw), (dctx, hctx), (dbt, hbt)] + ([(dind, hind)] if hind is not None else [])
-    h2d_bytes = sum(h.numel() * h.element_size() for _, h in h2d)
-    d2h_bytes = hidx.numel() * hidx.element_size()
+    hidx = [torch.empty((T, wl.topk), dtype=torch.int32).pin_memory() for _ in range(2)]
+    sets = []
+    for _ in range(2):
+        dq, dw, dctx = torch.empty_like(wl.q), torch.empty_like(wl.weights), torch.empty_like(wl.context_lens)
+        dind = None if hind is None else torch.empty_like(wl.indices)
+        dbt = torch.empty_like(wl.block_table)
+        didx = torch.empty_like(idx)
+        h2d = [(dq, hq), (dw, hw), (dctx, hctx), (dbt, hbt)] + ([(dind, hind)] if hind is not None else [])
+        sets.append(dict(h2d=h2d, didx=didx, calls=make_calls(dq, dw, dctx, dind, dbt, didx)))
+    h2d_bytes = sum(h.numel() * h.element_size() for _, h in sets[0]["h2d"])
+    d2h_bytes = hidx[0].numel() * hidx[0].element_size()
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_ready = [torch.cuda.Event() for _ in range(2)]     # inputs of the set copied in
+    ev_done = [torch.cuda.Event() for _ in range(2)]      # kernels of the set finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]       # result of the set copied out
+    for e in ev_done + ev_out:
+        e.record(stream)
 
-    def e2e_step():
-        for d, h in h2d:
-            d.copy_(h, non_blocking=True)
-        r = (L.dsa_paged_mqa_logits_metadata(*meta2) | L.dsa_fp8_fp4_paged_mqa_logits(*lg2)
-             | L.dsa_top_k_per_row(*tk2))
-        hidx.copy_(didx, non_blocking=True)
+    def e2e_step(i):
+        st = sets[i % 2]
+        s_in.wait_event(ev_done[i % 2])       # the kernels that read this set are done
+        with torch.cuda.stream(s_in):
+            for d, h in st["h2d"]:
+                d.copy_(h, non_blocking=True)
+        ev_ready[i % 2].record(s_in)
+        stream.wait_event(ev_ready[i % 2])
+        stream.wait_event(ev_out[i % 2])      # its previous result was copied out
+        m, lgc, tkc = st["calls"]
+        r = L.dsa_paged_mqa_logits_metadata(*m) | L.dsa_fp8_fp4_paged_mqa_logits(*lgc) | L.dsa_top_k_per_row(*tkc)
+        ev_done[i % 2].record(stream)
+        s_out.wait_event(ev_done[i % 2])
+        with torch.cuda.stream(s_out):
+            hidx[i % 2].copy_(st["didx"], non_blocking=True)
+        ev_out[i % 2].record(s_out)
         return r
 
-    for _ in range(3):
-        assert e2e_step() == 0
+    for i in range(4):
+        assert e2e_step(i) == 0
     torch.cuda.synchronize()
-    assert torch.equal(hidx, idx.cpu()), "e2e result differs from the device-resident run"
+    assert torch.equal(hidx[0], idx.cpu()) and torch.equal(hidx[1], idx.cpu()), \
+        "e2e result differs from the device-resident run"
     KE = args.e2e_steps
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(KE):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(KE):
+        e2e_step(i)
+    e1.record(s_out)   # after the last result copy, which follows the last step's kernels
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / KE
     if world > 1:
         tt = torch.tensor([e2e_ms], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(tt.item())
+    # the same step with nothing overlapped (copy in, kernels, copy out, all
+    # on one stream): the per-step latency a single request stream sees
+    st0 = sets[0]
+
+    def serial_step():
+        for d, h in st0["h2d"]:
+            d.copy_(h, non_blocking=True)
+        m, lgc, tkc = st0["calls"]
+        r = L.dsa_paged_mqa_logits_metadata(*m) | L.dsa_fp8_fp4_paged_mqa_logits(*lgc) | L.dsa_top_k_per_row(*tkc)
+        hidx[0].copy_(st0["didx"], non_blocking=True)
+        return r
+
+    for _ in range(3):
+        assert serial_step() == 0
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(KE):
+        serial_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_serial_ms = e0.elapsed_time(e1) / KE
 
     # ---- roofline of the dominant kernel (logits)
     hbm_gbs, bf16_tf, peak_src = peaks()
@@ -361,7 +405,7 @@ def run_ours(args, rank, world, local):
             "step_roofline_frac": round(max(t_mem, t_tc) / (ms_step * 1e-3), 4),
         },
         "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": "us/step",
-                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes},
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "serialized_value": round(e2e_serial_ms * 1e3, 3), "pipelining": "step i kernels overlap step i+1 input copy and step i-1 result copy"},
         "gpu_launches": 3 * K,
         "clocks": clk,
         "context": PAGES_CONTEXT,
