@@ -76,6 +76,14 @@ def lib():
             L.oracle_schedule.restype = ctypes.c_int
             L.oracle_schedule_words.argtypes = [i32, i32]
             L.oracle_schedule_words.restype = i64
+            L.oracle_dcp_global_id.argtypes = [i64, i32, i32, i32]
+            L.oracle_dcp_global_id.restype = i64
+            L.oracle_dcp_local_len.argtypes = [i64, i32, i32, i32]
+            L.oracle_dcp_local_len.restype = i64
+            L.oracle_dcp_pack.argtypes = [P, i64, P, i64, i32, i32, i32, i32, i32, P]
+            L.oracle_dcp_pack.restype = ctypes.c_int
+            L.oracle_dcp_merge.argtypes = [P, i32, i32, i32, P, i64]
+            L.oracle_dcp_merge.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -198,3 +206,42 @@ def workload_logits(wl, rows=None, with_bound=True, nthreads=0, out_cols=None):
                             wl.context_lens, wl.block_table,
                             wl.logits_stride if out_cols is None else out_cols,
                             rows=rows, with_bound=with_bound, nthreads=nthreads)
+
+
+# ---------------------------------------------------------------------------
+# DCP sharding and exact merge of per-rank top-k candidates
+# ---------------------------------------------------------------------------
+
+def dcp_global_id(local, rank, world, interleave):
+    return int(lib().oracle_dcp_global_id(int(local), int(rank), int(world), int(interleave)))
+
+
+def dcp_local_len(length, rank, world, interleave):
+    return int(lib().oracle_dcp_local_len(int(length), int(rank), int(world), int(interleave)))
+
+
+def dcp_pack(local_scores, local_idx, k, rank, world, interleave):
+    """[rows, k, 2] float64 (score, global id) of a rank's local top-k."""
+    sc = _np(local_scores, np.float64)
+    if sc.ndim == 1:
+        sc = sc.reshape(1, -1)
+    li = _np(local_idx, np.int32)
+    if li.ndim == 1:
+        li = li.reshape(1, -1)
+    out = np.zeros((sc.shape[0], int(k), 2), dtype=np.float64)
+    st = lib().oracle_dcp_pack(_ptr(sc), sc.shape[1], _ptr(li), li.shape[1], sc.shape[0], int(k),
+                               int(rank), int(world), int(interleave), _ptr(out))
+    if st != ORACLE_OK:
+        raise OracleError(st, "dcp_pack")
+    return out
+
+
+def dcp_merge(gathered, k):
+    """gathered [world, rows, k, 2] (score, global id) -> int32 [rows, k] global top-k."""
+    g = _np(gathered, np.float64)
+    world, rows = g.shape[0], g.shape[1]
+    out = np.zeros((rows, int(k)), dtype=np.int32)
+    st = lib().oracle_dcp_merge(_ptr(g), world, rows, int(k), _ptr(out), int(k))
+    if st != ORACLE_OK:
+        raise OracleError(st, "dcp_merge")
+    return out

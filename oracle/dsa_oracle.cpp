@@ -430,4 +430,90 @@ int64_t oracle_schedule_words(int32_t num_sms, int32_t num_rows) {
   return 8 + (static_cast<int64_t>(num_sms) + 1) + 2 * (static_cast<int64_t>(num_rows) + 1);
 }
 
+// ---------------------------------------------------------------------------
+// DCP (decode context parallelism): each rank holds 1/world of every
+// request's keys and computes logits and a top-k over its shard; the ranks'
+// top-k candidates are merged into the global top-k (sparse_attn_indexer
+// docs, _merge_dcp_topk_global: pack (score, global id) per candidate,
+// all-gather rank-major [world, rows, k, 2], stable top-k over the
+// candidates; a token in the global top-k is in its owner's local top-k, so
+// the merge is exact).
+//
+// Readings (the page names the interleave size and the packed layout but
+// does not print the mapping or the output order):
+//   * keys go to ranks in blocks of `interleave` consecutive tokens, round
+//     robin: global token g lives on rank (g / I) mod world at local
+//     position (g / (I * world)) * I + g mod I;
+//   * a padded local slot (-1) packs as (-inf, -1) and is never chosen;
+//   * the merged row is the global top-k in this library's top-k order:
+//     larger score first, equal scores to the lower global id, NaN below
+//     every number; the chosen ids in ascending order, then -1 up to k.
+// ---------------------------------------------------------------------------
+int64_t oracle_dcp_global_id(int64_t local, int32_t rank, int32_t world, int32_t interleave) {
+  if (local < 0 || world < 1 || interleave < 1 || rank < 0 || rank >= world) return -1;
+  const int64_t I = interleave;
+  return ((local / I) * world + rank) * I + local % I;
+}
+
+int64_t oracle_dcp_local_len(int64_t len, int32_t rank, int32_t world, int32_t interleave) {
+  if (len <= 0 || world < 1 || interleave < 1 || rank < 0 || rank >= world) return 0;
+  int64_t n = 0;  // count the global tokens below len that live on `rank`
+  for (int64_t g = 0; g < len; ++g)
+    if ((g / interleave) % world == rank) ++n;
+  return n;
+}
+
+// packed[t][j] = (score of local column local_idx[t][j], its global id), or
+// (-inf, -1) for a padded slot.
+int oracle_dcp_pack(const double* local_scores, int64_t stride, const int32_t* local_idx,
+                    int64_t idx_stride, int32_t num_rows, int32_t k, int32_t rank, int32_t world,
+                    int32_t interleave, double* packed) {
+  if (!local_scores || !local_idx || !packed || num_rows < 0 || k < 1 || idx_stride < k ||
+      world < 1 || interleave < 1 || rank < 0 || rank >= world)
+    return ORACLE_ERR_ARG;
+  for (int t = 0; t < num_rows; ++t) {
+    for (int j = 0; j < k; ++j) {
+      const int32_t l = local_idx[static_cast<int64_t>(t) * idx_stride + j];
+      double* o = packed + (static_cast<int64_t>(t) * k + j) * 2;
+      if (l < 0 || l >= stride) {
+        o[0] = -std::numeric_limits<double>::infinity();
+        o[1] = -1.0;
+      } else {
+        o[0] = local_scores[static_cast<int64_t>(t) * stride + l];
+        o[1] = static_cast<double>(oracle_dcp_global_id(l, rank, world, interleave));
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+// gathered: [world][rows][k][2]; out: the global top-k ids of each row.
+int oracle_dcp_merge(const double* gathered, int32_t world, int32_t num_rows, int32_t k,
+                     int32_t* out_idx, int64_t out_stride) {
+  if (!gathered || !out_idx || world < 1 || num_rows < 0 || k < 1 || out_stride < k)
+    return ORACLE_ERR_ARG;
+  for (int t = 0; t < num_rows; ++t) {
+    std::vector<std::pair<double, int64_t>> cand;  // (score, global id)
+    for (int r = 0; r < world; ++r)
+      for (int j = 0; j < k; ++j) {
+        const double* c = gathered + ((static_cast<int64_t>(r) * num_rows + t) * k + j) * 2;
+        if (c[1] >= 0) cand.emplace_back(c[0], static_cast<int64_t>(c[1]));
+      }
+    auto better = [](const std::pair<double, int64_t>& x, const std::pair<double, int64_t>& y) {
+      const bool nx = std::isnan(x.first), ny = std::isnan(y.first);
+      if (nx != ny) return ny;  // a number before NaN
+      if (!nx && x.first != y.first) return g_plant == 8 ? x.first < y.first : x.first > y.first;
+      return g_plant == 9 ? x.second > y.second : x.second < y.second;
+    };
+    std::sort(cand.begin(), cand.end(), better);
+    const int64_t take = std::min<int64_t>(k, static_cast<int64_t>(cand.size()));
+    std::vector<int64_t> chosen;
+    for (int64_t i = 0; i < take; ++i) chosen.push_back(cand[static_cast<size_t>(i)].second);
+    std::sort(chosen.begin(), chosen.end());
+    int32_t* out = out_idx + static_cast<int64_t>(t) * out_stride;
+    for (int64_t i = 0; i < k; ++i) out[i] = i < take ? static_cast<int32_t>(chosen[static_cast<size_t>(i)]) : -1;
+  }
+  return ORACLE_OK;
+}
+
 }  // extern "C"

@@ -258,10 +258,54 @@ def check_fp4_bruteforce():
     check_bruteforce(kv_format=W.KV_FP4, seed=21)
 
 
+def check_dcp_mapping():
+    """Each rank's tokens, enumerated in global order, are its local positions
+    0, 1, ...; the mapping and the shard lengths must agree with that."""
+    for world in (1, 2, 3, 4):
+        for inter in (1, 2, 3, 5):
+            L = 97
+            owned = {r: [g for g in range(L) if (g // inter) % world == r] for r in range(world)}
+            assert sum(len(v) for v in owned.values()) == L
+            for r, gs in owned.items():
+                assert oracle.dcp_local_len(L, r, world, inter) == len(gs)
+                for local, g in enumerate(gs):
+                    assert oracle.dcp_global_id(local, r, world, inter) == g
+
+
+def _dcp_merge_of_shards(sc, ends, k, world, inter):
+    """Per-rank oracle top-k over each rank's own columns, packed, gathered
+    rank-major and merged."""
+    rows = sc.shape[0]
+    packs = []
+    for r in range(world):
+        cols = [g for g in range(sc.shape[1]) if (g // inter) % world == r]
+        loc = sc[:, cols] if cols else np.zeros((rows, 1))
+        loc_ends = np.array([sum(1 for g in cols if g < e) for e in ends], dtype=np.int32)
+        lidx = oracle.top_k_per_row(loc, loc_ends, k)
+        packs.append(oracle.dcp_pack(loc, lidx, k, r, world, inter))
+    return oracle.dcp_merge(np.stack(packs), k)
+
+
+def check_dcp_merge_is_global_topk(seed=0):
+    """The merge of per-rank top-k equals the top-k of the whole row (the
+    exactness argument of _merge_dcp_topk_global), ties and NaN included."""
+    rng = np.random.default_rng(seed)
+    rows, L = 5, 300
+    sc = np.round(rng.standard_normal((rows, L)) * 3) / 2   # coarse grid: many ties
+    sc[0, ::7] = np.nan
+    sc[1, :50] = -np.inf
+    ends = np.array([L, 260, 17, 1, 0], dtype=np.int32)
+    for world, inter, k in ((1, 1, 16), (2, 1, 16), (3, 4, 37), (4, 64, 64), (2, 7, 1), (3, 1, 300)):
+        got = _dcp_merge_of_shards(sc, ends, k, world, inter)
+        want = oracle.top_k_per_row(sc, ends, k)
+        assert np.array_equal(got, want), (world, inter, k)
+
+
 PIN_CHECKS = [
     check_e4m3_vs_torch, check_e2m1_vs_spec, check_bruteforce, check_one_hot_reads_key,
     check_relu_identities, check_weight_scaling, check_page_permutation,
     check_varlen_equals_padded, check_topk_bruteforce, check_fp4_bruteforce,
+    check_dcp_mapping, check_dcp_merge_is_global_topk,
 ]
 
 
@@ -410,6 +454,8 @@ PLANTS = {
     5: "head weight dropped",
     6: "FP4 block scale index d / 32 for d / 16",
     7: "top-k order reversed",
+    8: "DCP merge keeps the smallest scores",
+    9: "DCP merge breaks score ties to the higher global id",
 }
 
 
