@@ -7,6 +7,7 @@ block_kv = 64, 1..6 rows per request, top-k 2048) unless --workload says
 otherwise.  Inputs are synthetic and seeded (workloads.config).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --dcp-world R [--dcp-interleave I]
 
 Prints one JSON line (rank 0).  `value` is device time per step with inputs
 resident in HBM; `e2e` is the same step through the C ABI from pinned host
@@ -14,6 +15,13 @@ buffers, with the per-step host->device input copies and the device->host
 read of the top-k indices inside the timed region.  `--impl reference` times
 the CPU oracle (the only other implementation of the method here) on a
 bounded sample of the same workload and scales it to one step.
+
+`--dcp-world R` times decode context parallelism on one GPU instead: each of
+R ranks' steps (metadata, logits and top-k over its 1/R of every request's
+keys, then the candidate pack) run in turn, the packs are stacked by a
+device copy where R GPUs would all-gather them, and the merge kernel gives
+the global top-k, which is checked against the unsharded step's.  It prints
+one JSON line of per-rank and merge kernel times.
 """
 from __future__ import annotations
 
@@ -50,6 +58,10 @@ def parse():
     ap.add_argument("--cpu-budget-s", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dcp-world", type=int, default=0,
+                    help="time the decode-context-parallel step instead: the workload's keys split "
+                         "over this many ranks, every rank emulated in turn on this GPU")
+    ap.add_argument("--dcp-interleave", type=int, default=1)
     return ap.parse_args()
 
 
@@ -418,6 +430,137 @@ def run_ours(args, rank, world, local):
 
 
 # ---------------------------------------------------------------------------
+# decode context parallelism, the ranks emulated in turn on one GPU
+# ---------------------------------------------------------------------------
+
+def run_dcp(args, local):
+    import torch
+    import sparse_attention_indexer_paged_gb300 as dsa
+    import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsa.build()
+    L = dsa.lib()
+    R, inter = args.dcp_world, args.dcp_interleave
+    base = W.config(args.workload)
+    shards = [W.dcp_shard(base, r, R, inter).to(dev) for r in range(R)]
+    glob = base.to(dev)
+    T, k, S = glob.num_rows, glob.topk, dsa.device_num_sms()
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ldt = torch.float32 if glob.logits_dtype == 0 else torch.bfloat16
+
+    def calls(wl, r):
+        sched = torch.empty(dsa.schedule_words(S, T), dtype=torch.int32, device=dev)
+        logits = torch.empty((T, wl.logits_stride), dtype=ldt, device=dev)
+        idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        packed = torch.empty((T, k, 2), dtype=torch.float32, device=dev)
+        meta = (P(wl.context_lens), P(wl.indices), T, 64, S, P(sched), sp)
+        lg = (P(wl.q), P(wl.kv_cache), wl.page_stride, wl.num_pages, wl.kv_format, P(wl.weights),
+              P(wl.context_lens), P(wl.block_table), wl.block_table.stride(0), P(wl.indices), P(sched), S,
+              P(logits), wl.logits_dtype, wl.logits_stride, T, 64, 128, 64, P(status), sp)
+        tk = (P(logits), wl.logits_dtype, wl.logits_stride, None, P(wl.context_lens), T, k, P(idx),
+              idx.stride(0), P(status), sp)
+        pk = (P(logits), wl.logits_dtype, wl.logits_stride, P(idx), idx.stride(0), T, k, r, R, inter,
+              P(packed), sp)
+        return dict(keep=(sched, logits, idx), packed=packed, meta=meta, lg=lg, tk=tk, pk=pk)
+
+    ranks = [calls(sh, r) for r, sh in enumerate(shards)]
+    gathered = torch.empty((R, T, k, 2), dtype=torch.float32, device=dev)
+    merged = torch.empty((T, k), dtype=torch.int32, device=dev)
+    mg = (P(gathered), R, T, k, P(merged), merged.stride(0), sp)
+    ref = calls(glob, 0)
+
+    def step(ev=None):
+        rc = 0
+        for r, c in enumerate(ranks):
+            if ev is not None:
+                ev[r][0].record(stream)
+            rc |= L.dsa_paged_mqa_logits_metadata(*c["meta"])
+            if ev is not None:
+                ev[r][1].record(stream)
+            rc |= L.dsa_fp8_fp4_paged_mqa_logits(*c["lg"])
+            if ev is not None:
+                ev[r][2].record(stream)
+            rc |= L.dsa_top_k_per_row(*c["tk"])
+            if ev is not None:
+                ev[r][3].record(stream)
+            rc |= L.dsa_dcp_pack_topk(*c["pk"])
+            if ev is not None:
+                ev[r][4].record(stream)
+        for r, c in enumerate(ranks):      # where R GPUs would all-gather
+            gathered[r].copy_(c["packed"])
+        if ev is not None:
+            ev[R][0].record(stream)
+        rc |= L.dsa_dcp_merge_topk(*mg)
+        if ev is not None:
+            ev[R][1].record(stream)
+        return rc
+
+    # the unsharded step, for the exactness check
+    assert (L.dsa_paged_mqa_logits_metadata(*ref["meta"]) | L.dsa_fp8_fp4_paged_mqa_logits(*ref["lg"])
+            | L.dsa_top_k_per_row(*ref["tk"])) == 0
+    for _ in range(max(args.warmup, 3)):
+        assert step() == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, dsa.status_string(int(status.item()))
+    exact = bool(torch.equal(merged, ref["keep"][2]))
+
+    K = args.steps
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(R + 1)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert int(status.item()) == 0, dsa.status_string(int(status.item()))
+
+    def avg(r, a, b):
+        return sum(e[r][a].elapsed_time(e[r][b]) for e in evs) / K * 1e3
+
+    per_rank = [dict(metadata=round(avg(r, 0, 1), 3), logits=round(avg(r, 1, 2), 3),
+                     top_k=round(avg(r, 2, 3), 3), pack=round(avg(r, 3, 4), 3), step=round(avg(r, 0, 4), 3))
+                for r in range(R)]
+    merge_us = avg(R, 0, 1)
+    crit = max(x["step"] for x in per_rank) + merge_us
+    hbm_gbs, _, peak_src = peaks()
+    merge_bytes = R * T * k * 8 + T * k * 4
+    merge_gbs = merge_bytes / (merge_us * 1e-6) / 1e9
+    return {
+        "metric": "indexer DCP decode µs/step on the critical path (slowest rank's step + merge; "
+                  "the all-gather not timed: one GPU)",
+        "value": round(crit, 3),
+        "unit": "us/step",
+        "higher_is_better": False,
+        "n_gpus": 1,
+        "steps": K,
+        "warmup": args.warmup,
+        "dtype": "e4m3 x e4m3 -> f32" if glob.kv_format == 0 else "e4m3 x e2m1 -> f32",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload} split over {R} DCP ranks (interleave {inter})",
+                   "shape": workload_desc(args.workload, base), "rows": T, "num_sms": S,
+                   "emulation": "ranks run in turn on one GPU; packs stacked by device copies"},
+        "exact_vs_unsharded": exact,
+        "kernels_us": {"per_rank": per_rank, "merge": round(merge_us, 3)},
+        "all_ranks_serial_us": round(t0.elapsed_time(t1) / K * 1e3, 3),
+        "merge_roofline": {"bound": "hbm", "algorithmic_bytes": merge_bytes, "achieved": round(merge_gbs, 1),
+                           "peak": hbm_gbs, "unit": "GB/s", "frac": round(merge_gbs / hbm_gbs, 4),
+                           "peak_source": peak_src},
+        "gpu_launches": (4 * R + 1) * K,
+        "clocks": clk,
+    }
+
+
+# ---------------------------------------------------------------------------
 # the oracle timed on the host cores
 # ---------------------------------------------------------------------------
 
@@ -496,6 +639,9 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, rank, world)
+    elif args.dcp_world > 0:
+        assert world == 1, "the DCP emulation runs in one process"
+        res = run_dcp(args, local)
     else:
         res = run_ours(args, rank, world, local)
     if rank == 0 and res is not None:

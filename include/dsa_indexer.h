@@ -72,6 +72,8 @@ enum { DSA_LOGITS_F32 = 0, DSA_LOGITS_BF16 = 1 };
 #define DSA_FP4_PAGE_BYTES 4864
 /* Largest k of dsa_top_k_per_row. */
 #define DSA_MAX_TOPK 2048
+/* Largest decode-context-parallel world the merge accepts. */
+#define DSA_DCP_MAX_WORLD 8
 
 /* Text of a status code (static storage). */
 const char* dsa_status_string(int status);
@@ -194,6 +196,58 @@ int dsa_top_k_per_row(const void* logits, int32_t logits_dtype, int64_t logits_s
                       const int32_t* row_starts, const int32_t* row_ends, int32_t num_rows,
                       int32_t k, int32_t* out_idx, int64_t out_stride, int32_t* status,
                       dsa_stream_t stream);
+
+/*
+ * dsa_dcp_pack_topk - packs one rank's local top-k for the decode context
+ * parallel merge ([DOCS] _merge_dcp_topk_global: every rank holds 1/world of
+ * each request's keys, scores them and takes a local top-k; the candidates
+ * travel as (score, global token id) fp32 pairs).
+ *
+ * Shard mapping (the page names the interleave size; this is the reading):
+ * keys go to ranks in blocks of `interleave` consecutive tokens, round robin,
+ * so local position l of rank r holds global token
+ * ((l / interleave) * world + r) * interleave + l % interleave.
+ *
+ *   logits       (device) fp32 or bf16 [num_rows][logits_stride]: this rank's
+ *                local logits; logits_stride * world < 2^24 so that global
+ *                ids are exact in fp32.
+ *   local_idx    (device) int32 [num_rows][idx_stride]: this rank's top-k
+ *                local columns (from dsa_top_k_per_row), -1 padded.
+ *   k            1 .. DSA_MAX_TOPK; idx_stride >= k.
+ *   dcp_rank, dcp_world, interleave: 0 <= rank < world <= DSA_DCP_MAX_WORLD,
+ *                interleave >= 1.
+ *   packed       (device) fp32 [num_rows][k][2]: (score, global id), or
+ *                (-inf, -1) for a padded or out-of-range local column.
+ */
+int dsa_dcp_pack_topk(const void* logits, int32_t logits_dtype, int64_t logits_stride,
+                      const int32_t* local_idx, int64_t idx_stride, int32_t num_rows, int32_t k,
+                      int32_t dcp_rank, int32_t dcp_world, int32_t interleave, float* packed,
+                      dsa_stream_t stream);
+
+/*
+ * dsa_dcp_merge_topk - the global top-k from every rank's packed candidates
+ * ([DOCS] _merge_dcp_topk_global: all-gather rank-major, then a stable top-k
+ * over the candidates; a token in the global top-k has at most k - 1 tokens
+ * above it, hence is in its own rank's local top-k, so the merge is exact).
+ *
+ *   gathered     (device) fp32 [dcp_world][num_rows][k][2], rank-major (the
+ *                layout an all-gather along dim 0 of the packs produces).
+ *   dcp_world    1 .. DSA_DCP_MAX_WORLD.
+ *   out_idx      (device) int32 [num_rows][out_stride], out_stride >= k: the
+ *                global ids of the k best candidates (larger score first,
+ *                equal scores to the lower id, NaN below every number) in
+ *                ascending order, then -1 up to k.  Candidates with id -1 are
+ *                never chosen.
+ *
+ * Candidate ids are integers in [0, 2^24), distinct within a row (as
+ * dsa_dcp_pack_topk writes them); their order inside the gathered rows is
+ * free.  A repeated id is written once.  Returns DSA_ERR_UNSUPPORTED for k or
+ * dcp_world out of range and DSA_ERR_INVALID_ARG for a null or misaligned
+ * pointer or out_stride < k; the caller owns every buffer and nothing is
+ * allocated.
+ */
+int dsa_dcp_merge_topk(const float* gathered, int32_t dcp_world, int32_t num_rows, int32_t k,
+                       int32_t* out_idx, int64_t out_stride, dsa_stream_t stream);
 
 /*
  * dsa_selftest_wait_timeout - exercises the failure path of the library's

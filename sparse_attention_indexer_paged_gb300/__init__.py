@@ -54,6 +54,8 @@ _SIGS = {
                                      ctypes.c_int),
     "dsa_top_k_per_row": ([_P, _I32, _I64, _P, _P, _I32, _I32, _P, _I64, _P, _P], ctypes.c_int),
     "dsa_selftest_wait_timeout": ([_I64, _P, _P], ctypes.c_int),
+    "dsa_dcp_pack_topk": ([_P, _I32, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P], ctypes.c_int),
+    "dsa_dcp_merge_topk": ([_P, _I32, _I32, _I32, _P, _I64, _P], ctypes.c_int),
 }
 EXPORTED = tuple(_SIGS)
 
@@ -206,3 +208,56 @@ def selftest_wait_timeout(timeout_ns, status):
     after timeout_ns and records DSA_ERR_TIMEOUT in `status` (device int32)."""
     _check(lib().dsa_selftest_wait_timeout(int(timeout_ns), _ptr(status), _stream(status.device)),
            "selftest_wait_timeout")
+
+
+# ---------------------------------------------------------------------------
+# decode context parallelism: per-rank top-k -> (score, global id) packs ->
+# rank-major all-gather -> exact merge into the global top-k
+# ---------------------------------------------------------------------------
+
+def dcp_pack_topk(logits, local_idx, k, rank, world, interleave, out=None):
+    """This rank's local top-k columns as fp32 (score, global id) pairs [rows, k, 2]."""
+    if logits.dtype == torch.float32:
+        dt = LOGITS_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = LOGITS_BF16
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    assert logits.stride(-1) == 1 and local_idx.dtype == torch.int32 and local_idx.stride(-1) == 1
+    R = int(logits.shape[0])
+    if out is None:
+        out = torch.empty((R, int(k), 2), dtype=torch.float32, device=logits.device)
+    assert out.is_contiguous() and out.shape == (R, int(k), 2)
+    _check(lib().dsa_dcp_pack_topk(_ptr(logits), dt, int(logits.stride(0)), _ptr(local_idx),
+                                   int(local_idx.stride(0)), R, int(k), int(rank), int(world),
+                                   int(interleave), _ptr(out), _stream(logits.device)), "dcp_pack_topk")
+    return out
+
+
+def dcp_merge_topk(gathered, k, out=None):
+    """gathered fp32 [world, rows, k, 2] (rank-major) -> int32 [rows, k] global top-k ids."""
+    assert gathered.dtype == torch.float32 and gathered.is_contiguous() and gathered.dim() == 4
+    world, R = int(gathered.shape[0]), int(gathered.shape[1])
+    if out is None:
+        out = torch.empty((R, int(k)), dtype=torch.int32, device=gathered.device)
+    _check(lib().dsa_dcp_merge_topk(_ptr(gathered), world, R, int(k), _ptr(out), int(out.stride(0)),
+                                    _stream(gathered.device)), "dcp_merge_topk")
+    return out
+
+
+def dcp_gather_candidates(packed, world, group=None):
+    """All-gather every rank's packs along a new leading dim: [world, rows, k, 2],
+    rank r's pack at index r (torch.distributed; NCCL on GPUs)."""
+    packed = packed.contiguous()
+    flat = torch.empty((int(world) * packed.shape[0],) + tuple(packed.shape[1:]), dtype=packed.dtype,
+                       device=packed.device)
+    torch.distributed.all_gather_into_tensor(flat, packed, group=group)
+    return flat.view((int(world),) + tuple(packed.shape))
+
+
+def dcp_topk(logits, local_idx, k, rank, world, interleave, group=None, out=None):
+    """The global top-k of a decode-context-parallel step on this rank: pack the
+    local top-k, all-gather over `group`, merge (every rank gets the result)."""
+    packed = dcp_pack_topk(logits, local_idx, k, rank, world, interleave)
+    gathered = dcp_gather_candidates(packed, world, group) if world > 1 else packed.unsqueeze(0)
+    return dcp_merge_topk(gathered, k, out=out)

@@ -194,6 +194,36 @@ int dsa_top_k_per_row(const void* logits, int32_t logits_dtype, int64_t logits_s
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int dsa_dcp_pack_topk(const void* logits, int32_t logits_dtype, int64_t logits_stride,
+                      const int32_t* local_idx, int64_t idx_stride, int32_t num_rows, int32_t k,
+                      int32_t dcp_rank, int32_t dcp_world, int32_t interleave, float* packed,
+                      dsa_stream_t stream) {
+  if (logits_dtype != DSA_LOGITS_F32 && logits_dtype != DSA_LOGITS_BF16) return DSA_ERR_UNSUPPORTED;
+  if (k < 1 || k > DSA_MAX_TOPK || dcp_world < 1 || dcp_world > DSA_DCP_MAX_WORLD) return DSA_ERR_UNSUPPORTED;
+  if (num_rows < 0 || idx_stride < k || dcp_rank < 0 || dcp_rank >= dcp_world || interleave < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (logits_stride < 1 || logits_stride * dcp_world >= (int64_t{1} << 24)) return DSA_ERR_INVALID_ARG;
+  if (num_rows == 0) return DSA_OK;
+  if (!logits || !local_idx || !packed || !aligned(packed, 8)) return DSA_ERR_INVALID_ARG;
+  const int dev = check_device();
+  if (dev != DSA_OK) return dev;
+  return launch_status(launch_dcp_pack(logits, logits_dtype, logits_stride, local_idx, idx_stride, num_rows, k,
+                                       dcp_rank, dcp_world, interleave, packed,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dsa_dcp_merge_topk(const float* gathered, int32_t dcp_world, int32_t num_rows, int32_t k,
+                       int32_t* out_idx, int64_t out_stride, dsa_stream_t stream) {
+  if (k < 1 || k > DSA_MAX_TOPK || dcp_world < 1 || dcp_world > DSA_DCP_MAX_WORLD) return DSA_ERR_UNSUPPORTED;
+  if (num_rows < 0 || out_stride < k) return DSA_ERR_INVALID_ARG;
+  if (num_rows == 0) return DSA_OK;
+  if (!gathered || !out_idx || !aligned(gathered, 8)) return DSA_ERR_INVALID_ARG;
+  const int dev = check_device();
+  if (dev != DSA_OK) return dev;
+  return launch_status(launch_dcp_merge(gathered, dcp_world, num_rows, k, out_idx, out_stride,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int dsa_selftest_wait_timeout(int64_t timeout_ns, int32_t* status, dsa_stream_t stream) {
   if (timeout_ns < 1000 || timeout_ns > 1000000000 || status == nullptr) return DSA_ERR_INVALID_ARG;
   const int dev = check_device();

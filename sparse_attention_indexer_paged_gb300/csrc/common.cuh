@@ -75,6 +75,12 @@ cudaError_t launch_top_k(const void* logits, int32_t logits_dtype, int64_t logit
                          int32_t k, int32_t* out_idx, int64_t out_stride, int32_t* status,
                          cudaStream_t stream);
 
+cudaError_t launch_dcp_pack(const void* logits, int32_t logits_dtype, int64_t logits_stride,
+                            const int32_t* local_idx, int64_t idx_stride, int32_t num_rows, int32_t k,
+                            int32_t rank, int32_t world, int32_t interleave, float* packed,
+                            cudaStream_t stream);
+cudaError_t launch_dcp_merge(const float* gathered, int32_t world, int32_t num_rows, int32_t k,
+                             int32_t* out_idx, int64_t out_stride, cudaStream_t stream);
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, int32_t* status, cudaStream_t stream);
 
 // Tensor-map encoding through the driver entry point (no libcuda link).

@@ -116,6 +116,32 @@ def test_host_checks_selftest(lib):
     assert lib.dsa_selftest_wait_timeout(1_000_000, None, None) == dsa.DSA_ERR_INVALID_ARG
 
 
+def test_host_checks_dcp(lib):
+    E, U, OK = dsa.DSA_ERR_INVALID_ARG, dsa.DSA_ERR_UNSUPPORTED, dsa.DSA_OK
+    pack = lib.dsa_dcp_pack_topk
+    # logits, dtype, stride, idx, idx_stride, rows, k, rank, world, interleave, packed, stream
+    assert pack(P(16), 7, 64, P(16), 16, 2, 16, 0, 2, 1, P(16), None) == U           # logits dtype
+    assert pack(P(16), 0, 64, P(16), 16, 2, 0, 0, 2, 1, P(16), None) == U            # k < 1
+    assert pack(P(16), 0, 64, P(16), 16, 2, 4096, 0, 2, 1, P(16), None) == U         # k > max
+    assert pack(P(16), 0, 64, P(16), 16, 2, 16, 0, 9, 1, P(16), None) == U           # world > max
+    assert pack(P(16), 0, 64, P(16), 16, 2, 16, 2, 2, 1, P(16), None) == E           # rank >= world
+    assert pack(P(16), 0, 64, P(16), 16, 2, 16, 0, 2, 0, P(16), None) == E           # interleave < 1
+    assert pack(P(16), 0, 64, P(16), 8, 2, 16, 0, 2, 1, P(16), None) == E            # idx_stride < k
+    assert pack(P(16), 0, 1 << 22, P(16), 16, 2, 16, 0, 4, 1, P(16), None) == E      # ids past 2^24
+    assert pack(P(16), 0, 64, P(16), 16, 2, 16, 0, 2, 1, P(20), None) == E       # packed alignment
+    assert pack(P(16), 0, 64, None, 16, 2, 16, 0, 2, 1, P(16), None) == E            # null
+    assert pack(None, 0, 64, None, 16, 0, 16, 0, 2, 1, None, None) == OK             # no rows
+    merge = lib.dsa_dcp_merge_topk
+    # gathered, world, rows, k, out, out_stride, stream
+    assert merge(P(16), 0, 2, 16, P(16), 16, None) == U
+    assert merge(P(16), 9, 2, 16, P(16), 16, None) == U
+    assert merge(P(16), 2, 2, 4096, P(16), 4096, None) == U
+    assert merge(P(16), 2, 2, 16, P(16), 15, None) == E
+    assert merge(P(20), 2, 2, 16, P(16), 16, None) == E
+    assert merge(P(16), 2, 2, 16, None, 16, None) == E
+    assert merge(None, 2, 0, 16, None, 16, None) == OK
+
+
 def test_product_path_has_no_fallback():
     """The package imports nothing from the oracle and has no CPU compute path."""
     pkg = os.path.dirname(dsa.__file__)

@@ -376,3 +376,70 @@ def padded_rows(wl: Workload):
             out.append(t + j if j < n else -1)
         t += n
     return torch.tensor(out, dtype=torch.long), max_n
+
+
+# ---------------------------------------------------------------------------
+# decode context parallelism: one rank's shard of a workload
+# ---------------------------------------------------------------------------
+
+def dcp_owner(g, world: int, interleave: int):
+    """Rank holding global token g: blocks of `interleave` tokens, round robin."""
+    return (g // interleave) % world
+
+
+def dcp_shard(wl: Workload, rank: int, world: int, interleave: int) -> Workload:
+    """Rank `rank`'s shard of `wl`: each request's tokens owned by the rank, in
+    global order, repacked into fresh pages of the same format (local position
+    l = the l-th owned token), a local block table and local causal limits
+    (owned tokens below each row's limit).  q, weights and request ids are
+    unchanged."""
+    fmt = wl.kv_format
+    kv = wl.kv_cache.cpu()
+    bt = wl.block_table.cpu()
+    ctx = wl.context_lens.cpu().to(torch.int64)
+    ind = None if wl.indices is None else wl.indices.cpu()
+    T = int(ctx.shape[0])
+    src = _page_views(kv, fmt)
+    # requests: runs of equal ids (every row alone without ids)
+    runs = []
+    t = 0
+    while t < T:
+        u = t + 1
+        while ind is not None and u < T and int(ind[u]) == int(ind[t]):
+            u += 1
+        runs.append((t, u))
+        t = u
+    pages, row_pages, ctx_loc = [], [None] * T, torch.zeros(T, dtype=torch.int32)
+    n_pages = 0
+    for t0, t1 in runs:
+        lens = ctx[t0:t1].clamp(min=0)
+        t_big = t0 + int(torch.argmax(lens))
+        lmax = int(lens.max())
+        g = torch.arange(lmax, dtype=torch.int64)
+        own = g[dcp_owner(g, world, interleave) == rank]
+        n_loc = int(own.shape[0])
+        np_loc = (n_loc + PAGE_TOKENS - 1) // PAGE_TOKENS
+        new = torch.zeros((np_loc, kv.shape[1]), dtype=torch.uint8)
+        dst = _page_views(new, fmt)
+        if n_loc:
+            pg = bt[t_big, own // PAGE_TOKENS].to(torch.int64)
+            sl = own % PAGE_TOKENS
+            loc = torch.arange(n_loc, dtype=torch.int64)
+            for key in src:
+                dst[key][loc // PAGE_TOKENS, loc % PAGE_TOKENS] = src[key][pg, sl]
+        pages.append(new)
+        ids = torch.arange(n_pages, n_pages + np_loc, dtype=torch.int32)
+        n_pages += np_loc
+        for tt in range(t0, t1):
+            row_pages[tt] = ids
+            gg = torch.arange(int(lens[tt - t0]), dtype=torch.int64)
+            ctx_loc[tt] = int((dcp_owner(gg, world, interleave) == rank).sum())
+    width = max(1, max(int(r.shape[0]) for r in row_pages))
+    bt_loc = torch.full((T, width), -1, dtype=torch.int32)
+    for tt in range(T):
+        bt_loc[tt, : row_pages[tt].shape[0]] = row_pages[tt]
+    pool = torch.cat(pages) if n_pages else torch.zeros((1, kv.shape[1]), dtype=torch.uint8)
+    stride = round_up(max(1, int(ctx_loc.max()) if T else 1), 64)
+    return Workload(f"{wl.name}-dcp{rank}of{world}i{interleave}", fmt, wl.q.cpu(), wl.weights.cpu(),
+                    ctx_loc, ind, bt_loc, pool.contiguous(), int(kv.shape[1]), stride, wl.topk,
+                    wl.logits_dtype, list(wl.request_lens), list(wl.rows_per_request), wl.seed)
