@@ -84,6 +84,8 @@ def lib():
             L.oracle_dcp_pack.restype = ctypes.c_int
             L.oracle_dcp_merge.argtypes = [P, i32, i32, i32, P, i64]
             L.oracle_dcp_merge.restype = ctypes.c_int
+            L.oracle_decode_chunk_ranges.argtypes = [i64, i64, i64, P, i64]
+            L.oracle_decode_chunk_ranges.restype = i64
             _lib = L
     return _lib
 
@@ -245,3 +247,18 @@ def dcp_merge(gathered, k):
     if st != ORACLE_OK:
         raise OracleError(st, "dcp_merge")
     return out
+
+
+# ---------------------------------------------------------------------------
+# row chunking of the decode step under a logits budget
+# ---------------------------------------------------------------------------
+
+def decode_chunk_ranges(rows, width, budget):
+    """[(start, end), ...] slices of the rows whose BF16 logits fit `budget`
+    bytes; [] means one pass over all rows."""
+    cap = max(1, (int(rows) + 15) // 16)
+    buf = np.zeros(2 * cap, dtype=np.int32)
+    n = lib().oracle_decode_chunk_ranges(int(rows), int(width), int(budget), _ptr(buf), cap)
+    if n < 0:
+        raise OracleError(-n, "decode_chunk_ranges")
+    return [(int(buf[2 * i]), int(buf[2 * i + 1])) for i in range(n)]

@@ -516,4 +516,39 @@ int oracle_dcp_merge(const double* gathered, int32_t world, int32_t num_rows, in
   return ORACLE_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Row chunking of the decode step under a logits budget (sparse_attn_indexer
+// docs, _decode_chunk_ranges: the rows are independent, so they may be cut
+// into slices whose BF16 logits, rows x width x 2 bytes, fit the budget; a
+// slice is a whole number of 16-row units except for the tail, the slices
+// are as few as the budget allows and as even as the units allow, the larger
+// ones first).
+//
+// Returns the number of slices written to ranges[2 * i] (start),
+// ranges[2 * i + 1] (end); 0 means one pass over all rows (no rows, a zero
+// budget, or everything fits).  -ORACLE_ERR_ARG for a negative budget, a
+// non-positive width, a budget below 16 rows, or more slices than max_ranges.
+// ---------------------------------------------------------------------------
+int64_t oracle_decode_chunk_ranges(int64_t rows, int64_t width, int64_t budget, int32_t* ranges,
+                                   int64_t max_ranges) {
+  if (budget < 0 || width < 1 || rows < 0) return -ORACLE_ERR_ARG;
+  if (rows == 0 || budget == 0 || rows * width * 2 <= budget) return 0;
+  const int64_t rows_per_slice = budget / (2 * width) / 16 * 16;  // the most rows a slice may hold
+  if (rows_per_slice < 16) return -ORACLE_ERR_ARG;
+  const int64_t units = g_plant == 10 ? rows / 16 : (rows + 15) / 16;  // 16-row units, the last partial
+  const int64_t per = rows_per_slice / 16;                              // units a slice may hold
+  const int64_t count = (units + per - 1) / per;                        // fewest slices
+  if (count > max_ranges || !ranges) return -ORACLE_ERR_ARG;
+  const int64_t base = units / count, extra = units % count;            // the first `extra` get one more
+  int64_t start = 0;
+  for (int64_t i = 0; i < count; ++i) {
+    const bool more = g_plant == 11 ? i >= count - extra : i < extra;
+    const int64_t end = std::min(rows, start + 16 * (base + (more ? 1 : 0)));
+    ranges[2 * i] = static_cast<int32_t>(start);
+    ranges[2 * i + 1] = static_cast<int32_t>(end);
+    start = end;
+  }
+  return count;
+}
+
 }  // extern "C"

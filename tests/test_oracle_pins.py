@@ -301,11 +301,54 @@ def check_dcp_merge_is_global_topk(seed=0):
         assert np.array_equal(got, want), (world, inter, k)
 
 
+def check_chunk_ranges():
+    """Row chunking under a BF16 logits budget (sparse_attn_indexer docs,
+    _decode_chunk_ranges).  Worked by hand from the rule's statement:
+      134 rows x 120064 columns, 16 MiB: a slice may hold
+        floor(16777216 / 240128) = 69 -> 64 rows = 4 units; 134 rows = 9 units
+        (the last partial); ceil(9 / 4) = 3 slices of 3 units: 48, 48, 38.
+      1000 rows x 4096 columns, 819200 B: 100 -> 96 rows = 6 units; 63 units;
+        11 slices, 63 = 11 * 5 + 8, so eight of 6 units then three of 5:
+        96 x 8, 80, 80, then the tail 1000 - 928 = 72.
+      40 rows x 64 columns, 5120 B (= 40 rows exactly): fits, one pass.
+    Then properties any correct reading has, on a sweep."""
+    assert oracle.decode_chunk_ranges(134, 120064, 16 << 20) == [(0, 48), (48, 96), (96, 134)]
+    want = [(96 * i, 96 * (i + 1)) for i in range(8)] + [(768, 848), (848, 928), (928, 1000)]
+    assert oracle.decode_chunk_ranges(1000, 4096, 819200) == want
+    assert oracle.decode_chunk_ranges(40, 64, 5120) == []
+    assert oracle.decode_chunk_ranges(0, 64, 100) == []
+    assert oracle.decode_chunk_ranges(17, 64, 0) == []
+    assert oracle.decode_chunk_ranges(33, 64, 16 * 64 * 2) == [(0, 16), (16, 32), (32, 33)]
+    for bad in ((10, 64, -1), (100, 64, 15 * 64 * 2), (100, 0, 1000)):
+        with pytest.raises(oracle.OracleError):
+            oracle.decode_chunk_ranges(*bad)
+    rng = np.random.default_rng(4)
+    for _ in range(400):
+        rows = int(rng.integers(1, 3000))
+        width = int(rng.integers(1, 200)) * 64
+        per_rows = int(rng.integers(16, 4000))
+        budget = per_rows * width * 2 + int(rng.integers(0, width * 2))
+        r = oracle.decode_chunk_ranges(rows, width, budget)
+        if rows * width * 2 <= budget:
+            assert r == []
+            continue
+        limit = budget // (2 * width) // 16 * 16
+        assert r[0][0] == 0 and r[-1][1] == rows
+        sizes = [e - s for s, e in r]
+        assert all(r[i][1] == r[i + 1][0] for i in range(len(r) - 1))
+        assert all(0 < n <= limit for n in sizes)                  # every slice fits the budget
+        assert all(n % 16 == 0 for n in sizes[:-1])               # whole units but the tail
+        units = [(n + 15) // 16 for n in sizes]
+        assert (len(r) - 1) * (limit // 16) < (rows + 15) // 16   # no fewer slices would do
+        assert max(units) - min(units) <= 1                       # as even as the units allow
+        assert units == sorted(units, reverse=True)               # larger slices first
+
+
 PIN_CHECKS = [
     check_e4m3_vs_torch, check_e2m1_vs_spec, check_bruteforce, check_one_hot_reads_key,
     check_relu_identities, check_weight_scaling, check_page_permutation,
     check_varlen_equals_padded, check_topk_bruteforce, check_fp4_bruteforce,
-    check_dcp_mapping, check_dcp_merge_is_global_topk,
+    check_dcp_mapping, check_dcp_merge_is_global_topk, check_chunk_ranges,
 ]
 
 
@@ -456,6 +499,8 @@ PLANTS = {
     7: "top-k order reversed",
     8: "DCP merge keeps the smallest scores",
     9: "DCP merge breaks score ties to the higher global id",
+    10: "row chunking counts whole 16-row units only (drops the partial one)",
+    11: "row chunking gives the smaller slices first",
 }
 
 
