@@ -8,6 +8,7 @@ otherwise.  Inputs are synthetic and seeded (workloads.config).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --dcp-world R [--dcp-interleave I]
+    python bench.py --logits-budget BYTES
 
 Prints one JSON line (rank 0).  `value` is device time per step with inputs
 resident in HBM; `e2e` is the same step through the C ABI from pinned host
@@ -22,6 +23,11 @@ keys, then the candidate pack) run in turn, the packs are stacked by a
 device copy where R GPUs would all-gather them, and the merge kernel gives
 the global top-k, which is checked against the unsharded step's.  It prints
 one JSON line of per-rank and merge kernel times.
+
+`--logits-budget BYTES` times the step as the one native call
+dsa_indexer_decode_topk, its rows in slices whose logits fit BYTES (each
+slice with its own schedule, one reused scratch), beside the same call
+unsliced, and checks that both give the same top-k.
 """
 from __future__ import annotations
 
@@ -62,6 +68,9 @@ def parse():
                     help="time the decode-context-parallel step instead: the workload's keys split "
                          "over this many ranks, every rank emulated in turn on this GPU")
     ap.add_argument("--dcp-interleave", type=int, default=1)
+    ap.add_argument("--logits-budget", type=int, default=0,
+                    help="time the whole step as one native call whose rows run in slices "
+                         "whose logits fit this many bytes")
     return ap.parse_args()
 
 
@@ -561,6 +570,79 @@ def run_dcp(args, local):
 
 
 # ---------------------------------------------------------------------------
+# the step in row slices under a logits budget
+# ---------------------------------------------------------------------------
+
+def run_chunked(args, local):
+    import torch
+    import sparse_attention_indexer_paged_gb300 as dsa
+    import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsa.build()
+    L = dsa.lib()
+    wl = W.config(args.workload, device=dev)
+    T, k, S = wl.num_rows, wl.topk, dsa.device_num_sms()
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    eb = 4 if wl.logits_dtype == 0 else 2
+
+    def plan(budget):
+        sb, sw = dsa.indexer_decode_scratch(T, wl.logits_dtype, wl.logits_stride, budget, S)
+        scr = torch.empty(sb, dtype=torch.uint8, device=dev)
+        sched = torch.empty(sw, dtype=torch.int32, device=dev)
+        out = torch.empty((T, k), dtype=torch.int32, device=dev)
+        a = (P(wl.q), P(wl.kv_cache), wl.page_stride, wl.num_pages, wl.kv_format, P(wl.weights),
+             P(wl.context_lens), P(wl.block_table), wl.block_table.stride(0), P(wl.indices), T, 64, 128, 64,
+             S, wl.logits_dtype, wl.logits_stride, budget, P(scr), sb, P(sched), sw, k, P(out), out.stride(0),
+             P(status), sp)
+        return dict(args=a, keep=(scr, sched), out=out, scratch_bytes=sb)
+
+    runs = {"sliced": plan(args.logits_budget), "one_pass": plan(0)}
+    res = {}
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    for name, r in runs.items():
+        for _ in range(max(args.warmup, 3)):
+            assert L.dsa_indexer_decode_topk(*r["args"]) == 0
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            L.dsa_indexer_decode_topk(*r["args"])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = t0.elapsed_time(t1) / args.steps * 1e3
+    clk = clocks.stop()
+    assert int(status.item()) == 0, dsa.status_string(int(status.item()))
+    same = bool(torch.equal(runs["sliced"]["out"], runs["one_pass"]["out"]))
+    ranges = dsa.decode_chunk_ranges(T, wl.logits_stride * eb // 2, args.logits_budget)
+    return {
+        "metric": "indexer decode µs/step as one native call, rows in slices under a logits budget",
+        "value": round(res["sliced"], 3),
+        "unit": "us/step",
+        "higher_is_better": False,
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "dtype": "e4m3 x e4m3 -> f32" if wl.kv_format == 0 else "e4m3 x e2m1 -> f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "shape": workload_desc(args.workload, wl), "rows": T,
+                   "logits_budget_bytes": args.logits_budget, "slices": ranges or [[0, T]],
+                   "scratch_bytes": runs["sliced"]["scratch_bytes"],
+                   "one_pass_scratch_bytes": runs["one_pass"]["scratch_bytes"], "num_sms": S},
+        "one_pass_us": round(res["one_pass"], 3),
+        "same_topk_as_one_pass": same,
+        "gpu_launches": 3 * max(1, len(ranges)) * args.steps,
+        "clocks": clk,
+    }
+
+
+# ---------------------------------------------------------------------------
 # the oracle timed on the host cores
 # ---------------------------------------------------------------------------
 
@@ -639,6 +721,9 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, rank, world)
+    elif args.logits_budget > 0:
+        assert world == 1, "the sliced step runs in one process"
+        res = run_chunked(args, local)
     elif args.dcp_world > 0:
         assert world == 1, "the DCP emulation runs in one process"
         res = run_dcp(args, local)

@@ -269,6 +269,59 @@ int dsa_dcp_merge_topk(const float* gathered, int32_t dcp_world, int32_t num_row
  */
 int dsa_selftest_wait_timeout(int64_t timeout_ns, int32_t* status, dsa_stream_t stream);
 
+/*
+ * dsa_decode_chunk_ranges - host only: the row slices of a decode step whose
+ * logits fit a byte budget ([DOCS] _decode_chunk_ranges: the rows are
+ * independent; a slice is a whole number of 16-row units except the tail,
+ * the slices are as few as the budget allows and as even as the units allow,
+ * the larger ones first).
+ *
+ *   rows, width  rows and logits columns per row; a row costs 2 * width
+ *                bytes (BF16 logits; pass 2 * stride for fp32 logits).
+ *   budget       bytes, >= 0; 0 means no budget.
+ *   ranges       (host) int32 [max_ranges][2]: (start, end) per slice.
+ *   num_ranges   (host) receives the slice count; 0 means one pass over all
+ *                rows (no rows, no budget, or everything fits).
+ * DSA_ERR_INVALID_ARG for a negative budget or rows, width < 1, a budget
+ * below 16 rows, or more slices than max_ranges.  No device is touched.
+ */
+int dsa_decode_chunk_ranges(int64_t rows, int64_t width, int64_t budget, int32_t* ranges,
+                            int32_t max_ranges, int32_t* num_ranges);
+
+/*
+ * dsa_indexer_decode_scratch - host only: the sizes the caller allocates for
+ * dsa_indexer_decode_topk, i.e. the logits of the largest slice and its
+ * schedule.  The logits of a slice cost logits_stride bytes x 4 (fp32) or
+ * x 2 (bf16) per row; the budget is counted in those bytes.
+ */
+int dsa_indexer_decode_scratch(int32_t num_rows, int32_t logits_dtype, int64_t logits_stride,
+                               int64_t logits_budget, int32_t num_sms, int64_t* scratch_bytes,
+                               int64_t* schedule_words);
+
+/*
+ * dsa_indexer_decode_topk - the whole decode step: for each row slice of
+ * dsa_decode_chunk_ranges (or all rows when the logits fit the budget), the
+ * slice's own schedule (dsa_paged_mqa_logits_metadata on the slice's rows,
+ * as [DOCS] does for a row range of the varlen decode), its logits into the
+ * caller's scratch, and its top-k into out_idx rows [start, end).
+ *
+ * Arguments are those of the three calls, for all rows; the slices are
+ * pointer offsets into them.  logits_scratch and schedule hold at least what
+ * dsa_indexer_decode_scratch returns and are reused by every slice (the
+ * calls are stream-ordered).  Results equal one pass over all rows bit for
+ * bit: a row's logits do not depend on the other rows.  Returns the first
+ * error of the calls it issues; device faults go to `status`.
+ */
+int dsa_indexer_decode_topk(const void* q, const void* kv_cache, int64_t page_stride_bytes,
+                            int64_t num_pages, int32_t kv_format, const float* weights,
+                            const int32_t* context_lens, const int32_t* block_table,
+                            int64_t block_table_stride, const int32_t* indices, int32_t num_rows,
+                            int32_t num_heads, int32_t head_dim, int32_t block_kv, int32_t num_sms,
+                            int32_t logits_dtype, int64_t logits_stride, int64_t logits_budget,
+                            void* logits_scratch, int64_t scratch_bytes, int32_t* schedule,
+                            int64_t schedule_words, int32_t k, int32_t* out_idx, int64_t out_stride,
+                            int32_t* status, dsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -56,6 +56,11 @@ _SIGS = {
     "dsa_selftest_wait_timeout": ([_I64, _P, _P], ctypes.c_int),
     "dsa_dcp_pack_topk": ([_P, _I32, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P], ctypes.c_int),
     "dsa_dcp_merge_topk": ([_P, _I32, _I32, _I32, _P, _I64, _P], ctypes.c_int),
+    "dsa_decode_chunk_ranges": ([_I64, _I64, _I64, _P, _I32, _P], ctypes.c_int),
+    "dsa_indexer_decode_scratch": ([_I32, _I32, _I64, _I64, _I32, _P, _P], ctypes.c_int),
+    "dsa_indexer_decode_topk": ([_P, _P, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _I32, _I32, _I32,
+                                 _I32, _I32, _I32, _I64, _I64, _P, _I64, _P, _I64, _I32, _P, _I64,
+                                 _P, _P], ctypes.c_int),
 }
 EXPORTED = tuple(_SIGS)
 
@@ -261,3 +266,61 @@ def dcp_topk(logits, local_idx, k, rank, world, interleave, group=None, out=None
     packed = dcp_pack_topk(logits, local_idx, k, rank, world, interleave)
     gathered = dcp_gather_candidates(packed, world, group) if world > 1 else packed.unsqueeze(0)
     return dcp_merge_topk(gathered, k, out=out)
+
+
+def decode_chunk_ranges(rows, width, budget):
+    """[(start, end), ...] row slices whose BF16 logits (2 * width bytes a row)
+    fit `budget` bytes; [] means one pass over all rows."""
+    cap = max(1, (int(rows) + 15) // 16)
+    buf = (ctypes.c_int32 * (2 * cap))()
+    n = ctypes.c_int32(0)
+    _check(lib().dsa_decode_chunk_ranges(int(rows), int(width), int(budget), ctypes.cast(buf, _P), cap,
+                                         ctypes.byref(n)), "decode_chunk_ranges")
+    return [(int(buf[2 * i]), int(buf[2 * i + 1])) for i in range(n.value)]
+
+
+def indexer_decode_scratch(num_rows, logits_dtype, logits_stride, logits_budget, num_sms):
+    """(logits scratch bytes, schedule words) that indexer_decode_topk needs."""
+    sb, sw = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib().dsa_indexer_decode_scratch(int(num_rows), int(logits_dtype), int(logits_stride),
+                                            int(logits_budget), int(num_sms), ctypes.byref(sb),
+                                            ctypes.byref(sw)), "indexer_decode_scratch")
+    return int(sb.value), int(sw.value)
+
+
+def indexer_decode_topk(q, kv_cache, weights, context_lens, block_table, k, indices=None,
+                        kv_format=KV_FP8, logits_dtype=LOGITS_F32, logits_stride=None,
+                        logits_budget=0, num_sms=None, out=None, status=None, scratch=None,
+                        schedule=None, page_stride=None):
+    """The whole decode step (schedule, logits, top-k) in one native call; with
+    a logits budget (bytes) the rows run in slices whose logits fit it.
+    Returns int32 [T, k] top-k columns, ascending, -1 padded."""
+    device = q.device
+    T = int(q.shape[0])
+    if num_sms is None:
+        num_sms = device_num_sms()
+    ctx = _dev_i32(context_lens, device)
+    bt = _dev_i32(block_table, device)
+    ind = _dev_i32(indices, device)
+    if logits_stride is None:
+        mx = int(ctx.max().item()) if T else 0
+        logits_stride = max(BLOCK_KV, (mx + BLOCK_KV - 1) // BLOCK_KV * BLOCK_KV)
+    sb, sw = indexer_decode_scratch(T, logits_dtype, logits_stride, logits_budget, num_sms)
+    if scratch is None:
+        scratch = torch.empty(max(sb, 16), dtype=torch.uint8, device=device)
+    if schedule is None:
+        schedule = torch.empty(max(sw, 1), dtype=torch.int32, device=device)
+    if out is None:
+        out = torch.empty((T, int(k)), dtype=torch.int32, device=device)
+    assert out.dtype == torch.int32 and out.stride(-1) == 1
+    qq = q.view(torch.uint8) if q.dtype != torch.uint8 else q
+    assert qq.is_contiguous() and weights.is_contiguous() and weights.dtype == torch.float32
+    assert kv_cache.dim() == 2 and kv_cache.stride(1) == 1
+    pstride = kv_cache.stride(0) if page_stride is None else int(page_stride)
+    _check(lib().dsa_indexer_decode_topk(
+        _ptr(qq), _ptr(kv_cache), pstride, int(kv_cache.shape[0]), int(kv_format), _ptr(weights),
+        _ptr(ctx), _ptr(bt), int(bt.stride(0)), _ptr(ind), T, NUM_HEADS, HEAD_DIM, BLOCK_KV,
+        int(num_sms), int(logits_dtype), int(logits_stride), int(logits_budget), _ptr(scratch),
+        int(scratch.numel() * scratch.element_size()), _ptr(schedule), int(schedule.numel()), int(k),
+        _ptr(out), int(out.stride(0)), _ptr(status), _stream(device)), "indexer_decode_topk")
+    return out
