@@ -85,6 +85,8 @@ def lib():
             L.oracle_dcp_merge.argtypes = [P, i32, i32, i32, P, i64]
             L.oracle_dcp_merge.restype = ctypes.c_int
             L.oracle_decode_chunk_ranges.argtypes = [i64, i64, i64, P, i64]
+            L.oracle_prefill_rows.argtypes = [P, P, i32, P, i32, P, P]
+            L.oracle_prefill_rows.restype = ctypes.c_int
             L.oracle_decode_chunk_ranges.restype = i64
             _lib = L
     return _lib
@@ -262,3 +264,30 @@ def decode_chunk_ranges(rows, width, budget):
     if n < 0:
         raise OracleError(-n, "decode_chunk_ranges")
     return [(int(buf[2 * i]), int(buf[2 * i + 1])) for i in range(n)]
+
+
+# ---------------------------------------------------------------------------
+# prefill rows over the paged cache
+# ---------------------------------------------------------------------------
+
+def prefill_rows(cu_seqlen_ks, cu_seqlen_ke, local_cu_seq_lens):
+    """(context_lens, request_ids) int32 [T] of prefill rows tagged (ks, ke)."""
+    ks = _np(cu_seqlen_ks, np.int32)
+    ke = _np(cu_seqlen_ke, np.int32)
+    cu = _np(local_cu_seq_lens, np.int32)
+    T, B = ks.shape[0], cu.shape[0] - 1
+    ctx = np.zeros(T, dtype=np.int32)
+    req = np.zeros(T, dtype=np.int32)
+    st = lib().oracle_prefill_rows(_ptr(ks), _ptr(ke), T, _ptr(cu), B, _ptr(ctx), _ptr(req))
+    if st != ORACLE_OK:
+        raise OracleError(st, "prefill_rows")
+    return ctx, req
+
+
+def prefill_logits(pf, rows=None, with_bound=True, nthreads=0):
+    """Oracle logits of a workloads.Prefill (selected rows, or all): each row's
+    keys [0, ke - ks) of its request, read through the request's block-table row."""
+    ctx, req = prefill_rows(pf.cu_seqlen_ks, pf.cu_seqlen_ke, pf.local_cu_seq_lens)
+    bt = _np(pf.block_table, np.int32)[req]          # the row-indexed view of the request table
+    return paged_mqa_logits(pf.q, pf.kv_cache, pf.page_stride, pf.kv_format, pf.weights, ctx, bt,
+                            pf.logits_stride, rows=rows, with_bound=with_bound, nthreads=nthreads)

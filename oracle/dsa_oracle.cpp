@@ -517,6 +517,41 @@ int oracle_dcp_merge(const double* gathered, int32_t world, int32_t num_rows, in
 }
 
 // ---------------------------------------------------------------------------
+// Prefill rows over the paged cache (sparse_attn_indexer docs, the CPU
+// indexer's prefill branch of forward_cpu): a prefill chunk tags each token
+// row t with cu_seqlen_ks[t], the start of its request in the chunk's
+// concatenated key range (local_cu_seq_lens[0..B]), and cu_seqlen_ke[t], the
+// end of the keys it sees.  Its request is the last r with
+// local_cu_seq_lens[r] <= ks (a sorted search to the right, minus one), its
+// causal length is ke - ks, and it reads the keys through that request's
+// block-table row; the logits are then the decode definition above with
+// L_t = ke - ks.  A row whose request index falls outside [0, B) (possible
+// only for a length-0 row at the very end) reads request B - 1: it touches no
+// page.  Returns ORACLE_ERR_ARG for a negative length.
+// ---------------------------------------------------------------------------
+int oracle_prefill_rows(const int32_t* cu_seqlen_ks, const int32_t* cu_seqlen_ke, int32_t num_rows,
+                        const int32_t* local_cu_seq_lens, int32_t num_requests, int32_t* context_lens,
+                        int32_t* request_ids) {
+  if (num_rows < 0 || num_requests < 1 || (num_rows > 0 && (!cu_seqlen_ks || !cu_seqlen_ke ||
+                                                           !local_cu_seq_lens || !context_lens ||
+                                                           !request_ids)))
+    return ORACLE_ERR_ARG;
+  for (int t = 0; t < num_rows; ++t) {
+    const int32_t ks = cu_seqlen_ks[t], ke = cu_seqlen_ke[t];
+    int32_t at_or_below = 0;  // offsets <= ks among the B + 1 request starts
+    for (int r = 0; r <= num_requests; ++r)
+      if (local_cu_seq_lens[r] <= ks) ++at_or_below;
+    int32_t req = at_or_below - 1;
+    if (req < 0) req = 0;
+    if (req >= num_requests) req = num_requests - 1;
+    if (ke - ks < 0) return ORACLE_ERR_ARG;
+    request_ids[t] = req;
+    context_lens[t] = g_plant == 12 ? ke : ke - ks;
+  }
+  return ORACLE_OK;
+}
+
+// ---------------------------------------------------------------------------
 // Row chunking of the decode step under a logits budget (sparse_attn_indexer
 // docs, _decode_chunk_ranges: the rows are independent, so they may be cut
 // into slices whose BF16 logits, rows x width x 2 bytes, fit the budget; a

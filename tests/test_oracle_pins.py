@@ -344,11 +344,30 @@ def check_chunk_ranges():
         assert units == sorted(units, reverse=True)               # larger slices first
 
 
+def check_prefill_rows():
+    """Prefill row tags -> (causal length, request), worked by hand from the
+    CPU indexer's prefill branch (request = sorted search of ks to the right,
+    minus one; length = ke - ks).  Requests [0,5), [5,5) (empty), [5,9):
+      (0, 3) -> request 0, length 3      (0, 5) -> 0, 5
+      (5, 6) -> three starts <= 5, so request 2, length 1
+      (5, 9) -> 2, 4                      (9, 9) -> past the last start: 2, length 0
+    Then the prefill logits of a chunk equal the decode logits (pinned by
+    brute force) of the same rows with the same causal limits."""
+    ctx, req = oracle.prefill_rows([0, 0, 5, 5, 9], [3, 5, 6, 9, 9], [0, 5, 5, 9])
+    assert ctx.tolist() == [3, 5, 1, 4, 0] and req.tolist() == [0, 0, 2, 2, 2]
+    for kv_format in (W.KV_FP8, W.KV_FP4):
+        wl = W.build("pf", [300, 517, 0, 70], [100, 40, 1, 3], kv_format=kv_format, topk=32, seed=7)
+        pf = W.prefill_view(wl)
+        got, _ = oracle.prefill_logits(pf, with_bound=False)
+        want, _ = oracle.workload_logits(wl, with_bound=False)
+        assert np.array_equal(got, want)
+
+
 PIN_CHECKS = [
     check_e4m3_vs_torch, check_e2m1_vs_spec, check_bruteforce, check_one_hot_reads_key,
     check_relu_identities, check_weight_scaling, check_page_permutation,
     check_varlen_equals_padded, check_topk_bruteforce, check_fp4_bruteforce,
-    check_dcp_mapping, check_dcp_merge_is_global_topk, check_chunk_ranges,
+    check_dcp_mapping, check_dcp_merge_is_global_topk, check_chunk_ranges, check_prefill_rows,
 ]
 
 
@@ -501,6 +520,7 @@ PLANTS = {
     9: "DCP merge breaks score ties to the higher global id",
     10: "row chunking counts whole 16-row units only (drops the partial one)",
     11: "row chunking gives the smaller slices first",
+    12: "prefill causal length taken as ke instead of ke - ks",
 }
 
 

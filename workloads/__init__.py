@@ -314,6 +314,8 @@ def config_spec(name: str) -> dict:
     mtp         B=128, two rows each (indices=i//2), L ~ U{8192..65536}, k=2048, seed 2
     varlen      B=40, L = 120000 + U{-2048..2048}, rows ~ U{1..6}, k=2048, seed 3
     fp4_varlen  as varlen with FP4 keys and BF16 logits, seed 4
+    prefill     B=2, L=8192, the last 4096 tokens of each prompt as rows (T=8192),
+                k=2048, seed 5 (use prefill_view for the prefill-tagged form)
     """
     g = torch.Generator()
     if name == "tiny":
@@ -335,6 +337,9 @@ def config_spec(name: str) -> dict:
         if name == "fp4_varlen":
             kw.update(kv_format=KV_FP4, logits_dtype=LOGITS_BF16)
         return kw
+    if name == "prefill":
+        # a prefill chunk: the second halves of two 8192-token prompts
+        return dict(request_lens=[8192, 8192], rows_per_request=[4096, 4096], topk=2048, seed=5)
     raise ValueError(f"unknown workload {name!r}")
 
 
@@ -443,3 +448,66 @@ def dcp_shard(wl: Workload, rank: int, world: int, interleave: int) -> Workload:
     return Workload(f"{wl.name}-dcp{rank}of{world}i{interleave}", fmt, wl.q.cpu(), wl.weights.cpu(),
                     ctx_loc, ind, bt_loc, pool.contiguous(), int(kv.shape[1]), stride, wl.topk,
                     wl.logits_dtype, list(wl.request_lens), list(wl.rows_per_request), wl.seed)
+
+
+# ---------------------------------------------------------------------------
+# prefill chunks in the prefill-tagged form
+# ---------------------------------------------------------------------------
+
+@dataclass
+class Prefill:
+    """A prefill chunk over the paged cache, tagged as the indexer's prefill
+    path tags it: the requests' keys laid end to end (local_cu_seq_lens,
+    [B + 1]), each token row t tagged with its request's start ks and the end
+    ke of the keys it sees; block_table is per request."""
+
+    q: torch.Tensor                  # uint8 [T, H, D]
+    weights: torch.Tensor            # float32 [T, H]
+    cu_seqlen_ks: torch.Tensor       # int32 [T]
+    cu_seqlen_ke: torch.Tensor       # int32 [T]
+    local_cu_seq_lens: torch.Tensor  # int32 [B + 1]
+    block_table: torch.Tensor        # int32 [B, max_pages]
+    kv_cache: torch.Tensor
+    kv_format: int
+    page_stride: int
+    logits_stride: int
+    topk: int
+    logits_dtype: int
+
+    @property
+    def num_rows(self) -> int:
+        return int(self.cu_seqlen_ks.shape[0])
+
+    @property
+    def num_requests(self) -> int:
+        return int(self.local_cu_seq_lens.shape[0]) - 1
+
+    def to(self, device) -> "Prefill":
+        return Prefill(*(x.to(device) if isinstance(x, torch.Tensor) else x
+                         for x in (self.q, self.weights, self.cu_seqlen_ks, self.cu_seqlen_ke,
+                                   self.local_cu_seq_lens, self.block_table, self.kv_cache)),
+                       self.kv_format, self.page_stride, self.logits_stride, self.topk,
+                       self.logits_dtype)
+
+
+def prefill_view(wl: Workload) -> Prefill:
+    """The prefill-tagged form of a workload whose rows are the last n_r
+    tokens of each request (row j of request r at causal limit
+    L_r - n_r + 1 + j): ks = the request's start in the concatenated keys,
+    ke = ks + L_t, and one block-table row per request."""
+    lens = [int(x) for x in wl.request_lens]
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    ks, last = [], []
+    t = 0
+    for r, n in enumerate(wl.rows_per_request):
+        ks += [cu[r]] * int(n)
+        t += int(n)
+        last.append(t - 1)
+    ks = torch.tensor(ks, dtype=torch.int32)
+    ctx = wl.context_lens.cpu()
+    bt = wl.block_table.cpu()[torch.tensor(last, dtype=torch.int64)].contiguous()
+    return Prefill(wl.q.cpu(), wl.weights.cpu(), ks, ks + ctx, torch.tensor(cu, dtype=torch.int32), bt,
+                   wl.kv_cache.cpu(), wl.kv_format, wl.page_stride, wl.logits_stride, wl.topk,
+                   wl.logits_dtype)
