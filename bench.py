@@ -9,6 +9,7 @@ otherwise.  Inputs are synthetic and seeded (workloads.config).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --dcp-world R [--dcp-interleave I]
     python bench.py --logits-budget BYTES
+    python bench.py --workload prefill
 
 Prints one JSON line (rank 0).  `value` is device time per step with inputs
 resident in HBM; `e2e` is the same step through the C ABI from pinned host
@@ -28,6 +29,10 @@ one JSON line of per-rank and merge kernel times.
 dsa_indexer_decode_topk, its rows in slices whose logits fit BYTES (each
 slice with its own schedule, one reused scratch), beside the same call
 unsliced, and checks that both give the same top-k.
+
+`--workload prefill` times the prefill step over the paged cache (row tags
+-> lengths and requests, schedule, logits, top-k) on a chunk of 2 x 4096
+rows of two 8192-token prompts; its roofline is the FP8 tensor rate.
 """
 from __future__ import annotations
 
@@ -59,7 +64,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="varlen",
-                    choices=["tiny", "plain", "mtp", "varlen", "fp4_varlen"])
+                    choices=["tiny", "plain", "mtp", "varlen", "fp4_varlen", "prefill"])
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
@@ -570,6 +575,100 @@ def run_dcp(args, local):
 
 
 # ---------------------------------------------------------------------------
+# prefill over the paged cache
+# ---------------------------------------------------------------------------
+
+def run_prefill(args, local):
+    import torch
+    import sparse_attention_indexer_paged_gb300 as dsa
+    import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsa.build()
+    L = dsa.lib()
+    wl = W.config(args.workload)
+    pf = W.prefill_view(wl).to(dev)
+    T, B, k, S = pf.num_rows, pf.num_requests, pf.topk, dsa.device_num_sms()
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ctx = torch.empty(T, dtype=torch.int32, device=dev)
+    req = torch.empty(T, dtype=torch.int32, device=dev)
+    sched = torch.empty(dsa.schedule_words(S, T), dtype=torch.int32, device=dev)
+    ldt = torch.float32 if pf.logits_dtype == 0 else torch.bfloat16
+    logits = torch.empty((T, pf.logits_stride), dtype=ldt, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    rows_a = (P(pf.cu_seqlen_ks), P(pf.cu_seqlen_ke), T, P(pf.local_cu_seq_lens), B, P(ctx), P(req), P(status), sp)
+    meta_a = (P(ctx), P(req), T, 64, S, P(sched), sp)
+    lg_a = (P(pf.q), P(pf.kv_cache), pf.page_stride, int(pf.kv_cache.shape[0]), pf.kv_format, P(pf.weights),
+            P(ctx), P(req), P(pf.block_table), pf.block_table.stride(0), B, P(sched), S, P(logits),
+            pf.logits_dtype, pf.logits_stride, T, 64, 128, 64, P(status), sp)
+    tk_a = (P(logits), pf.logits_dtype, pf.logits_stride, None, P(ctx), T, k, P(idx), idx.stride(0), P(status), sp)
+
+    def step(ev=None):
+        rc = 0
+        calls = ((L.dsa_prefill_rows, rows_a), (L.dsa_paged_mqa_logits_metadata, meta_a),
+                 (L.dsa_prefill_mqa_logits, lg_a), (L.dsa_top_k_per_row, tk_a))
+        for i, (fn, a) in enumerate(calls):
+            if ev is not None:
+                ev[i].record(stream)
+            rc |= fn(*a)
+        if ev is not None:
+            ev[4].record(stream)
+        return rc
+
+    for _ in range(max(args.warmup, 3)):
+        assert step() == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, dsa.status_string(int(status.item()))
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert int(status.item()) == 0, dsa.status_string(int(status.item()))
+    ms = t0.elapsed_time(t1) / K
+    names = ("prefill_rows", "metadata", "logits", "top_k")
+    us = {n: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / K * 1e3 for i, n in enumerate(names)}
+    hbm_gbs, bf16_tf, peak_src = peaks()
+    fp8_tf = bf16_tf * FP8_PEAK_RATIO
+    lens = ctx.cpu().to(torch.int64)
+    flops = int(lens.sum()) * 64 * 128 * 2
+    achieved = flops / (us["logits"] * 1e-6) / 1e12
+    return {
+        "metric": "indexer prefill µs/step over the paged cache (rows, schedule, logits, top-k)",
+        "value": round(ms * 1e3, 3),
+        "unit": "us/step",
+        "higher_is_better": False,
+        "n_gpus": 1,
+        "steps": K,
+        "warmup": args.warmup,
+        "dtype": "e4m3 x e4m3 -> f32" if pf.kv_format == 0 else "e4m3 x e2m1 -> f32",
+        "data": "synthetic",
+        "config": {"workload": "prefill: 2 requests x 8192-token prompts, their last 4096 tokens as rows "
+                               "(T=8192, causal lengths 4097..8192), q and keys e4m3, H=64, D=128, "
+                               "top-k 2048, fp32 logits", "rows": T, "num_sms": S},
+        "kernels_us": {n: round(v, 3) for n, v in us.items()},
+        "roofline": {"kernel": "logits", "bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": fp8_tf, "unit": "TFLOP/s", "frac": round(achieved / fp8_tf, 4),
+                     "flops": flops, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 x {FP8_PEAK_RATIO} (nominal fp8:bf16 ratio)"},
+        "gpu_launches": 4 * K,
+        "clocks": clk,
+    }
+
+
+# ---------------------------------------------------------------------------
 # the step in row slices under a logits budget
 # ---------------------------------------------------------------------------
 
@@ -721,6 +820,9 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, rank, world)
+    elif args.workload == "prefill":
+        assert world == 1, "the prefill bench runs in one process"
+        res = run_prefill(args, local)
     elif args.logits_budget > 0:
         assert world == 1, "the sliced step runs in one process"
         res = run_chunked(args, local)

@@ -270,6 +270,46 @@ int dsa_dcp_merge_topk(const float* gathered, int32_t dcp_world, int32_t num_row
 int dsa_selftest_wait_timeout(int64_t timeout_ns, int32_t* status, dsa_stream_t stream);
 
 /*
+ * dsa_prefill_rows - prefill token rows over the paged cache ([DOCS] the CPU
+ * indexer's prefill branch of forward_cpu: a prefill chunk lays its
+ * requests' keys end to end, local_cu_seq_lens [B + 1] being the requests'
+ * starts, and tags row t with cu_seqlen_ks[t], its request's start, and
+ * cu_seqlen_ke[t], the end of the keys it sees).  Writes, per row, its
+ * request (the last r with local_cu_seq_lens[r] <= ks, clamped to
+ * [0, B - 1]; a length-0 row past the last start reads no key) and its
+ * causal length ke - ks.  These are the context_lens and request_ids of
+ * dsa_paged_mqa_logits_metadata (as indices) and dsa_prefill_mqa_logits.
+ *
+ *   cu_seqlen_ks, cu_seqlen_ke  (device) int32 [num_rows].
+ *   local_cu_seq_lens           (device) int32 [num_requests + 1], non-decreasing.
+ *   context_lens, request_ids   (device) int32 [num_rows], written.
+ *   status                      (device, may be null) a negative length sets
+ *                               DSA_ERR_INVALID_ARG there (the row gets 0).
+ */
+int dsa_prefill_rows(const int32_t* cu_seqlen_ks, const int32_t* cu_seqlen_ke, int32_t num_rows,
+                     const int32_t* local_cu_seq_lens, int32_t num_requests, int32_t* context_lens,
+                     int32_t* request_ids, int32_t* status, dsa_stream_t stream);
+
+/*
+ * dsa_prefill_mqa_logits - the logits of prefill rows, read straight from
+ * the paged cache (the pages' prefill mqa_logits over their ragged
+ * cu_seqlen_ks/ke, without gathering the keys): as dsa_fp8_fp4_paged_mqa_logits
+ * with context_lens = ke - ks and a block table per request, block_table
+ * [num_requests][block_table_stride], that row r reads through
+ * request_ids[r].  The schedule comes from dsa_paged_mqa_logits_metadata on
+ * (context_lens, request_ids); rows of a request must be adjacent.  Column s
+ * of row t is the request's token s (0 <= s < ke - ks), -inf up to
+ * round_up(ke - ks, 64); a request id outside [0, num_requests) sets
+ * DSA_ERR_BAD_BLOCK in `status`.
+ */
+int dsa_prefill_mqa_logits(const void* q, const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages,
+                           int32_t kv_format, const float* weights, const int32_t* context_lens,
+                           const int32_t* request_ids, const int32_t* block_table, int64_t block_table_stride,
+                           int32_t num_requests, const int32_t* schedule, int32_t num_sms, void* logits,
+                           int32_t logits_dtype, int64_t logits_stride, int32_t num_rows, int32_t num_heads,
+                           int32_t head_dim, int32_t block_kv, int32_t* status, dsa_stream_t stream);
+
+/*
  * dsa_decode_chunk_ranges - host only: the row slices of a decode step whose
  * logits fit a byte budget ([DOCS] _decode_chunk_ranges: the rows are
  * independent; a slice is a whole number of 16-row units except the tail,

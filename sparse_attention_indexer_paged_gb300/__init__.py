@@ -56,6 +56,9 @@ _SIGS = {
     "dsa_selftest_wait_timeout": ([_I64, _P, _P], ctypes.c_int),
     "dsa_dcp_pack_topk": ([_P, _I32, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P], ctypes.c_int),
     "dsa_dcp_merge_topk": ([_P, _I32, _I32, _I32, _P, _I64, _P], ctypes.c_int),
+    "dsa_prefill_rows": ([_P, _P, _I32, _P, _I32, _P, _P, _P, _P], ctypes.c_int),
+    "dsa_prefill_mqa_logits": ([_P, _P, _I64, _I64, _I32, _P, _P, _P, _P, _I64, _I32, _P, _I32, _P,
+                                _I32, _I64, _I32, _I32, _I32, _I32, _P, _P], ctypes.c_int),
     "dsa_decode_chunk_ranges": ([_I64, _I64, _I64, _P, _I32, _P], ctypes.c_int),
     "dsa_indexer_decode_scratch": ([_I32, _I32, _I64, _I64, _I32, _P, _P], ctypes.c_int),
     "dsa_indexer_decode_topk": ([_P, _P, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _I32, _I32, _I32,
@@ -324,3 +327,64 @@ def indexer_decode_topk(q, kv_cache, weights, context_lens, block_table, k, indi
         int(scratch.numel() * scratch.element_size()), _ptr(schedule), int(schedule.numel()), int(k),
         _ptr(out), int(out.stride(0)), _ptr(status), _stream(device)), "indexer_decode_topk")
     return out
+
+
+def prefill_rows(cu_seqlen_ks, cu_seqlen_ke, local_cu_seq_lens, status=None):
+    """(context_lens, request_ids) int32 [T] of prefill rows tagged (ks, ke)."""
+    device = cu_seqlen_ks.device
+    T = int(cu_seqlen_ks.shape[0])
+    ks = _dev_i32(cu_seqlen_ks, device)
+    ke = _dev_i32(cu_seqlen_ke, device)
+    cu = _dev_i32(local_cu_seq_lens, device)
+    ctx = torch.empty(T, dtype=torch.int32, device=device)
+    req = torch.empty(T, dtype=torch.int32, device=device)
+    _check(lib().dsa_prefill_rows(_ptr(ks), _ptr(ke), T, _ptr(cu), int(cu.shape[0]) - 1, _ptr(ctx), _ptr(req),
+                                  _ptr(status), _stream(device)), "prefill_rows")
+    return ctx, req
+
+
+def prefill_mqa_logits(q, kv_cache, weights, context_lens, request_ids, block_table, schedule,
+                       kv_format=KV_FP8, logits_dtype=LOGITS_F32, logits_stride=None, num_sms=None,
+                       out=None, status=None, page_stride=None):
+    """Logits [T, logits_stride] of prefill rows over the paged cache; block_table
+    is per request ([B, max_pages]) and row t reads row request_ids[t]."""
+    device = q.device
+    T = int(q.shape[0])
+    if num_sms is None:
+        num_sms = device_num_sms()
+    ctx = _dev_i32(context_lens, device)
+    req = _dev_i32(request_ids, device)
+    bt = _dev_i32(block_table, device)
+    if logits_stride is None:
+        mx = int(ctx.max().item()) if T else 0
+        logits_stride = max(BLOCK_KV, (mx + BLOCK_KV - 1) // BLOCK_KV * BLOCK_KV)
+    dt = torch.float32 if logits_dtype == LOGITS_F32 else torch.bfloat16
+    if out is None:
+        out = torch.empty((T, logits_stride), dtype=dt, device=device)
+    assert out.dtype == dt and out.stride(-1) == 1 and out.stride(0) == logits_stride
+    qq = q.view(torch.uint8) if q.dtype != torch.uint8 else q
+    assert qq.is_contiguous() and weights.is_contiguous() and weights.dtype == torch.float32
+    pstride = kv_cache.stride(0) if page_stride is None else int(page_stride)
+    _check(lib().dsa_prefill_mqa_logits(
+        _ptr(qq), _ptr(kv_cache), pstride, int(kv_cache.shape[0]), int(kv_format), _ptr(weights), _ptr(ctx),
+        _ptr(req), _ptr(bt), int(bt.stride(0)), int(bt.shape[0]), _ptr(schedule), int(num_sms), _ptr(out),
+        int(logits_dtype), int(logits_stride), T, NUM_HEADS, HEAD_DIM, BLOCK_KV, _ptr(status),
+        _stream(device)), "prefill_mqa_logits")
+    return out
+
+
+def prefill_topk(q, kv_cache, weights, cu_seqlen_ks, cu_seqlen_ke, local_cu_seq_lens, block_table, k,
+                 kv_format=KV_FP8, logits_dtype=LOGITS_F32, logits_stride=None, num_sms=None,
+                 status=None, logits_out=None):
+    """The prefill step over the paged cache: row tags -> (length, request),
+    schedule, logits, top-k.  Returns (top-k [T, k] int32 request-local token
+    positions, ascending, -1 padded; logits)."""
+    if num_sms is None:
+        num_sms = device_num_sms()
+    ctx, req = prefill_rows(cu_seqlen_ks, cu_seqlen_ke, local_cu_seq_lens, status=status)
+    sched = paged_mqa_logits_metadata(ctx, req, num_sms)
+    logits = prefill_mqa_logits(q, kv_cache, weights, ctx, req, block_table, sched, kv_format=kv_format,
+                                logits_dtype=logits_dtype, logits_stride=logits_stride, num_sms=num_sms,
+                                out=logits_out, status=status)
+    idx = top_k_per_row(logits, None, ctx, k, status=status)
+    return idx, logits

@@ -124,14 +124,19 @@ int dsa_paged_mqa_logits_metadata(const int32_t* context_lens, const int32_t* in
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int dsa_fp8_fp4_paged_mqa_logits(const void* q, const void* kv_cache, int64_t page_stride_bytes,
-                                 int64_t num_pages, int32_t kv_format, const float* weights,
-                                 const int32_t* context_lens, const int32_t* block_table,
-                                 int64_t block_table_stride, const int32_t* indices,
-                                 const int32_t* schedule, int32_t num_sms, void* logits,
-                                 int32_t logits_dtype, int64_t logits_stride, int32_t num_rows,
-                                 int32_t num_heads, int32_t head_dim, int32_t block_kv,
-                                 int32_t* status, dsa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The logits call of decode (row-indexed block table) and of prefill (a
+// block table per request, read through the rows' request ids).
+int logits_call(const void* q, const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages,
+                int32_t kv_format, const float* weights, const int32_t* context_lens,
+                const int32_t* block_table, int64_t block_table_stride, const int32_t* bt_rows,
+                int32_t bt_num_rows, const int32_t* indices, const int32_t* schedule, int32_t num_sms,
+                void* logits, int32_t logits_dtype, int64_t logits_stride, int32_t num_rows,
+                int32_t num_heads, int32_t head_dim, int32_t block_kv, int32_t* status,
+                dsa_stream_t stream) {
   if (num_heads != kHeads || head_dim != kHeadDim || block_kv != kPageTokens)
     return DSA_ERR_UNSUPPORTED;
   if (kv_format != DSA_KV_FP8 && kv_format != DSA_KV_FP4) return DSA_ERR_UNSUPPORTED;
@@ -161,6 +166,8 @@ int dsa_fp8_fp4_paged_mqa_logits(const void* q, const void* kv_cache, int64_t pa
   a.context_lens = context_lens;
   a.block_table = block_table;
   a.bt_stride = block_table_stride;
+  a.bt_rows = bt_rows;
+  a.bt_num_rows = bt_num_rows;
   a.indices = indices;
   a.schedule = schedule;
   a.num_sms = num_sms;
@@ -174,6 +181,49 @@ int dsa_fp8_fp4_paged_mqa_logits(const void* q, const void* kv_cache, int64_t pa
   if (e == cudaErrorInvalidValue) return DSA_ERR_INVALID_ARG;
   if (e == cudaErrorNotSupported) return DSA_ERR_UNSUPPORTED;
   return launch_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dsa_fp8_fp4_paged_mqa_logits(const void* q, const void* kv_cache, int64_t page_stride_bytes,
+                                 int64_t num_pages, int32_t kv_format, const float* weights,
+                                 const int32_t* context_lens, const int32_t* block_table,
+                                 int64_t block_table_stride, const int32_t* indices,
+                                 const int32_t* schedule, int32_t num_sms, void* logits,
+                                 int32_t logits_dtype, int64_t logits_stride, int32_t num_rows,
+                                 int32_t num_heads, int32_t head_dim, int32_t block_kv,
+                                 int32_t* status, dsa_stream_t stream) {
+  return logits_call(q, kv_cache, page_stride_bytes, num_pages, kv_format, weights, context_lens, block_table,
+                     block_table_stride, nullptr, 0, indices, schedule, num_sms, logits, logits_dtype,
+                     logits_stride, num_rows, num_heads, head_dim, block_kv, status, stream);
+}
+
+int dsa_prefill_rows(const int32_t* cu_seqlen_ks, const int32_t* cu_seqlen_ke, int32_t num_rows,
+                     const int32_t* local_cu_seq_lens, int32_t num_requests, int32_t* context_lens,
+                     int32_t* request_ids, int32_t* status, dsa_stream_t stream) {
+  if (num_rows < 0 || num_requests < 1) return DSA_ERR_INVALID_ARG;
+  if (num_rows == 0) return DSA_OK;
+  if (!cu_seqlen_ks || !cu_seqlen_ke || !local_cu_seq_lens || !context_lens || !request_ids)
+    return DSA_ERR_INVALID_ARG;
+  const int dev = check_device();
+  if (dev != DSA_OK) return dev;
+  return launch_status(launch_prefill_rows(cu_seqlen_ks, cu_seqlen_ke, num_rows, local_cu_seq_lens, num_requests,
+                                           context_lens, request_ids, status,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dsa_prefill_mqa_logits(const void* q, const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages,
+                           int32_t kv_format, const float* weights, const int32_t* context_lens,
+                           const int32_t* request_ids, const int32_t* block_table, int64_t block_table_stride,
+                           int32_t num_requests, const int32_t* schedule, int32_t num_sms, void* logits,
+                           int32_t logits_dtype, int64_t logits_stride, int32_t num_rows, int32_t num_heads,
+                           int32_t head_dim, int32_t block_kv, int32_t* status, dsa_stream_t stream) {
+  if (num_rows > 0 && (request_ids == nullptr || num_requests < 1)) return DSA_ERR_INVALID_ARG;
+  return logits_call(q, kv_cache, page_stride_bytes, num_pages, kv_format, weights, context_lens, block_table,
+                     block_table_stride, request_ids, num_requests, request_ids, schedule, num_sms, logits,
+                     logits_dtype, logits_stride, num_rows, num_heads, head_dim, block_kv, status, stream);
 }
 
 int dsa_top_k_per_row(const void* logits, int32_t logits_dtype, int64_t logits_stride,

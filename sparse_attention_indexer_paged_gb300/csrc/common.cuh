@@ -57,6 +57,8 @@ struct LogitsArgs {
   const int32_t* context_lens;
   const int32_t* block_table;
   int64_t bt_stride;
+  const int32_t* bt_rows = nullptr;  // per-row block-table row (null: row-indexed table)
+  int32_t bt_num_rows = 0;
   const int32_t* indices;
   const int32_t* schedule;
   int32_t num_sms;
@@ -79,6 +81,9 @@ cudaError_t launch_dcp_pack(const void* logits, int32_t logits_dtype, int64_t lo
                             const int32_t* local_idx, int64_t idx_stride, int32_t num_rows, int32_t k,
                             int32_t rank, int32_t world, int32_t interleave, float* packed,
                             cudaStream_t stream);
+cudaError_t launch_prefill_rows(const int32_t* ks, const int32_t* ke, int32_t num_rows, const int32_t* starts,
+                                int32_t num_requests, int32_t* ctx, int32_t* req, int32_t* status,
+                                cudaStream_t stream);
 cudaError_t launch_dcp_merge(const float* gathered, int32_t world, int32_t num_rows, int32_t k,
                              int32_t* out_idx, int64_t out_stride, cudaStream_t stream);
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, int32_t* status, cudaStream_t stream);

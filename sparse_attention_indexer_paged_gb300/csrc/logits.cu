@@ -132,6 +132,8 @@ struct Params {
   const int32_t* ctx;
   const int32_t* block_table;
   int64_t bt_stride;
+  const int32_t* bt_rows;  // block-table row of each row (null: the row itself)
+  int32_t bt_num_rows;     // rows of the block table when bt_rows is set
   const int32_t* indices;
   const int32_t* schedule;
   int32_t num_sms;
@@ -140,6 +142,21 @@ struct Params {
   int32_t num_rows;
   int32_t* status;
 };
+
+// The block-table row that row `row` reads its pages from: the row itself,
+// or, with a per-row map (prefill rows reading their request's table), the
+// mapped row; a mapped row outside the table is reported and row 0 read.
+__device__ __forceinline__ const int32_t* table_row(const Params& p, int row) {
+  int64_t tr = row;
+  if (p.bt_rows != nullptr) {
+    tr = __ldg(p.bt_rows + row);
+    if (tr < 0 || tr >= p.bt_num_rows) {
+      report(p.status, kErrBadBlock);
+      tr = 0;
+    }
+  }
+  return p.block_table + tr * p.bt_stride;
+}
 
 struct Bars {
   uint32_t kv_full, kv_empty, raw_full, raw_empty, sc_full, sc_empty, q_full, q_empty, w_full,
@@ -465,7 +482,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     bool ok = true;
     while (ok && walk.next(lane)) {
       const int r0 = walk.r0, n = walk.n;
-      const int32_t* bt_row = p.block_table + static_cast<int64_t>(r0 + n - 1) * p.bt_stride;
+      const int32_t* bt_row = table_row(p, r0 + n - 1);
       int32_t lane_blk = -1;  // block id of page (pg_base + lane)
       int pg_base = -32;
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
@@ -531,7 +548,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         int it = 0;
         bool ok = true;
         while (ok && walk.next(lane)) {
-          const int32_t* bt_row = p.block_table + static_cast<int64_t>(walk.r0 + walk.n - 1) * p.bt_stride;
+          const int32_t* bt_row = table_row(p, walk.r0 + walk.n - 1);
           int32_t lane_blk = -1;
           int pg_base = -32;
           for (int j = walk.j0; j < walk.j1; ++j, ++it) {
@@ -778,6 +795,8 @@ Params make_params(const LogitsArgs& a) {
   p.ctx = a.context_lens;
   p.block_table = a.block_table;
   p.bt_stride = a.bt_stride;
+  p.bt_rows = a.bt_rows;
+  p.bt_num_rows = a.bt_num_rows;
   p.indices = a.indices;
   p.schedule = a.schedule;
   p.num_sms = a.num_sms;
