@@ -754,7 +754,8 @@ def _oracle_sample(wl, rows, cols):
     t0 = time.perf_counter()
     lg, _ = oracle.paged_mqa_logits(wl.q, wl.kv_cache, wl.page_stride, wl.kv_format, wl.weights,
                                     ctx, wl.block_table, int(max(cols, 1)),
-                                    rows=np.array(rows, dtype=np.int32), with_bound=False)
+                                    rows=np.array(rows, dtype=np.int32), with_bound=False,
+                                    q_scale=wl.q_scale)
     oracle.top_k_per_row(lg, ctx.numpy()[rows], wl.topk)
     return time.perf_counter() - t0, int(sum(int(ctx[r]) for r in rows))
 

@@ -65,9 +65,11 @@ def lib():
             L.oracle_e4m3_value.restype = dbl
             L.oracle_e2m1_value.argtypes = [u8]
             L.oracle_e2m1_value.restype = dbl
+            L.oracle_ue8m0_value.argtypes = [u8]
+            L.oracle_ue8m0_value.restype = dbl
             L.oracle_validate.argtypes = [P, P, P, i64, i32, i64, i32, i64]
             L.oracle_validate.restype = ctypes.c_int
-            L.oracle_paged_mqa_logits.argtypes = [P, P, i64, i64, i32, P, P, P, i64, i32, i32,
+            L.oracle_paged_mqa_logits.argtypes = [P, P, P, i64, i64, i32, P, P, P, i64, i32, i32,
                                                   i32, i32, P, i32, P, P, i64, i32]
             L.oracle_paged_mqa_logits.restype = ctypes.c_int
             L.oracle_top_k_per_row.argtypes = [P, i64, P, P, i32, i32, P, i64, i32]
@@ -123,6 +125,10 @@ def e2m1_value(nibble: int) -> float:
     return lib().oracle_e2m1_value(int(nibble) & 0xF)
 
 
+def ue8m0_value(code: int) -> float:
+    return lib().oracle_ue8m0_value(int(code) & 0xFF)
+
+
 def validate(context_lens, indices, block_table, num_pages, logits_stride, block_kv=64) -> int:
     cl = _np(context_lens, np.int32)
     ind = _np(indices, np.int32)
@@ -134,23 +140,25 @@ def validate(context_lens, indices, block_table, num_pages, logits_stride, block
 
 
 def paged_mqa_logits(q, kv_cache, page_stride, kv_format, weights, context_lens, block_table,
-                     out_cols, rows=None, with_bound=True, block_kv=64, nthreads=0):
-    """fp64 logits (and bound) of the selected rows: arrays [n_sel, out_cols]."""
+                     out_cols, rows=None, with_bound=True, block_kv=64, nthreads=0, q_scale=None):
+    """fp64 logits (and bound) of the selected rows: arrays [n_sel, out_cols].
+    q is e4m3 [T, H, D]; with q_scale (MXFP4 keys), packed e2m1 [T, H, D/2]."""
     qn = _np(q, np.uint8)
+    qs = _np(q_scale, np.uint8)
     kv = _np(kv_cache, np.uint8)
     w = _np(weights, np.float32)
     cl = _np(context_lens, np.int32)
     bt = _np(block_table, np.int32)
     T = cl.shape[0]
     H = w.shape[1] if w.ndim == 2 else w.size // max(T, 1)
-    D = qn.size // max(T * H, 1)
+    D = qn.size // max(T * H, 1) * (2 if qs is not None else 1)
     bt2 = bt.reshape(T, -1)
     rws = None if rows is None else _np(rows, np.int32)
     n_sel = T if rws is None else rws.shape[0]
     num_pages = kv.shape[0] if kv.ndim == 2 else kv.size // page_stride
     logits = np.empty((n_sel, out_cols), dtype=np.float64)
     bound = np.empty((n_sel, out_cols), dtype=np.float64) if with_bound else None
-    st = lib().oracle_paged_mqa_logits(_ptr(qn), _ptr(kv), int(page_stride), int(num_pages),
+    st = lib().oracle_paged_mqa_logits(_ptr(qn), _ptr(qs), _ptr(kv), int(page_stride), int(num_pages),
                                        int(kv_format), _ptr(w), _ptr(cl), _ptr(bt2),
                                        bt2.shape[1], T, H, D, int(block_kv), _ptr(rws),
                                        n_sel, _ptr(logits), _ptr(bound), int(out_cols),
@@ -209,7 +217,8 @@ def workload_logits(wl, rows=None, with_bound=True, nthreads=0, out_cols=None):
     return paged_mqa_logits(wl.q, wl.kv_cache, wl.page_stride, wl.kv_format, wl.weights,
                             wl.context_lens, wl.block_table,
                             wl.logits_stride if out_cols is None else out_cols,
-                            rows=rows, with_bound=with_bound, nthreads=nthreads)
+                            rows=rows, with_bound=with_bound, nthreads=nthreads,
+                            q_scale=getattr(wl, "q_scale", None))
 
 
 # ---------------------------------------------------------------------------
@@ -290,4 +299,5 @@ def prefill_logits(pf, rows=None, with_bound=True, nthreads=0):
     ctx, req = prefill_rows(pf.cu_seqlen_ks, pf.cu_seqlen_ke, pf.local_cu_seq_lens)
     bt = _np(pf.block_table, np.int32)[req]          # the row-indexed view of the request table
     return paged_mqa_logits(pf.q, pf.kv_cache, pf.page_stride, pf.kv_format, pf.weights, ctx, bt,
-                            pf.logits_stride, rows=rows, with_bound=with_bound, nthreads=nthreads)
+                            pf.logits_stride, rows=rows, with_bound=with_bound, nthreads=nthreads,
+                            q_scale=getattr(pf, "q_scale", None))

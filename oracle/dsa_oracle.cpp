@@ -41,6 +41,7 @@ namespace {
 
 constexpr int kKvFp8 = 0;
 constexpr int kKvFp4 = 1;
+constexpr int kKvMxfp4 = 2;
 
 // Planted-mistake switch used only by the oracle's own pin tests, to show that
 // every pin can fail.  0 = the correct definition.
@@ -80,6 +81,12 @@ double decode_e2m1(uint8_t nibble) {
   return sign ? -mag : mag;
 }
 
+// OCP Microscaling E8M0 scale: 2^(code - 127); code 255 is NaN.
+double decode_ue8m0(uint8_t code) {
+  if (code == 0xFF) return std::numeric_limits<double>::quiet_NaN();
+  return std::ldexp(1.0, static_cast<int>(code) - (g_plant == 13 ? 128 : 127));
+}
+
 float load_f32(const uint8_t* p) {
   float f;
   std::memcpy(&f, p, 4);
@@ -91,15 +98,29 @@ float load_f32(const uint8_t* p) {
 //   FP8: values [64][D] e4m3 at 0, fp32 scale[64] after the values.
 //   FP4: packed e2m1 [64][D/2] at 0 (element 2i in the low nibble of byte i),
 //        e4m3 block scales [64][D/16] after them, fp32 token scale[64] last.
+//   MXFP4: packed e2m1 [64][D/2] at 0 (as FP4), then ue8m0 scales [64][D/32];
+//        no token scale (it is 1).
 // (Per-token payload: sparse_attn_indexer docs, _gather_workspace_shapes and
-// kv_cache_as_quant_view; the split of values and scales inside the page and
-// the two-level FP4 scale are this build's storage reading.)
+// kv_cache_as_quant_view -- MXFP4 is head_dim/2 packed bytes plus
+// head_dim/MXFP4_BLOCK_SIZE ue8m0 scales, with the OCP MX block of 32; the
+// split of values and scales inside the page and the two-level FP4 scale are
+// this build's storage reading.)
 double decode_token(const uint8_t* page, int kv_format, int slot, int D, int block_kv,
                     double* k) {
   if (kv_format == kKvFp8) {
     const uint8_t* v = page + static_cast<int64_t>(slot) * D;
     for (int d = 0; d < D; ++d) k[d] = decode_e4m3(v[d]);
     return load_f32(page + static_cast<int64_t>(block_kv) * D + 4 * slot);
+  }
+  if (kv_format == kKvMxfp4) {
+    const uint8_t* v = page + static_cast<int64_t>(slot) * (D / 2);
+    const uint8_t* es = page + static_cast<int64_t>(block_kv) * (D / 2) + static_cast<int64_t>(slot) * (D / 32);
+    for (int d = 0; d < D; ++d) {
+      const uint8_t byte = v[d / 2];
+      const uint8_t nib = (d % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+      k[d] = decode_e2m1(nib) * decode_ue8m0(es[d / 32]);
+    }
+    return 1.0;
   }
   const uint8_t* v = page + static_cast<int64_t>(slot) * (D / 2);
   const uint8_t* bs = page + static_cast<int64_t>(block_kv) * (D / 2) +
@@ -152,6 +173,8 @@ void oracle_set_plant(int p) { g_plant = p; }
 double oracle_e4m3_value(uint8_t code) { return decode_e4m3(code); }
 
 double oracle_e2m1_value(uint8_t nibble) { return decode_e2m1(nibble & 0xF); }
+
+double oracle_ue8m0_value(uint8_t code) { return decode_ue8m0(code); }
 
 // Preconditions of the varlen decode call (PR 56811 "Fix
 // fp8_fp4_paged_mqa_logits MQA kpool varlen path for speculative decode",
@@ -206,7 +229,10 @@ int oracle_validate(const int32_t* context_lens, const int32_t* indices,
 }
 
 // Paged MQA logits in fp64 (definition in the header comment).
-//   q        [num_rows][H][D] e4m3 codes
+//   q        [num_rows][H][D] e4m3 codes; with q_scale (MXFP4 keys only, the
+//            pages' FP4 path quantises q with scales too: sparse_attn_indexer
+//            docs, forward_cuda), packed e2m1 [num_rows][H][D/2] and q_scale
+//            ue8m0 [num_rows][H][D/32]
 //   weights  [num_rows][H] fp32 (the per-token q scale is folded into them:
 //            sparse_attn_indexer docs, SparseAttnIndexer.forward_cuda)
 //   rows     which rows to evaluate (NULL: all rows, in order); output row i
@@ -214,7 +240,7 @@ int oracle_validate(const int32_t* context_lens, const int32_t* indices,
 //   logits   [n_sel][out_cols] fp64; columns >= L_t are -inf
 //   bound    [n_sel][out_cols] fp64 or NULL: kscale * sum_h sum_d |w q k|, the
 //            magnitude the accuracy tolerance is stated against
-int oracle_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_cache, int64_t page_stride,
+int oracle_paged_mqa_logits(const uint8_t* q, const uint8_t* q_scale, const uint8_t* kv_cache, int64_t page_stride,
                             int64_t num_pages, int32_t kv_format, const float* weights,
                             const int32_t* context_lens, const int32_t* block_table,
                             int64_t bt_stride, int32_t num_rows, int32_t H, int32_t D,
@@ -223,7 +249,8 @@ int oracle_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_cache, int64_t p
                             int32_t nthreads) {
   if (!q || !kv_cache || !weights || !context_lens || !block_table || !logits) return ORACLE_ERR_ARG;
   if (H <= 0 || D <= 0 || D % 32 != 0 || block_kv <= 0 || num_rows < 0) return ORACLE_ERR_ARG;
-  if (kv_format != kKvFp8 && kv_format != kKvFp4) return ORACLE_ERR_ARG;
+  if (kv_format != kKvFp8 && kv_format != kKvFp4 && kv_format != kKvMxfp4) return ORACLE_ERR_ARG;
+  if ((kv_format == kKvMxfp4) != (q_scale != nullptr)) return ORACLE_ERR_ARG;
   if (n_sel < 0) return ORACLE_ERR_ARG;
   const int n_eval = rows ? n_sel : num_rows;
   for (int i = 0; i < n_eval; ++i) {
@@ -249,8 +276,15 @@ int oracle_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_cache, int64_t p
     const int t = rows ? rows[i] : i;
     const int32_t L = context_lens[t];
     std::vector<double> qd(static_cast<size_t>(H) * D), k(D);
-    for (int64_t j = 0; j < static_cast<int64_t>(H) * D; ++j)
-      qd[j] = decode_e4m3(q[static_cast<int64_t>(t) * H * D + j]);
+    for (int64_t j = 0; j < static_cast<int64_t>(H) * D; ++j) {
+      if (q_scale == nullptr) {
+        qd[j] = decode_e4m3(q[static_cast<int64_t>(t) * H * D + j]);
+      } else {  // MXFP4 q: packed e2m1 [H][D/2] and ue8m0 scales [H][D/32] per row
+        const uint8_t byte = q[(static_cast<int64_t>(t) * H * D + j) / 2];
+        const uint8_t nib = (j % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+        qd[j] = decode_e2m1(nib) * decode_ue8m0(q_scale[(static_cast<int64_t>(t) * H * D + j) / 32]);
+      }
+    }
     double* out = logits + static_cast<int64_t>(i) * out_cols;
     double* bnd = bound ? bound + static_cast<int64_t>(i) * out_cols : nullptr;
     for (int64_t s = c0; s < c1; ++s) {

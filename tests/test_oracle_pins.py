@@ -74,6 +74,10 @@ def dense_keys(wl, t):
     el = np.empty((L, 128))
     el[:, 0::2] = lo
     el[:, 1::2] = hi
+    if wl.kv_format == W.KV_MXFP4:
+        esc = kv[page[:, None], 4096 + slot[:, None] * 4 + np.arange(4)[None, :]]
+        es = torch.from_numpy(esc.copy()).view(torch.float8_e8m0fnu).double().numpy()
+        return el * np.repeat(es, 32, axis=1), np.ones(L)
     bsc = kv[page[:, None], 4096 + slot[:, None] * 8 + np.arange(8)[None, :]]
     bs = torch.from_numpy(bsc.copy()).view(torch.float8_e4m3fn).double().numpy()
     vals = el * np.repeat(bs, 16, axis=1)
@@ -83,7 +87,15 @@ def dense_keys(wl, t):
 
 
 def dense_q(wl, t):
-    return wl.q[t].view(torch.float8_e4m3fn).double().numpy()  # [H, D]
+    if wl.q_scale is None:
+        return wl.q[t].view(torch.float8_e4m3fn).double().numpy()  # [H, D]
+    tab = _e2m1_table()
+    packed = wl.q[t].numpy()                                        # [H, D/2]
+    el = np.empty((packed.shape[0], 2 * packed.shape[1]))
+    el[:, 0::2] = tab[packed & 0xF]
+    el[:, 1::2] = tab[packed >> 4]
+    es = wl.q_scale[t].view(torch.float8_e8m0fnu).double().numpy()  # [H, D/32]
+    return el * np.repeat(es, 32, axis=1)
 
 
 def small_workload(seed=0, H=64, kv_format=W.KV_FP8, lens=(150, 77, 203), rows=(1, 3, 2)):
@@ -108,6 +120,15 @@ def check_e4m3_vs_torch():
             assert math.isnan(got)
         else:
             assert got == val and math.copysign(1, got) == math.copysign(1, val)
+
+
+def check_ue8m0_vs_torch():
+    """The OCP MX E8M0 scale against torch's float8_e8m0fnu, all 256 codes."""
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).double().numpy()
+    mine = np.array([oracle.ue8m0_value(c) for c in range(256)])
+    assert np.array_equal(np.isnan(ref), np.isnan(mine))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], mine[ok])
 
 
 def check_e2m1_vs_spec():
@@ -148,7 +169,8 @@ def check_one_hot_reads_key():
 
 def _neg_q(wl):
     w2 = W.Workload(**{**wl.__dict__})
-    w2.q = wl.q ^ 0x80                                # exact negation of every code
+    # exact negation of every code: the e4m3 sign bit, or both e2m1 nibbles' sign bits
+    w2.q = wl.q ^ (0x88 if wl.q_scale is not None else 0x80)
     return w2
 
 
@@ -256,6 +278,11 @@ def check_topk_bruteforce(seed=0):
 
 def check_fp4_bruteforce():
     check_bruteforce(kv_format=W.KV_FP4, seed=21)
+
+
+def check_mxfp4_bruteforce():
+    check_bruteforce(kv_format=W.KV_MXFP4, seed=23)
+    check_relu_identities(kv_format=W.KV_MXFP4)
 
 
 def check_dcp_mapping():
@@ -367,6 +394,7 @@ PIN_CHECKS = [
     check_e4m3_vs_torch, check_e2m1_vs_spec, check_bruteforce, check_one_hot_reads_key,
     check_relu_identities, check_weight_scaling, check_page_permutation,
     check_varlen_equals_padded, check_topk_bruteforce, check_fp4_bruteforce,
+    check_ue8m0_vs_torch, check_mxfp4_bruteforce,
     check_dcp_mapping, check_dcp_merge_is_global_topk, check_chunk_ranges, check_prefill_rows,
 ]
 
@@ -521,6 +549,7 @@ PLANTS = {
     10: "row chunking counts whole 16-row units only (drops the partial one)",
     11: "row chunking gives the smaller slices first",
     12: "prefill causal length taken as ke instead of ke - ks",
+    13: "ue8m0 scale with bias 128 instead of 127",
 }
 
 

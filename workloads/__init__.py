@@ -27,6 +27,18 @@ Storage formats (one page = ``PAGE_TOKENS`` = 64 tokens, head_dim D = 128):
 
   The stored key is ``k[s, d] = e2m1 * e4m3(block_scale[s, d // 16]) * g[s]``.
 
+* MXFP4 page, ``MXFP4_PAGE_BYTES`` = 4352 B (the pages' own FP4 cache:
+  ``head_dim // 2`` packed bytes and ``head_dim // 32`` ue8m0 scales a token,
+  ``_gather_workspace_shapes``)::
+
+      [0, 4096)     token j's 64 bytes of packed e2m1 (as FP4)
+      [4096, 4352)  token j's 4 ue8m0 block scales at 4096 + 4*j
+                    (block b covers elements 32b .. 32b+31)
+
+  The stored key is ``k[s, d] = e2m1 * 2^(block_scale[s, d // 32] - 127)``;
+  q is stored the same way (packed e2m1 ``[T, H, D/2]`` and ue8m0
+  ``q_scale [T, H, D/32]``).
+
 Pages live in a pool ``kv_cache`` of shape ``[num_pages, page_stride]`` (uint8);
 ``page_stride`` is at least the page size and a multiple of 16.  Pages that no
 request uses, and the tail of each request's last page, are poisoned (e4m3 NaN
@@ -50,6 +62,7 @@ HEAD_DIM = 128
 
 KV_FP8 = 0
 KV_FP4 = 1
+KV_MXFP4 = 2
 
 LOGITS_F32 = 0
 LOGITS_BF16 = 1
@@ -61,6 +74,10 @@ FP4_BSCALE_OFFSET = FP4_VALUES_BYTES                 # 4096
 FP4_BSCALE_BYTES = PAGE_TOKENS * HEAD_DIM // 16      # 512
 FP4_GSCALE_OFFSET = FP4_BSCALE_OFFSET + FP4_BSCALE_BYTES  # 4608
 FP4_PAGE_BYTES = FP4_GSCALE_OFFSET + PAGE_TOKENS * 4  # 4864
+MX_BLOCK = 32
+MXFP4_SCALE_OFFSET = FP4_VALUES_BYTES                 # 4096
+MXFP4_PAGE_BYTES = MXFP4_SCALE_OFFSET + PAGE_TOKENS * HEAD_DIM // MX_BLOCK  # 4352
+UE8M0_NAN = 0xFF
 
 E4M3_NAN = 0x7F
 E4M3_MAX = 448.0
@@ -68,7 +85,7 @@ E2M1_MAX = 6.0
 
 
 def page_bytes(kv_format: int) -> int:
-    return FP8_PAGE_BYTES if kv_format == KV_FP8 else FP4_PAGE_BYTES
+    return {KV_FP8: FP8_PAGE_BYTES, KV_FP4: FP4_PAGE_BYTES, KV_MXFP4: MXFP4_PAGE_BYTES}[kv_format]
 
 
 def round_up(x: int, m: int) -> int:
@@ -94,6 +111,7 @@ class Workload:
     request_lens: list[int] = field(default_factory=list)
     rows_per_request: list[int] = field(default_factory=list)
     seed: int = 0
+    q_scale: torch.Tensor | None = None  # uint8 [T, H, D/32] ue8m0 (MXFP4 only; q is then packed e2m1)
 
     @property
     def num_rows(self) -> int:
@@ -110,7 +128,7 @@ class Workload:
                         mv(self.context_lens), mv(self.indices), mv(self.block_table),
                         mv(self.kv_cache), self.page_stride, self.logits_stride,
                         self.topk, self.logits_dtype, list(self.request_lens),
-                        list(self.rows_per_request), self.seed)
+                        list(self.rows_per_request), self.seed, mv(self.q_scale))
 
 
 # ---------------------------------------------------------------------------
@@ -177,6 +195,28 @@ def quantize_keys_fp4(keys: torch.Tensor):
     codes = torch.where((denom > 0)[..., None], codes, torch.zeros_like(codes)).view(n, d)
     packed = codes[:, 0::2] | (codes[:, 1::2] << 4)
     return packed, bs_codes, g
+
+
+def quantize_mxfp4(x: torch.Tensor):
+    """OCP MX FP4 quantisation of x [..., D] in blocks of 32 along the last dim.
+
+    Shared scale 2^(floor(log2(amax_b)) - 2) (2 = the largest e2m1 exponent),
+    stored as the ue8m0 code floor(log2(amax_b)) - 2 + 127 (127, scale 1, for an
+    all-zero block); element code = e2m1(x / scale), saturating at +-6.
+    Returns (packed uint8 [..., D/2], scale codes uint8 [..., D/32]).
+    """
+    shp = x.shape
+    d = shp[-1]
+    blocks = x.reshape(-1, d // MX_BLOCK, MX_BLOCK).to(torch.float32)
+    amax = blocks.abs().amax(dim=-1)
+    expo = torch.where(amax > 0, torch.floor(torch.log2(torch.where(amax > 0, amax, torch.ones_like(amax)))) - 2,
+                       torch.zeros_like(amax))
+    expo = expo.clamp(-127, 127)
+    codes_s = (expo + 127).to(torch.uint8)
+    scale = torch.exp2(expo)
+    codes = e2m1_codes(blocks / scale[..., None]).view(-1, d)
+    packed = codes[:, 0::2] | (codes[:, 1::2] << 4)
+    return packed.view(*shp[:-1], d // 2), codes_s.view(*shp[:-1], d // MX_BLOCK)
 
 
 # ---------------------------------------------------------------------------
@@ -250,15 +290,23 @@ def build(name: str, request_lens, rows_per_request, *, kv_format=KV_FP8, topk=2
             codes, scale = quantize_keys_fp8(keys)
             views["values"][page, slot] = codes
             views["scale"][page, slot] = scale.contiguous().view(torch.uint8).view(-1, 4)
-        else:
+        elif kv_format == KV_FP4:
             packed, bs, g = quantize_keys_fp4(keys)
             views["values"][page, slot] = packed
             views["bscale"][page, slot] = bs
             views["scale"][page, slot] = g.contiguous().view(torch.uint8).view(-1, 4)
+        else:
+            packed, es = quantize_mxfp4(keys)
+            views["values"][page, slot] = packed
+            views["bscale"][page, slot] = es
         del keys
 
-    q = e4m3_codes(torch.randn((T, heads, head_dim), generator=gen, device=device,
-                               dtype=torch.float32))
+    qf = torch.randn((T, heads, head_dim), generator=gen, device=device, dtype=torch.float32)
+    q_scale = None
+    if kv_format == KV_MXFP4:
+        q, q_scale = quantize_mxfp4(qf)
+    else:
+        q = e4m3_codes(qf)
     weights = (torch.randn((T, heads), generator=gen, device=device, dtype=torch.float32)
                / math.sqrt(heads))
     max_ctx = max(ctx) if ctx else 0
@@ -266,7 +314,7 @@ def build(name: str, request_lens, rows_per_request, *, kv_format=KV_FP8, topk=2
     return Workload(name, kv_format, q, weights, context_lens.to(device),
                     None if indices is None else indices.to(device),
                     block_table.to(device), kv, stride, lstride, int(topk), int(logits_dtype),
-                    L_r, n_r, seed)
+                    L_r, n_r, seed, q_scale)
 
 
 def _poison(kv: torch.Tensor, kv_format: int) -> None:
@@ -275,6 +323,10 @@ def _poison(kv: torch.Tensor, kv_format: int) -> None:
         kv[:, :FP8_VALUES_BYTES] = E4M3_NAN
         kv[:, FP8_VALUES_BYTES:FP8_PAGE_BYTES] = nan4.repeat(PAGE_TOKENS).to(kv.device)
         kv[:, FP8_PAGE_BYTES:] = 0xA5
+    elif kv_format == KV_MXFP4:
+        kv[:, :FP4_VALUES_BYTES] = 0x77          # e2m1 +6 in both nibbles
+        kv[:, MXFP4_SCALE_OFFSET:MXFP4_PAGE_BYTES] = UE8M0_NAN
+        kv[:, MXFP4_PAGE_BYTES:] = 0xA5
     else:
         kv[:, :FP4_VALUES_BYTES] = 0x77          # e2m1 +6 in both nibbles
         kv[:, FP4_BSCALE_OFFSET:FP4_GSCALE_OFFSET] = E4M3_NAN
@@ -289,6 +341,12 @@ def _page_views(kv: torch.Tensor, kv_format: int) -> dict:
         return {
             "values": kv.as_strided((n, PAGE_TOKENS, HEAD_DIM), (stride, HEAD_DIM, 1), 0),
             "scale": kv.as_strided((n, PAGE_TOKENS, 4), (stride, 4, 1), FP8_VALUES_BYTES),
+        }
+    if kv_format == KV_MXFP4:
+        return {
+            "values": kv.as_strided((n, PAGE_TOKENS, HEAD_DIM // 2), (stride, HEAD_DIM // 2, 1), 0),
+            "bscale": kv.as_strided((n, PAGE_TOKENS, HEAD_DIM // MX_BLOCK), (stride, HEAD_DIM // MX_BLOCK, 1),
+                                    MXFP4_SCALE_OFFSET),
         }
     return {
         "values": kv.as_strided((n, PAGE_TOKENS, HEAD_DIM // 2), (stride, HEAD_DIM // 2, 1), 0),
@@ -447,7 +505,8 @@ def dcp_shard(wl: Workload, rank: int, world: int, interleave: int) -> Workload:
     stride = round_up(max(1, int(ctx_loc.max()) if T else 1), 64)
     return Workload(f"{wl.name}-dcp{rank}of{world}i{interleave}", fmt, wl.q.cpu(), wl.weights.cpu(),
                     ctx_loc, ind, bt_loc, pool.contiguous(), int(kv.shape[1]), stride, wl.topk,
-                    wl.logits_dtype, list(wl.request_lens), list(wl.rows_per_request), wl.seed)
+                    wl.logits_dtype, list(wl.request_lens), list(wl.rows_per_request), wl.seed,
+                    None if wl.q_scale is None else wl.q_scale.cpu())
 
 
 # ---------------------------------------------------------------------------
@@ -473,6 +532,7 @@ class Prefill:
     logits_stride: int
     topk: int
     logits_dtype: int
+    q_scale: torch.Tensor | None = None  # MXFP4 q scales
 
     @property
     def num_rows(self) -> int:
@@ -487,7 +547,7 @@ class Prefill:
                          for x in (self.q, self.weights, self.cu_seqlen_ks, self.cu_seqlen_ke,
                                    self.local_cu_seq_lens, self.block_table, self.kv_cache)),
                        self.kv_format, self.page_stride, self.logits_stride, self.topk,
-                       self.logits_dtype)
+                       self.logits_dtype, None if self.q_scale is None else self.q_scale.to(device))
 
 
 def prefill_view(wl: Workload) -> Prefill:
@@ -510,4 +570,4 @@ def prefill_view(wl: Workload) -> Prefill:
     bt = wl.block_table.cpu()[torch.tensor(last, dtype=torch.int64)].contiguous()
     return Prefill(wl.q.cpu(), wl.weights.cpu(), ks, ks + ctx, torch.tensor(cu, dtype=torch.int32), bt,
                    wl.kv_cache.cpu(), wl.kv_format, wl.page_stride, wl.logits_stride, wl.topk,
-                   wl.logits_dtype)
+                   wl.logits_dtype, None if wl.q_scale is None else wl.q_scale.cpu())
