@@ -64,7 +64,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="varlen",
-                    choices=["tiny", "plain", "mtp", "varlen", "fp4_varlen", "prefill"])
+                    choices=["tiny", "plain", "mtp", "varlen", "fp4_varlen", "mxfp4_varlen", "prefill"])
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
@@ -98,10 +98,11 @@ def peaks():
 
 def workload_desc(name, wl):
     T = wl.num_rows
-    fmt = "FP8 e4m3" if wl.kv_format == 0 else "FP4 e2m1 + e4m3/16 + fp32/token"
+    fmt = ["FP8 e4m3", "FP4 e2m1 + e4m3/16 + fp32/token", "MXFP4 e2m1 + ue8m0/32"][wl.kv_format]
+    qf = "MXFP4 e2m1 + ue8m0/32" if wl.q_scale is not None else "e4m3"
     return (f"{name}: B={len(wl.request_lens)} requests, context {min(wl.request_lens)}.."
             f"{max(wl.request_lens)}, rows/request {min(wl.rows_per_request)}.."
-            f"{max(wl.rows_per_request)} (T={T}), q e4m3, keys {fmt}, H=64, D=128, "
+            f"{max(wl.rows_per_request)} (T={T}), q {qf}, keys {fmt}, H=64, D=128, "
             f"block_kv=64, top-k {wl.topk}, logits {'fp32' if wl.logits_dtype == 0 else 'bf16'}")
 
 
@@ -110,7 +111,7 @@ def algorithmic_bytes(wl):
     import workloads as W
     ctx = wl.context_lens.cpu().tolist()
     ind = None if wl.indices is None else wl.indices.cpu().tolist()
-    per_tok = 132 if wl.kv_format == W.KV_FP8 else 76
+    per_tok = {W.KV_FP8: 132, W.KV_FP4: 76, W.KV_MXFP4: 68}[wl.kv_format]  # values + scales a token
     logit_b = 4 if wl.logits_dtype == W.LOGITS_F32 else 2
     # groups = runs of equal request ids, at most 8 rows
     key_bytes = 0
@@ -126,7 +127,8 @@ def algorithmic_bytes(wl):
         bt_bytes += (lmax + 63) // 64 * 4
         t = u
     logits_bytes = sum(max(c, 0) for c in ctx) * logit_b
-    small = T * 64 * 128 + T * 64 * 4 + T * 4 * 2 + bt_bytes
+    q_bytes = T * 64 * 128 if wl.q_scale is None else T * 64 * (64 + 4)
+    small = q_bytes + T * 64 * 4 + T * 4 * 2 + bt_bytes
     flops = 2 * 64 * 128 * sum(max(c, 0) for c in ctx)
     return key_bytes, logits_bytes, small, flops
 
@@ -228,16 +230,21 @@ def run_ours(args, rank, world, local):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
 
-    def make_calls(q, w, ctx, ind, bt, out_idx):
+    mx = wl.kv_format == W.KV_MXFP4
+    logits_fn = L.dsa_mxfp4_paged_mqa_logits if mx else L.dsa_fp8_fp4_paged_mqa_logits
+
+    def make_calls(q, w, ctx, ind, bt, out_idx, qs=None):
         meta = (P(ctx), P(ind), T, 64, S, P(sched), sp)
-        lg = (P(q), P(wl.kv_cache), wl.page_stride, wl.num_pages, wl.kv_format, P(w), P(ctx),
-              P(bt), bt.stride(0), P(ind), P(sched), S, P(logits), wl.logits_dtype,
-              wl.logits_stride, T, 64, 128, 64, P(status), sp)
+        # MXFP4 keys: the MXFP4 entry point with the q scales; else the key format
+        head = (P(q), P(qs), P(wl.kv_cache), wl.page_stride, wl.num_pages) if mx else \
+               (P(q), P(wl.kv_cache), wl.page_stride, wl.num_pages, wl.kv_format)
+        lg = head + (P(w), P(ctx), P(bt), bt.stride(0), P(ind), P(sched), S, P(logits), wl.logits_dtype,
+                     wl.logits_stride, T, 64, 128, 64, P(status), sp)
         tk = (P(logits), wl.logits_dtype, wl.logits_stride, None, P(ctx), T, wl.topk,
               P(out_idx), out_idx.stride(0), P(status), sp)
         return meta, lg, tk
 
-    meta, lg, tk = make_calls(wl.q, wl.weights, wl.context_lens, wl.indices, wl.block_table, idx)
+    meta, lg, tk = make_calls(wl.q, wl.weights, wl.context_lens, wl.indices, wl.block_table, idx, wl.q_scale)
 
     def step(ev=None):
         if ev is not None:
@@ -245,7 +252,7 @@ def run_ours(args, rank, world, local):
         r1 = L.dsa_paged_mqa_logits_metadata(*meta)
         if ev is not None:
             ev[1].record(stream)
-        r2 = L.dsa_fp8_fp4_paged_mqa_logits(*lg)
+        r2 = logits_fn(*lg)
         if ev is not None:
             ev[2].record(stream)
         r3 = L.dsa_top_k_per_row(*tk)
@@ -293,6 +300,7 @@ def run_ours(args, rank, world, local):
     # i-1's result copy, so device inputs and outputs are double buffered
     # and three streams are ordered by events.
     hq = wl.q.cpu().pin_memory()
+    hqs = None if wl.q_scale is None else wl.q_scale.cpu().pin_memory()
     hw = wl.weights.cpu().pin_memory()
     hctx = wl.context_lens.cpu().pin_memory()
     hind = None if wl.indices is None else wl.indices.cpu().pin_memory()
@@ -301,11 +309,14 @@ def run_ours(args, rank, world, local):
     sets = []
     for _ in range(2):
         dq, dw, dctx = torch.empty_like(wl.q), torch.empty_like(wl.weights), torch.empty_like(wl.context_lens)
+        dqs = None if wl.q_scale is None else torch.empty_like(wl.q_scale)
         dind = None if hind is None else torch.empty_like(wl.indices)
         dbt = torch.empty_like(wl.block_table)
         didx = torch.empty_like(idx)
         h2d = [(dq, hq), (dw, hw), (dctx, hctx), (dbt, hbt)] + ([(dind, hind)] if hind is not None else [])
-        sets.append(dict(h2d=h2d, didx=didx, calls=make_calls(dq, dw, dctx, dind, dbt, didx)))
+        if dqs is not None:
+            h2d.append((dqs, hqs))
+        sets.append(dict(h2d=h2d, didx=didx, calls=make_calls(dq, dw, dctx, dind, dbt, didx, dqs)))
     h2d_bytes = sum(h.numel() * h.element_size() for _, h in sets[0]["h2d"])
     d2h_bytes = hidx[0].numel() * hidx[0].element_size()
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
@@ -325,7 +336,7 @@ def run_ours(args, rank, world, local):
         stream.wait_event(ev_ready[i % 2])
         stream.wait_event(ev_out[i % 2])      # its previous result was copied out
         m, lgc, tkc = st["calls"]
-        r = L.dsa_paged_mqa_logits_metadata(*m) | L.dsa_fp8_fp4_paged_mqa_logits(*lgc) | L.dsa_top_k_per_row(*tkc)
+        r = L.dsa_paged_mqa_logits_metadata(*m) | logits_fn(*lgc) | L.dsa_top_k_per_row(*tkc)
         ev_done[i % 2].record(stream)
         s_out.wait_event(ev_done[i % 2])
         with torch.cuda.stream(s_out):
@@ -362,7 +373,7 @@ def run_ours(args, rank, world, local):
         for d, h in st0["h2d"]:
             d.copy_(h, non_blocking=True)
         m, lgc, tkc = st0["calls"]
-        r = L.dsa_paged_mqa_logits_metadata(*m) | L.dsa_fp8_fp4_paged_mqa_logits(*lgc) | L.dsa_top_k_per_row(*tkc)
+        r = L.dsa_paged_mqa_logits_metadata(*m) | logits_fn(*lgc) | L.dsa_top_k_per_row(*tkc)
         hidx[0].copy_(st0["didx"], non_blocking=True)
         return r
 
@@ -398,7 +409,7 @@ def run_ours(args, rank, world, local):
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3" if wl.kv_format == 0 else "fp4_e2m1+fp8_e4m3",
+        "dtype": ["fp8_e4m3", "fp4_e2m1+fp8_e4m3", "mxfp4_e2m1+ue8m0"][wl.kv_format],
         "data": "synthetic (seeded workloads.config; no dataset or weights)",
         "config": {
             "workload": workload_desc(args.workload, wl),
@@ -602,7 +613,7 @@ def run_prefill(args, local):
     idx = torch.empty((T, k), dtype=torch.int32, device=dev)
     rows_a = (P(pf.cu_seqlen_ks), P(pf.cu_seqlen_ke), T, P(pf.local_cu_seq_lens), B, P(ctx), P(req), P(status), sp)
     meta_a = (P(ctx), P(req), T, 64, S, P(sched), sp)
-    lg_a = (P(pf.q), P(pf.kv_cache), pf.page_stride, int(pf.kv_cache.shape[0]), pf.kv_format, P(pf.weights),
+    lg_a = (P(pf.q), P(pf.q_scale), P(pf.kv_cache), pf.page_stride, int(pf.kv_cache.shape[0]), pf.kv_format, P(pf.weights),
             P(ctx), P(req), P(pf.block_table), pf.block_table.stride(0), B, P(sched), S, P(logits),
             pf.logits_dtype, pf.logits_stride, T, 64, 128, 64, P(status), sp)
     tk_a = (P(logits), pf.logits_dtype, pf.logits_stride, None, P(ctx), T, k, P(idx), idx.stride(0), P(status), sp)
@@ -694,7 +705,7 @@ def run_chunked(args, local):
         scr = torch.empty(sb, dtype=torch.uint8, device=dev)
         sched = torch.empty(sw, dtype=torch.int32, device=dev)
         out = torch.empty((T, k), dtype=torch.int32, device=dev)
-        a = (P(wl.q), P(wl.kv_cache), wl.page_stride, wl.num_pages, wl.kv_format, P(wl.weights),
+        a = (P(wl.q), P(wl.q_scale), P(wl.kv_cache), wl.page_stride, wl.num_pages, wl.kv_format, P(wl.weights),
              P(wl.context_lens), P(wl.block_table), wl.block_table.stride(0), P(wl.indices), T, 64, 128, 64,
              S, wl.logits_dtype, wl.logits_stride, budget, P(scr), sb, P(sched), sw, k, P(out), out.stride(0),
              P(status), sp)

@@ -56,7 +56,7 @@ typedef enum {
   DSA_ERR_NO_DEVICE = 7          /* no usable sm_103 device */
 } dsa_status_t;
 
-enum { DSA_KV_FP8 = 0, DSA_KV_FP4 = 1 };
+enum { DSA_KV_FP8 = 0, DSA_KV_FP4 = 1, DSA_KV_MXFP4 = 2 };
 enum { DSA_LOGITS_F32 = 0, DSA_LOGITS_BF16 = 1 };
 
 /* Tokens per page, heads and head dimension of the supported shape. */
@@ -70,6 +70,8 @@ enum { DSA_LOGITS_F32 = 0, DSA_LOGITS_BF16 = 1 };
    allocation, [DOCS] forward_cpu) and must be a multiple of 16. */
 #define DSA_FP8_PAGE_BYTES 8448
 #define DSA_FP4_PAGE_BYTES 4864
+/* MXFP4 page: packed e2m1 [64][64 B] then ue8m0 block scales [64][4] (block 32) */
+#define DSA_MXFP4_PAGE_BYTES 4352
 /* Largest k of dsa_top_k_per_row. */
 #define DSA_MAX_TOPK 2048
 /* Largest decode-context-parallel world the merge accepts. */
@@ -144,7 +146,8 @@ int dsa_paged_mqa_logits_metadata(const int32_t* context_lens, const int32_t* in
  *                kv_cache + p * page_stride_bytes.
  *   page_stride_bytes >= page bytes of kv_format, multiple of 16.
  *   num_pages    pages in the pool, >= 1.
- *   kv_format    DSA_KV_FP8 or DSA_KV_FP4.
+ *   kv_format    DSA_KV_FP8 or DSA_KV_FP4 (DSA_KV_MXFP4 keys take MXFP4 q:
+ *                dsa_mxfp4_paged_mqa_logits; here they are DSA_ERR_INVALID_ARG).
  *   weights      (device) fp32 [num_rows][64], 16-byte aligned.
  *   context_lens (device) int32 [num_rows] (as for the metadata call).
  *   block_table  (device) int32 [num_rows][block_table_stride]: page ids of
@@ -172,6 +175,36 @@ int dsa_fp8_fp4_paged_mqa_logits(const void* q, const void* kv_cache, int64_t pa
                                  int32_t logits_dtype, int64_t logits_stride, int32_t num_rows,
                                  int32_t num_heads, int32_t head_dim, int32_t block_kv,
                                  int32_t* status, dsa_stream_t stream);
+
+/*
+ * dsa_mxfp4_paged_mqa_logits - the logits of the pages' own FP4 form: MXFP4
+ * keys and q ([DOCS] kv_cache_as_quant_view and _gather_workspace_shapes: an
+ * MXFP4 token is head_dim / 2 bytes of packed e2m1 and head_dim /
+ * MXFP4_BLOCK_SIZE ue8m0 scales; forward_cuda: the FP4 q is a (values,
+ * scales) pair).  Block size 32 (the OCP MX block).
+ *
+ *   logits[t, s] = sum_h weights[t, h] * max(0, sum_d q[t,h,d] * k[s,d]),
+ *   q[t,h,d] = e2m1 * 2^(q_scale[t,h,d/32] - 127),
+ *   k[s,d]   = e2m1 * 2^(page scale of (s, d/32) - 127)     (no token scale).
+ *
+ *   q        (device) packed e2m1 [num_rows][64][64], element 2i in the low
+ *            nibble of byte i; 16-byte aligned.
+ *   q_scale  (device) ue8m0 [num_rows][64][4], 16-byte aligned.
+ *   kv_cache pages of DSA_MXFP4_PAGE_BYTES: packed e2m1 [64][64], then
+ *            ue8m0 [64][4].
+ * The other arguments, the -inf tail and the status word are those of
+ * dsa_fp8_fp4_paged_mqa_logits.  The products are formed exactly (f16
+ * operands scaled by 2^(e - e_max) of their token or row, that factor
+ * applied to the fp32 result) unless a block's scale lies more than 2^14
+ * below its token's or row's largest, when f16 keeps fewer of its bits; a
+ * scale code 255 (NaN) gives a non-finite logit.
+ */
+int dsa_mxfp4_paged_mqa_logits(const void* q, const void* q_scale, const void* kv_cache, int64_t page_stride_bytes,
+                               int64_t num_pages, const float* weights, const int32_t* context_lens,
+                               const int32_t* block_table, int64_t block_table_stride, const int32_t* indices,
+                               const int32_t* schedule, int32_t num_sms, void* logits, int32_t logits_dtype,
+                               int64_t logits_stride, int32_t num_rows, int32_t num_heads, int32_t head_dim,
+                               int32_t block_kv, int32_t* status, dsa_stream_t stream);
 
 /*
  * dsa_top_k_per_row - the k largest logits of each row.
@@ -300,9 +333,11 @@ int dsa_prefill_rows(const int32_t* cu_seqlen_ks, const int32_t* cu_seqlen_ke, i
  * (context_lens, request_ids); rows of a request must be adjacent.  Column s
  * of row t is the request's token s (0 <= s < ke - ks), -inf up to
  * round_up(ke - ks, 64); a request id outside [0, num_requests) sets
- * DSA_ERR_BAD_BLOCK in `status`.
+ * DSA_ERR_BAD_BLOCK in `status`.  q_scale is NULL, or the MXFP4 q scales
+ * when kv_format is DSA_KV_MXFP4 (q then packed e2m1, as in
+ * dsa_mxfp4_paged_mqa_logits).
  */
-int dsa_prefill_mqa_logits(const void* q, const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages,
+int dsa_prefill_mqa_logits(const void* q, const void* q_scale, const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages,
                            int32_t kv_format, const float* weights, const int32_t* context_lens,
                            const int32_t* request_ids, const int32_t* block_table, int64_t block_table_stride,
                            int32_t num_requests, const int32_t* schedule, int32_t num_sms, void* logits,
@@ -346,13 +381,14 @@ int dsa_indexer_decode_scratch(int32_t num_rows, int32_t logits_dtype, int64_t l
  * caller's scratch, and its top-k into out_idx rows [start, end).
  *
  * Arguments are those of the three calls, for all rows; the slices are
- * pointer offsets into them.  logits_scratch and schedule hold at least what
+ * pointer offsets into them (q_scale: NULL, or the MXFP4 q scales when
+ * kv_format is DSA_KV_MXFP4).  logits_scratch and schedule hold at least what
  * dsa_indexer_decode_scratch returns and are reused by every slice (the
  * calls are stream-ordered).  Results equal one pass over all rows bit for
  * bit: a row's logits do not depend on the other rows.  Returns the first
  * error of the calls it issues; device faults go to `status`.
  */
-int dsa_indexer_decode_topk(const void* q, const void* kv_cache, int64_t page_stride_bytes,
+int dsa_indexer_decode_topk(const void* q, const void* q_scale, const void* kv_cache, int64_t page_stride_bytes,
                             int64_t num_pages, int32_t kv_format, const float* weights,
                             const int32_t* context_lens, const int32_t* block_table,
                             int64_t block_table_stride, const int32_t* indices, int32_t num_rows,

@@ -31,6 +31,7 @@ DSA_ERR_NO_DEVICE = 7
 
 KV_FP8 = 0
 KV_FP4 = 1
+KV_MXFP4 = 2
 LOGITS_F32 = 0
 LOGITS_BF16 = 1
 
@@ -39,6 +40,7 @@ NUM_HEADS = 64
 HEAD_DIM = 128
 FP8_PAGE_BYTES = 8448
 FP4_PAGE_BYTES = 4864
+MXFP4_PAGE_BYTES = 4352
 MAX_TOPK = 2048
 
 # C entry points and their argument types
@@ -57,11 +59,13 @@ _SIGS = {
     "dsa_dcp_pack_topk": ([_P, _I32, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P], ctypes.c_int),
     "dsa_dcp_merge_topk": ([_P, _I32, _I32, _I32, _P, _I64, _P], ctypes.c_int),
     "dsa_prefill_rows": ([_P, _P, _I32, _P, _I32, _P, _P, _P, _P], ctypes.c_int),
-    "dsa_prefill_mqa_logits": ([_P, _P, _I64, _I64, _I32, _P, _P, _P, _P, _I64, _I32, _P, _I32, _P,
+    "dsa_mxfp4_paged_mqa_logits": ([_P, _P, _P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _I32, _P, _I32, _I64,
+                                    _I32, _I32, _I32, _I32, _P, _P], ctypes.c_int),
+    "dsa_prefill_mqa_logits": ([_P, _P, _P, _I64, _I64, _I32, _P, _P, _P, _P, _I64, _I32, _P, _I32, _P,
                                 _I32, _I64, _I32, _I32, _I32, _I32, _P, _P], ctypes.c_int),
     "dsa_decode_chunk_ranges": ([_I64, _I64, _I64, _P, _I32, _P], ctypes.c_int),
     "dsa_indexer_decode_scratch": ([_I32, _I32, _I64, _I64, _I32, _P, _P], ctypes.c_int),
-    "dsa_indexer_decode_topk": ([_P, _P, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _I32, _I32, _I32,
+    "dsa_indexer_decode_topk": ([_P, _P, _P, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _I32, _I32, _I32,
                                  _I32, _I32, _I32, _I64, _I64, _P, _I64, _P, _I64, _I32, _P, _I64,
                                  _P, _P], ctypes.c_int),
 }
@@ -153,13 +157,15 @@ def paged_mqa_logits_metadata(context_lens, indices=None, num_sms=None, block_kv
 def fp8_fp4_paged_mqa_logits(q, kv_cache, weights, context_lens, block_table, schedule,
                              indices=None, kv_format=KV_FP8, logits_dtype=LOGITS_F32,
                              logits_stride=None, num_sms=None, out=None, status=None,
-                             page_stride=None):
+                             page_stride=None, q_scale=None):
     """Varlen paged MQA logits [num_rows, logits_stride] (fp32 or bf16).
 
     q [T, 64, 128] e4m3 codes (uint8 or float8_e4m3fn); kv_cache [num_pages,
     page_stride] uint8 pages; weights [T, 64] fp32; context_lens [T];
     block_table [T, max_pages] int32; schedule from paged_mqa_logits_metadata.
-    Columns >= round_up(L_t, 64) of a row are not specified.
+    Columns >= round_up(L_t, 64) of a row are not specified.  MXFP4 keys
+    (kv_format=KV_MXFP4) take MXFP4 q: packed e2m1 [T, 64, 64] and q_scale
+    ue8m0 [T, 64, 4].
     """
     device = q.device
     T = int(q.shape[0])
@@ -181,6 +187,14 @@ def fp8_fp4_paged_mqa_logits(q, kv_cache, weights, context_lens, block_table, sc
     assert qq.is_contiguous() and weights.is_contiguous() and weights.dtype == torch.float32
     assert kv_cache.dim() == 2 and kv_cache.stride(1) == 1
     pstride = kv_cache.stride(0) if page_stride is None else int(page_stride)
+    if kv_format == KV_MXFP4:
+        assert q_scale is not None and q_scale.is_contiguous()
+        _check(lib().dsa_mxfp4_paged_mqa_logits(
+            _ptr(qq), _ptr(q_scale), _ptr(kv_cache), pstride, int(kv_cache.shape[0]), _ptr(weights),
+            _ptr(ctx), _ptr(bt), int(bt.stride(0)), _ptr(ind), _ptr(schedule), int(num_sms),
+            _ptr(out), int(logits_dtype), int(logits_stride), T, NUM_HEADS, HEAD_DIM, BLOCK_KV,
+            _ptr(status), _stream(device)), "mxfp4_paged_mqa_logits")
+        return out
     _check(lib().dsa_fp8_fp4_paged_mqa_logits(
         _ptr(qq), _ptr(kv_cache), pstride, int(kv_cache.shape[0]), int(kv_format), _ptr(weights),
         _ptr(ctx), _ptr(bt), int(bt.stride(0)), _ptr(ind), _ptr(schedule), int(num_sms),
@@ -294,7 +308,7 @@ def indexer_decode_scratch(num_rows, logits_dtype, logits_stride, logits_budget,
 def indexer_decode_topk(q, kv_cache, weights, context_lens, block_table, k, indices=None,
                         kv_format=KV_FP8, logits_dtype=LOGITS_F32, logits_stride=None,
                         logits_budget=0, num_sms=None, out=None, status=None, scratch=None,
-                        schedule=None, page_stride=None):
+                        schedule=None, page_stride=None, q_scale=None):
     """The whole decode step (schedule, logits, top-k) in one native call; with
     a logits budget (bytes) the rows run in slices whose logits fit it.
     Returns int32 [T, k] top-k columns, ascending, -1 padded."""
@@ -321,7 +335,7 @@ def indexer_decode_topk(q, kv_cache, weights, context_lens, block_table, k, indi
     assert kv_cache.dim() == 2 and kv_cache.stride(1) == 1
     pstride = kv_cache.stride(0) if page_stride is None else int(page_stride)
     _check(lib().dsa_indexer_decode_topk(
-        _ptr(qq), _ptr(kv_cache), pstride, int(kv_cache.shape[0]), int(kv_format), _ptr(weights),
+        _ptr(qq), _ptr(q_scale), _ptr(kv_cache), pstride, int(kv_cache.shape[0]), int(kv_format), _ptr(weights),
         _ptr(ctx), _ptr(bt), int(bt.stride(0)), _ptr(ind), T, NUM_HEADS, HEAD_DIM, BLOCK_KV,
         int(num_sms), int(logits_dtype), int(logits_stride), int(logits_budget), _ptr(scratch),
         int(scratch.numel() * scratch.element_size()), _ptr(schedule), int(schedule.numel()), int(k),
@@ -345,7 +359,7 @@ def prefill_rows(cu_seqlen_ks, cu_seqlen_ke, local_cu_seq_lens, status=None):
 
 def prefill_mqa_logits(q, kv_cache, weights, context_lens, request_ids, block_table, schedule,
                        kv_format=KV_FP8, logits_dtype=LOGITS_F32, logits_stride=None, num_sms=None,
-                       out=None, status=None, page_stride=None):
+                       out=None, status=None, page_stride=None, q_scale=None):
     """Logits [T, logits_stride] of prefill rows over the paged cache; block_table
     is per request ([B, max_pages]) and row t reads row request_ids[t]."""
     device = q.device
@@ -366,7 +380,7 @@ def prefill_mqa_logits(q, kv_cache, weights, context_lens, request_ids, block_ta
     assert qq.is_contiguous() and weights.is_contiguous() and weights.dtype == torch.float32
     pstride = kv_cache.stride(0) if page_stride is None else int(page_stride)
     _check(lib().dsa_prefill_mqa_logits(
-        _ptr(qq), _ptr(kv_cache), pstride, int(kv_cache.shape[0]), int(kv_format), _ptr(weights), _ptr(ctx),
+        _ptr(qq), _ptr(q_scale), _ptr(kv_cache), pstride, int(kv_cache.shape[0]), int(kv_format), _ptr(weights), _ptr(ctx),
         _ptr(req), _ptr(bt), int(bt.stride(0)), int(bt.shape[0]), _ptr(schedule), int(num_sms), _ptr(out),
         int(logits_dtype), int(logits_stride), T, NUM_HEADS, HEAD_DIM, BLOCK_KV, _ptr(status),
         _stream(device)), "prefill_mqa_logits")
@@ -375,7 +389,7 @@ def prefill_mqa_logits(q, kv_cache, weights, context_lens, request_ids, block_ta
 
 def prefill_topk(q, kv_cache, weights, cu_seqlen_ks, cu_seqlen_ke, local_cu_seq_lens, block_table, k,
                  kv_format=KV_FP8, logits_dtype=LOGITS_F32, logits_stride=None, num_sms=None,
-                 status=None, logits_out=None):
+                 status=None, logits_out=None, q_scale=None):
     """The prefill step over the paged cache: row tags -> (length, request),
     schedule, logits, top-k.  Returns (top-k [T, k] int32 request-local token
     positions, ascending, -1 padded; logits)."""
@@ -385,6 +399,6 @@ def prefill_topk(q, kv_cache, weights, cu_seqlen_ks, cu_seqlen_ke, local_cu_seq_
     sched = paged_mqa_logits_metadata(ctx, req, num_sms)
     logits = prefill_mqa_logits(q, kv_cache, weights, ctx, req, block_table, sched, kv_format=kv_format,
                                 logits_dtype=logits_dtype, logits_stride=logits_stride, num_sms=num_sms,
-                                out=logits_out, status=status)
+                                out=logits_out, status=status, q_scale=q_scale)
     idx = top_k_per_row(logits, None, ctx, k, status=status)
     return idx, logits

@@ -130,7 +130,8 @@ namespace {
 
 // The logits call of decode (row-indexed block table) and of prefill (a
 // block table per request, read through the rows' request ids).
-int logits_call(const void* q, const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages,
+int logits_call(const void* q, const void* q_scale, const void* kv_cache, int64_t page_stride_bytes,
+                int64_t num_pages,
                 int32_t kv_format, const float* weights, const int32_t* context_lens,
                 const int32_t* block_table, int64_t block_table_stride, const int32_t* bt_rows,
                 int32_t bt_num_rows, const int32_t* indices, const int32_t* schedule, int32_t num_sms,
@@ -139,13 +140,18 @@ int logits_call(const void* q, const void* kv_cache, int64_t page_stride_bytes, 
                 dsa_stream_t stream) {
   if (num_heads != kHeads || head_dim != kHeadDim || block_kv != kPageTokens)
     return DSA_ERR_UNSUPPORTED;
-  if (kv_format != DSA_KV_FP8 && kv_format != DSA_KV_FP4) return DSA_ERR_UNSUPPORTED;
+  if (kv_format != DSA_KV_FP8 && kv_format != DSA_KV_FP4 && kv_format != DSA_KV_MXFP4) return DSA_ERR_UNSUPPORTED;
   if (logits_dtype != DSA_LOGITS_F32 && logits_dtype != DSA_LOGITS_BF16) return DSA_ERR_UNSUPPORTED;
   if (num_rows < 0 || num_sms < 1 || num_sms > 1023) return DSA_ERR_INVALID_ARG;
   if (num_rows == 0) return DSA_OK;
   if (!q || !kv_cache || !weights || !context_lens || !block_table || !schedule || !logits)
     return DSA_ERR_INVALID_ARG;
-  const int64_t page_bytes = kv_format == DSA_KV_FP8 ? DSA_FP8_PAGE_BYTES : DSA_FP4_PAGE_BYTES;
+  // MXFP4 q comes with its ue8m0 scales; the other formats take e4m3 q alone
+  if ((kv_format == DSA_KV_MXFP4) != (q_scale != nullptr) || (q_scale && !aligned(q_scale, 16)))
+    return DSA_ERR_INVALID_ARG;
+  const int64_t page_bytes = kv_format == DSA_KV_FP8   ? DSA_FP8_PAGE_BYTES
+                             : kv_format == DSA_KV_FP4 ? DSA_FP4_PAGE_BYTES
+                                                       : DSA_MXFP4_PAGE_BYTES;
   if (page_stride_bytes < page_bytes || page_stride_bytes % 16 != 0) return DSA_ERR_INVALID_ARG;
   if (num_pages < 1 || num_pages > INT32_MAX) return DSA_ERR_INVALID_ARG;
   if (block_table_stride < 1 || logits_stride < 1 || logits_stride % 8 != 0 || logits_stride >= INT32_MAX)
@@ -158,6 +164,7 @@ int logits_call(const void* q, const void* kv_cache, int64_t page_stride_bytes, 
   if (dev != DSA_OK) return dev;
   LogitsArgs a;
   a.q = static_cast<const uint8_t*>(q);
+  a.q_scale = static_cast<const uint8_t*>(q_scale);
   a.kv_cache = static_cast<const uint8_t*>(kv_cache);
   a.page_stride = page_stride_bytes;
   a.num_pages = num_pages;
@@ -177,7 +184,9 @@ int logits_call(const void* q, const void* kv_cache, int64_t page_stride_bytes, 
   a.num_rows = num_rows;
   a.status = status;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t e = kv_format == DSA_KV_FP8 ? launch_logits_fp8(a, st) : launch_logits_fp4(a, st);
+  const cudaError_t e = kv_format == DSA_KV_FP8   ? launch_logits_fp8(a, st)
+                        : kv_format == DSA_KV_FP4 ? launch_logits_fp4(a, st)
+                                                  : launch_logits_mxfp4(a, st);
   if (e == cudaErrorInvalidValue) return DSA_ERR_INVALID_ARG;
   if (e == cudaErrorNotSupported) return DSA_ERR_UNSUPPORTED;
   return launch_status(e);
@@ -195,8 +204,20 @@ int dsa_fp8_fp4_paged_mqa_logits(const void* q, const void* kv_cache, int64_t pa
                                  int32_t logits_dtype, int64_t logits_stride, int32_t num_rows,
                                  int32_t num_heads, int32_t head_dim, int32_t block_kv,
                                  int32_t* status, dsa_stream_t stream) {
-  return logits_call(q, kv_cache, page_stride_bytes, num_pages, kv_format, weights, context_lens, block_table,
-                     block_table_stride, nullptr, 0, indices, schedule, num_sms, logits, logits_dtype,
+  return logits_call(q, nullptr, kv_cache, page_stride_bytes, num_pages, kv_format, weights, context_lens,
+                     block_table, block_table_stride, nullptr, 0, indices, schedule, num_sms, logits, logits_dtype,
+                     logits_stride, num_rows, num_heads, head_dim, block_kv, status, stream);
+}
+
+int dsa_mxfp4_paged_mqa_logits(const void* q, const void* q_scale, const void* kv_cache, int64_t page_stride_bytes,
+                               int64_t num_pages, const float* weights, const int32_t* context_lens,
+                               const int32_t* block_table, int64_t block_table_stride, const int32_t* indices,
+                               const int32_t* schedule, int32_t num_sms, void* logits, int32_t logits_dtype,
+                               int64_t logits_stride, int32_t num_rows, int32_t num_heads, int32_t head_dim,
+                               int32_t block_kv, int32_t* status, dsa_stream_t stream) {
+  if (num_rows > 0 && q_scale == nullptr) return DSA_ERR_INVALID_ARG;
+  return logits_call(q, q_scale, kv_cache, page_stride_bytes, num_pages, DSA_KV_MXFP4, weights, context_lens,
+                     block_table, block_table_stride, nullptr, 0, indices, schedule, num_sms, logits, logits_dtype,
                      logits_stride, num_rows, num_heads, head_dim, block_kv, status, stream);
 }
 
@@ -214,15 +235,15 @@ int dsa_prefill_rows(const int32_t* cu_seqlen_ks, const int32_t* cu_seqlen_ke, i
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int dsa_prefill_mqa_logits(const void* q, const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages,
+int dsa_prefill_mqa_logits(const void* q, const void* q_scale, const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages,
                            int32_t kv_format, const float* weights, const int32_t* context_lens,
                            const int32_t* request_ids, const int32_t* block_table, int64_t block_table_stride,
                            int32_t num_requests, const int32_t* schedule, int32_t num_sms, void* logits,
                            int32_t logits_dtype, int64_t logits_stride, int32_t num_rows, int32_t num_heads,
                            int32_t head_dim, int32_t block_kv, int32_t* status, dsa_stream_t stream) {
   if (num_rows > 0 && (request_ids == nullptr || num_requests < 1)) return DSA_ERR_INVALID_ARG;
-  return logits_call(q, kv_cache, page_stride_bytes, num_pages, kv_format, weights, context_lens, block_table,
-                     block_table_stride, request_ids, num_requests, request_ids, schedule, num_sms, logits,
+  return logits_call(q, q_scale, kv_cache, page_stride_bytes, num_pages, kv_format, weights, context_lens,
+                     block_table, block_table_stride, request_ids, num_requests, request_ids, schedule, num_sms, logits,
                      logits_dtype, logits_stride, num_rows, num_heads, head_dim, block_kv, status, stream);
 }
 

@@ -49,6 +49,7 @@ cudaError_t launch_metadata(const int32_t* context_lens, const int32_t* indices,
 
 struct LogitsArgs {
   const uint8_t* q;
+  const uint8_t* q_scale = nullptr;  // MXFP4: ue8m0 [T][H][D/32]
   const uint8_t* kv_cache;
   int64_t page_stride;
   int64_t num_pages;
@@ -71,6 +72,7 @@ struct LogitsArgs {
 
 cudaError_t launch_logits_fp8(const LogitsArgs& a, cudaStream_t stream);
 cudaError_t launch_logits_fp4(const LogitsArgs& a, cudaStream_t stream);
+cudaError_t launch_logits_mxfp4(const LogitsArgs& a, cudaStream_t stream);
 
 cudaError_t launch_top_k(const void* logits, int32_t logits_dtype, int64_t logits_stride,
                          const int32_t* row_starts, const int32_t* row_ends, int32_t num_rows,

@@ -88,7 +88,7 @@ int dsa_indexer_decode_scratch(int32_t num_rows, int32_t logits_dtype, int64_t l
   return DSA_OK;
 }
 
-int dsa_indexer_decode_topk(const void* q, const void* kv_cache, int64_t page_stride_bytes,
+int dsa_indexer_decode_topk(const void* q, const void* q_scale, const void* kv_cache, int64_t page_stride_bytes,
                             int64_t num_pages, int32_t kv_format, const float* weights,
                             const int32_t* context_lens, const int32_t* block_table,
                             int64_t block_table_stride, const int32_t* indices, int32_t num_rows,
@@ -104,6 +104,7 @@ int dsa_indexer_decode_topk(const void* q, const void* kv_cache, int64_t page_st
   if (num_rows == 0) return DSA_OK;
   if (!q || !weights || !context_lens || !block_table || !logits_scratch || !schedule || !out_idx)
     return DSA_ERR_INVALID_ARG;
+  if ((kv_format == DSA_KV_MXFP4) != (q_scale != nullptr)) return DSA_ERR_INVALID_ARG;
   const int64_t eb = logit_bytes(logits_dtype);
   SlicePlan p;
   int st = plan_slices(num_rows, logits_stride * eb / 2, logits_budget, &p);
@@ -121,11 +122,20 @@ int dsa_indexer_decode_topk(const void* q, const void* kv_cache, int64_t page_st
     const int32_t* ind = indices ? indices + s : nullptr;
     st = dsa_paged_mqa_logits_metadata(ctx, ind, rows, block_kv, num_sms, schedule, stream);
     if (st != DSA_OK) return st;
-    st = dsa_fp8_fp4_paged_mqa_logits(qb + s * int64_t{kHeads} * kHeadDim, kv_cache, page_stride_bytes, num_pages,
-                                      kv_format, weights + s * kHeads, ctx,
+    if (kv_format == DSA_KV_MXFP4) {  // q: packed e2m1 with ue8m0 scales
+      st = dsa_mxfp4_paged_mqa_logits(qb + s * int64_t{kHeads} * (kHeadDim / 2),
+                                      static_cast<const uint8_t*>(q_scale) + s * int64_t{kHeads} * (kHeadDim / 32),
+                                      kv_cache, page_stride_bytes, num_pages, weights + s * kHeads, ctx,
                                       block_table + s * block_table_stride, block_table_stride, ind, schedule,
                                       num_sms, logits_scratch, logits_dtype, logits_stride, rows, num_heads,
                                       head_dim, block_kv, status, stream);
+    } else {
+      st = dsa_fp8_fp4_paged_mqa_logits(qb + s * int64_t{kHeads} * kHeadDim, kv_cache, page_stride_bytes, num_pages,
+                                        kv_format, weights + s * kHeads, ctx,
+                                        block_table + s * block_table_stride, block_table_stride, ind, schedule,
+                                        num_sms, logits_scratch, logits_dtype, logits_stride, rows, num_heads,
+                                        head_dim, block_kv, status, stream);
+    }
     if (st != DSA_OK) return st;
     st = dsa_top_k_per_row(logits_scratch, logits_dtype, logits_stride, nullptr, ctx, rows, k,
                            out_idx + s * out_stride, out_stride, status, stream);

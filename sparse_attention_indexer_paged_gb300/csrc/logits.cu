@@ -58,8 +58,8 @@ namespace {
 // (3, 2, 20-23) share the dequantisation; 24 warps leave 80 registers, so
 // the pair is read in two 32-column pieces.
 template <int kFmt> constexpr int kEpiWgOf = 4;
-template <int kFmt> constexpr int kThreadsOf = kFmt == DSA_KV_FP4 ? 768 : 640;
-template <int kFmt> constexpr int kPieceCols = kFmt == DSA_KV_FP4 ? 32 : 64;
+template <int kFmt> constexpr int kThreadsOf = kFmt == DSA_KV_FP8 ? 640 : 768;
+template <int kFmt> constexpr int kPieceCols = kFmt == DSA_KV_FP8 ? 64 : 32;
 constexpr int kFp4Converters = 6;
 constexpr int kSlots = 8;  // 64-column TMEM slots; pair p of the CTA's stream uses slot p mod 8
 constexpr int kScaleStages = 16;   // key scale ring
@@ -69,6 +69,10 @@ constexpr int kWBufFloats = kGroupMaxRows * kHeads;       // 512
 constexpr int kPageValBytesFp8 = kPageTokens * kHeadDim;  // 8192
 constexpr int kFp4PageBytes = DSA_FP4_PAGE_BYTES;         // 4864: values, block scales, token scales
 constexpr int kFp4GScaleOffset = kPageTokens * (kHeadDim / 2 + kHeadDim / 16);  // 4608
+constexpr int kMxPageBytes = DSA_MXFP4_PAGE_BYTES;         // 4352: values, ue8m0 block scales
+constexpr int kMxScaleOffset = kPageTokens * (kHeadDim / 2);  // 4096
+// whole pages copied raw and dequantised by the converter warps
+template <int kFmt> constexpr int kDqPageBytes = kFmt == DSA_KV_MXFP4 ? kMxPageBytes : kFp4PageBytes;
 constexpr int kScaleStageFloats = kTileTokens;            // 128 key scales per tile
 constexpr int kMaxKStages = 8;
 constexpr int kMaxRawStages = 8;
@@ -90,22 +94,25 @@ template <> struct Lay<DSA_KV_FP8> {
   static constexpr int kOffQ = kOffKv + kKStages * kKStageBytes;
   static constexpr int kOffRaw = kOffQ + kGroupMaxRows * kQRowBytes;
 };
-template <> struct Lay<DSA_KV_FP4> {
+template <int kPageBytes> struct LayDq {
   static constexpr int kKStages = 2;
   static constexpr int kKStageBytes = 2 * kTileTokens * 128;  // 32768
   static constexpr int kRawStages = 8;
-  static constexpr int kRawStageBytes = 2 * kFp4PageBytes;    // 9728
+  static constexpr int kRawStageBytes = 2 * kPageBytes;       // 9728 (FP4), 8704 (MXFP4)
   static constexpr int kQHalfBytes = kFp4PassRows * kHeads * 128;  // 32768
   static constexpr int kOffQ = 0;
   static constexpr int kOffKv = kOffQ + 2 * kQHalfBytes;
   static constexpr int kOffRaw = kOffKv + kKStages * kKStageBytes;
 };
+template <> struct Lay<DSA_KV_FP4> : LayDq<kFp4PageBytes> {};
+template <> struct Lay<DSA_KV_MXFP4> : LayDq<kMxPageBytes> {};
 template <int kFmt> struct Smem : Lay<kFmt> {
   using B = Lay<kFmt>;
   static constexpr int kOffScale = B::kOffRaw + B::kRawStages * B::kRawStageBytes;
   static constexpr int kOffW = kOffScale + kScaleStages * kScaleStageFloats * 4;
   static constexpr int kOffCtx = kOffW + 2 * kWBufFloats * 4;  // causal limits of the group's rows
-  static constexpr int kOffBar = kOffCtx + 2 * kGroupMaxRows * 4;
+  static constexpr int kOffRowF = kOffCtx + 2 * kGroupMaxRows * 4;  // MXFP4: q scale factor of each row
+  static constexpr int kOffBar = kOffRowF + 2 * kGroupMaxRows * 4;
   // barriers: kv_full[8], kv_empty[8], raw_full[2], raw_empty[2], sc_full[SS],
   // sc_empty[SS], q_full, q_empty, w_full[2], w_empty[2], tm_full[2][4], tm_empty[2][4], mma_done
   static constexpr int kNumBars = 2 * kMaxKStages + 2 * kMaxRawStages + 2 * kScaleStages + 2 + 4 + 16 + 1;
@@ -120,11 +127,13 @@ template <int kFmt> struct Smem : Lay<kFmt> {
   static_assert(kBytes <= 232448, "over the per-CTA shared memory limit");
 };
 static_assert(kSlots * kPairCols == kTmemCols, "TMEM slots");
-static_assert(kFp4AHalfLo == (kTileTokens * 128) >> 4 && kFp4BHalfLo == Lay<DSA_KV_FP4>::kQHalfBytes >> 4,
+static_assert(kFp4AHalfLo == (kTileTokens * 128) >> 4 && kFp4BHalfLo == Lay<DSA_KV_FP4>::kQHalfBytes >> 4 &&
+                  kFp4BHalfLo == Lay<DSA_KV_MXFP4>::kQHalfBytes >> 4,
               "f16 operand halves as laid out by the dequantising warp");
 
 struct Params {
   const uint8_t* q;
+  const uint8_t* q_scale;  // MXFP4: ue8m0 [T][H][D/32]
   const uint8_t* kv_cache;
   int64_t page_stride;
   int64_t num_pages;
@@ -263,7 +272,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                   const Params p) {
   using L = Smem<kFmt>;
-  constexpr bool kFp4 = kFmt == DSA_KV_FP4;
+  constexpr bool kDq = kFmt != DSA_KV_FP8;   // dequantising pipeline: FP4 and MXFP4 keys
+  constexpr bool kMx = kFmt == DSA_KV_MXFP4;
   constexpr int kEpiWg = kEpiWgOf<kFmt>;
   constexpr int kEpiWarps = 4 * kEpiWg;
   constexpr int kStages = L::kKStages;
@@ -312,7 +322,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bars.kvf(s), kFp4 ? kFp4Converters : 1);  // TMA (FP8) or the three dequantising warps (FP4)
+      mbar_init(bars.kvf(s), kDq ? kFp4Converters : 1);  // TMA (FP8) or the three dequantising warps (FP4)
       mbar_init(bars.kve(s), 1);  // the MMA commit of the tile
     }
     for (int s = 0; s < L::kRawStages; ++s) {
@@ -320,10 +330,10 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       mbar_init(bars.rwe(s), kFp4Converters);  // the dequantising warps
     }
     for (int s = 0; s < kScaleStages; ++s) {
-      mbar_init(bars.scf(s), kFp4 ? kFp4Converters : 1);  // bulk copy (FP8) or the three dequantising warps (FP4)
+      mbar_init(bars.scf(s), kDq ? kFp4Converters : 1);  // bulk copy (FP8) or the three dequantising warps (FP4)
       mbar_init(bars.sce(s), kEpiWarps);  // every epilogue warp has read the tile's scales
     }
-    mbar_init(bars.q_full, kFp4 ? kFp4Converters : 1);  // the MMA warp's TMA (FP8) or the three converting warps (FP4)
+    mbar_init(bars.q_full, kDq ? kFp4Converters : 1);  // the MMA warp's TMA (FP8) or the three converting warps (FP4)
     mbar_init(bars.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.wf(b), 1);
@@ -354,7 +364,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   const float* w_sm = reinterpret_cast<const float*>(smem + L::kOffW);
   int32_t* ctx_sm = reinterpret_cast<int32_t*>(smem + L::kOffCtx);
 
-  Walk<kFp4 ? kFp4PassRows : kGroupMaxRows> walk;
+  Walk<kDq ? kFp4PassRows : kGroupMaxRows> walk;
   walk.start(grs, gus, p.ctx, G, T, u0, u1, lane);
 
   // =================================================== FP4 dequantisation (warps 3, 2, 20-23)
@@ -366,9 +376,18 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   // conversion of every pass's q rows (e4m3 -> f16, exact) into the swizzled
   // B-operand layout.  Warp 2 first loads the pass's head weights and causal
   // limits (double buffered).
+  //
+  // MXFP4 keys and q (ue8m0 scale e_b per 32 elements): a token's pieces are
+  // scaled by 2^(e_b - e_max) in f16, e_max the token's largest block
+  // exponent, and 2^(e_max - 127) goes to the token-scale ring; q rows the
+  // same way with the row's largest exponent, whose factor the epilogue
+  // applies.  Every product stays exact unless a block lies more than 2^14
+  // below its token's (or row's) largest, where f16 keeps fewer bits of it.
   auto fp4_worker = [&]() {
-    using LF = Lay<DSA_KV_FP4>;
+    using LF = Lay<kFmt == DSA_KV_FP8 ? DSA_KV_FP4 : kFmt>;  // (compiled, never run, for FP8)
+    constexpr int kPg = kDqPageBytes<kFmt>;
     constexpr int kStride = 32 * kFp4Converters;
+    float* rowf_sm = reinterpret_cast<float*>(smem + L::kOffRowF);
     const int part = warp == 3 ? 0 : (warp == 2 ? 1 : warp - (4 + kEpiWarps) + 2);
     const uint64_t pol_keep = policy_evict_last();
     const uint32_t q_half = static_cast<uint32_t>(LF::kQHalfBytes);
@@ -376,11 +395,24 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     bool ok = true;
     while (ok && walk.next(lane)) {
       const int r0 = walk.r0, n = walk.n;
+      // MXFP4: largest q scale exponent of each row of the pass (lane r holds row r's)
+      uint32_t row_emax = 0;
+      if constexpr (kMx) {
+        for (int r = 0; r < n; ++r) {
+          const uint2 e8 = __ldg(reinterpret_cast<const uint2*>(p.q_scale + static_cast<int64_t>(r0 + r) * kHeads *
+                                                                              (kHeadDim / 32)) + lane);
+          uint32_t m = max_byte4(__vmaxu4(e8.x, e8.y));
+#pragma unroll
+          for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (lane == r) row_emax = m;
+        }
+      }
       if (part == 1) {
         const int wb = nw & 1;
         ok = warp_wait(bars.we(wb), ((nw >> 1) & 1) ^ 1, abort_flag, p.status);
         if (!ok) break;
         if (lane < n) ctx_sm[wb * kGroupMaxRows + lane] = walk.lane_ctx;
+        if (kMx && lane < n) rowf_sm[wb * kGroupMaxRows + lane] = ue8m0_to_f32(row_emax);
         __threadfence_block();
         __syncwarp();
         if (lane == 0) {
@@ -393,7 +425,35 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       // q rows of the pass, once the previous pass's MMAs have completed
       ok = warp_wait(bars.q_empty, (nq & 1) ^ 1, abort_flag, p.status);
       if (!ok) break;
-      {
+      if constexpr (kMx) {
+        // 8 e2m1 codes (4 bytes) per step with their block's relative scale
+        const uint32_t* qsrc = reinterpret_cast<const uint32_t*>(p.q + static_cast<int64_t>(r0) * kHeads * (kHeadDim / 2));
+        const uint8_t* qsc = p.q_scale + static_cast<int64_t>(r0) * kHeads * (kHeadDim / 32);
+        const int nchunks = n * kHeads * (kHeadDim / 8);
+        // every lane gets all rows' exponents before the loop, whose trip
+        // count differs between lanes
+        int em[kFp4PassRows];
+#pragma unroll
+        for (int r = 0; r < kFp4PassRows; ++r) em[r] = static_cast<int>(__shfl_sync(0xffffffffu, row_emax, r));
+        for (int i = part * 32 + lane; i < nchunks; i += kStride) {
+          const uint32_t c = __ldg(qsrc + i);
+          const int R = i >> 4;      // q row (row * 64 + head) within the pass
+          const int c16 = i & 15;    // 8-element chunk along d
+          const int rr = R >> 6;
+          const int emax = rr == 0 ? em[0] : (rr == 1 ? em[1] : (rr == 2 ? em[2] : em[3]));
+          const uint32_t f = pow2_f16x2(static_cast<int>(__ldg(qsc + R * (kHeadDim / 32) + (c16 >> 2))) - emax);
+          uint32_t h[4];
+          e2m1x8_to_f16x2(c, h);
+          uint4 o;
+          o.x = hmul2_u32(h[0], f);
+          o.y = hmul2_u32(h[1], f);
+          o.z = hmul2_u32(h[2], f);
+          o.w = hmul2_u32(h[3], f);
+          const uint32_t off = static_cast<uint32_t>(c16 >> 3) * q_half + static_cast<uint32_t>(R >> 3) * 1024u +
+                               static_cast<uint32_t>(R & 7) * 128u + (static_cast<uint32_t>((c16 & 7) ^ (R & 7)) << 4);
+          *reinterpret_cast<uint4*>(smem + LF::kOffQ + off) = o;
+        }
+      } else {
         // 8 e4m3 codes per step; the warps take interleaved 32-chunk blocks
         const uint2* qsrc = reinterpret_cast<const uint2*>(p.q + static_cast<int64_t>(r0) * kHeads * kHeadDim);
         const int nchunks = n * kHeads * (kHeadDim / 8);
@@ -424,19 +484,33 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
              warp_wait(bars.sce(ss), ((it / kScaleStages) & 1) ^ 1, abort_flag, p.status);
         if (!ok) break;
         const uint8_t* raw = smem + LF::kOffRaw + rs * LF::kRawStageBytes;
-        for (int t = part * 32 + lane; t < kTileTokens; t += kStride)  // token scales -> scale ring
-          scale_sm[ss * kScaleStageFloats + t] =
-              *reinterpret_cast<const float*>(raw + (t >> 6) * kFp4PageBytes + kFp4GScaleOffset + (t & 63) * 4);
+        for (int t = part * 32 + lane; t < kTileTokens; t += kStride) {  // token scales -> scale ring
+          if constexpr (kMx)
+            scale_sm[ss * kScaleStageFloats + t] = ue8m0_to_f32(
+                max_byte4(*reinterpret_cast<const uint32_t*>(raw + (t >> 6) * kPg + kMxScaleOffset + (t & 63) * 4)));
+          else
+            scale_sm[ss * kScaleStageFloats + t] =
+                *reinterpret_cast<const float*>(raw + (t >> 6) * kPg + kFp4GScaleOffset + (t & 63) * 4);
+        }
         uint8_t* tile = smem + LF::kOffKv + st * LF::kKStageBytes;
 #pragma unroll 1
         for (int k = part * 32 + lane; k < kTileTokens * 4; k += kStride) {
           const int tk = k >> 2, q4 = k & 3;  // token within the tile, 32-element piece
-          const uint8_t* tokp = raw + (tk >> 6) * kFp4PageBytes;
+          const uint8_t* tokp = raw + (tk >> 6) * kPg;
           const int slot = tk & 63;
           const uint4 pv = *reinterpret_cast<const uint4*>(tokp + slot * (kHeadDim / 2) + q4 * 16);
-          // block scales of the piece's two 16-element blocks
-          const uint32_t s2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(tokp + kPageTokens * (kHeadDim / 2) + slot * 8 + q4 * 2));
-          const uint32_t sb[2] = {__byte_perm(s2, 0, 0x1010), __byte_perm(s2, 0, 0x3232)};
+          uint32_t sb[2];
+          if constexpr (kMx) {
+            // the piece is one 32-element block: 2^(e_b - e_max of the token)
+            const uint32_t e4 = *reinterpret_cast<const uint32_t*>(tokp + kMxScaleOffset + slot * 4);
+            sb[0] = sb[1] = pow2_f16x2(static_cast<int>((e4 >> (8 * q4)) & 0xffu) - static_cast<int>(max_byte4(e4)));
+          } else {
+            // block scales of the piece's two 16-element blocks
+            const uint32_t s2 = e4m3x2_to_f16x2(
+                *reinterpret_cast<const uint16_t*>(tokp + kPageTokens * (kHeadDim / 2) + slot * 8 + q4 * 2));
+            sb[0] = __byte_perm(s2, 0, 0x1010);
+            sb[1] = __byte_perm(s2, 0, 0x3232);
+          }
           const uint32_t words[4] = {pv.x, pv.y, pv.z, pv.w};
           const uint32_t row = static_cast<uint32_t>(tk >> 3) * 1024u + static_cast<uint32_t>(tk & 7) * 128u;
 #pragma unroll
@@ -473,11 +547,11 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     // one coalesced load and handed out by shuffle; lane 0 waits and issues.
     // Nothing here waits on a group boundary, so the ring runs ahead across
     // groups.
-    if constexpr (!kFp4) {
+    if constexpr (!kDq) {
       if (lane == 0) prefetch_tensormap(&tm_kv);
     }
     const uint64_t pol_stream = policy_evict_first();  // K pages are read once
-    constexpr int kRing = kFp4 ? L::kRawStages : kStages;
+    constexpr int kRing = kDq ? L::kRawStages : kStages;
     int it = 0;  // tiles issued
     bool ok = true;
     while (ok && walk.next(lane)) {
@@ -503,21 +577,22 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         const int32_t blk1 = __shfl_sync(0xffffffffu, lane_blk, 2 * j + 1 - pg_base);
         if (lane == 0) {
           const int st = it % kRing;
-          const uint32_t empty_bar = kFp4 ? bars.rwe(st) : bars.kve(st);
-          const uint32_t full_bar = kFp4 ? bars.rwf(st) : bars.kvf(st);
+          const uint32_t empty_bar = kDq ? bars.rwe(st) : bars.kve(st);
+          const uint32_t full_bar = kDq ? bars.rwf(st) : bars.kvf(st);
           ok = wait_or_abort(empty_bar, ((it / kRing) & 1) ^ 1, abort_flag, p.status);
           if (ok) {
             const int npg = (blk0 >= 0 ? 1 : 0) + (blk1 >= 0 ? 1 : 0);
-            if constexpr (kFp4) {
-              // whole pages: packed values, block scales and token scales
-              mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(npg * kFp4PageBytes));
+            if constexpr (kDq) {
+              // whole pages: packed values and their scales
+              constexpr int kPg = kDqPageBytes<kFmt>;
+              mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(npg * kPg));
               const uint32_t dst = sbase + L::kOffRaw + st * L::kRawStageBytes;
               if (blk0 >= 0)
-                bulk_load(dst, p.kv_cache + static_cast<int64_t>(blk0) * p.page_stride, kFp4PageBytes,
-                          full_bar, pol_stream);
+                bulk_load(dst, p.kv_cache + static_cast<int64_t>(blk0) * p.page_stride, kPg, full_bar,
+                          pol_stream);
               if (blk1 >= 0)
-                bulk_load(dst + kFp4PageBytes, p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride,
-                          kFp4PageBytes, full_bar, pol_stream);
+                bulk_load(dst + kPg, p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride, kPg, full_bar,
+                          pol_stream);
             } else {
               mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(npg * kPageValBytesFp8));
               if (blk0 >= 0)
@@ -536,10 +611,10 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     // phase that already completed returns at once).
     if (lane == 0) {
       for (int i = max(0, it - kRing); i < it; ++i)
-        wait_drain(kFp4 ? bars.rwf(i % kRing) : bars.kvf(i % kRing), (i / kRing) & 1);
+        wait_drain(kDq ? bars.rwf(i % kRing) : bars.kvf(i % kRing), (i / kRing) & 1);
     }
   } else if (warp == 2 || warp == 3 || warp >= 4 + kEpiWarps) {
-    if constexpr (!kFp4) {
+    if constexpr (!kDq) {
       if (warp == 3) {
         // =================================================== key scales (FP8)
         // Runs ahead of the K pipeline by up to kScaleStages tiles, gated only
@@ -628,10 +703,10 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     const uint32_t id_base = idesc(0, 0, 128, 0);
     const uint32_t a_lo0 = sdesc_lo(s_kv), q_lo0 = sdesc_lo(s_q);
     constexpr uint32_t kStageLo = L::kKStageBytes >> 4;
-    constexpr uint32_t kQRowLo = (kFp4 ? kHeads * 128 : kHeads * kHeadDim) >> 4;  // one q row (64 heads) of B
+    constexpr uint32_t kQRowLo = (kDq ? kHeads * 128 : kHeads * kHeadDim) >> 4;  // one q row (64 heads) of B
     const uint32_t issue = elect_one() ? 1u : 0u;
     const bool leader = issue != 0;
-    if constexpr (!kFp4) {
+    if constexpr (!kDq) {
       if (leader) prefetch_tensormap(&tm_q);
     }
     const uint64_t pol_keep = policy_evict_last();  // q
@@ -639,7 +714,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     bool ok = true;
     while (ok && walk.next(lane)) {
       const uint32_t n = static_cast<uint32_t>(walk.n);
-      if constexpr (!kFp4) {
+      if constexpr (!kDq) {
         // Q buffer free once the previous group's MMAs have completed
         ok = warp_wait(bars.q_empty, (gi & 1) ^ 1, abort_flag, p.status);
         if (!ok) break;
@@ -671,7 +746,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem + c * kPairCols;
-          if constexpr (!kFp4) mma_fp8_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20));
+          if constexpr (!kDq) mma_fp8_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20));
           else mma_f16_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20));
           left -= len;
           pos += len;
@@ -720,6 +795,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       const int lim = static_cast<int>(min(static_cast<int64_t>(walk.npages) * kPageTokens, p.logits_stride));
       const float* w_grp = w_sm + wb * kWBufFloats;
       const int32_t* ctx_grp = ctx_sm + wb * kGroupMaxRows;
+      const float* rowf_grp = reinterpret_cast<const float*>(smem + L::kOffRowF) + wb * kGroupMaxRows;
       OutT* const out_grp = out + static_cast<int64_t>(walk.r0) * p.logits_stride;
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
         const uint32_t ss = it & (kScaleStages - 1);
@@ -759,7 +835,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
               ca = __ffma2_rn(make_float2(fabsf(x23.x), fabsf(x23.y)), make_float2(w4.z, w4.w), ca);
             }
           }
-          const float acc = 0.5f * ((cx.x + cx.y) + (ca.x + ca.y));
+          float acc = 0.5f * ((cx.x + cx.y) + (ca.x + ca.y));
+          if constexpr (kMx) acc *= rowf_grp[r];  // the row's q scale factor, a power of two
           const float logit = (scol < ctx_grp[r]) ? kscale * acc : -INFINITY;
           if (in_span) store_logit(out_grp + static_cast<int64_t>(r) * p.logits_stride + scol, logit);
         }
@@ -788,6 +865,7 @@ namespace {
 Params make_params(const LogitsArgs& a) {
   Params p;
   p.q = a.q;
+  p.q_scale = a.q_scale;
   p.kv_cache = a.kv_cache;
   p.page_stride = a.page_stride;
   p.num_pages = a.num_pages;
@@ -850,6 +928,13 @@ cudaError_t launch_logits_fp4(const LogitsArgs& a, cudaStream_t stream) {
   alignas(64) CUtensorMap unused{};
   const Params p = make_params(a);
   return launch<DSA_KV_FP4>(a, unused, unused, p, stream);
+}
+
+cudaError_t launch_logits_mxfp4(const LogitsArgs& a, cudaStream_t stream) {
+  // as FP4: plain bulk copies of whole pages, q converted by the kernel
+  alignas(64) CUtensorMap unused{};
+  const Params p = make_params(a);
+  return launch<DSA_KV_MXFP4>(a, unused, unused, p, stream);
 }
 
 }  // namespace dsa

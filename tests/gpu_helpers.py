@@ -34,7 +34,7 @@ def run_path(wl, num_sms=None, use_indices=True, logits_out=None):
     logits = dsa.fp8_fp4_paged_mqa_logits(
         g.q, g.kv_cache, g.weights, g.context_lens, g.block_table, sched, indices=ind,
         kv_format=g.kv_format, logits_dtype=g.logits_dtype, logits_stride=g.logits_stride,
-        num_sms=num_sms, status=status, out=logits_out)
+        num_sms=num_sms, status=status, out=logits_out, q_scale=g.q_scale)
     idx = dsa.top_k_per_row(logits, None, g.context_lens, g.topk, status=status)
     torch.cuda.synchronize()
     return dict(sched=sched, logits=logits, idx=idx, status=status, num_sms=num_sms, dev_wl=g)

@@ -64,7 +64,7 @@ def test_decode_step_host_checks(lib):
     P = ctypes.c_void_p
 
     def call(**kw):
-        a = dict(q=P(16), kv=P(16), pst=8448, npages=4, fmt=0, w=P(16), ctx=P(16), bt=P(16), bts=4,
+        a = dict(q=P(16), qs=None, kv=P(16), pst=8448, npages=4, fmt=0, w=P(16), ctx=P(16), bt=P(16), bts=4,
                  ind=None, T=64, H=64, D=128, bkv=64, nsms=8, odt=1, ost=256, budget=16 * 256 * 2,
                  scr=P(16), scrb=16 * 256 * 2, sched=P(16), schw=10**6, k=16, out=P(16), outs=16,
                  status=None, stream=None)
@@ -92,7 +92,7 @@ MANY_ROWS = dict(request_lens=[300, 517, 70, 1000, 129, 2100, 64, 700, 1500, 65]
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("kv_format,ldt", [(W.KV_FP8, W.LOGITS_F32), (W.KV_FP8, W.LOGITS_BF16),
-                                           (W.KV_FP4, W.LOGITS_BF16)])
+                                           (W.KV_FP4, W.LOGITS_BF16), (W.KV_MXFP4, W.LOGITS_BF16)])
 @pytest.mark.parametrize("slice_rows", [16, 32, 48, 0])
 def test_chunked_step_equals_one_pass(kv_format, ldt, slice_rows):
     from gpu_helpers import run_path
@@ -105,7 +105,8 @@ def test_chunked_step_equals_one_pass(kv_format, ldt, slice_rows):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = dsa.indexer_decode_topk(g.q, g.kv_cache, g.weights, g.context_lens, g.block_table, g.topk,
                                   indices=g.indices, kv_format=kv_format, logits_dtype=ldt,
-                                  logits_stride=g.logits_stride, logits_budget=budget, status=status)
+                                  logits_stride=g.logits_stride, logits_budget=budget, status=status,
+                                  q_scale=g.q_scale)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert torch.equal(out, ref["idx"])

@@ -267,3 +267,46 @@ def test_fp4_full_size_sampled():
     ref, bound, _ = check_logits(host, out["logits"], rows=rows)
     check_topk_exact(out["logits"], out["idx"], host.context_lens, wl.topk)
     check_topk_tie_band(out["idx"], ref, bound, host.context_lens, wl.topk, rows)
+
+
+# ---------------------------------------------------------------- MXFP4 keys and q
+
+@pytest.mark.parametrize("logits_dtype", [W.LOGITS_F32, W.LOGITS_BF16])
+def test_mxfp4_mixed_ragged(logits_dtype):
+    _full_check(W.build("mxfp4", **MIXED, topk=64, kv_format=W.KV_MXFP4, logits_dtype=logits_dtype,
+                        seed=41))
+
+
+@pytest.mark.parametrize("S", [1, 7])
+def test_mxfp4_any_sm_split(S):
+    _full_check(W.build("mxfp4", [700, 1300], [3, 5], topk=128, kv_format=W.KV_MXFP4, seed=42), num_sms=S)
+
+
+def test_mxfp4_padded_page_stride():
+    _full_check(W.build("mxfp4", [500, 90], [2, 1], topk=32, kv_format=W.KV_MXFP4,
+                        page_stride=4352 + 16 * 5, seed=43))
+
+
+def test_mxfp4_block_scales_far_below_the_largest():
+    """Blocks 2^12 below their token's or row's largest scale (still exact in
+    the f16 operands) and 2^20 below (fewer bits kept; within tolerance)."""
+    wl = W.build("mxfp4", [300, 517], [2, 3], topk=64, kv_format=W.KV_MXFP4, seed=44)
+    es = W._page_views(wl.kv_cache, W.KV_MXFP4)["bscale"]          # [pages, 64, 4] ue8m0
+    ok = es != W.UE8M0_NAN
+    es[..., 1] = torch.where(ok[..., 1], (es[..., 1].int() - 12).clamp(min=0).to(torch.uint8), es[..., 1])
+    es[::2, :, 3] = torch.where(ok[::2, :, 3], (es[::2, :, 3].int() - 20).clamp(min=0).to(torch.uint8),
+                                es[::2, :, 3])
+    wl.q_scale[:, ::3, 2] = (wl.q_scale[:, ::3, 2].int() - 12).clamp(min=0).to(torch.uint8)
+    wl.q_scale[:, 1::5, 0] = (wl.q_scale[:, 1::5, 0].int() - 20).clamp(min=0).to(torch.uint8)
+    _full_check(wl)
+
+
+def test_mxfp4_full_size_sampled():
+    wl = W.config("mxfp4_varlen", device="cuda")
+    out = run_path(wl)
+    assert int(out["status"].item()) == 0, dsa.status_string(int(out["status"].item()))
+    host = wl.to("cpu")
+    rows = sample_rows(wl.num_rows, 4, seed=6)
+    ref, bound, _ = check_logits(host, out["logits"], rows=rows)
+    check_topk_exact(out["logits"], out["idx"], host.context_lens, wl.topk)
+    check_topk_tie_band(out["idx"], ref, bound, host.context_lens, wl.topk, rows)

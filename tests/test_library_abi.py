@@ -43,6 +43,7 @@ def test_constants_match_header():
     src = open(HEADER).read()
     for macro, val in (("DSA_FP8_PAGE_BYTES", dsa.FP8_PAGE_BYTES),
                        ("DSA_FP4_PAGE_BYTES", dsa.FP4_PAGE_BYTES),
+                       ("DSA_MXFP4_PAGE_BYTES", dsa.MXFP4_PAGE_BYTES),
                        ("DSA_MAX_TOPK", dsa.MAX_TOPK), ("DSA_BLOCK_KV", dsa.BLOCK_KV)):
         assert re.search(rf"#define {macro} {val}\b", src), macro
 

@@ -30,17 +30,20 @@ def test_host_checks_prefill(lib):
     assert f(P(16), None, 4, P(16), 2, P(16), P(16), None, None) == E
     assert f(None, None, 0, None, 2, None, None, None, None) == OK
     g = lib.dsa_prefill_mqa_logits
-    a = [P(16), P(16), 8448, 4, 0, P(16), P(16), P(16), P(16), 4, 2, P(16), 8, P(16), 0, 64, 4, 64, 128, 64,
-         None, None]
+    a = [P(16), None, P(16), 8448, 4, 0, P(16), P(16), P(16), P(16), 4, 2, P(16), 8, P(16), 0, 64, 4, 64, 128,
+         64, None, None]
     bad = list(a)
-    bad[7] = None                                   # request ids
+    bad[8] = None                                   # request ids
     assert g(*bad) == E
     bad = list(a)
-    bad[10] = 0                                     # no requests
+    bad[11] = 0                                     # no requests
     assert g(*bad) == E
     bad = list(a)
-    bad[17] = 32                                    # heads
+    bad[18] = 32                                    # heads
     assert g(*bad) == dsa.DSA_ERR_UNSUPPORTED
+    bad = list(a)
+    bad[1] = P(16)                                  # q scales with FP8 keys
+    assert g(*bad) == E
 
 
 def _view(pf, ctx):
@@ -51,7 +54,8 @@ def _run(pf, status):
     g = pf.to("cuda")
     idx, logits = dsa.prefill_topk(g.q, g.kv_cache, g.weights, g.cu_seqlen_ks, g.cu_seqlen_ke,
                                    g.local_cu_seq_lens, g.block_table, g.topk, kv_format=g.kv_format,
-                                   logits_dtype=g.logits_dtype, logits_stride=g.logits_stride, status=status)
+                                   logits_dtype=g.logits_dtype, logits_stride=g.logits_stride, status=status,
+                                   q_scale=g.q_scale)
     torch.cuda.synchronize()
     return idx, logits
 
@@ -77,7 +81,7 @@ def test_prefill_rows_kernel_equals_oracle():
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("kv_format,ldt", [(W.KV_FP8, W.LOGITS_F32), (W.KV_FP8, W.LOGITS_BF16),
-                                           (W.KV_FP4, W.LOGITS_BF16)])
+                                           (W.KV_FP4, W.LOGITS_BF16), (W.KV_MXFP4, W.LOGITS_BF16)])
 def test_prefill_logits_and_topk_vs_oracle(kv_format, ldt):
     from gpu_helpers import check_logits, check_topk_exact, check_topk_tie_band
     wl = W.build("pf", **MIX, kv_format=kv_format, logits_dtype=ldt, topk=64, seed=31)

@@ -372,6 +372,7 @@ def config_spec(name: str) -> dict:
     mtp         B=128, two rows each (indices=i//2), L ~ U{8192..65536}, k=2048, seed 2
     varlen      B=40, L = 120000 + U{-2048..2048}, rows ~ U{1..6}, k=2048, seed 3
     fp4_varlen  as varlen with FP4 keys and BF16 logits, seed 4
+    mxfp4_varlen  as varlen with MXFP4 keys and q and BF16 logits, seed 6
     prefill     B=2, L=8192, the last 4096 tokens of each prompt as rows (T=8192),
                 k=2048, seed 5 (use prefill_view for the prefill-tagged form)
     """
@@ -386,14 +387,16 @@ def config_spec(name: str) -> dict:
         g.manual_seed(2)
         return dict(request_lens=_uniform_ints(g, 8192, 65536, 128),
                     rows_per_request=[2] * 128, topk=2048, seed=2)
-    if name in ("varlen", "fp4_varlen"):
-        seed = 3 if name == "varlen" else 4
+    if name in ("varlen", "fp4_varlen", "mxfp4_varlen"):
+        seed = {"varlen": 3, "fp4_varlen": 4, "mxfp4_varlen": 6}[name]
         g.manual_seed(seed)
         lens = [120000 + d for d in _uniform_ints(g, -2048, 2048, 40)]
         rows = _uniform_ints(g, 1, 6, 40)
         kw = dict(request_lens=lens, rows_per_request=rows, topk=2048, seed=seed)
         if name == "fp4_varlen":
             kw.update(kv_format=KV_FP4, logits_dtype=LOGITS_BF16)
+        if name == "mxfp4_varlen":
+            kw.update(kv_format=KV_MXFP4, logits_dtype=LOGITS_BF16)
         return kw
     if name == "prefill":
         # a prefill chunk: the second halves of two 8192-token prompts
