@@ -526,12 +526,195 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Short rows (every row fits in kCols columns: the row stride is at most
+// kCols).  The row's keys stay in shared memory.  An exact radix select over
+// digits of up to 11 bits, starting at the highest bit where the row's keys
+// differ and stopping once the chosen bin is taken whole, finds the k-th
+// largest key tau; one ordered ballot pass over the row then writes the
+// columns above tau and the lowest columns equal to tau, ascending.  512
+// threads and kCols * 4 + 8 KB of shared memory let several rows share an
+// SM, where the long-row kernel keeps one.
+constexpr int kShortThreads = 512;
+constexpr int kShortWarps = kShortThreads / 32;
+template <int kCols> constexpr int kShortSmem = kCols * 4 + kBins * 4;
+
+__device__ __forceinline__ uint32_t short_excl_sum(uint32_t v, uint32_t* buf, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t inc = warp_incl_sum(v);
+  if (lane == 31) buf[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t s = warp_incl_sum(lane < kShortWarps ? buf[lane] : 0u);
+    if (lane < kShortWarps) buf[lane] = s;
+  }
+  __syncthreads();
+  const uint32_t before = warp ? buf[warp - 1] : 0u;
+  *total = buf[kShortWarps - 1];
+  __syncthreads();
+  return before + inc - v;
+}
+
+template <typename LT, int kCols>
+__global__ void __launch_bounds__(kShortThreads, kCols <= 8192 ? 4 : 3)
+    topk_short_kernel(const LT* __restrict__ logits, int64_t stride, const int32_t* __restrict__ starts,
+                      const int32_t* __restrict__ ends, int32_t k, int32_t* __restrict__ out,
+                      int64_t out_stride) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);  // [kCols], column a + i at i
+  uint32_t* hist = keys + kCols;                       // [kBins]
+  __shared__ uint32_t scan_buf[kShortWarps];
+  __shared__ uint32_t s_max, s_or_bits, s_bin, s_above, s_cnt;
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const LT* rp = logits + static_cast<int64_t>(row) * stride;
+  int32_t* op = out + static_cast<int64_t>(row) * out_stride;
+  const int64_t a = starts ? max(starts[row], 0) : 0;
+  const int64_t b = min(static_cast<int64_t>(ends[row]), stride);
+  const int n = b > a ? static_cast<int>(b - a) : 0;  // <= stride <= kCols
+  if (n <= k) {
+    for (int i = tid; i < k; i += kShortThreads) op[i] = i < n ? static_cast<int32_t>(a + i) : -1;
+    return;
+  }
+  if (tid == 0) {
+    s_max = 0;
+    s_or_bits = 0;
+  }
+  // 1. the row's keys and their largest value
+  uint32_t mx = 0;
+#pragma unroll 8
+  for (int i = tid; i < n; i += kShortThreads) {
+    const uint32_t key = order_key(load_score<LT>(rp, a + i));
+    keys[i] = key;
+    mx = max(mx, key);
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  __syncthreads();  // s_max initialised
+  if (lane == 0) atomicMax(&s_max, mx);
+  __syncthreads();
+  const uint32_t kmax = s_max;
+  uint32_t x = 0;
+  for (int i = tid; i < n; i += kShortThreads) x |= keys[i] ^ kmax;
+  x = __reduce_or_sync(0xffffffffu, x);
+  if (lane == 0 && x) atomicOr(&s_or_bits, x);
+  __syncthreads();
+  const uint32_t diff = s_or_bits;
+  // 2. the k-th largest key: digits from the highest differing bit down
+  uint32_t prefix = kmax, remaining = static_cast<uint32_t>(k);
+  bool whole = false;  // the last chosen bin is taken whole: keys >= prefix are exactly k
+  if (diff != 0) {
+    int top = 31 - __clz(diff);
+    uint32_t mask = top == 31 ? 0u : ~((2u << top) - 1u);
+    prefix = kmax & mask;
+#pragma unroll 1
+    while (top >= 0) {
+      const int lo = max(top - 10, 0);
+      const uint32_t nbins = 1u << (top - lo + 1);
+      for (int i = tid; i < static_cast<int>(nbins); i += kShortThreads) hist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < n; i += kShortThreads) {
+        const uint32_t key = keys[i];
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> lo) & (nbins - 1)], 1u);
+      }
+      __syncthreads();
+      // thread t owns bins nbins-1-4t down to nbins-4-4t (descending order)
+      const int hb = static_cast<int>(nbins) - 1 - 4 * tid;
+      uint32_t h[4], sum = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h[e] = hb - e >= 0 ? hist[hb - e] : 0u;
+        sum += h[e];
+      }
+      uint32_t tot;
+      const uint32_t ab = short_excl_sum(sum, scan_buf, &tot);
+      if (ab < remaining && ab + sum >= remaining) {
+        uint32_t acc = ab;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (acc + h[e] >= remaining) {
+            s_bin = static_cast<uint32_t>(hb - e);
+            s_above = acc;
+            s_cnt = h[e];
+            break;
+          }
+          acc += h[e];
+        }
+      }
+      __syncthreads();
+      prefix |= s_bin << lo;
+      mask |= (nbins - 1u) << lo;
+      remaining -= s_above;
+      whole = s_cnt == remaining;
+      __syncthreads();
+      if (whole) break;
+      top = lo - 1;
+    }
+  }
+  // now: whole -> the chosen columns are those with key >= prefix; else tau =
+  // prefix, chosen = keys above tau plus the first `remaining` keys equal to it
+  const uint32_t take_eq = whole ? 0u : remaining;
+  // 3. ascending output: warp w walks its block of columns 32 at a time
+  const int per_warp = (n + kShortThreads - 1) / kShortThreads * 32;
+  const int c0 = warp * per_warp, c1 = min(c0 + per_warp, n);
+  uint32_t gt_w = 0, eq_w = 0;
+  for (int c = c0; c < c1; c += 32) {
+    const int i = c + lane;
+    const uint32_t key = i < c1 ? keys[i] : 0u;
+    const bool g = i < c1 && (whole ? key >= prefix : key > prefix);
+    const bool e = i < c1 && !whole && key == prefix;
+    gt_w += __popc(__ballot_sync(0xffffffffu, g));
+    eq_w += __popc(__ballot_sync(0xffffffffu, e));
+  }
+  uint32_t tot;
+  const uint32_t wbase = short_excl_sum(lane == 0 ? (gt_w | (eq_w << 16)) : 0u, scan_buf, &tot);
+  const uint32_t wb = __shfl_sync(0xffffffffu, wbase, 0);
+  uint32_t gt_run = wb & 0xffffu, eq_run = wb >> 16;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int c = c0; c < c1; c += 32) {
+    const int i = c + lane;
+    const uint32_t key = i < c1 ? keys[i] : 0u;
+    const bool g = i < c1 && (whole ? key >= prefix : key > prefix);
+    const bool e = i < c1 && !whole && key == prefix;
+    const uint32_t bg = __ballot_sync(0xffffffffu, g), be = __ballot_sync(0xffffffffu, e);
+    const uint32_t gb = gt_run + __popc(bg & lt), eb = eq_run + __popc(be & lt);
+    uint32_t pos = 0xffffffffu;
+    if (g) pos = gb + min(eb, take_eq);
+    else if (e && eb < take_eq) pos = gb + eb;
+    if (pos < static_cast<uint32_t>(k)) op[pos] = static_cast<int32_t>(a + i);
+    gt_run += __popc(bg);
+    eq_run += __popc(be);
+  }
+}
+
+template <typename LT, int kCols>
+cudaError_t launch_short(const void* logits, int64_t stride, const int32_t* starts, const int32_t* ends,
+                         int32_t num_rows, int32_t k, int32_t* out, int64_t out_stride, cudaStream_t stream) {
+  const cudaError_t e = cudaFuncSetAttribute(topk_short_kernel<LT, kCols>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kShortSmem<kCols>);
+  if (e != cudaSuccess) return e;
+  topk_short_kernel<LT, kCols><<<num_rows, kShortThreads, kShortSmem<kCols>, stream>>>(
+      static_cast<const LT*>(logits), stride, starts, ends, k, out, out_stride);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_top_k(const void* logits, int32_t logits_dtype, int64_t logits_stride,
                          const int32_t* row_starts, const int32_t* row_ends, int32_t num_rows,
                          int32_t k, int32_t* out_idx, int64_t out_stride, int32_t* status,
                          cudaStream_t stream) {
+  // short rows: several rows per SM
+  if (logits_stride <= 8192)
+    return logits_dtype == DSA_LOGITS_BF16
+               ? launch_short<__nv_bfloat16, 8192>(logits, logits_stride, row_starts, row_ends, num_rows, k, out_idx,
+                                                   out_stride, stream)
+               : launch_short<float, 8192>(logits, logits_stride, row_starts, row_ends, num_rows, k, out_idx,
+                                           out_stride, stream);
+  if (logits_stride <= 16384)
+    return logits_dtype == DSA_LOGITS_BF16
+               ? launch_short<__nv_bfloat16, 16384>(logits, logits_stride, row_starts, row_ends, num_rows, k,
+                                                    out_idx, out_stride, stream)
+               : launch_short<float, 16384>(logits, logits_stride, row_starts, row_ends, num_rows, k, out_idx,
+                                            out_stride, stream);
   cudaError_t e;
   if (logits_dtype == DSA_LOGITS_BF16) {
     e = cudaFuncSetAttribute(topk_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,

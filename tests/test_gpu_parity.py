@@ -57,11 +57,12 @@ def test_metadata_ragged_groups():
         assert np.array_equal(got.cpu().numpy(), oracle.schedule(wl.context_lens, wl.indices, S))
 
 
-def test_metadata_long_batch():
+@pytest.mark.parametrize("requests", [450, 900])
+def test_metadata_long_batch(requests):
     """More rows than one CTA pass (chunked scans), random run lengths and zero-length rows."""
     rng = np.random.default_rng(5)
     ctx, ids = [], []
-    for r in range(900):
+    for r in range(requests):
         n = int(rng.integers(1, 14))
         L = int(rng.integers(0, 3000))
         for j in range(n):
@@ -72,6 +73,16 @@ def test_metadata_long_batch():
     for S in (1, 148, 1023):
         got = dsa.paged_mqa_logits_metadata(ctx.cuda(), ids.cuda(), S)
         assert np.array_equal(got.cpu().numpy(), oracle.schedule(ctx, ids, S)), S
+
+
+@pytest.mark.parametrize("T", [1023, 1024, 1025, 4097])
+def test_metadata_chunk_boundaries(T):
+    rng = np.random.default_rng(T)
+    ctx = torch.from_numpy(rng.integers(0, 5000, T).astype(np.int32))
+    for ids in (None, torch.arange(T, dtype=torch.int32) // 3):
+        for S in (7, 152):
+            got = dsa.paged_mqa_logits_metadata(ctx.cuda(), None if ids is None else ids.cuda(), S)
+            assert np.array_equal(got.cpu().numpy(), oracle.schedule(ctx, ids, S)), (T, S)
 
 
 # ---------------------------------------------------------------- logits + top-k, small
@@ -209,6 +220,32 @@ def test_topk_standalone(dtype):
         got = dsa.top_k_per_row(x, starts.cuda(), ends.cuda(), k).cpu().numpy()
         ref = oracle.top_k_per_row(x.float().cpu().double().numpy(), ends, k, row_starts=starts)
         assert np.array_equal(got, ref), k
+
+
+@pytest.mark.parametrize("C", [5000, 8192, 16384])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_topk_short_rows(C, dtype):
+    """Row strides of at most 16384 columns take the short-row kernel."""
+    g = torch.Generator().manual_seed(C)
+    R = 14
+    x = torch.randn((R, C), generator=g) * 3
+    x[1] = torch.round(x[1] * 2)           # heavy ties
+    x[2, C // 3:] = float("-inf")
+    x[3, ::9] = float("nan")
+    x[4] = 0.0
+    x[4, ::2] = -0.0
+    x[5, :] = torch.arange(C, dtype=torch.float32)
+    x[12] = 1.5                            # every key equal
+    x[13, :] = torch.randn(C, generator=g) * 1e-30  # tiny magnitudes, both signs
+    x = x.to(dtype).cuda()
+    ends = torch.tensor([C, C, C, C, C, C, 1, 0, 2047, 2049, C - 3, 17, C, C], dtype=torch.int32)
+    starts = torch.tensor([0, 3, 0, 7, 0, 1000, 0, 0, 0, 0, 5, 0, 2, 0], dtype=torch.int32)
+    for k in (1, 7, 256, 2048):
+        got = dsa.top_k_per_row(x, starts.cuda(), ends.cuda(), k).cpu().numpy()
+        ref = oracle.top_k_per_row(x.float().cpu().double().numpy(), ends, k, row_starts=starts)
+        assert np.array_equal(got, ref), k
+        got = dsa.top_k_per_row(x, None, ends.cuda(), k).cpu().numpy()
+        assert np.array_equal(got, oracle.top_k_per_row(x.float().cpu().double().numpy(), ends, k)), k
 
 
 # ---------------------------------------------------------------- full-size workloads, sampled
