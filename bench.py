@@ -133,13 +133,21 @@ def algorithmic_bytes(wl):
     return key_bytes, logits_bytes, small, flops
 
 
+def kernel_source_sha(kernel_file):
+    """Hash of a kernel's source file and the headers it includes."""
+    csrc = os.path.join(ROOT, "sparse_attention_indexer_paged_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in (kernel_file, "ptx.cuh", "common.cuh"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def profile_traffic(kernel_file, summary_name):
     """dram bytes per launch from the committed ncu summary, if it matches the current source."""
     path = os.path.join(ROOT, "profiles", summary_name)
-    src = os.path.join(ROOT, "sparse_attention_indexer_paged_gb300", "csrc", kernel_file)
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = kernel_source_sha(kernel_file)
         m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
         s = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
         if m and s and s.group(1) == sha:
@@ -395,8 +403,7 @@ def run_ours(args, rank, world, local):
     fp8_tf = bf16_tf * FP8_PEAK_RATIO
     t_mem = alg_bytes / (hbm_gbs * 1e9)
     t_tc = flops / (fp8_tf * 1e12)
-    traffic = profile_traffic("logits.cu", f"logits_{'fp8' if wl.kv_format == 0 else 'fp4'}_"
-                              f"{args.workload}_ncu.md")
+    traffic = profile_traffic("logits.cu", f"logits_{args.workload}_ncu.md")
     step_bytes = alg_bytes + logit_b + T * wl.topk * 4   # + top-k re-read of logits and index write
     result = {
         "metric": METRIC,

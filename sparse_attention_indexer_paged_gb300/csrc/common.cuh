@@ -38,7 +38,6 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s
 constexpr uint64_t kDrainTimeoutNs = 200000000ull;   // 0.2 s
 // Longest a waiting thread sleeps inside one try_wait before it re-checks
 // the abort flag and the clock (it wakes earlier when the phase completes).
-constexpr uint32_t kSuspendHintNs = 100000;            // 0.1 ms
 
 // ----------------------------------------------------------------- launchers
 // (defined in the kernel translation units, called by api.cu after the

@@ -55,19 +55,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// As mbar_try_wait, but a thread whose phase is not complete may be
-// suspended (not spinning, so it takes no issue slots) until the phase
-// completes or kSuspendHintNs passes.
+// The test the bounded waits repeat: mbarrier.try_wait without a time hint
+// may suspend the thread for a system-dependent time before returning false
+// (measured 3 % faster in the logits kernel than an explicit 0.1 ms hint,
+// and no slower than pure polling).
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
-      : "memory");
-  return ok != 0;
+  return mbar_try_wait(bar, parity);
 }
 
 // Wait until the phase of `bar` with the given parity has completed.  Returns
