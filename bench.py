@@ -79,6 +79,16 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(x, device, world):
+    """The largest of every rank's x (a float); x itself with one rank."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -296,11 +306,7 @@ def run_ours(args, rank, world, local):
     logit_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / K
     topk_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K
     assert int(status.item()) == 0, dsa.status_string(int(status.item()))
-    ms_step = total_ms / K
-    if world > 1:
-        tt = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = max_over_ranks(total_ms / K, dev, world)
 
     # ---- end to end through the C ABI from pinned host buffers.  Every step
     # copies its inputs host -> device and reads its result back; a serving
@@ -368,11 +374,7 @@ def run_ours(args, rank, world, local):
         e2e_step(i)
     e1.record(s_out)   # after the last result copy, which follows the last step's kernels
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / KE
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / KE, dev, world)
     # the same step with nothing overlapped (copy in, kernels, copy out, all
     # on one stream): the per-step latency a single request stream sees
     st0 = sets[0]
@@ -393,7 +395,7 @@ def run_ours(args, rank, world, local):
         serial_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_serial_ms = e0.elapsed_time(e1) / KE
+    e2e_serial_ms = max_over_ranks(e0.elapsed_time(e1) / KE, dev, world)
 
     # ---- roofline of the dominant kernel (logits)
     hbm_gbs, bf16_tf, peak_src = peaks()
