@@ -76,12 +76,18 @@ template <int kFmt> constexpr int kDqPageBytes = kFmt == DSA_KV_MXFP4 ? kMxPageB
 constexpr int kScaleStageFloats = kTileTokens;            // 128 key scales per tile
 constexpr int kMaxKStages = 8;
 constexpr int kMaxRawStages = 8;
-constexpr int kFp4PassRows = 4;  // q rows per MMA pass over a tile, FP4 keys
+// q rows per MMA pass over a tile (dequantising formats): the f16 q of a
+// pass and the raw page ring share shared memory, so MXFP4's smaller pages
+// leave room for 6-row passes (every varlen group of up to 6 rows converts
+// each tile once) where FP4 keeps 4 rows and a deeper page ring.
+template <int kFmt> constexpr int kPassRowsOf = kFmt == DSA_KV_MXFP4 ? 6 : 4;
+template <int kFmt> constexpr int kRawStagesOf = kFmt == DSA_KV_MXFP4 ? 6 : 8;
+constexpr int kMaxPassRows = 6;
 
 // Shared memory layouts (offsets from a 1024-aligned base).
 //   FP8: K ring of e4m3 tiles [128 tokens][128 B] filled by TMA, Q rows e4m3.
 //   FP4: raw page pairs (bulk copies of whole pages), dequantised f16 K tiles
-//        [2 k-halves][128 tokens][128 B], Q rows in f16 [2 k-halves][512][128 B];
+//        [2 k-halves][128 tokens][128 B], Q rows in f16 [2 k-halves][pass rows x 64 heads][128 B];
 //        all MMA operands K-major with the 128-byte swizzle.
 template <int kFmt> struct Lay;
 template <> struct Lay<DSA_KV_FP8> {
@@ -94,18 +100,20 @@ template <> struct Lay<DSA_KV_FP8> {
   static constexpr int kOffQ = kOffKv + kKStages * kKStageBytes;
   static constexpr int kOffRaw = kOffQ + kGroupMaxRows * kQRowBytes;
 };
-template <int kPageBytes> struct LayDq {
+template <int kPageBytes, int kRows, int kRaw> struct LayDq {
   static constexpr int kKStages = 2;
   static constexpr int kKStageBytes = 2 * kTileTokens * 128;  // 32768
-  static constexpr int kRawStages = 8;
+  static constexpr int kRawStages = kRaw;
   static constexpr int kRawStageBytes = 2 * kPageBytes;       // 9728 (FP4), 8704 (MXFP4)
-  static constexpr int kQHalfBytes = kFp4PassRows * kHeads * 128;  // 32768
+  static constexpr int kQHalfBytes = kRows * kHeads * 128;    // one k-half of the pass's f16 q
   static constexpr int kOffQ = 0;
   static constexpr int kOffKv = kOffQ + 2 * kQHalfBytes;
   static constexpr int kOffRaw = kOffKv + kKStages * kKStageBytes;
 };
-template <> struct Lay<DSA_KV_FP4> : LayDq<kFp4PageBytes> {};
-template <> struct Lay<DSA_KV_MXFP4> : LayDq<kMxPageBytes> {};
+template <> struct Lay<DSA_KV_FP4>
+    : LayDq<kFp4PageBytes, kPassRowsOf<DSA_KV_FP4>, kRawStagesOf<DSA_KV_FP4>> {};
+template <> struct Lay<DSA_KV_MXFP4>
+    : LayDq<kMxPageBytes, kPassRowsOf<DSA_KV_MXFP4>, kRawStagesOf<DSA_KV_MXFP4>> {};
 template <int kFmt> struct Smem : Lay<kFmt> {
   using B = Lay<kFmt>;
   static constexpr int kOffScale = B::kOffRaw + B::kRawStages * B::kRawStageBytes;
@@ -127,9 +135,10 @@ template <int kFmt> struct Smem : Lay<kFmt> {
   static_assert(kBytes <= 232448, "over the per-CTA shared memory limit");
 };
 static_assert(kSlots * kPairCols == kTmemCols, "TMEM slots");
-static_assert(kFp4AHalfLo == (kTileTokens * 128) >> 4 && kFp4BHalfLo == Lay<DSA_KV_FP4>::kQHalfBytes >> 4 &&
-                  kFp4BHalfLo == Lay<DSA_KV_MXFP4>::kQHalfBytes >> 4,
-              "f16 operand halves as laid out by the dequantising warp");
+static_assert(kFp4AHalfLo == (kTileTokens * 128) >> 4, "f16 K operand halves as laid out by the dequantising warps");
+static_assert(kPassRowsOf<DSA_KV_FP4> <= kMaxPassRows && kPassRowsOf<DSA_KV_MXFP4> <= kMaxPassRows &&
+                  kRawStagesOf<DSA_KV_FP4> <= kMaxRawStages && kRawStagesOf<DSA_KV_MXFP4> <= kMaxRawStages,
+              "pass rows and raw stages");
 
 struct Params {
   const uint8_t* q;
@@ -364,7 +373,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   const float* w_sm = reinterpret_cast<const float*>(smem + L::kOffW);
   int32_t* ctx_sm = reinterpret_cast<int32_t*>(smem + L::kOffCtx);
 
-  Walk<kDq ? kFp4PassRows : kGroupMaxRows> walk;
+  Walk<kDq ? kPassRowsOf<kFmt> : kGroupMaxRows> walk;
   walk.start(grs, gus, p.ctx, G, T, u0, u1, lane);
 
   // =================================================== FP4 dequantisation (warps 3, 2, 20-23)
@@ -432,15 +441,17 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         const int nchunks = n * kHeads * (kHeadDim / 8);
         // every lane gets all rows' exponents before the loop, whose trip
         // count differs between lanes
-        int em[kFp4PassRows];
+        int em[kMaxPassRows];
 #pragma unroll
-        for (int r = 0; r < kFp4PassRows; ++r) em[r] = static_cast<int>(__shfl_sync(0xffffffffu, row_emax, r));
+        for (int r = 0; r < kMaxPassRows; ++r) em[r] = static_cast<int>(__shfl_sync(0xffffffffu, row_emax, r));
         for (int i = part * 32 + lane; i < nchunks; i += kStride) {
           const uint32_t c = __ldg(qsrc + i);
           const int R = i >> 4;      // q row (row * 64 + head) within the pass
           const int c16 = i & 15;    // 8-element chunk along d
           const int rr = R >> 6;
-          const int emax = rr == 0 ? em[0] : (rr == 1 ? em[1] : (rr == 2 ? em[2] : em[3]));
+          int emax = em[0];
+#pragma unroll
+          for (int r = 1; r < kMaxPassRows; ++r) emax = rr == r ? em[r] : emax;
           const uint32_t f = pow2_f16x2(static_cast<int>(__ldg(qsc + R * (kHeadDim / 32) + (c16 >> 2))) - emax);
           uint32_t h[4];
           e2m1x8_to_f16x2(c, h);
@@ -704,6 +715,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     const uint32_t a_lo0 = sdesc_lo(s_kv), q_lo0 = sdesc_lo(s_q);
     constexpr uint32_t kStageLo = L::kKStageBytes >> 4;
     constexpr uint32_t kQRowLo = (kDq ? kHeads * 128 : kHeads * kHeadDim) >> 4;  // one q row (64 heads) of B
+    // dequantising formats: the B operand's second k-half follows the pass's first
+    constexpr uint32_t kQHalfLo = Lay<kFmt == DSA_KV_FP8 ? DSA_KV_FP4 : kFmt>::kQHalfBytes >> 4;
     const uint32_t issue = elect_one() ? 1u : 0u;
     const bool leader = issue != 0;
     if constexpr (!kDq) {
@@ -747,7 +760,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem + c * kPairCols;
           if constexpr (!kDq) mma_fp8_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20));
-          else mma_f16_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20));
+          else mma_f16_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20), kQHalfLo);
           left -= len;
           pos += len;
           b_lo += len * kQRowLo;

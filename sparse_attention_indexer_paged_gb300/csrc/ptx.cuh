@@ -288,10 +288,10 @@ __device__ __forceinline__ void mma_fp8_k128(uint32_t issue, uint32_t d_tmem, ui
 //   separate swizzled blocks (the A block of a 128-token tile is 16 KB, the B
 //   block of the Q rows is kFp4QHalfBytes), four steps inside each.
 constexpr uint32_t kFp4AHalfLo = (128 * 128) >> 4;
-constexpr uint32_t kFp4BHalfLo = (4 * 64 * 128) >> 4;  // four q rows of 64 heads
+// b_half_lo: the distance of the B operand's second k-half (the pass's q rows) >> 4
 __device__ __forceinline__ void mma_f16_k128(uint32_t issue, uint32_t d_tmem, uint32_t a_lo,
-                                             uint32_t b_lo, uint32_t hi, uint32_t idesc_v) {
-  const uint32_t a2 = a_lo + kFp4AHalfLo, b2 = b_lo + kFp4BHalfLo;
+                                             uint32_t b_lo, uint32_t hi, uint32_t idesc_v, uint32_t b_half_lo) {
+  const uint32_t a2 = a_lo + kFp4AHalfLo, b2 = b_lo + b_half_lo;
   asm volatile(
       "{\n\t.reg .pred p, f, t;\n\t.reg .b64 da, db;\n\t.reg .b32 al, bl;\n\t"
       "setp.ne.b32 p, %0, 0;\n\t"
