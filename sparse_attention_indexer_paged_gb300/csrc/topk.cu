@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(kShortThreads, kCols <= 8192 ? 4 : 3)
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);  // [kCols], column a + i at i
   uint32_t* hist = keys + kCols;                       // [kBins]
   __shared__ uint32_t scan_buf[kShortWarps];
-  __shared__ uint32_t s_max, s_or_bits, s_bin, s_above, s_cnt;
+  __shared__ uint32_t s_max, s_min, s_bin, s_above, s_cnt;
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const LT* rp = logits + static_cast<int64_t>(row) * stride;
   int32_t* op = out + static_cast<int64_t>(row) * out_stride;
@@ -575,29 +575,64 @@ __global__ void __launch_bounds__(kShortThreads, kCols <= 8192 ? 4 : 3)
     for (int i = tid; i < k; i += kShortThreads) op[i] = i < n ? static_cast<int32_t>(a + i) : -1;
     return;
   }
+  constexpr int kQuads = kCols / 4 / kShortThreads;  // 4-column groups a thread covers
+  static_assert(kQuads % 4 == 0, "quads come in batches of 4");
+  uint4* keys4 = reinterpret_cast<uint4*>(keys);
   if (tid == 0) {
     s_max = 0;
-    s_or_bits = 0;
+    s_min = 0xffffffffu;
   }
-  // 1. the row's keys and their largest value
-  uint32_t mx = 0;
+  // 1. the row's keys, their largest and smallest: the keys all share the
+  // bits above the highest bit where the largest and smallest differ
+  uint32_t mx = 0, mn = 0xffffffffu;
+  if ((a & 3) == 0) {  // 16-byte (bf16: 8-byte) aligned groups of 4 columns, 4 loads in flight
+#pragma unroll
+    for (int u0 = 0; u0 < kQuads; u0 += 4) {
+      typename Vec4<LT>::T v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = 4 * (tid + (u0 + u) * kShortThreads);
+        if (i + 3 < n) v[u] = Vec4<LT>::load(rp, a + i);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = tid + (u0 + u) * kShortThreads, i = 4 * q;
+        if (i >= n) continue;
+        uint32_t kq[4];
+        if (i + 3 < n) {
+          Vec4<LT>::keys(v[u], kq);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) kq[e] = i + e < n ? order_key(load_score<LT>(rp, a + i + e)) : 0u;
+        }
+        keys4[q] = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (i + e < n) {
+            mx = max(mx, kq[e]);
+            mn = min(mn, kq[e]);
+          }
+      }
+    }
+  } else {
 #pragma unroll 8
-  for (int i = tid; i < n; i += kShortThreads) {
-    const uint32_t key = order_key(load_score<LT>(rp, a + i));
-    keys[i] = key;
-    mx = max(mx, key);
+    for (int i = tid; i < n; i += kShortThreads) {
+      const uint32_t key = order_key(load_score<LT>(rp, a + i));
+      keys[i] = key;
+      mx = max(mx, key);
+      mn = min(mn, key);
+    }
   }
   mx = __reduce_max_sync(0xffffffffu, mx);
-  __syncthreads();  // s_max initialised
-  if (lane == 0) atomicMax(&s_max, mx);
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  __syncthreads();  // s_max, s_min initialised
+  if (lane == 0) {
+    atomicMax(&s_max, mx);
+    atomicMin(&s_min, mn);
+  }
   __syncthreads();
   const uint32_t kmax = s_max;
-  uint32_t x = 0;
-  for (int i = tid; i < n; i += kShortThreads) x |= keys[i] ^ kmax;
-  x = __reduce_or_sync(0xffffffffu, x);
-  if (lane == 0 && x) atomicOr(&s_or_bits, x);
-  __syncthreads();
-  const uint32_t diff = s_or_bits;
+  const uint32_t diff = kmax ^ s_min;
   // 2. the k-th largest key: digits from the highest differing bit down
   uint32_t prefix = kmax, remaining = static_cast<uint32_t>(k);
   bool whole = false;  // the last chosen bin is taken whole: keys >= prefix are exactly k
@@ -611,9 +646,15 @@ __global__ void __launch_bounds__(kShortThreads, kCols <= 8192 ? 4 : 3)
       const uint32_t nbins = 1u << (top - lo + 1);
       for (int i = tid; i < static_cast<int>(nbins); i += kShortThreads) hist[i] = 0;
       __syncthreads();
-      for (int i = tid; i < n; i += kShortThreads) {
-        const uint32_t key = keys[i];
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> lo) & (nbins - 1)], 1u);
+#pragma unroll
+      for (int u = 0; u < kQuads; ++u) {
+        const int q = tid + u * kShortThreads, i = 4 * q;
+        if (i >= n) continue;
+        const uint4 k4 = keys4[q];
+        const uint32_t kq[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (i + e < n && (kq[e] & mask) == prefix) atomicAdd(&hist[(kq[e] >> lo) & (nbins - 1)], 1u);
       }
       __syncthreads();
       // thread t owns bins nbins-1-4t down to nbins-4-4t (descending order)
