@@ -681,7 +681,7 @@ def run_prefill(args, local):
         "kernels_us": {n: round(v, 3) for n, v in us.items()},
         "roofline": {"kernel": "logits", "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": fp8_tf, "unit": "TFLOP/s", "frac": round(achieved / fp8_tf, 4),
-                     "flops": flops, "traffic": None,
+                     "flops": flops, "traffic": profile_traffic("logits.cu", "logits_prefill_ncu.md"),
                      "peak_source": f"{peak_src} bf16 x {FP8_PEAK_RATIO} (nominal fp8:bf16 ratio)"},
         "gpu_launches": 4 * K,
         "clocks": clk,
