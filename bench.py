@@ -12,7 +12,9 @@ otherwise.  Inputs are synthetic and seeded (workloads.config).
     python bench.py --workload prefill
 
 Prints one JSON line (rank 0).  `value` is device time per step with inputs
-resident in HBM; `e2e` is the same step through the C ABI from pinned host
+resident in HBM, the step (three kernels) replayed from a CUDA graph as a
+serving loop runs it (`direct_launch_value`: the same steps launched call by
+call); `e2e` is the same step through the C ABI from pinned host
 buffers, with the per-step host->device input copies and the device->host
 read of the top-k indices inside the timed region.  `--impl reference` times
 the CPU oracle (the only other implementation of the method here) on a
@@ -251,15 +253,16 @@ def run_ours(args, rank, world, local):
     mx = wl.kv_format == W.KV_MXFP4
     logits_fn = L.dsa_mxfp4_paged_mqa_logits if mx else L.dsa_fp8_fp4_paged_mqa_logits
 
-    def make_calls(q, w, ctx, ind, bt, out_idx, qs=None):
-        meta = (P(ctx), P(ind), T, 64, S, P(sched), sp)
+    def make_calls(q, w, ctx, ind, bt, out_idx, qs=None, strm=None):
+        sp_ = sp if strm is None else strm
+        meta = (P(ctx), P(ind), T, 64, S, P(sched), sp_)
         # MXFP4 keys: the MXFP4 entry point with the q scales; else the key format
         head = (P(q), P(qs), P(wl.kv_cache), wl.page_stride, wl.num_pages) if mx else \
                (P(q), P(wl.kv_cache), wl.page_stride, wl.num_pages, wl.kv_format)
         lg = head + (P(w), P(ctx), P(bt), bt.stride(0), P(ind), P(sched), S, P(logits), wl.logits_dtype,
-                     wl.logits_stride, T, 64, 128, 64, P(status), sp)
+                     wl.logits_stride, T, 64, 128, 64, P(status), sp_)
         tk = (P(logits), wl.logits_dtype, wl.logits_stride, None, P(ctx), T, wl.topk,
-              P(out_idx), out_idx.stride(0), P(status), sp)
+              P(out_idx), out_idx.stride(0), P(status), sp_)
         return meta, lg, tk
 
     meta, lg, tk = make_calls(wl.q, wl.weights, wl.context_lens, wl.indices, wl.block_table, idx, wl.q_scale)
@@ -284,56 +287,115 @@ def run_ours(args, rank, world, local):
     assert int(status.item()) == 0, dsa.status_string(int(status.item()))
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
+    # The step as a CUDA graph (metadata, logits and top-k captured once on a
+    # stream of their own): how a serving loop runs a decode step.
+    gstream = torch.cuda.Stream(device=dev)
+    gsp = ctypes.c_void_p(gstream.cuda_stream)
+    meta_g, lg_g, tk_g = meta[:-1] + (gsp,), lg[:-1] + (gsp,), tk[:-1] + (gsp,)
+
+    def gstep():
+        return L.dsa_paged_mqa_logits_metadata(*meta_g) | logits_fn(*lg_g) | L.dsa_top_k_per_row(*tk_g)
+
+    gstream.wait_stream(stream)
+    with torch.cuda.stream(gstream):
+        for _ in range(3):
+            assert gstep() == 0
+    gstream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gstream, capture_error_mode="relaxed"):
+        assert gstep() == 0
+    with torch.cuda.stream(gstream):
+        for _ in range(max(args.warmup, 3)):
+            graph.replay()
+    torch.cuda.synchronize()
+
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
+    # timed: K graph replays (the value), then K directly launched steps
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    t0.record(stream)
-    for i in range(K):
-        step(evs[i])
-    t1.record(stream)
+    with torch.cuda.stream(gstream):
+        t0.record(gstream)
+        for _ in range(K):
+            graph.replay()
+        t1.record(gstream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    d0.record(stream)
+    for _ in range(K):
+        step()
+    d1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    total_ms = t0.elapsed_time(t1)
-    meta_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / K
-    logit_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / K
-    topk_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K
     assert int(status.item()) == 0, dsa.status_string(int(status.item()))
-    ms_step = max_over_ranks(total_ms / K, dev, world)
+    ms_step = max_over_ranks(t0.elapsed_time(t1) / K, dev, world)
+    direct_ms = max_over_ranks(d0.elapsed_time(d1) / K, dev, world)
+    # per-kernel breakdown: a separate loop with events between the kernels
+    KB = min(K, 500)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KB)]
+    for i in range(KB):
+        step(evs[i])
+    torch.cuda.synchronize()
+    meta_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / KB
+    logit_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / KB
+    topk_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / KB
+    assert int(status.item()) == 0, dsa.status_string(int(status.item()))
 
     # ---- end to end through the C ABI from pinned host buffers.  Every step
     # copies its inputs host -> device and reads its result back; a serving
     # loop overlaps step i's kernels with step i+1's input copy and step
     # i-1's result copy, so device inputs and outputs are double buffered
     # and three streams are ordered by events.
-    hq = wl.q.cpu().pin_memory()
-    hqs = None if wl.q_scale is None else wl.q_scale.cpu().pin_memory()
-    hw = wl.weights.cpu().pin_memory()
-    hctx = wl.context_lens.cpu().pin_memory()
-    hind = None if wl.indices is None else wl.indices.cpu().pin_memory()
-    hbt = wl.block_table.cpu().pin_memory()
+    # A step's inputs travel as one copy: they sit at 256-byte-aligned offsets
+    # of one pinned host buffer and of one device buffer per set.  The kernels
+    # of each set run as a CUDA graph on a compute stream of their own.
+    parts = [("q", wl.q), ("w", wl.weights), ("ctx", wl.context_lens), ("bt", wl.block_table)]
+    if wl.indices is not None:
+        parts.append(("ind", wl.indices))
+    if wl.q_scale is not None:
+        parts.append(("qs", wl.q_scale))
+    layout, off = {}, 0
+    for name, t in parts:
+        layout[name] = (off, t)
+        off = (off + t.numel() * t.element_size() + 255) // 256 * 256
+    blob_bytes = off
+
+    def blob_view(blob, name):
+        o, t = layout[name]
+        return blob[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+
+    hblob = torch.zeros(blob_bytes, dtype=torch.uint8).pin_memory()
+    for name, t in parts:
+        blob_view(hblob, name).copy_(t.cpu())
     hidx = [torch.empty((T, wl.topk), dtype=torch.int32).pin_memory() for _ in range(2)]
+    s_in, s_out, s_cmp = (torch.cuda.Stream(device=dev) for _ in range(3))
+    csp = ctypes.c_void_p(s_cmp.cuda_stream)
     sets = []
     for _ in range(2):
-        dq, dw, dctx = torch.empty_like(wl.q), torch.empty_like(wl.weights), torch.empty_like(wl.context_lens)
-        dqs = None if wl.q_scale is None else torch.empty_like(wl.q_scale)
-        dind = None if hind is None else torch.empty_like(wl.indices)
-        dbt = torch.empty_like(wl.block_table)
+        dblob = torch.empty(blob_bytes, dtype=torch.uint8, device=dev)
+        dv = {name: blob_view(dblob, name) for name, _ in parts}
         didx = torch.empty_like(idx)
-        h2d = [(dq, hq), (dw, hw), (dctx, hctx), (dbt, hbt)] + ([(dind, hind)] if hind is not None else [])
-        if dqs is not None:
-            h2d.append((dqs, hqs))
-        sets.append(dict(h2d=h2d, didx=didx, calls=make_calls(dq, dw, dctx, dind, dbt, didx, dqs)))
-    h2d_bytes = sum(h.numel() * h.element_size() for _, h in sets[0]["h2d"])
+        calls = make_calls(dv["q"], dv["w"], dv["ctx"], dv.get("ind"), dv["bt"], didx, dv.get("qs"), strm=csp)
+        dblob.copy_(hblob)
+        torch.cuda.synchronize()
+        m, lgc, tkc = calls
+        with torch.cuda.stream(s_cmp):
+            assert (L.dsa_paged_mqa_logits_metadata(*m) | logits_fn(*lgc) | L.dsa_top_k_per_row(*tkc)) == 0
+        s_cmp.synchronize()
+        graph_set = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_set, stream=s_cmp, capture_error_mode="relaxed"):
+            assert (L.dsa_paged_mqa_logits_metadata(*m) | logits_fn(*lgc) | L.dsa_top_k_per_row(*tkc)) == 0
+        sets.append(dict(dblob=dblob, didx=didx, graph=graph_set))
+    h2d_bytes = blob_bytes
     d2h_bytes = hidx[0].numel() * hidx[0].element_size()
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev_ready = [torch.cuda.Event() for _ in range(2)]     # inputs of the set copied in
     ev_done = [torch.cuda.Event() for _ in range(2)]      # kernels of the set finished
     ev_out = [torch.cuda.Event() for _ in range(2)]       # result of the set copied out
@@ -344,19 +406,18 @@ def run_ours(args, rank, world, local):
         st = sets[i % 2]
         s_in.wait_event(ev_done[i % 2])       # the kernels that read this set are done
         with torch.cuda.stream(s_in):
-            for d, h in st["h2d"]:
-                d.copy_(h, non_blocking=True)
+            st["dblob"].copy_(hblob, non_blocking=True)
         ev_ready[i % 2].record(s_in)
-        stream.wait_event(ev_ready[i % 2])
-        stream.wait_event(ev_out[i % 2])      # its previous result was copied out
-        m, lgc, tkc = st["calls"]
-        r = L.dsa_paged_mqa_logits_metadata(*m) | logits_fn(*lgc) | L.dsa_top_k_per_row(*tkc)
-        ev_done[i % 2].record(stream)
+        s_cmp.wait_event(ev_ready[i % 2])
+        s_cmp.wait_event(ev_out[i % 2])       # its previous result was copied out
+        with torch.cuda.stream(s_cmp):
+            st["graph"].replay()
+        ev_done[i % 2].record(s_cmp)
         s_out.wait_event(ev_done[i % 2])
         with torch.cuda.stream(s_out):
             hidx[i % 2].copy_(st["didx"], non_blocking=True)
         ev_out[i % 2].record(s_out)
-        return r
+        return 0
 
     for i in range(4):
         assert e2e_step(i) == 0
@@ -380,20 +441,19 @@ def run_ours(args, rank, world, local):
     st0 = sets[0]
 
     def serial_step():
-        for d, h in st0["h2d"]:
-            d.copy_(h, non_blocking=True)
-        m, lgc, tkc = st0["calls"]
-        r = L.dsa_paged_mqa_logits_metadata(*m) | logits_fn(*lgc) | L.dsa_top_k_per_row(*tkc)
-        hidx[0].copy_(st0["didx"], non_blocking=True)
-        return r
+        with torch.cuda.stream(s_cmp):
+            st0["dblob"].copy_(hblob, non_blocking=True)
+            st0["graph"].replay()
+            hidx[0].copy_(st0["didx"], non_blocking=True)
+        return 0
 
     for _ in range(3):
         assert serial_step() == 0
     torch.cuda.synchronize()
-    e0.record(stream)
+    e0.record(s_cmp)
     for _ in range(KE):
         serial_step()
-    e1.record(stream)
+    e1.record(s_cmp)
     torch.cuda.synchronize()
     e2e_serial_ms = max_over_ranks(e0.elapsed_time(e1) / KE, dev, world)
 
@@ -451,8 +511,11 @@ def run_ours(args, rank, world, local):
             "step_roofline_frac": round(max(t_mem, t_tc) / (ms_step * 1e-3), 4),
         },
         "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": "us/step",
-                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "serialized_value": round(e2e_serial_ms * 1e3, 3), "pipelining": "step i kernels overlap step i+1 input copy and step i-1 result copy"},
-        "gpu_launches": 3 * K,
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "serialized_value": round(e2e_serial_ms * 1e3, 3), "pipelining": "step i kernels overlap step i+1 input copy and step i-1 result copy; a step's inputs are one copy from a pinned staging buffer and its kernels one CUDA graph replay"},
+        "launch": "value: the step (metadata, logits, top-k) captured once as a CUDA graph and "
+                  "replayed K times; direct_launch_value: the same K steps launched one call at a time",
+        "direct_launch_value": round(direct_ms * 1e3, 3),
+        "gpu_launches": 6 * K,
         "clocks": clk,
         "context": PAGES_CONTEXT,
     }

@@ -347,3 +347,47 @@ def test_mxfp4_full_size_sampled():
     ref, bound, _ = check_logits(host, out["logits"], rows=rows)
     check_topk_exact(out["logits"], out["idx"], host.context_lens, wl.topk)
     check_topk_tie_band(out["idx"], ref, bound, host.context_lens, wl.topk, rows)
+
+
+# ---------------------------------------------------------------- CUDA graphs
+
+def test_step_replays_from_a_cuda_graph():
+    """The three calls allocate, free and synchronise nothing, so a decode
+    step captures into a CUDA graph; replaying it after the inputs change in
+    place gives the direct run's results for the new inputs."""
+    wl = W.build("graph", **MIXED, topk=64, seed=51).to("cuda")
+    S = dsa.device_num_sms()
+    sched = torch.empty(dsa.schedule_words(S, wl.num_rows), dtype=torch.int32, device="cuda")
+    logits = torch.empty((wl.num_rows, wl.logits_stride), dtype=torch.float32, device="cuda")
+    idx = torch.empty((wl.num_rows, wl.topk), dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q, w = wl.q.clone(), wl.weights.clone()
+
+    def step():
+        dsa.paged_mqa_logits_metadata(wl.context_lens, wl.indices, S, out=sched)
+        dsa.fp8_fp4_paged_mqa_logits(q, wl.kv_cache, w, wl.context_lens, wl.block_table, sched,
+                                     indices=wl.indices, logits_stride=wl.logits_stride, num_sms=S,
+                                     out=logits, status=st)
+        dsa.top_k_per_row(logits, None, wl.context_lens, wl.topk, out=idx, status=st)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    first = idx.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+        step()
+    q.copy_(torch.roll(wl.q, 1, dims=0))         # new inputs, same buffers
+    w.copy_(wl.weights * 2.0 - 0.1)
+    idx.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    replayed = idx.clone()
+    step()                                        # the same step launched directly
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(replayed, idx)
+    assert not torch.equal(replayed, first)

@@ -328,6 +328,27 @@ def check_dcp_merge_is_global_topk(seed=0):
         assert np.array_equal(got, want), (world, inter, k)
 
 
+def check_all_zero_keys():
+    """All-zero keys (e4m3 code 0, scale 1): every logit below L_t is exactly 0,
+    and the top-k is the first k positions (equal scores go to the lower
+    column)."""
+    wl = small_workload(seed=9)
+    views = W._page_views(wl.kv_cache, wl.kv_format)
+    views["values"][:] = 0
+    views["scale"][:] = torch.tensor([1.0], dtype=torch.float32).view(torch.uint8)
+    lg, _ = oracle.workload_logits(wl, with_bound=False)
+    ctx = wl.context_lens.numpy()
+    for t in range(wl.num_rows):
+        L = int(ctx[t])
+        assert np.all(lg[t, :L] == 0.0) and np.all(np.isneginf(lg[t, L:]))
+    k = 16
+    got = oracle.top_k_per_row(lg, ctx, k)
+    for t in range(wl.num_rows):
+        L = int(ctx[t])
+        want = list(range(min(k, L))) + [-1] * (k - min(k, L))
+        assert got[t].tolist() == want
+
+
 def check_chunk_ranges():
     """Row chunking under a BF16 logits budget (sparse_attn_indexer docs,
     _decode_chunk_ranges).  Worked by hand from the rule's statement:
@@ -396,6 +417,7 @@ PIN_CHECKS = [
     check_varlen_equals_padded, check_topk_bruteforce, check_fp4_bruteforce,
     check_ue8m0_vs_torch, check_mxfp4_bruteforce,
     check_dcp_mapping, check_dcp_merge_is_global_topk, check_chunk_ranges, check_prefill_rows,
+    check_all_zero_keys,
 ]
 
 
