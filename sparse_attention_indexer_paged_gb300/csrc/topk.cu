@@ -9,7 +9,7 @@
 //
 // Sampled path (rows up to kFastMaxCols columns), one full read of the row:
 //   sample  every sv-th 4-column group (at most kSampleQuads groups); the
-//           sample's ks-th largest key (ks ~ 1.25 k / sv, two radix rounds),
+//           sample's ks-th largest key (ks ~ 1.5 k / sv, two radix rounds),
 //           cut to its top 22 bits, is a threshold t;
 //   pass    keys >= t go to per-warp candidate slices (one shared counter per
 //           warp), packed afterwards;
@@ -38,7 +38,10 @@ constexpr int kBitmapWords = kFastMaxCols / 32;
 constexpr int kCandCap = 8192;         // (key, column) candidates held in shared memory
 constexpr int kLoadsInFlight = 4;      // 16-byte loads per thread per iteration
 constexpr int kStageBytes = 65536;     // threshold sample keys, then the warps' candidate columns
-constexpr int kSampleQuads = kStageBytes / 16;  // 4-column groups in the threshold sample
+// 4-column groups in the threshold sample: 4096 keys, one 16-byte load per
+// thread (a 16384-key sample measured ~3 us slower per launch)
+constexpr int kSampleQuads = 1024;
+static_assert(kSampleQuads * 16 <= kStageBytes, "the sample keys fit the stage area");
 
 // dynamic shared memory map
 constexpr int kOffHist = 0;                                   // uint32 [kBins]
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (b - wa <= kFastMaxCols && stride % (16 / static_cast<int64_t>(sizeof(LT))) == 0) {
     // ---- sampled threshold: every sv-th 4-column group, at most kSampleQuads
     // groups; the sample's ks-th largest key, rounded down to its top 22
-    // bits, is a threshold t that about 1.25 k keys of the row reach
+    // bits, is a threshold t that about 1.5 k keys of the row reach
     const int64_t a4 = a & ~static_cast<int64_t>(3);
     const int64_t nquads = (b - a4 + 3) >> 2;
     const int64_t sv = (nquads + kSampleQuads - 1) / kSampleQuads;
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid < kWarps) s_wcount[tid] = 0;
     const int ns = 4 * nsq;
-    const int64_t want = sv == 1 ? k : (5 * static_cast<int64_t>(k)) / (4 * sv) + 16;
+    const int64_t want = sv == 1 ? k : (3 * static_cast<int64_t>(k)) / (2 * sv) + 16;
     uint32_t t = 0;
     if (want < ns) {
       uint32_t prefix = 0, prefix_mask = 0, remaining = static_cast<uint32_t>(want);
