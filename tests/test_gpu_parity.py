@@ -276,6 +276,27 @@ def test_topk_long_row_general_path():
         assert np.array_equal(got, ref), k
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_topk_sampled_path_boundary(dtype):
+    """Rows of 2^18 - 1, 2^18 and 2^18 + 1 columns: the last one no longer fits
+    the sampled path's bitmaps and takes the exact passes; the stride 16384 + 8
+    also sits just above the short-row kernel's largest stride."""
+    g = torch.Generator().manual_seed(13)
+    C = (1 << 18) + 8
+    x = torch.randn((4, C), generator=g)
+    x[3] = torch.round(x[3] * 4)                # heavy ties across the whole row
+    x = x.to(dtype).cuda()
+    ends = torch.tensor([(1 << 18) - 1, 1 << 18, (1 << 18) + 1, C], dtype=torch.int32)
+    for k in (1, 2048):
+        got = dsa.top_k_per_row(x, None, ends.cuda(), k).cpu().numpy()
+        ref = oracle.top_k_per_row(x.float().cpu().double().numpy(), ends, k)
+        assert np.array_equal(got, ref), k
+    x2 = x[:, :16392].contiguous()              # stride 16392: the long-row kernel on short rows
+    ends2 = torch.tensor([16392, 9000, 2049, 1], dtype=torch.int32)
+    got = dsa.top_k_per_row(x2, None, ends2.cuda(), 2048).cpu().numpy()
+    assert np.array_equal(got, oracle.top_k_per_row(x2.float().cpu().double().numpy(), ends2, 2048))
+
+
 # ---------------------------------------------------------------- FP4 keys (e2m1 + e4m3/16 + fp32/token)
 
 @pytest.mark.parametrize("logits_dtype", [W.LOGITS_F32, W.LOGITS_BF16])
