@@ -179,7 +179,10 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples (the JSON line carries their summary): DSA_CLOCKS_DIR, else the temp dir
+        import tempfile
+        out_dir = os.environ.get("DSA_CLOCKS_DIR", tempfile.gettempdir())
+        self.path = os.path.join(out_dir, f"dsa_clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:

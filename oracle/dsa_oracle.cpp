@@ -104,7 +104,7 @@ float load_f32(const uint8_t* p) {
 // kv_cache_as_quant_view -- MXFP4 is head_dim/2 packed bytes plus
 // head_dim/MXFP4_BLOCK_SIZE ue8m0 scales, with the OCP MX block of 32; the
 // split of values and scales inside the page and the two-level FP4 scale are
-// this build's storage reading.)
+// the storage reading this oracle and its library share by definition.)
 double decode_token(const uint8_t* page, int kv_format, int slot, int D, int block_kv,
                     double* k) {
   if (kv_format == kKvFp8) {
@@ -375,7 +375,7 @@ int oracle_top_k_per_row(const double* scores, int64_t stride, const int32_t* ro
 //
 // The pages fix the inputs and the purpose (balance (request, K-block) work
 // over the SMs, grouping consecutive equal request ids) but not the split
-// rule.  This build's rule, written out:
+// rule.  The rule the library's metadata call states, written out:
 //   1. runs  = maximal runs of consecutive rows with equal request id
 //              (indices == NULL: every row is its own run);
 //   2. groups = each run cut into consecutive pieces of at most
