@@ -6,10 +6,37 @@ outputs the caller did not pass (torch is used for device memory and streams
 only).  Every step of the path runs in the library's kernels; there is no
 fallback.  If the library has not been built, every call raises.
 
+Decode step (the three calls of the C ABI):
+
     sched  = paged_mqa_logits_metadata(context_lens, indices, num_sms)
     logits = fp8_fp4_paged_mqa_logits(q, kv_cache, weights, context_lens,
                                       block_table, sched, indices=indices)
     idx    = top_k_per_row(logits, None, context_lens, k)
+
+The same step as one native call, optionally in row slices whose logits fit a
+byte budget:
+
+    idx = indexer_decode_topk(q, kv_cache, weights, context_lens, block_table,
+                              k, indices=indices, logits_budget=16 << 20)
+
+MXFP4 keys and q (kv_format=KV_MXFP4; q packed e2m1 with ue8m0 q_scale):
+
+    logits = fp8_fp4_paged_mqa_logits(..., kv_format=KV_MXFP4, q_scale=q_scale)
+
+Prefill rows tagged (cu_seqlen_ks, cu_seqlen_ke), straight from the paged
+cache with a block table per request:
+
+    idx, logits = prefill_topk(q, kv_cache, weights, cu_seqlen_ks, cu_seqlen_ke,
+                               local_cu_seq_lens, block_table, k)
+
+Decode context parallelism (this rank's shard of every request's keys; the
+gather goes through torch.distributed):
+
+    idx = dcp_topk(logits, local_idx, k, rank, world, interleave)
+
+Every call is stream-ordered on the current CUDA stream and allocates,
+frees and synchronises nothing inside the library, so a step can be
+captured into a CUDA graph.
 """
 from __future__ import annotations
 
