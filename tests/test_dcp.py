@@ -20,7 +20,7 @@ MIXED = dict(request_lens=[300, 517, 70, 1000, 129], rows_per_request=[1, 3, 2, 
 # CPU
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("kv_format", [W.KV_FP8, W.KV_FP4])
+@pytest.mark.parametrize("kv_format", [W.KV_FP8, W.KV_FP4, W.KV_MXFP4])
 def test_shard_holds_the_ranks_tokens(kv_format):
     wl = W.build("dcp", **MIXED, kv_format=kv_format, topk=32, seed=3)
     src = W._page_views(wl.kv_cache, kv_format)
@@ -133,8 +133,9 @@ def test_dcp_emulated_equals_unsharded_step(world, inter):
 
 
 @pytest.mark.gpu
-def test_dcp_emulated_fp4_bf16_logits():
-    wl = W.build("dcp", **MIXED, kv_format=W.KV_FP4, logits_dtype=W.LOGITS_BF16, topk=48, seed=12)
+@pytest.mark.parametrize("kv_format", [W.KV_FP4, W.KV_MXFP4])
+def test_dcp_emulated_fp4_bf16_logits(kv_format):
+    wl = W.build("dcp", **MIXED, kv_format=kv_format, logits_dtype=W.LOGITS_BF16, topk=48, seed=12)
     glob, _, gathered, merged = _emulated(wl, 3, 2)
     assert torch.equal(merged.cpu(), glob["idx"].cpu())
     assert np.array_equal(merged.cpu().numpy(), oracle.dcp_merge(gathered.cpu().double().numpy(), wl.topk))
