@@ -3,20 +3,24 @@
 // below its row end; forward_cpu: -1 pads the output; as_fp32_logits: BF16
 // logits are read as their exact fp32 values).
 //
-// One CTA per row.  Scores map to order-preserving 32-bit keys (NaN lowest,
-// -0 == +0); the k-th largest key tau and the number of keys equal to tau
-// that are kept (the lowest columns among them) are found by radix select.
+// One CTA per row: 1024 threads and one row per SM, or 512 threads and two
+// rows per SM where a grid has more rows than the device has SMs.  Scores map
+// to order-preserving 32-bit keys (NaN lowest, -0 == +0); the k-th largest
+// key tau and the number of keys equal to tau that are kept (the lowest
+// columns among them) are found by radix select.
 //
 // Sampled path (rows up to kFastMaxCols columns), one full read of the row:
 //   sample  every sv-th 4-column group (at most kSampleQuads groups); the
 //           sample's ks-th largest key (ks ~ 1.5 k / sv, two radix rounds),
 //           cut to its top 22 bits, is a threshold t;
-//   pass    keys >= t go to per-warp candidate slices (one shared counter per
-//           warp), packed afterwards;
+//   pass    scores at or above t's float form go to per-warp candidate
+//           slices (a ballot per key position, the count in a register),
+//           packed afterwards;
 //   then    if at least k and at most kCandCap keys reached t, tau is found
-//           on the candidates alone (all keys >= tau are among them), the
-//           kept candidates set their bits in two shared-memory bitmaps and
-//           one block-wide scan over the bitmaps writes the chosen columns in
+//           on the candidates alone (all keys >= tau are among them; radix
+//           digits start at their highest differing bit), the kept
+//           candidates set their bits in two shared-memory bitmaps and one
+//           block-wide scan over the bitmaps writes the chosen columns in
 //           ascending order.
 // Otherwise (the sample missed, or the row is longer) the exact passes run:
 // a histogram of the top 11 key bits, then either the bitmap/candidate pass
@@ -29,35 +33,58 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kPerThread = 8;          // elements per thread per chunk of the ordered pass
-constexpr int kFastMaxCols = 1 << 18;  // columns the two shared-memory bitmaps cover
-constexpr int kBitmapWords = kFastMaxCols / 32;
-constexpr int kCandCap = 8192;         // (key, column) candidates held in shared memory
 constexpr int kLoadsInFlight = 4;      // 16-byte loads per thread per iteration
-constexpr int kStageBytes = 65536;     // threshold sample keys, then the warps' candidate columns
-// 4-column groups in the threshold sample: 4096 keys, one 16-byte load per
-// thread (a 16384-key sample measured ~3 us slower per launch)
+// 4-column groups in the threshold sample: 4096 keys (a 16384-key sample
+// measured ~3 us slower per launch)
 constexpr int kSampleQuads = 1024;
-static_assert(kSampleQuads * 16 <= kStageBytes, "the sample keys fit the stage area");
 
-// dynamic shared memory map
-constexpr int kOffHist = 0;                                   // uint32 [kBins]
-constexpr int kOffSel = kOffHist + kBins * 4;                 // uint32 [kBitmapWords]
-constexpr int kOffTie = kOffSel + kBitmapWords * 4;           // uint32 [kBitmapWords]
-constexpr int kOffCandKey = kOffTie + kBitmapWords * 4;       // uint32 [kCandCap]
-constexpr int kOffCandCol = kOffCandKey + kCandCap * 4;       // int32  [kCandCap]
-constexpr int kOffStage = kOffCandCol + kCandCap * 4;
-constexpr int kSmemBytes = kOffStage + kStageBytes;
-static_assert(kSmemBytes <= 232448, "over the per-CTA shared memory limit");
+// Geometry of the long-row kernel: kT threads; two shared-memory bitmaps
+// over kMaxCols columns; kCap (key, column) candidates; kMinBlocks CTAs an SM
+// must hold.  The stage area takes the threshold sample's keys, then the
+// warps' candidate columns.
+template <int kT, int kMaxCols, int kCap, int kMinBlocks_>
+struct TopkCfg {
+  static constexpr int kThreads = kT;
+  static constexpr int kWarps = kT / 32;
+  static constexpr int kMinBlocks = kMinBlocks_;
+  static constexpr int kFastMaxCols = kMaxCols;
+  static constexpr int kBitmapWords = kMaxCols / 32;
+  static constexpr int kCandCap = kCap;
+  static constexpr int kStageBytes = kSampleQuads * 16 > kCap * 4 ? kSampleQuads * 16 : kCap * 4;
+  // dynamic shared memory map
+  static constexpr int kOffHist = 0;                              // uint32 [kBins]
+  static constexpr int kOffSel = kOffHist + kBins * 4;            // uint32 [kBitmapWords]
+  static constexpr int kOffTie = kOffSel + kBitmapWords * 4;      // uint32 [kBitmapWords]
+  static constexpr int kOffCandKey = kOffTie + kBitmapWords * 4;  // uint32 [kCandCap]
+  static constexpr int kOffCandCol = kOffCandKey + kCandCap * 4;  // int32  [kCandCap]
+  static constexpr int kOffStage = kOffCandCol + kCandCap * 4;
+  static constexpr int kSmemBytes = kOffStage + kStageBytes;
+  static_assert(kBins % kT == 0 && kT <= 1024, "each thread owns a whole number of histogram bins");
+  static_assert(kCap % (32 * kWarps) == 0, "whole warp slices of candidates");
+  static_assert(kSmemBytes * kMinBlocks <= 232448 - 1024 * (kMinBlocks - 1), "over the shared memory of an SM");
+};
+// one row per SM, rows up to 2^18 columns on the sampled path
+using WideCfg = TopkCfg<1024, 1 << 18, 8192, 1>;
+// two rows per SM (grids of more rows than SMs), rows up to 2^17 columns
+using HalfCfg = TopkCfg<512, 1 << 17, 6144, 2>;
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   uint32_t u = __float_as_uint(x);
   if ((u & 0x7fffffffu) > 0x7f800000u) return 0u;  // NaN: below every number
   if (u == 0x80000000u) u = 0u;                     // -0 == +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The smallest score whose key reaches t (t >= 1): for every non-NaN score x,
+// order_key(x) >= t exactly when x >= key_floor(t).  NaN scores fail the
+// comparison, as their key 0 fails t >= 1; a t above the key of +inf gives
+// NaN, which no score reaches.
+__device__ __forceinline__ float key_floor(uint32_t t) {
+  if (t & 0x80000000u) return __uint_as_float(t & 0x7fffffffu);
+  const uint32_t u = ~t;  // a negative score's key is its complemented bits
+  return u > 0xff800000u ? -INFINITY : __uint_as_float(u);
 }
 
 template <typename LT>
@@ -84,6 +111,12 @@ template <> struct Vec4<float> {
     k[2] = order_key(v.z);
     k[3] = order_key(v.w);
   }
+  __device__ static void vals(const T& v, float (&x)[4]) {
+    x[0] = v.x;
+    x[1] = v.y;
+    x[2] = v.z;
+    x[3] = v.w;
+  }
 };
 template <> struct Vec4<__nv_bfloat16> {
   using T = uint2;
@@ -95,6 +128,12 @@ template <> struct Vec4<__nv_bfloat16> {
     k[1] = order_key(__uint_as_float(v.x & 0xffff0000u));
     k[2] = order_key(__uint_as_float(v.y << 16));
     k[3] = order_key(__uint_as_float(v.y & 0xffff0000u));
+  }
+  __device__ static void vals(const T& v, float (&x)[4]) {
+    x[0] = __uint_as_float(v.x << 16);
+    x[1] = __uint_as_float(v.x & 0xffff0000u);
+    x[2] = __uint_as_float(v.y << 16);
+    x[3] = __uint_as_float(v.y & 0xffff0000u);
   }
 };
 
@@ -108,13 +147,19 @@ __device__ __forceinline__ uint32_t warp_incl_sum(uint32_t x) {
   return x;
 }
 
-// Exclusive block prefix sum of 32-bit values; *total = block sum.
+// Exclusive prefix sum of 32-bit values over a block of kT threads; *total =
+// block sum.
+template <int kT>
 __device__ __forceinline__ uint32_t block_excl_sum(uint32_t v, uint32_t* buf, uint32_t* total) {
+  constexpr int kWarps = kT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t inc = warp_incl_sum(v);
   if (lane == 31) buf[warp] = inc;
   __syncthreads();
-  if (warp == 0) buf[lane] = warp_incl_sum(buf[lane]);
+  if (warp == 0) {
+    const uint32_t x = warp_incl_sum(lane < kWarps ? buf[lane] : 0u);
+    if (lane < kWarps) buf[lane] = x;
+  }
   __syncthreads();
   const uint32_t before = warp ? buf[warp - 1] : 0u;
   *total = buf[kWarps - 1];
@@ -124,7 +169,7 @@ __device__ __forceinline__ uint32_t block_excl_sum(uint32_t v, uint32_t* buf, ui
 
 // Walk the row [a, b) in 4-column groups with kLoadsInFlight loads per thread
 // in flight; fn(first column, keys[4], valid mask) for every group.
-template <typename LT, typename F>
+template <int kThreads, typename LT, typename F>
 __device__ __forceinline__ void for_each_quad(const LT* rp, int64_t a, int64_t b, F&& fn) {
   const int64_t a4 = a & ~static_cast<int64_t>(3);
   constexpr int64_t kStep = 4 * static_cast<int64_t>(kThreads) * kLoadsInFlight;
@@ -161,29 +206,32 @@ __device__ __forceinline__ void for_each_quad(const LT* rp, int64_t a, int64_t b
 }
 
 // Finds the bin holding the `remaining`-th largest key among the histogram's
-// nbins bins (thread t owns bins nbins-1-2t and nbins-2-2t).  Returns the bin
-// and, in *above, the number of keys in higher bins.
+// nbins bins (thread t of kT owns the kBins / kT bins below nbins - kPer t,
+// highest first).  Returns the bin and, in *above, the number of keys in
+// higher bins.
+template <int kT>
 __device__ __forceinline__ uint32_t find_bin(const uint32_t* hist, uint32_t nbins,
                                              uint32_t remaining, uint32_t* scan_buf,
                                              uint32_t* s_bin, uint32_t* s_above,
                                              uint32_t* above) {
-  const int tid = threadIdx.x;
-  uint32_t h_hi = 0, h_lo = 0;
-  const int hi = static_cast<int>(nbins) - 1 - 2 * tid;
-  if (hi >= 1) {
-    h_hi = hist[hi];
-    h_lo = hist[hi - 1];
+  constexpr int kPer = kBins / kT;
+  const int hi = static_cast<int>(nbins) - 1 - kPer * static_cast<int>(threadIdx.x);
+  uint32_t h[kPer];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    h[e] = hi - e >= 0 ? hist[hi - e] : 0u;
+    sum += h[e];
   }
   uint32_t tot;
-  const uint32_t ab = block_excl_sum(h_hi + h_lo, scan_buf, &tot);
-  if (hi >= 1) {
-    if (ab < remaining && ab + h_hi >= remaining) {
-      *s_bin = static_cast<uint32_t>(hi);
-      *s_above = ab;
-    } else if (ab + h_hi < remaining && ab + h_hi + h_lo >= remaining) {
-      *s_bin = static_cast<uint32_t>(hi - 1);
-      *s_above = ab + h_hi;
+  uint32_t run = block_excl_sum<kT>(sum, scan_buf, &tot);
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    if (hi - e >= 0 && run < remaining && run + h[e] >= remaining) {
+      *s_bin = static_cast<uint32_t>(hi - e);
+      *s_above = run;
     }
+    run += h[e];
   }
   __syncthreads();
   const uint32_t bin = *s_bin;
@@ -193,41 +241,81 @@ __device__ __forceinline__ uint32_t find_bin(const uint32_t* hist, uint32_t nbin
 }
 
 // Exact selection among the shared-memory candidates (every key of the row
-// that can be in its top-k is among them), then the ordered output: keys
-// above tau set their column's bit in `sel`, the first take_eq keys equal to
-// tau (lowest columns) come from `tie`, and a block-wide scan over the
-// bitmaps writes the columns in ascending order.  `prefix`/`prefix_mask`
-// hold key bits already fixed by earlier rounds (starting at `round`: 0 for
-// none, 1 for the top 11 bits) and `remaining` the rank still to find below
-// them.  sel/tie must be zero for the words [0, nwords).
+// that can be in its top-k is among them, and all of them share the key bits
+// above those the earlier passes left open), then the ordered output.  The
+// `remaining`-th largest candidate is found by radix select over digits of
+// up to 11 bits, starting at the highest bit where the candidates' largest
+// and smallest keys differ and stopping once the chosen bin is taken whole
+// (the candidates are the top few percent of the row and would crowd into
+// one or two bins of a fixed top digit).  Chosen candidates above the last
+// digit's bin, or in it when it is taken whole, set their column's bit in
+// `sel`; otherwise the first take_eq keys equal to tau (lowest columns) come
+// from `tie`.  A block-wide scan over the bitmaps writes the columns in
+// ascending order.  sel/tie must be zero for the words [0, nwords) except
+// for columns already chosen by the caller (set in sel).
+template <int kThreads>
 __device__ __forceinline__ void select_candidates_and_write(
     const uint32_t* cand_key, const int32_t* cand_col, int nc, uint32_t* sel, uint32_t* tie,
-    int nwords, int64_t wa, uint32_t prefix, uint32_t prefix_mask, uint32_t remaining, int round,
-    uint32_t* hist, uint32_t* scan_buf, uint32_t* s_bin, uint32_t* s_above, int32_t* op) {
-  const int tid = threadIdx.x;
-  uint32_t above;
+    int nwords, int64_t wa, uint32_t remaining, uint32_t* hist, uint32_t* scan_buf, uint32_t* s_bin,
+    uint32_t* s_above, uint32_t* s_max, uint32_t* s_min, int32_t* op) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t mx = 0, mn = 0xffffffffu;
+  for (int i = tid; i < nc; i += kThreads) {
+    const uint32_t key = cand_key[i];
+    mx = max(mx, key);
+    mn = min(mn, key);
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  if (tid == 0) {
+    *s_max = 0;
+    *s_min = 0xffffffffu;
+  }
+  __syncthreads();
+  if (lane == 0) {
+    atomicMax(s_max, mx);
+    atomicMin(s_min, mn);
+  }
+  __syncthreads();
+  const uint32_t kmax = *s_max;
+  const uint32_t diff = kmax ^ *s_min;
+  uint32_t prefix = kmax;  // all candidates equal: tau is their key
+  bool whole = false;      // the last bin is taken whole: keys >= prefix are the chosen ones
+  if (diff != 0) {
+    int top = 31 - __clz(diff);
+    uint32_t mask = top == 31 ? 0u : ~((2u << top) - 1u);
+    prefix = kmax & mask;
 #pragma unroll 1
-  for (; round < 3; ++round) {
-    const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
-    const uint32_t nbins = round == 2 ? 1024u : 2048u;
-    for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < nc; i += kThreads) {
-      const uint32_t key = cand_key[i];
-      if ((key & prefix_mask) == prefix) atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
+    while (top >= 0) {
+      const int lo = max(top - 10, 0);
+      const uint32_t nbins = 1u << (top - lo + 1);
+      for (int i = tid; i < static_cast<int>(nbins); i += kThreads) hist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < nc; i += kThreads) {
+        const uint32_t key = cand_key[i];
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> lo) & (nbins - 1)], 1u);
+      }
+      __syncthreads();
+      uint32_t above;
+      const uint32_t bin = find_bin<kThreads>(hist, nbins, remaining, scan_buf, s_bin, s_above, &above);
+      const uint32_t cnt = hist[bin];
+      __syncthreads();  // hist is cleared by the next digit
+      prefix |= bin << lo;
+      mask |= (nbins - 1) << lo;
+      remaining -= above;
+      if (cnt == remaining) {
+        whole = true;
+        break;
+      }
+      top = lo - 1;
     }
-    __syncthreads();
-    const uint32_t bin = find_bin(hist, nbins, remaining, scan_buf, s_bin, s_above, &above);
-    prefix |= bin << shift;
-    prefix_mask |= (nbins - 1) << shift;
-    remaining -= above;
   }
   const uint32_t tau = prefix;
-  const uint32_t take_eq = remaining;
+  const uint32_t take_eq = whole ? 0u : remaining;
   for (int i = tid; i < nc; i += kThreads) {
     const uint32_t key = cand_key[i];
     const int64_t off = cand_col[i] - wa;
-    if (key > tau) atomicOr(&sel[off >> 5], 1u << (off & 31));
+    if (whole ? key >= tau : key > tau) atomicOr(&sel[off >> 5], 1u << (off & 31));
     else if (key == tau) atomicOr(&tie[off >> 5], 1u << (off & 31));
   }
   __syncthreads();
@@ -239,7 +327,7 @@ __device__ __forceinline__ void select_candidates_and_write(
     ntie += __popc(tie[w]);
   }
   uint32_t tot;
-  const uint32_t ex = block_excl_sum(nsel | (ntie << 16), scan_buf, &tot);
+  const uint32_t ex = block_excl_sum<kThreads>(nsel | (ntie << 16), scan_buf, &tot);
   uint32_t sel_before = ex & 0xffffu, tie_before = ex >> 16;
   for (int w = w0; w < w1; ++w) {
     uint32_t ms = sel[w], mt = tie[w];
@@ -260,11 +348,15 @@ __device__ __forceinline__ void select_candidates_and_write(
   }
 }
 
-template <typename LT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename LT, typename C>
+__global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
     topk_kernel(const LT* __restrict__ logits, int64_t stride, const int32_t* __restrict__ starts,
                 const int32_t* __restrict__ ends, int32_t k, int32_t* __restrict__ out,
                 int64_t out_stride, int32_t* status) {
+  constexpr int kThreads = C::kThreads, kWarps = C::kWarps;
+  constexpr int kFastMaxCols = C::kFastMaxCols, kCandCap = C::kCandCap;
+  constexpr int kOffHist = C::kOffHist, kOffSel = C::kOffSel, kOffTie = C::kOffTie;
+  constexpr int kOffCandKey = C::kOffCandKey, kOffCandCol = C::kOffCandCol, kOffStage = C::kOffStage;
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
   uint32_t* sel = reinterpret_cast<uint32_t*>(smem + kOffSel);
@@ -272,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* cand_key = reinterpret_cast<uint32_t*>(smem + kOffCandKey);
   int32_t* cand_col = reinterpret_cast<int32_t*>(smem + kOffCandCol);
   __shared__ uint32_t scan_buf[kWarps];
-  __shared__ uint32_t s_bin, s_above, s_ncand;
+  __shared__ uint32_t s_bin, s_above, s_ncand, s_max, s_min;
   __shared__ uint32_t s_wcount[kWarps];
 
   const int row = blockIdx.x;
@@ -319,10 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       sel[i] = 0;
       tie[i] = 0;
     }
-    if (tid < kWarps) s_wcount[tid] = 0;
     const int ns = 4 * nsq;
     const int64_t want = sv == 1 ? k : (3 * static_cast<int64_t>(k)) / (2 * sv) + 16;
-    uint32_t t = 0;
+    uint32_t t = 0;  // stays 0 (every key) if the sample is not larger than want
     if (want < ns) {
       uint32_t prefix = 0, prefix_mask = 0, remaining = static_cast<uint32_t>(want);
 #pragma unroll 1
@@ -335,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((key & prefix_mask) == prefix) atomicAdd(&hist[(key >> shift) & 2047u], 1u);
         }
         __syncthreads();
-        const uint32_t bin = find_bin(hist, 2048, remaining, scan_buf, &s_bin, &s_above, &above);
+        const uint32_t bin = find_bin<kThreads>(hist, 2048, remaining, scan_buf, &s_bin, &s_above, &above);
         prefix |= bin << shift;
         prefix_mask |= 2047u << shift;
         remaining -= above;
@@ -343,12 +434,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       t = prefix;
     }
     __syncthreads();
-    // ---- one pass over the row: keys >= t become candidates.  Each warp
-    // appends to its own slice of the candidate arrays (its own counter, so
-    // only lanes of one warp ever contend); the slices are packed afterwards.
+    // ---- one pass over the row: keys >= t become candidates.  The scores
+    // are compared with t's float form; only candidates are turned into keys.
+    // t >= 1 leaves out NaN scores (key 0): if fewer than k keys then reach
+    // t, the exact passes below run.  Each warp appends to its own slice of
+    // the candidate arrays, its count held in a register (a ballot per key
+    // position places the lanes' candidates, no shared atomics); the slices
+    // are packed afterwards.
+    t = max(t, 1u);
+    const float tf = key_floor(t);
     constexpr int kWarpCap = kCandCap / kWarps;
     uint32_t* wkey = cand_key + warp * kWarpCap;  // this warp's slice, packed later
     int32_t* wcol = reinterpret_cast<int32_t*>(smem + kOffStage) + warp * kWarpCap;
+    const uint32_t lanes_below = (1u << lane) - 1u;
+    uint32_t wcount = 0;  // candidates this warp has seen (the same in every lane)
     constexpr int64_t kStep = 4 * static_cast<int64_t>(kThreads) * kLoadsInFlight;
     for (int64_t base = a4; base < b; base += kStep) {
       typename Vec4<LT>::T v[kLoadsInFlight];
@@ -360,26 +459,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < kLoadsInFlight; ++u) {
         const int64_t i = base + 4 * (tid + static_cast<int64_t>(u) * kThreads);
-        if (i >= b) continue;
-        uint32_t kq[4];
+        float xq[4];
         if (i + 3 < b && i >= a) {
-          Vec4<LT>::keys(v[u], kq);
+          Vec4<LT>::vals(v[u], xq);
         } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) kq[e] = (i + e >= a && i + e < b) ? order_key(load_score<LT>(rp, i + e)) : 0u;
+          for (int e = 0; e < 4; ++e) xq[e] = (i + e >= a && i + e < b) ? load_score<LT>(rp, i + e) : __int_as_float(0x7fffffff);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          if (kq[e] >= t && i + e >= a && i + e < b) {
-            const uint32_t slot = atomicAdd(&s_wcount[warp], 1u);
+          const bool c = xq[e] >= tf;
+          const uint32_t m = __ballot_sync(0xffffffffu, c);
+          if (c) {
+            const uint32_t slot = wcount + __popc(m & lanes_below);
             if (slot < static_cast<uint32_t>(kWarpCap)) {
-              wkey[slot] = kq[e];
+              wkey[slot] = order_key(xq[e]);
               wcol[slot] = static_cast<int32_t>(i + e);
             }
           }
+          wcount += __popc(m);
         }
       }
     }
+    if (lane == 0) s_wcount[warp] = wcount;
     __syncthreads();
     // pack the slices: cand_key in place (slices only move down), columns
     // from the ring area into cand_col
@@ -418,8 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     const uint32_t nc = s_ncand;
     if (nc >= static_cast<uint32_t>(k) && nc <= static_cast<uint32_t>(kCandCap)) {
-      select_candidates_and_write(cand_key, cand_col, static_cast<int>(nc), sel, tie, nwords, wa, 0u, 0u,
-                                  static_cast<uint32_t>(k), 0, hist, scan_buf, &s_bin, &s_above, op);
+      select_candidates_and_write<kThreads>(cand_key, cand_col, static_cast<int>(nc), sel, tie, nwords, wa,
+                                            static_cast<uint32_t>(k), hist, scan_buf, &s_bin, &s_above, &s_max,
+                                            &s_min, op);
       return;
     }
     __syncthreads();  // the sample missed (rare): exact passes below
@@ -428,13 +531,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- pass 1: top 11 key bits
   for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
   __syncthreads();
-  for_each_quad<LT>(rp, a, b, [&](int64_t, const uint32_t (&kq)[4], uint32_t valid) {
+  for_each_quad<kThreads, LT>(rp, a, b, [&](int64_t, const uint32_t (&kq)[4], uint32_t valid) {
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       if ((valid >> e) & 1u) atomicAdd(&hist[kq[e] >> 21], 1u);
   });
   __syncthreads();
-  const uint32_t b1 = find_bin(hist, 2048, static_cast<uint32_t>(k), scan_buf, &s_bin, &s_above, &above);
+  const uint32_t b1 = find_bin<kThreads>(hist, 2048, static_cast<uint32_t>(k), scan_buf, &s_bin, &s_above, &above);
   uint32_t remaining = static_cast<uint32_t>(k) - above;
   const uint32_t c1 = hist[b1];
   __syncthreads();
@@ -448,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) s_ncand = 0;
     __syncthreads();
     // ---- pass 2: mark keys above the bin, collect the bin's candidates
-    for_each_quad<LT>(rp, a, b, [&](int64_t i, const uint32_t (&kq)[4], uint32_t valid) {
+    for_each_quad<kThreads, LT>(rp, a, b, [&](int64_t i, const uint32_t (&kq)[4], uint32_t valid) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         if (!((valid >> e) & 1u)) continue;
@@ -467,8 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     });
     __syncthreads();
     const int nc = min(static_cast<int>(s_ncand), kCandCap);
-    select_candidates_and_write(cand_key, cand_col, nc, sel, tie, nwords, wa, b1 << 21, 0x7ffu << 21,
-                                remaining, 1, hist, scan_buf, &s_bin, &s_above, op);
+    select_candidates_and_write<kThreads>(cand_key, cand_col, nc, sel, tie, nwords, wa, remaining, hist, scan_buf,
+                                          &s_bin, &s_above, &s_max, &s_min, op);
     return;
   }
 
@@ -481,14 +584,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t nbins = pass == 0 ? 2048u : 1024u;
     for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
     __syncthreads();
-    for_each_quad<LT>(rp, a, b, [&](int64_t, const uint32_t (&kq)[4], uint32_t valid) {
+    for_each_quad<kThreads, LT>(rp, a, b, [&](int64_t, const uint32_t (&kq)[4], uint32_t valid) {
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         if (((valid >> e) & 1u) && (kq[e] & prefix_mask) == prefix)
           atomicAdd(&hist[(kq[e] >> shift) & (nbins - 1)], 1u);
     });
     __syncthreads();
-    const uint32_t bin = find_bin(hist, nbins, remaining, scan_buf, &s_bin, &s_above, &above);
+    const uint32_t bin = find_bin<kThreads>(hist, nbins, remaining, scan_buf, &s_bin, &s_above, &above);
     prefix |= bin << shift;
     prefix_mask |= (nbins - 1) << shift;
     remaining -= above;
@@ -511,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t packed =
         static_cast<uint32_t>(__popc(gt_bits)) | (static_cast<uint32_t>(__popc(eq_bits)) << 16);
     uint32_t tot;
-    const uint32_t ex = block_excl_sum(packed, scan_buf, &tot);
+    const uint32_t ex = block_excl_sum<kThreads>(packed, scan_buf, &tot);
     uint32_t gt_before = gt_run + (ex & 0xffffu);
     uint32_t eq_before = eq_run + (ex >> 16);
 #pragma unroll
@@ -729,6 +832,18 @@ __global__ void __launch_bounds__(kShortThreads, kCols <= 8192 ? 4 : 3)
   }
 }
 
+template <typename LT, typename C>
+cudaError_t launch_long(const void* logits, int64_t stride, const int32_t* starts, const int32_t* ends,
+                        int32_t num_rows, int32_t k, int32_t* out, int64_t out_stride, int32_t* status,
+                        cudaStream_t stream) {
+  const cudaError_t e =
+      cudaFuncSetAttribute(topk_kernel<LT, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  topk_kernel<LT, C><<<num_rows, C::kThreads, C::kSmemBytes, stream>>>(static_cast<const LT*>(logits), stride,
+                                                                       starts, ends, k, out, out_stride, status);
+  return cudaGetLastError();
+}
+
 template <typename LT, int kCols>
 cudaError_t launch_short(const void* logits, int64_t stride, const int32_t* starts, const int32_t* ends,
                          int32_t num_rows, int32_t k, int32_t* out, int64_t out_stride, cudaStream_t stream) {
@@ -759,23 +874,22 @@ cudaError_t launch_top_k(const void* logits, int32_t logits_dtype, int64_t logit
                                                     out_idx, out_stride, stream)
                : launch_short<float, 16384>(logits, logits_stride, row_starts, row_ends, num_rows, k, out_idx,
                                             out_stride, stream);
-  cudaError_t e;
-  if (logits_dtype == DSA_LOGITS_BF16) {
-    e = cudaFuncSetAttribute(topk_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
-    if (e != cudaSuccess) return e;
-    topk_kernel<__nv_bfloat16><<<num_rows, kThreads, kSmemBytes, stream>>>(
-        static_cast<const __nv_bfloat16*>(logits), logits_stride, row_starts, row_ends, k, out_idx,
-        out_stride, status);
-  } else {
-    e = cudaFuncSetAttribute(topk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
-    if (e != cudaSuccess) return e;
-    topk_kernel<float><<<num_rows, kThreads, kSmemBytes, stream>>>(static_cast<const float*>(logits),
-                                                                    logits_stride, row_starts,
-                                                                    row_ends, k, out_idx, out_stride, status);
-  }
-  return cudaGetLastError();
+  // long rows: one row per SM, or two where the grid has more rows than the
+  // device has SMs and every row fits the half geometry
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const bool half = num_rows > sms && logits_stride <= HalfCfg::kFastMaxCols;
+  if (logits_dtype == DSA_LOGITS_BF16)
+    return half ? launch_long<__nv_bfloat16, HalfCfg>(logits, logits_stride, row_starts, row_ends, num_rows, k,
+                                                      out_idx, out_stride, status, stream)
+                : launch_long<__nv_bfloat16, WideCfg>(logits, logits_stride, row_starts, row_ends, num_rows, k,
+                                                      out_idx, out_stride, status, stream);
+  return half ? launch_long<float, HalfCfg>(logits, logits_stride, row_starts, row_ends, num_rows, k, out_idx,
+                                            out_stride, status, stream)
+              : launch_long<float, WideCfg>(logits, logits_stride, row_starts, row_ends, num_rows, k, out_idx,
+                                            out_stride, status, stream);
 }
 
 }  // namespace dsa

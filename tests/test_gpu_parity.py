@@ -297,6 +297,35 @@ def test_topk_sampled_path_boundary(dtype):
     assert np.array_equal(got, oracle.top_k_per_row(x2.float().cpu().double().numpy(), ends2, 2048))
 
 
+@pytest.mark.parametrize("C", [40000, 131072, 131080])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_topk_more_rows_than_sms(C, dtype):
+    """More rows than SMs with strides up to 2^17 take the two-rows-per-SM
+    geometry (2^17 + 8 keeps the one-row geometry): special rows as in the
+    short-row test, plus rows of random lengths up to the stride."""
+    S = dsa.device_num_sms()
+    R = S + 48
+    g = torch.Generator().manual_seed(C + R)
+    x = torch.randn((R, C), generator=g)
+    x[1] = torch.round(x[1] * 2)           # heavy ties: the sample's candidates overflow
+    x[2, C // 3:] = float("-inf")
+    x[3, ::9] = float("nan")
+    x[4] = 0.0
+    x[4, ::2] = -0.0
+    x[5, :] = torch.arange(C, dtype=torch.float32)
+    x[12] = 1.5                            # every key equal
+    x[13, :] = torch.randn(C, generator=g) * 1e-30
+    x = x.to(dtype).cuda()
+    ends = torch.randint(0, C + 1, (R,), generator=g, dtype=torch.int32)
+    ends[:14] = torch.tensor([C, C, C, C, C, C, 1, 0, 2047, 2049, C - 3, 17, C, C], dtype=torch.int32)
+    starts = torch.randint(0, 4000, (R,), generator=g, dtype=torch.int32)
+    starts[:14] = torch.tensor([0, 3, 0, 7, 0, 1000, 0, 0, 0, 0, 5, 0, 2, 0], dtype=torch.int32)
+    host = x.float().cpu().double().numpy()
+    for k in (7, 2048):
+        got = dsa.top_k_per_row(x, starts.cuda(), ends.cuda(), k).cpu().numpy()
+        assert np.array_equal(got, oracle.top_k_per_row(host, ends, k, row_starts=starts)), k
+
+
 # ---------------------------------------------------------------- FP4 keys (e2m1 + e4m3/16 + fp32/token)
 
 @pytest.mark.parametrize("logits_dtype", [W.LOGITS_F32, W.LOGITS_BF16])
