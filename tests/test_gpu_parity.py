@@ -315,11 +315,18 @@ def test_topk_more_rows_than_sms(C, dtype):
     x[5, :] = torch.arange(C, dtype=torch.float32)
     x[12] = 1.5                            # every key equal
     x[13, :] = torch.randn(C, generator=g) * 1e-30
+    x[14, ::37] = float("inf")             # +inf among finite scores
+    x[15, :] = torch.randn(C, generator=g) * 1e-39   # subnormal fp32 magnitudes
+    x[16, :] = float("nan")                # NaN-dominated: the sample threshold falls to NaN
+    x[16, ::13] = torch.randn(C // 13 + 1, generator=g)[: x[16, ::13].numel()]
+    x[17, :] = float("-inf")               # -inf everywhere but a few columns
+    x[17, ::501] = torch.randn(x[17, ::501].numel(), generator=g)
     x = x.to(dtype).cuda()
     ends = torch.randint(0, C + 1, (R,), generator=g, dtype=torch.int32)
-    ends[:14] = torch.tensor([C, C, C, C, C, C, 1, 0, 2047, 2049, C - 3, 17, C, C], dtype=torch.int32)
+    ends[:18] = torch.tensor([C, C, C, C, C, C, 1, 0, 2047, 2049, C - 3, 17, C, C, C, C, C, C],
+                             dtype=torch.int32)
     starts = torch.randint(0, 4000, (R,), generator=g, dtype=torch.int32)
-    starts[:14] = torch.tensor([0, 3, 0, 7, 0, 1000, 0, 0, 0, 0, 5, 0, 2, 0], dtype=torch.int32)
+    starts[:18] = torch.tensor([0, 3, 0, 7, 0, 1000, 0, 0, 0, 0, 5, 0, 2, 0, 0, 9, 0, 1], dtype=torch.int32)
     host = x.float().cpu().double().numpy()
     for k in (7, 2048):
         got = dsa.top_k_per_row(x, starts.cuda(), ends.cuda(), k).cpu().numpy()
