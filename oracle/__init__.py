@@ -33,7 +33,7 @@ ORACLE_ERR_STRIDE = 6
 # the schedule rule's constants (the metadata call's tile and grouping sizes)
 TILE_TOKENS = 128
 GROUP_MAX_ROWS = 8
-TILE_WEIGHT = 6
+TILE_WEIGHT = 7
 ROW_WEIGHT = 5
 
 

@@ -15,12 +15,15 @@ constexpr int kPageTokens = DSA_BLOCK_KV;   // 64 tokens per page
 
 // Schedule rule: a tile is two pages (128 keys, the M of one MMA); runs of
 // equal request ids are cut into groups of at most kGroupMaxRows rows; every
-// tile of group g weighs kTileWeight + kRowWeight * rows(g), the measured
-// ratio of a tile's fixed cost (K stream, MMA issue) to the cost of each
-// (tile, row) pair it carries (MMA columns, epilogue).
+// tile of group g weighs kTileWeight + kRowWeight * rows(g): a tile's fixed
+// cost (K stream, MMA issue) against the cost of each (tile, row) pair it
+// carries (MMA columns, epilogue).  An SM of 1-row groups is bound by its K
+// stream and one of 6-row groups by its epilogue, so the ratio is the one
+// that measured fastest across both (7:5 against 6:5, 4:3, 3:2, 8:5, 2:1 on
+// the 40-request varlen FP8 and FP4 workloads).
 constexpr int kTileTokens = 128;
 constexpr int kGroupMaxRows = 8;
-constexpr int kTileWeight = 6;
+constexpr int kTileWeight = 7;
 constexpr int kRowWeight = 5;
 constexpr int32_t kScheduleMagic = 0x44534131;
 constexpr int kScheduleHeaderWords = 8;
