@@ -222,8 +222,11 @@ int dsa_mxfp4_paged_mqa_logits(const void* q, const void* q_scale, const void* k
  *   k            1 .. DSA_MAX_TOPK.
  *   out_idx      (device) int32 [num_rows][out_stride], out_stride >= k:
  *                the chosen columns in ascending order, then -1 up to k.
+ *   status       (device) int32 or NULL: the selection has no device-side
+ *                fault to report and never writes it.
  * Order: larger logit first; equal logits go to the lower column; -0 == +0;
- * NaN ranks below every number.
+ * NaN ranks below every number.  Needs no workspace: each row's working set
+ * lives in its CTA's shared memory.
  */
 int dsa_top_k_per_row(const void* logits, int32_t logits_dtype, int64_t logits_stride,
                       const int32_t* row_starts, const int32_t* row_ends, int32_t num_rows,
