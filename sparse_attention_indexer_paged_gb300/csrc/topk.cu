@@ -384,8 +384,8 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
   const int nwords = static_cast<int>((b - wa + 31) >> 5);
   const int lane = tid & 31, warp = tid >> 5;
   uint32_t above;
-  // the sampled path streams the row with 16-byte bulk copies: rows must
-  // start on 16 bytes and the rounded-up end stay inside the row stride
+  // the sampled path reads whole 4-column groups as one vector load (16
+  // bytes of fp32, 8 of bf16): every row must start on a 16-byte boundary
   if (b - wa <= kFastMaxCols && stride % (16 / static_cast<int64_t>(sizeof(LT))) == 0) {
     // ---- sampled threshold: every sv-th 4-column group, at most kSampleQuads
     // groups; the sample's ks-th largest key, rounded down to its top 22
@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
     }
     const int ns = 4 * nsq;
     const int64_t want = sv == 1 ? k : (3 * static_cast<int64_t>(k)) / (2 * sv) + 16;
-    uint32_t t = 0;  // stays 0 (every key) if the sample is not larger than want
+    uint32_t t = 0;  // stays 0 if the sample is not larger than want: every non-NaN score qualifies
     if (want < ns) {
       uint32_t prefix = 0, prefix_mask = 0, remaining = static_cast<uint32_t>(want);
 #pragma unroll 1
