@@ -476,7 +476,7 @@ def run_ours(args, rank, world, local):
         "unit": "us/step",
         "n_gpus": world,
         "steps": K,
-        "warmup": args.warmup,
+        "warmup": max(args.warmup, 3),  # warm-ups actually run
         "ms_per_step": round(ms_step, 6),
         "higher_is_better": False,
         "scaling": "weak",
@@ -643,7 +643,7 @@ def run_dcp(args, local):
         "higher_is_better": False,
         "n_gpus": 1,
         "steps": K,
-        "warmup": args.warmup,
+        "warmup": max(args.warmup, 3),  # warm-ups actually run
         "dtype": "e4m3 x e4m3 -> f32" if glob.kv_format == 0 else "e4m3 x e2m1 -> f32",
         "data": "synthetic",
         "config": {"workload": f"{args.workload} split over {R} DCP ranks (interleave {inter})",
@@ -738,7 +738,7 @@ def run_prefill(args, local):
         "higher_is_better": False,
         "n_gpus": 1,
         "steps": K,
-        "warmup": args.warmup,
+        "warmup": max(args.warmup, 3),  # warm-ups actually run
         "dtype": "e4m3 x e4m3 -> f32" if pf.kv_format == 0 else "e4m3 x e2m1 -> f32",
         "data": "synthetic",
         "config": {"workload": "prefill: 2 requests x 8192-token prompts, their last 4096 tokens as rows "
@@ -813,7 +813,7 @@ def run_chunked(args, local):
         "higher_is_better": False,
         "n_gpus": 1,
         "steps": args.steps,
-        "warmup": args.warmup,
+        "warmup": max(args.warmup, 3),  # warm-ups actually run
         "dtype": "e4m3 x e4m3 -> f32" if wl.kv_format == 0 else "e4m3 x e2m1 -> f32",
         "data": "synthetic",
         "config": {"workload": args.workload, "shape": workload_desc(args.workload, wl), "rows": T,
