@@ -2,7 +2,8 @@
 for: request counts, context ranges, rows per request and their causal
 limits (every named workload, without building its key pool), and the paging
 and quantisation recipe on small builds (block tables, poisoned unused pages,
-per-token e4m3 key scales, e4m3 queries, head weights ~ N(0, 1) / sqrt(H))."""
+per-token e4m3 key scales, e4m3 queries, head weights ~ N(0, 1) / sqrt(H)),
+and the FP4 and MXFP4 quantisers against the error bounds of their formats."""
 import math
 
 import pytest
@@ -97,3 +98,54 @@ def test_builds_are_seeded():
     for f in ("q", "weights", "block_table", "kv_cache"):
         assert torch.equal(getattr(a, f), getattr(b, f)), f
     assert not torch.equal(a.kv_cache, c.kv_cache)
+
+
+def _e2m1(codes):
+    mag = torch.tensor([0, 0.5, 1, 1.5, 2, 3, 4, 6], dtype=torch.float32)[(codes & 7).long()]
+    return torch.where((codes & 8) != 0, -mag, mag)
+
+
+def _unpack(packed):
+    lo, hi = packed & 0xF, packed >> 4                # element 2i is the low nibble of byte i
+    return torch.stack((lo, hi), dim=-1).flatten(-2)
+
+
+def test_fp4_quantiser_invariants():
+    g0 = torch.Generator().manual_seed(21)
+    k = torch.randn((257, W.HEAD_DIM), generator=g0) * torch.rand((257, 1), generator=g0) * 5
+    k[3] = 0.0                                        # an all-zero token
+    k[4, :16] = 0.0                                   # an all-zero block
+    packed, bs, g = W.quantize_keys_fp4(k)
+    assert packed.shape == (257, W.HEAD_DIM // 2) and bs.shape == (257, W.HEAD_DIM // 16)
+    amax = k.abs().amax(dim=-1)
+    assert float(g[3]) == 1.0
+    nz = amax > 0
+    assert torch.allclose(g[nz] * 448.0 * 6.0, amax[nz], rtol=1e-6)
+    bsv = W.e4m3_decode(bs)                           # per-16 block scales, e4m3
+    codes = _e2m1(_unpack(packed)).view(257, -1, 16)
+    step = bsv * g[:, None]                           # one block's unit
+    deq = codes * step[..., None]
+    err = (deq - k.view(257, -1, 16)).abs()
+    assert (err <= step[..., None] + 1e-30).all()     # within one unit: half the widest e2m1 gap
+    bmax = k.view(257, -1, 16).abs().amax(dim=-1)
+    live = bmax > 0
+    assert (codes.abs().amax(dim=-1)[live] == 6.0).all()   # each block's largest element saturates the code range
+    assert (codes[4, 0] == 0).all() and (codes[3] == 0).all()
+
+
+def test_mxfp4_quantiser_invariants():
+    g0 = torch.Generator().manual_seed(22)
+    x = torch.randn((9, 5, W.HEAD_DIM), generator=g0) * 3
+    x[0, 0, :32] = 0.0                                # an all-zero block
+    packed, sc = W.quantize_mxfp4(x)
+    assert packed.shape == (9, 5, W.HEAD_DIM // 2) and sc.shape == (9, 5, W.HEAD_DIM // 32)
+    blocks = x.view(9, 5, -1, 32)
+    amax = blocks.abs().amax(dim=-1)
+    live = amax > 0
+    want = torch.floor(torch.log2(amax[live])) - 2 + 127
+    assert torch.equal(sc[live].float(), want) and int(sc[0, 0, 0]) == 127
+    scale = torch.exp2(sc.float() - 127)
+    codes = _e2m1(_unpack(packed)).view(9, 5, -1, 32)
+    err = (codes * scale[..., None] - blocks).abs()
+    assert (err <= 2 * scale[..., None]).all()        # saturation at 6 of a block max in [4, 8) units
+    assert (codes[0, 0, 0] == 0).all()
