@@ -53,7 +53,8 @@ typedef enum {
   DSA_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
   DSA_ERR_BAD_BLOCK = 5,         /* (device) page id outside [0, num_pages) or past the table */
   DSA_ERR_TIMEOUT = 6,           /* (device) a pipeline wait ran out; the kernel returned early */
-  DSA_ERR_NO_DEVICE = 7          /* no usable sm_103 device */
+  DSA_ERR_NO_DEVICE = 7,         /* no usable sm_103 device */
+  DSA_ERR_SCRATCH_TOO_SMALL = 8  /* the step needs more than the library's fixed scratch array holds */
 } dsa_status_t;
 
 enum { DSA_KV_FP8 = 0, DSA_KV_FP4 = 1, DSA_KV_MXFP4 = 2 };
@@ -400,6 +401,51 @@ int dsa_indexer_decode_topk(const void* q, const void* q_scale, const void* kv_c
                             void* logits_scratch, int64_t scratch_bytes, int32_t* schedule,
                             int64_t schedule_words, int32_t k, int32_t* out_idx, int64_t out_stride,
                             int32_t* status, dsa_stream_t stream);
+
+/* Sizes of the fixed device scratch array of dsa_indexer_decode_topk_static:
+   schedule words, then logits bytes (8 MiB + 64 KiB in all, held by every GPU
+   that loads the library until the process exits). */
+#define DSA_STATIC_SCHEDULE_WORDS 16384
+#define DSA_STATIC_LOGITS_BYTES 8388608
+
+/*
+ * dsa_indexer_decode_topk_static - dsa_indexer_decode_topk for callers that
+ * cannot allocate device memory.  The pages have no counterpart: it exists
+ * for code that runs where cudaMalloc is not allowed or not available (inside
+ * an allocator's own callbacks, in a plugin whose framework owns every
+ * allocation and passes only the op's tensors, on a serving path whose memory
+ * is fixed after start-up).  Such a caller still passes every input and the
+ * output; the step's intermediate logits and its schedule live in a fixed
+ * array of the library's device image (DSA_STATIC_LOGITS_BYTES of logits,
+ * DSA_STATIC_SCHEDULE_WORDS of schedule), and the call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Arguments are those of dsa_indexer_decode_topk without the budget, scratch
+ * and schedule buffers.  The rows run in slices whose logits fit the array
+ * (the rule of dsa_decode_chunk_ranges with budget DSA_STATIC_LOGITS_BYTES);
+ * the top-k equals dsa_indexer_decode_topk's bit for bit.
+ *   DSA_ERR_SCRATCH_TOO_SMALL  when 16 rows of logits (all rows, if fewer)
+ *                              exceed DSA_STATIC_LOGITS_BYTES
+ *                              (logits_stride x 4 bytes a row for fp32, x 2
+ *                              for bf16), or a slice's schedule exceeds
+ *                              DSA_STATIC_SCHEDULE_WORDS; nothing is launched.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call on a device shares the one array and leaves its
+ * contents behind: nothing in it needs to start at zero (every word a call
+ * reads, that call wrote first), but calls whose work overlaps on the GPU (two
+ * streams, or two host threads on one device) race on it and must be ordered
+ * by the caller.
+ */
+int dsa_indexer_decode_topk_static(const void* q, const void* q_scale, const void* kv_cache,
+                                   int64_t page_stride_bytes, int64_t num_pages, int32_t kv_format,
+                                   const float* weights, const int32_t* context_lens,
+                                   const int32_t* block_table, int64_t block_table_stride,
+                                   const int32_t* indices, int32_t num_rows, int32_t num_heads,
+                                   int32_t head_dim, int32_t block_kv, int32_t num_sms,
+                                   int32_t logits_dtype, int64_t logits_stride, int32_t k,
+                                   int32_t* out_idx, int64_t out_stride, int32_t* status,
+                                   dsa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -55,6 +55,7 @@ DSA_ERR_CUDA = 4
 DSA_ERR_BAD_BLOCK = 5
 DSA_ERR_TIMEOUT = 6
 DSA_ERR_NO_DEVICE = 7
+DSA_ERR_SCRATCH_TOO_SMALL = 8
 
 KV_FP8 = 0
 KV_FP4 = 1
@@ -69,6 +70,9 @@ FP8_PAGE_BYTES = 8448
 FP4_PAGE_BYTES = 4864
 MXFP4_PAGE_BYTES = 4352
 MAX_TOPK = 2048
+# fixed device scratch of indexer_decode_topk_static
+STATIC_SCHEDULE_WORDS = 16384
+STATIC_LOGITS_BYTES = 8 << 20
 
 # C entry points and their argument types
 _P, _I32, _I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
@@ -95,6 +99,8 @@ _SIGS = {
     "dsa_indexer_decode_topk": ([_P, _P, _P, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _I32, _I32, _I32,
                                  _I32, _I32, _I32, _I64, _I64, _P, _I64, _P, _I64, _I32, _P, _I64,
                                  _P, _P], ctypes.c_int),
+    "dsa_indexer_decode_topk_static": ([_P, _P, _P, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _I32, _I32, _I32,
+                                        _I32, _I32, _I32, _I64, _I32, _P, _I64, _P, _P], ctypes.c_int),
 }
 EXPORTED = tuple(_SIGS)
 
@@ -367,6 +373,40 @@ def indexer_decode_topk(q, kv_cache, weights, context_lens, block_table, k, indi
         int(num_sms), int(logits_dtype), int(logits_stride), int(logits_budget), _ptr(scratch),
         int(scratch.numel() * scratch.element_size()), _ptr(schedule), int(schedule.numel()), int(k),
         _ptr(out), int(out.stride(0)), _ptr(status), _stream(device)), "indexer_decode_topk")
+    return out
+
+
+def indexer_decode_topk_static(q, kv_cache, weights, context_lens, block_table, k, indices=None,
+                               kv_format=KV_FP8, logits_dtype=LOGITS_F32, logits_stride=None, num_sms=None,
+                               out=None, status=None, page_stride=None, q_scale=None):
+    """indexer_decode_topk without any device allocation inside the library:
+    the step's logits and schedule live in the library's fixed device array
+    (STATIC_LOGITS_BYTES of logits), and the rows run in slices that fit it.
+    For callers that cannot allocate device memory; calls that overlap on the
+    GPU share that array and must be ordered by the caller.  Returns int32
+    [T, k] top-k columns (allocated here only when `out` is None)."""
+    device = q.device
+    T = int(q.shape[0])
+    if num_sms is None:
+        num_sms = device_num_sms()
+    ctx = _dev_i32(context_lens, device)
+    bt = _dev_i32(block_table, device)
+    ind = _dev_i32(indices, device)
+    if logits_stride is None:
+        mx = int(ctx.max().item()) if T else 0
+        logits_stride = max(BLOCK_KV, (mx + BLOCK_KV - 1) // BLOCK_KV * BLOCK_KV)
+    if out is None:
+        out = torch.empty((T, int(k)), dtype=torch.int32, device=device)
+    assert out.dtype == torch.int32 and out.stride(-1) == 1
+    qq = q.view(torch.uint8) if q.dtype != torch.uint8 else q
+    assert qq.is_contiguous() and weights.is_contiguous() and weights.dtype == torch.float32
+    assert kv_cache.dim() == 2 and kv_cache.stride(1) == 1
+    pstride = kv_cache.stride(0) if page_stride is None else int(page_stride)
+    _check(lib().dsa_indexer_decode_topk_static(
+        _ptr(qq), _ptr(q_scale), _ptr(kv_cache), pstride, int(kv_cache.shape[0]), int(kv_format), _ptr(weights),
+        _ptr(ctx), _ptr(bt), int(bt.stride(0)), _ptr(ind), T, NUM_HEADS, HEAD_DIM, BLOCK_KV,
+        int(num_sms), int(logits_dtype), int(logits_stride), int(k), _ptr(out), int(out.stride(0)),
+        _ptr(status), _stream(device)), "indexer_decode_topk_static")
     return out
 
 

@@ -15,7 +15,8 @@ CSRC = os.path.join(_PKG, "csrc")
 INCLUDE = os.path.join(_ROOT, "include")
 BUILD_DIR = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libdsa_indexer.so")
-SOURCES = ("api.cu", "metadata.cu", "logits.cu", "topk.cu", "selftest.cu", "dcp.cu", "decode_step.cu", "prefill.cu")
+SOURCES = ("api.cu", "metadata.cu", "logits.cu", "topk.cu", "selftest.cu", "dcp.cu", "decode_step.cu", "prefill.cu",
+           "decode_static.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -89,6 +89,7 @@ const char* dsa_status_string(int status) {
     case DSA_ERR_BAD_BLOCK: return "page id outside the pool or past the block table";
     case DSA_ERR_TIMEOUT: return "a pipeline wait ran out; the kernel returned early";
     case DSA_ERR_NO_DEVICE: return "no sm_103 device";
+    case DSA_ERR_SCRATCH_TOO_SMALL: return "the step needs more than the library's fixed scratch array holds";
     default: return "unknown status";
   }
 }
