@@ -85,7 +85,7 @@ const char* dsa_status_string(int status);
 int dsa_version(void);
 
 /* Number of int32 words of a schedule for `num_sms` SMs and `num_rows` rows:
-   8 + (num_sms + 1) + 2 * (num_rows + 1). */
+   8 + 2 * (num_sms + 1) + 5 * (num_rows + 1). */
 int64_t dsa_schedule_words(int32_t num_sms, int32_t num_rows);
 
 /* SM count of the current device (what the metadata call should balance
@@ -108,18 +108,27 @@ int32_t dsa_device_num_sms(void);
  *                Rows of one request must be adjacent ([PR56811] Purpose).
  *                NULL means every row is its own request (plain decode;
  *                equal to indices = arange(num_rows)).
- *   num_rows     >= 0.
+ *   num_rows     0 .. 2^24 - 1 (else DSA_ERR_UNSUPPORTED).
  *   block_kv     must be 64.
- *   num_sms      >= 1 (normally dsa_device_num_sms()); the logits call must
- *                be given the same value.
+ *   num_sms      1 .. 1023 (normally dsa_device_num_sms()); the logits call
+ *                must be given the same value.
  *   schedule     (device) int32 [dsa_schedule_words(num_sms, num_rows)], out.
  *
- * Rule: runs of equal ids are cut into groups of at most 8 rows; group g
- * covers ceil(max L_t / 128) tiles of 128 keys; a tile weighs 4 + rows(g);
- * SM i starts at the first tile whose preceding weight reaches i/num_sms of
- * the total.  Layout: header[8] = {0x44534131, num_rows, varlen flag,
- * num_sms, num_groups, num_tiles, 128, 8}, sm_start[num_sms + 1],
- * group_row_start[num_rows + 1], group_tile_start[num_rows + 1].
+ * Rule (the pages fix the purpose, not the split; this is the library's):
+ * runs of equal ids are cut into groups of at most 8 rows; a unit is one
+ * 128-key tile of a group (ceil(max L_t / 128) units per group) and costs its
+ * SM one K tile from HBM plus one (tile, row) pair of MMA and epilogue work
+ * per row.  The groups are ordered by row count (stable) and their units laid
+ * end to end; SM i takes units from both ends of that sequence, so that every
+ * SM owns floor or ceil of units / num_sms units and, as nearly as the group
+ * sizes allow, the same number of (tile, row) pairs.  Layout:
+ * header[8] = {0x44534132, num_rows, varlen flag, num_sms, num_groups,
+ * num_units, 128, 8}, left[num_sms + 1], right[num_sms + 1] (SM i owns sorted
+ * units [left[i], left[i+1]) and [right[i+1], right[i])),
+ * group_row_start[num_rows + 1], position[num_rows + 1] (first row of the
+ * group at sorted position k | its rows << 24), unit_start[num_rows + 1],
+ * pairs_before low and high words [num_rows + 1] each; entries past the last
+ * group hold num_rows, num_rows, num_units and the pair total.
  */
 int dsa_paged_mqa_logits_metadata(const int32_t* context_lens, const int32_t* indices,
                                   int32_t num_rows, int32_t block_kv, int32_t num_sms,
@@ -140,7 +149,10 @@ int dsa_paged_mqa_logits_metadata(const int32_t* context_lens, const int32_t* in
  *   FP8 keys: k[s, d] = e4m3 code; kscale[s] = the page's fp32 scale.
  *   FP4 keys: k[s, d] = e2m1 * e4m3 block scale of d / 16; kscale[s] = the
  *             page's fp32 token scale.
- *   Columns at or past round_up(L_t, 64) are not written.
+ *   Columns from round_up(L_t, 64) up to round_up(L_max, 64) (clipped to the
+ *   stride), L_max the largest causal limit of the row's group (up to 8
+ *   adjacent rows of one request), may also be written as -inf; columns past
+ *   that are not written.
  *
  *   q            (device) e4m3 [num_rows][64][128], 16-byte aligned.
  *   kv_cache     (device) page pool, 16-byte aligned; page p at

@@ -30,13 +30,6 @@ ORACLE_ERR_BLOCK_TABLE = 4
 ORACLE_ERR_BLOCK_ID = 5
 ORACLE_ERR_STRIDE = 6
 
-# the schedule rule's constants (the metadata call's tile and grouping sizes)
-TILE_TOKENS = 128
-GROUP_MAX_ROWS = 8
-TILE_WEIGHT = 7
-ROW_WEIGHT = 5
-
-
 def build(force: bool = False) -> str:
     """Compile the oracle with g++ (plain -O2, IEEE arithmetic)."""
     os.makedirs(_BUILD, exist_ok=True)
@@ -74,10 +67,6 @@ def lib():
             L.oracle_paged_mqa_logits.restype = ctypes.c_int
             L.oracle_top_k_per_row.argtypes = [P, i64, P, P, i32, i32, P, i64, i32]
             L.oracle_top_k_per_row.restype = ctypes.c_int
-            L.oracle_schedule.argtypes = [P, P, i32, i32, i32, i32, i32, i32, P]
-            L.oracle_schedule.restype = ctypes.c_int
-            L.oracle_schedule_words.argtypes = [i32, i32]
-            L.oracle_schedule_words.restype = i64
             L.oracle_dcp_global_id.argtypes = [i64, i32, i32, i32]
             L.oracle_dcp_global_id.restype = i64
             L.oracle_dcp_local_len.argtypes = [i64, i32, i32, i32]
@@ -182,34 +171,6 @@ def top_k_per_row(scores, row_ends, k, row_starts=None, nthreads=0):
     if st != ORACLE_OK:
         raise OracleError(st, "top_k_per_row")
     return out
-
-
-def schedule_words(num_sms: int, num_rows: int) -> int:
-    return int(lib().oracle_schedule_words(int(num_sms), int(num_rows)))
-
-
-def schedule(context_lens, indices, num_sms, tile_tokens=TILE_TOKENS,
-             group_max_rows=GROUP_MAX_ROWS, tile_weight=TILE_WEIGHT, row_weight=ROW_WEIGHT):
-    """The schedule words the metadata call must produce (int32 array)."""
-    cl = _np(context_lens, np.int32)
-    ind = _np(indices, np.int32)
-    T = cl.shape[0]
-    out = np.zeros(schedule_words(num_sms, T), dtype=np.int32)
-    st = lib().oracle_schedule(_ptr(cl), _ptr(ind), T, int(num_sms), int(tile_tokens),
-                               int(group_max_rows), int(tile_weight), int(row_weight), _ptr(out))
-    if st != ORACLE_OK:
-        raise OracleError(st, "schedule")
-    return out
-
-
-def parse_schedule(words, num_sms, num_rows):
-    """Split schedule words into (header, sm_start, group_row_start, group_unit_start)."""
-    w = np.asarray(words)
-    hdr = w[:8]
-    sm = w[8: 8 + num_sms + 1]
-    grs = w[8 + num_sms + 1: 8 + num_sms + 1 + num_rows + 1]
-    gus = w[8 + num_sms + 1 + num_rows + 1: 8 + num_sms + 1 + 2 * (num_rows + 1)]
-    return hdr, sm, grs, gus
 
 
 def workload_logits(wl, rows=None, with_bound=True, nthreads=0, out_cols=None):

@@ -368,103 +368,6 @@ int oracle_top_k_per_row(const double* scores, int64_t stride, const int32_t* ro
 }
 
 // ---------------------------------------------------------------------------
-// Work schedule (the metadata call: PR 47469 Purpose and Changes,
-// get_paged_mqa_logits_metadata(seq_lens, block_kv, num_sms, indices); its
-// output shape is [num_sms + 1, ...] per sparse_attn_indexer docs,
-// _varlen_decode_rows, which passes schedule.shape[0] - 1 back as num_sms).
-//
-// The pages fix the inputs and the purpose (balance (request, K-block) work
-// over the SMs, grouping consecutive equal request ids) but not the split
-// rule.  The rule the library's metadata call states, written out:
-//   1. runs  = maximal runs of consecutive rows with equal request id
-//              (indices == NULL: every row is its own run);
-//   2. groups = each run cut into consecutive pieces of at most
-//              group_max_rows rows;
-//   3. group g: n_g rows, Lmax_g = max causal limit of its rows (negative
-//      counts as 0), tiles_g = ceil(Lmax_g / tile_tokens), every tile weighs
-//      tile_weight + row_weight * n_g;
-//   4. units are the (group, tile) pairs in group-major order; P(u) = total
-//      weight of the units before u, W = P(U);
-//   5. SM i (0 <= i <= num_sms) starts at the smallest u with
-//      P(u) * num_sms >= i * W; SM i owns units [start_i, start_{i+1}).
-//
-// Layout written (int32): header[8] = {magic 0x44534131, num_rows,
-// varlen (indices != NULL), num_sms, num_groups, num_units, tile_tokens,
-// group_max_rows}, then sm_start[num_sms + 1], then
-// group_row_start[num_rows + 1] (entries past num_groups are unused and
-// written as num_rows), then group_unit_start[num_rows + 1] (entries past
-// num_groups written as num_units).
-// ---------------------------------------------------------------------------
-int oracle_schedule(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
-                    int32_t num_sms, int32_t tile_tokens, int32_t group_max_rows,
-                    int32_t tile_weight, int32_t row_weight, int32_t* out) {
-  if (num_rows < 0 || num_sms <= 0 || tile_tokens <= 0 || group_max_rows <= 0 ||
-      tile_weight < 0 || row_weight < 0 || tile_weight + row_weight < 1 || !out ||
-      (num_rows > 0 && !context_lens))
-    return ORACLE_ERR_ARG;
-  std::vector<int32_t> group_row_start;
-  for (int t = 0; t < num_rows; ++t) {
-    const bool new_run = (t == 0) || !indices || indices[t] != indices[t - 1];
-    if (new_run) {
-      group_row_start.push_back(t);
-    } else if (t - group_row_start.back() >= group_max_rows) {
-      group_row_start.push_back(t);
-    }
-  }
-  const int G = static_cast<int>(group_row_start.size());
-  group_row_start.push_back(num_rows);
-  std::vector<int64_t> tiles(G), weight(G);
-  for (int g = 0; g < G; ++g) {
-    int64_t lmax = 0;
-    for (int t = group_row_start[g]; t < group_row_start[g + 1]; ++t)
-      lmax = std::max<int64_t>(lmax, context_lens[t]);
-    tiles[g] = (lmax + tile_tokens - 1) / tile_tokens;
-    weight[g] = tile_weight + static_cast<int64_t>(row_weight) * (group_row_start[g + 1] - group_row_start[g]);
-  }
-  // enumerate units one by one with their prefix weights
-  std::vector<int64_t> unit_prefix;  // P(u) for u = 0..U
-  std::vector<int32_t> group_unit_start(G + 1, 0);
-  int64_t P = 0;
-  for (int g = 0; g < G; ++g) {
-    group_unit_start[g] = static_cast<int32_t>(unit_prefix.size());
-    for (int64_t j = 0; j < tiles[g]; ++j) {
-      unit_prefix.push_back(P);
-      P += weight[g];
-    }
-  }
-  const int64_t U = static_cast<int64_t>(unit_prefix.size());
-  group_unit_start[G] = static_cast<int32_t>(U);
-  unit_prefix.push_back(P);
-  const int64_t W = P;
-  int32_t* hdr = out;
-  hdr[0] = 0x44534131;
-  hdr[1] = num_rows;
-  hdr[2] = indices ? 1 : 0;
-  hdr[3] = num_sms;
-  hdr[4] = G;
-  hdr[5] = static_cast<int32_t>(U);
-  hdr[6] = tile_tokens;
-  hdr[7] = group_max_rows;
-  int32_t* sm_start = out + 8;
-  for (int i = 0; i <= num_sms; ++i) {
-    int64_t u = 0;
-    while (u < U && unit_prefix[u] * num_sms < static_cast<int64_t>(i) * W) ++u;
-    sm_start[i] = static_cast<int32_t>(u);
-  }
-  int32_t* grs = sm_start + num_sms + 1;
-  int32_t* gus = grs + num_rows + 1;
-  for (int g = 0; g <= num_rows; ++g) {
-    grs[g] = g <= G ? group_row_start[g] : num_rows;
-    gus[g] = g <= G ? group_unit_start[g] : static_cast<int32_t>(U);
-  }
-  return ORACLE_OK;
-}
-
-int64_t oracle_schedule_words(int32_t num_sms, int32_t num_rows) {
-  return 8 + (static_cast<int64_t>(num_sms) + 1) + 2 * (static_cast<int64_t>(num_rows) + 1);
-}
-
-// ---------------------------------------------------------------------------
 // DCP (decode context parallelism): each rank holds 1/world of every
 // request's keys and computes logits and a top-k over its shard; the ranks'
 // top-k candidates are merged into the global top-k (sparse_attn_indexer

@@ -98,8 +98,7 @@ int dsa_version(void) { return 100; }
 
 int64_t dsa_schedule_words(int32_t num_sms, int32_t num_rows) {
   if (num_sms < 1 || num_rows < 0) return -1;
-  return kScheduleHeaderWords + (static_cast<int64_t>(num_sms) + 1) +
-         2 * (static_cast<int64_t>(num_rows) + 1);
+  return SchedLayout(num_sms, num_rows).words;
 }
 
 int32_t dsa_device_num_sms(void) {
@@ -117,7 +116,7 @@ int dsa_paged_mqa_logits_metadata(const int32_t* context_lens, const int32_t* in
                                   int32_t* schedule, dsa_stream_t stream) {
   if (num_rows < 0 || num_sms < 1 || schedule == nullptr) return DSA_ERR_INVALID_ARG;
   if (num_rows > 0 && context_lens == nullptr) return DSA_ERR_INVALID_ARG;
-  if (num_sms > 1023) return DSA_ERR_UNSUPPORTED;
+  if (num_sms > 1023 || num_rows > kMaxScheduleRows) return DSA_ERR_UNSUPPORTED;
   if (block_kv != kPageTokens) return DSA_ERR_UNSUPPORTED;
   const int dev = check_device();
   if (dev != DSA_OK) return dev;

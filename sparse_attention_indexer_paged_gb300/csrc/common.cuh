@@ -13,20 +13,43 @@ constexpr int kHeads = DSA_NUM_HEADS;       // 64
 constexpr int kHeadDim = DSA_HEAD_DIM;      // 128
 constexpr int kPageTokens = DSA_BLOCK_KV;   // 64 tokens per page
 
-// Schedule rule: a tile is two pages (128 keys, the M of one MMA); runs of
-// equal request ids are cut into groups of at most kGroupMaxRows rows; every
-// tile of group g weighs kTileWeight + kRowWeight * rows(g): a tile's fixed
-// cost (K stream, MMA issue) against the cost of each (tile, row) pair it
-// carries (MMA columns, epilogue).  An SM of 1-row groups is bound by its K
-// stream and one of 6-row groups by its epilogue, so the ratio is the one
-// that measured fastest across both (7:5 against 6:5, 4:3, 3:2, 8:5, 2:1 on
-// the 40-request varlen FP8 and FP4 workloads).
+// Schedule: a tile is two pages (128 keys, the M of one MMA); runs of equal
+// request ids are cut into groups of at most kGroupMaxRows rows; a unit is
+// one tile of one group.  The metadata call orders the groups by row count,
+// lays their units end to end and gives SM i the units between its two
+// boundaries at both ends of that sequence (metadata.cu states the rule).
+//
+// Layout (int32 words):
+//   header[8] = {kScheduleMagic, rows T, varlen flag, SMs S, groups G,
+//                units U, kTileTokens, kGroupMaxRows}
+//   left[S + 1]   SM i owns sorted units [left[i], left[i + 1]) ...
+//   right[S + 1]  ... and [right[i + 1], right[i])
+//   grs[T + 1]    first row of group g (row order); entries past G hold T
+//   pos[T + 1]    sorted position k: first row of its group | rows << 24;
+//                 entries past G hold T
+//   sus[T + 1]    first unit of sorted position k; entries past G hold U
+//   spp_lo[T + 1], spp_hi[T + 1]  (tile, row) pairs before position k
 constexpr int kTileTokens = 128;
 constexpr int kGroupMaxRows = 8;
-constexpr int kTileWeight = 7;
-constexpr int kRowWeight = 5;
-constexpr int32_t kScheduleMagic = 0x44534131;
+constexpr int32_t kScheduleMagic = 0x44534132;
 constexpr int kScheduleHeaderWords = 8;
+constexpr int kPosRowsShift = 24;
+constexpr int32_t kPosRowMask = (1 << kPosRowsShift) - 1;
+constexpr int32_t kMaxScheduleRows = kPosRowMask;  // rows must fit the position words
+
+struct SchedLayout {
+  int64_t left, right, grs, pos, sus, spp_lo, spp_hi, words;
+  __host__ __device__ SchedLayout(int64_t S, int64_t T) {
+    left = kScheduleHeaderWords;
+    right = left + (S + 1);
+    grs = right + (S + 1);
+    pos = grs + (T + 1);
+    sus = pos + (T + 1);
+    spp_lo = sus + (T + 1);
+    spp_hi = spp_lo + (T + 1);
+    words = spp_hi + (T + 1);
+  }
+};
 
 // Device status codes (same values as dsa_status_t).
 constexpr int kErrScheduleMismatch = DSA_ERR_SCHEDULE_MISMATCH;

@@ -59,9 +59,9 @@ namespace {
 // the pair is read in two 32-column pieces.
 template <int kFmt> constexpr int kEpiWgOf = 4;
 template <int kFmt> constexpr int kThreadsOf = kFmt == DSA_KV_FP8 ? 640 : 768;
-template <int kFmt> constexpr int kPieceCols = kFmt == DSA_KV_FP8 ? 64 : 32;
 constexpr int kFp4Converters = 6;
 constexpr int kSlots = 8;  // 64-column TMEM slots; pair p of the CTA's stream uses slot p mod 8
+constexpr int kTileRing = 8;  // tiles whose "pairs in TMEM" barrier phases are tracked at once
 constexpr int kScaleStages = 16;   // key scale ring
 constexpr int kTmemCols = 512;
 constexpr int kPairCols = 64;      // 64 heads of one pair
@@ -121,12 +121,13 @@ template <int kFmt> struct Smem : Lay<kFmt> {
   static constexpr int kOffCtx = kOffW + 2 * kWBufFloats * 4;  // causal limits of the group's rows
   static constexpr int kOffRowF = kOffCtx + 2 * kGroupMaxRows * 4;  // MXFP4: q scale factor of each row
   static constexpr int kOffBar = kOffRowF + 2 * kGroupMaxRows * 4;
-  // barriers: kv_full[8], kv_empty[8], raw_full[2], raw_empty[2], sc_full[SS],
-  // sc_empty[SS], q_full, q_empty, w_full[2], w_empty[2], tm_full[2][4], tm_empty[2][4], mma_done
-  static constexpr int kNumBars = 2 * kMaxKStages + 2 * kMaxRawStages + 2 * kScaleStages + 2 + 4 + 16 + 1;
+  // barriers: kv_full[8], kv_empty[8], raw_full[2], raw_empty[2], q_full, q_empty,
+  // w_full[2], w_empty[2], tm_empty[8], mma_done, tile_ready[8]
+  static constexpr int kNumBars = 2 * kMaxKStages + 2 * kMaxRawStages + 2 + 4 + 8 + 1 + kTileRing;
   static constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemAddr + 4;
-  static constexpr int kBytes = kOffAbort + 4 + 1024;  // + alignment slack
+  static constexpr int kOffWalk = kOffAbort + 4;  // WalkRanges
+  static constexpr int kBytes = kOffWalk + 6 * 4 + 1024;  // + alignment slack
   static_assert(B::kOffQ % 1024 == 0 && B::kOffKv % 1024 == 0 && B::kKStageBytes % 1024 == 0,
                 "MMA tiles need 1024-byte alignment");
   static_assert(B::kOffRaw % 16 == 0 && B::kRawStageBytes % 16 == 0, "bulk copies need 16 bytes");
@@ -135,6 +136,7 @@ template <int kFmt> struct Smem : Lay<kFmt> {
   static_assert(kBytes <= 232448, "over the per-CTA shared memory limit");
 };
 static_assert(kSlots * kPairCols == kTmemCols, "TMEM slots");
+static_assert(Lay<DSA_KV_FP8>::kKStages == kTileRing, "FP8 tiles signal their pairs on the K stage's own barrier");
 static_assert(kFp4AHalfLo == (kTileTokens * 128) >> 4, "f16 K operand halves as laid out by the dequantising warps");
 static_assert(kPassRowsOf<DSA_KV_FP4> <= kMaxPassRows && kPassRowsOf<DSA_KV_MXFP4> <= kMaxPassRows &&
                   kRawStagesOf<DSA_KV_FP4> <= kMaxRawStages && kRawStagesOf<DSA_KV_MXFP4> <= kMaxRawStages,
@@ -177,87 +179,120 @@ __device__ __forceinline__ const int32_t* table_row(const Params& p, int row) {
 }
 
 struct Bars {
-  uint32_t kv_full, kv_empty, raw_full, raw_empty, sc_full, sc_empty, q_full, q_empty, w_full,
-      w_empty, tm_full, tm_empty, mma_done;
+  uint32_t kv_full, kv_empty, raw_full, raw_empty, q_full, q_empty, w_full,
+      w_empty, tm_empty, mma_done, tile_ready;
   __device__ uint32_t kvf(int s) const { return kv_full + 8 * s; }
   __device__ uint32_t kve(int s) const { return kv_empty + 8 * s; }
   __device__ uint32_t rwf(int s) const { return raw_full + 8 * s; }
   __device__ uint32_t rwe(int s) const { return raw_empty + 8 * s; }
-  __device__ uint32_t scf(int s) const { return sc_full + 8 * s; }
-  __device__ uint32_t sce(int s) const { return sc_empty + 8 * s; }
   __device__ uint32_t wf(int b) const { return w_full + 8 * b; }
   __device__ uint32_t we(int b) const { return w_empty + 8 * b; }
-  // TMEM slot s: filled by the MMA, drained by the warpgroup of the pair in it
-  __device__ uint32_t tf(uint32_t s) const { return tm_full + 8 * s; }
+  // TMEM slot s: drained by the warpgroup of the pair in it
+  // Tile i's pairs are in TMEM: one MMA commit per tile.  With 8 K stages
+  // (FP8) this is the stage's kv_empty barrier; the dequantising formats have
+  // 2 stages and a ring of their own, so that a warp waiting for tile i never
+  // finds the barrier already two phases on.
+  __device__ uint32_t tr(uint32_t i, bool own_ring) const {
+    return own_ring ? tile_ready + 8 * (i & (kTileRing - 1)) : kv_empty + 8 * (i & (kTileRing - 1));
+  }
   __device__ uint32_t te(uint32_t s) const { return tm_empty + 8 * s; }
 };
 
-// The CTA's walk over its units: groups in order, and the tiles [j0, j1) of
-// each group that belong to this CTA.  A group of n rows is walked as
-// ceil(n / kPassRows) row passes over the same tiles (one pass when
-// kPassRows = 8; the FP4 path uses passes of 4 rows so that its f16 copy of
-// the q rows fits next to a deep page ring).  Every role runs the same walk
-// with all 32 lanes of its warp: the lanes search the group table 32
-// entries at a time and read a group's causal limits in parallel.
+// The CTA's walk over its units: two ranges of the schedule's sorted unit
+// sequence (one from each end), and within them the groups in sorted order
+// with the tiles [j0, j1) of each group that belong to this CTA.  A group of
+// n rows is walked as ceil(n / kPassRows) row passes over the same tiles (one
+// pass when kPassRows = 8; the FP4 path uses passes of 4 rows so that its f16
+// copy of the q rows fits next to a deep page ring).  Every role runs the
+// same walk with all 32 lanes of its warp: the lanes search the unit starts
+// 32 entries at a time and read a group's causal limits in parallel.  The
+// schedule arrays are found from the kernel parameters on each call, so the
+// walk keeps no pointers in registers.
+// This CTA's two unit ranges and the sorted position where each starts,
+// resolved once per CTA (warp 0, before the roles start) into shared memory.
+struct WalkRanges {
+  int32_t u0[2], u1[2], k0[2];
+};
+
+// this CTA's units: [a0, a1) from the light end, [b0, b1) from the heavy end
+__device__ __forceinline__ void cta_ranges(const int32_t* sched, int S, int T, int& a0, int& a1, int& b0, int& b1) {
+  const SchedLayout L(S, T);
+  const int U = sched[5];
+  a0 = min(max(sched[L.left + blockIdx.x], 0), U);
+  a1 = min(max(sched[L.left + blockIdx.x + 1], a0), U);
+  b1 = min(max(sched[L.right + blockIdx.x], a1), U);
+  b0 = min(max(sched[L.right + blockIdx.x + 1], a1), b1);
+}
+
+// The largest sorted position k in [0, G) with sus[k] <= u (sus is
+// non-decreasing, sus[0] = 0), by the whole warp: each round narrows
+// [lo, hi) 32-fold.
+__device__ __forceinline__ int seek_position(const int32_t* sus, int G, int u, int lane) {
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) >> 5;
+    const int idx = lo + lane * step;
+    const bool le = idx < hi && __ldg(sus + idx) <= u;
+    const uint32_t m = __ballot_sync(0xffffffffu, le);
+    lo += (31 - __clz(m | 1u)) * step;
+    hi = min(hi, lo + step);
+  }
+  return lo;
+}
+
 template <int kPassRows>
 struct Walk {
-  const int32_t* grs;
-  const int32_t* gus;
-  const int32_t* ctx;
-  int G, T, u, u_end, g;
+  int G, k, u, u_end, range;
   int g_r0, g_n, pass, npass;  // current group and row pass
   // current pass: rows [r0, r0 + n) of the group's tiles [j0, j1)
   int r0, n, npages, j0, j1;
   int32_t lane_ctx;  // causal limit of row r0 + lane (lanes below n)
 
-  __device__ void start(const int32_t* grs_, const int32_t* gus_, const int32_t* ctx_, int G_,
-                        int T_, int u0, int u1, int lane) {
-    T = T_;
-    grs = grs_;
-    gus = gus_;
-    ctx = ctx_;
-    G = G_;
-    u = u0;
-    u_end = u1;
+  __device__ void start(const int32_t* sched, const WalkRanges* wr) {
+    G = sched[4];
+    range = 0;
+    u = wr->u0[0];
+    u_end = wr->u1[0];
+    k = wr->k0[0];
     pass = npass = 0;
-    // largest g in [0, G) with gus[g] <= u (gus is non-decreasing, gus[0] = 0):
-    // each round narrows [lo, hi) 32-fold, keeping gus[lo] <= u
-    int lo = 0, hi = G;
-    while (hi - lo > 1) {
-      const int step = (hi - lo + 31) >> 5;
-      const int idx = lo + lane * step;
-      const bool le = idx < hi && __ldg(gus + idx) <= u;
-      const uint32_t m = __ballot_sync(0xffffffffu, le);
-      lo += (31 - __clz(m | 1u)) * step;
-      hi = min(hi, lo + step);
-    }
-    g = lo;
   }
 
   // Loads the next row pass that holds units of this CTA; false when done.
-  __device__ bool next(int lane) {
-    if (pass + 1 < npass) {
+  __device__ bool next(const int32_t* sched, int S, int T, const int32_t* ctx, const WalkRanges* wr, int lane) {
+    constexpr bool kOnePass = kPassRows >= kGroupMaxRows;  // every group in one pass
+    if (!kOnePass && pass + 1 < npass) {
       ++pass;  // same group and tiles, next rows
     } else {
-      while (u < u_end && g < G && __ldg(gus + g + 1) <= u) ++g;
-      if (u >= u_end || g >= G) return false;
-      const int gu0 = __ldg(gus + g), gu1 = __ldg(gus + g + 1);
-      g_r0 = __ldg(grs + g);
-      g_n = __ldg(grs + g + 1) - g_r0;
-      if (g_r0 < 0 || g_n <= 0 || g_n > kGroupMaxRows || g_r0 + g_n > T) return false;
+      const SchedLayout L(S, T);
+      const int32_t* sus = sched + L.sus;
+      while (u < u_end && k < G && __ldg(sus + k + 1) <= u) ++k;
+      if (u >= u_end || k >= G) {
+        if (range != 0) return false;
+        range = 1;  // on to the second range
+        u = wr->u0[1];
+        u_end = wr->u1[1];
+        k = wr->k0[1];
+        while (u < u_end && k < G && __ldg(sus + k + 1) <= u) ++k;
+        if (u >= u_end || k >= G) return false;
+      }
+      const int s0 = __ldg(sus + k), s1 = __ldg(sus + k + 1);
+      const int32_t w = __ldg(sched + L.pos + k);
+      g_r0 = w & kPosRowMask;
+      g_n = static_cast<int>(static_cast<uint32_t>(w) >> kPosRowsShift);
+      if (g_n <= 0 || g_n > kGroupMaxRows || g_r0 + g_n > T) return false;
       int lmax = lane < g_n ? __ldg(ctx + g_r0 + lane) : 0;
 #pragma unroll
       for (int o = 4; o; o >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));  // lanes 0..7
       lmax = __shfl_sync(0xffffffffu, lmax, 0);
       npages = (lmax + kPageTokens - 1) / kPageTokens;  // of the whole group: every pass writes its columns
-      j0 = u - gu0;
-      j1 = min(gu1, u_end) - gu0;
-      u = gu0 + j1;
+      j0 = u - s0;
+      j1 = min(s1, u_end) - s0;
+      u = s0 + j1;
       pass = 0;
-      npass = (g_n + kPassRows - 1) / kPassRows;
+      npass = kOnePass ? 1 : (g_n + kPassRows - 1) / kPassRows;
     }
-    r0 = g_r0 + pass * kPassRows;
-    n = min(g_n - pass * kPassRows, kPassRows);
+    r0 = kOnePass ? g_r0 : g_r0 + pass * kPassRows;
+    n = kOnePass ? g_n : min(g_n - pass * kPassRows, kPassRows);
     lane_ctx = lane < n ? __ldg(ctx + r0 + lane) : 0;
     return true;
   }
@@ -270,8 +305,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
                                           int32_t* status) {
   return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag, status));
 }
-
-__device__ __forceinline__ float relu_f(uint32_t bits) { return fmaxf(__uint_as_float(bits), 0.0f); }
 
 __device__ __forceinline__ void store_logit(float* dst, float v) { *dst = v; }
 __device__ __forceinline__ void store_logit(__nv_bfloat16* dst, float v) { *dst = __float2bfloat16_rn(v); }
@@ -299,62 +332,61 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   const int T = p.num_rows;
   if (sched[0] != kScheduleMagic || sched[1] != T || sched[2] != (p.indices != nullptr ? 1 : 0) ||
       sched[3] != S || sched[6] != kTileTokens || sched[7] != kGroupMaxRows ||
-      static_cast<int>(gridDim.x) != S || sched[4] < 0 || sched[4] > T) {
+      static_cast<int>(gridDim.x) != S || sched[4] < 0 || sched[4] > T || sched[5] < 0) {
     if (threadIdx.x == 0 && blockIdx.x == 0) report(p.status, kErrScheduleMismatch);
     return;
   }
-  const int G = sched[4];
-  const int U = sched[5];
-  const int32_t* sm_start = sched + kScheduleHeaderWords;
-  const int32_t* grs = sm_start + S + 1;
-  const int32_t* gus = grs + T + 1;
-  const int u0 = min(max(sm_start[blockIdx.x], 0), U);
-  const int u1 = min(max(sm_start[blockIdx.x + 1], u0), U);
-  if (u0 >= u1 || G == 0) return;  // no work: the whole CTA leaves before any set-up
+  {
+    int a0, a1, b0, b1;
+    cta_ranges(sched, S, T, a0, a1, b0, b1);
+    if ((a0 >= a1 && b0 >= b1) || sched[4] == 0) return;  // no work: the whole CTA leaves before any set-up
+  }
 
   Bars bars;
   bars.kv_full = sbase + L::kOffBar;
   bars.kv_empty = bars.kv_full + 8 * kMaxKStages;
   bars.raw_full = bars.kv_empty + 8 * kMaxKStages;
   bars.raw_empty = bars.raw_full + 8 * kMaxRawStages;
-  bars.sc_full = bars.raw_empty + 8 * kMaxRawStages;
-  bars.sc_empty = bars.sc_full + 8 * kScaleStages;
-  bars.q_full = bars.sc_empty + 8 * kScaleStages;
+  bars.q_full = bars.raw_empty + 8 * kMaxRawStages;
   bars.q_empty = bars.q_full + 8;
   bars.w_full = bars.q_empty + 8;
   bars.w_empty = bars.w_full + 16;
-  bars.tm_full = bars.w_empty + 16;
-  bars.tm_empty = bars.tm_full + 8 * kSlots;
+  bars.tm_empty = bars.w_empty + 16;
   bars.mma_done = bars.tm_empty + 8 * kSlots;
+  bars.tile_ready = bars.mma_done + 8;
   uint32_t* tmem_addr_smem = reinterpret_cast<uint32_t*>(smem + L::kOffTmemAddr);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kOffAbort);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bars.kvf(s), kDq ? kFp4Converters : 1);  // TMA (FP8) or the three dequantising warps (FP4)
-      mbar_init(bars.kve(s), 1);  // the MMA commit of the tile
+      mbar_init(bars.kvf(s), kDq ? kFp4Converters : 1);  // TMA (FP8) or the dequantising warps (FP4, MXFP4)
+      mbar_init(bars.kve(s), 1);  // the MMA commit of the tile: stage free, the tile's pairs in TMEM
     }
     for (int s = 0; s < L::kRawStages; ++s) {
       mbar_init(bars.rwf(s), 1);
       mbar_init(bars.rwe(s), kFp4Converters);  // the dequantising warps
     }
-    for (int s = 0; s < kScaleStages; ++s) {
-      mbar_init(bars.scf(s), kDq ? kFp4Converters : 1);  // bulk copy (FP8) or the three dequantising warps (FP4)
-      mbar_init(bars.sce(s), kEpiWarps);  // every epilogue warp has read the tile's scales
-    }
-    mbar_init(bars.q_full, kDq ? kFp4Converters : 1);  // the MMA warp's TMA (FP8) or the three converting warps (FP4)
+    mbar_init(bars.q_full, kDq ? kFp4Converters : 1);  // the MMA warp's TMA (FP8) or the converting warps (FP4, MXFP4)
     mbar_init(bars.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.wf(b), 1);
       mbar_init(bars.we(b), kEpiWarps);
     }
-    for (uint32_t sl = 0; sl < kSlots; ++sl) {
-      mbar_init(bars.tf(sl), 1);  // the MMA commit of the slot's pair
+    for (uint32_t sl = 0; sl < kSlots; ++sl)
       mbar_init(bars.te(sl), 4);  // the four warps of the pair's warpgroup have read it
-    }
     mbar_init(bars.mma_done, 1);
+    for (int i = 0; i < kTileRing; ++i) mbar_init(bars.tile_ready + 8 * i, 1);  // the tile's MMA commit
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  WalkRanges* walk_ranges = reinterpret_cast<WalkRanges*>(smem + L::kOffWalk);
+  if (warp == 0) {
+    int a0, a1, b0, b1;
+    cta_ranges(sched, S, T, a0, a1, b0, b1);
+    const int32_t* sus = sched + SchedLayout(S, T).sus;
+    const int ka = seek_position(sus, sched[4], a0, lane);
+    const int kb = seek_position(sus, sched[4], b0, lane);
+    if (lane == 0) *walk_ranges = WalkRanges{{a0, b0}, {a1, b1}, {ka, kb}};
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_addr_smem), kTmemCols);
@@ -374,7 +406,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   int32_t* ctx_sm = reinterpret_cast<int32_t*>(smem + L::kOffCtx);
 
   Walk<kDq ? kPassRowsOf<kFmt> : kGroupMaxRows> walk;
-  walk.start(grs, gus, p.ctx, G, T, u0, u1, lane);
+  walk.start(sched, walk_ranges);
 
   // =================================================== FP4 dequantisation (warps 3, 2, 20-23)
   // The six warps share every tile: work item k (0..511) is 32 elements
@@ -402,7 +434,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     const uint32_t q_half = static_cast<uint32_t>(LF::kQHalfBytes);
     int it = 0, nq = 0, nw = 0;
     bool ok = true;
-    while (ok && walk.next(lane)) {
+    while (ok && walk.next(sched, S, T, p.ctx, walk_ranges, lane)) {
       const int r0 = walk.r0, n = walk.n;
       // MXFP4: largest q scale exponent of each row of the pass (lane r holds row r's)
       uint32_t row_emax = 0;
@@ -491,8 +523,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         const int st = it % LF::kKStages;
         const int ss = it % kScaleStages;
         ok = warp_wait(bars.rwf(rs), (it / LF::kRawStages) & 1, abort_flag, p.status) &&
-             warp_wait(bars.kve(st), ((it / LF::kKStages) & 1) ^ 1, abort_flag, p.status) &&
-             warp_wait(bars.sce(ss), ((it / kScaleStages) & 1) ^ 1, abort_flag, p.status);
+             warp_wait(bars.kve(st), ((it / LF::kKStages) & 1) ^ 1, abort_flag, p.status);
         if (!ok) break;
         const uint8_t* raw = smem + LF::kOffRaw + rs * LF::kRawStageBytes;
         for (int t = part * 32 + lane; t < kTileTokens; t += kStride) {  // token scales -> scale ring
@@ -545,7 +576,6 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         if (lane == 0) {
           mbar_arrive(bars.rwe(rs));
           mbar_arrive(bars.kvf(st));
-          mbar_arrive(bars.scf(ss));
         }
       }
     }
@@ -565,9 +595,9 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     constexpr int kRing = kDq ? L::kRawStages : kStages;
     int it = 0;  // tiles issued
     bool ok = true;
-    while (ok && walk.next(lane)) {
+    while (ok && walk.next(sched, S, T, p.ctx, walk_ranges, lane)) {
       const int r0 = walk.r0, n = walk.n;
-      const int32_t* bt_row = table_row(p, r0 + n - 1);
+      const int32_t* bt_row = table_row(p, walk.g_r0 + walk.g_n - 1);  // the group's last row
       int32_t lane_blk = -1;  // block id of page (pg_base + lane)
       int pg_base = -32;
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
@@ -605,12 +635,22 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
                 bulk_load(dst + kPg, p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride, kPg, full_bar,
                           pol_stream);
             } else {
-              mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(npg * kPageValBytesFp8));
-              if (blk0 >= 0)
+              // the two pages' values (tensor map, swizzled) and their key
+              // scales (plain copies into the scale ring), one barrier
+              const uint32_t sc_dst = s_scale + (it % kScaleStages) * kScaleStageFloats * 4;
+              mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(npg * (kPageValBytesFp8 + kPageTokens * 4)));
+              if (blk0 >= 0) {
                 tma_load_3d(s_kv + st * L::kKStageBytes, &tm_kv, 0, 0, blk0, full_bar, pol_stream);
-              if (blk1 >= 0)
+                bulk_load(sc_dst, p.kv_cache + static_cast<int64_t>(blk0) * p.page_stride + kPageValBytesFp8,
+                          kPageTokens * 4, full_bar, pol_stream);
+              }
+              if (blk1 >= 0) {
                 tma_load_3d(s_kv + st * L::kKStageBytes + kPageValBytesFp8, &tm_kv, 0, 0, blk1,
                             full_bar, pol_stream);
+                bulk_load(sc_dst + kPageTokens * 4,
+                          p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride + kPageValBytesFp8,
+                          kPageTokens * 4, full_bar, pol_stream);
+              }
             }
           }
         }
@@ -627,51 +667,8 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   } else if (warp == 2 || warp == 3 || warp >= 4 + kEpiWarps) {
     if constexpr (!kDq) {
       if (warp == 3) {
-        // =================================================== key scales (FP8)
-        // Runs ahead of the K pipeline by up to kScaleStages tiles, gated only
-        // by the epilogue.  Block ids come 32 at a time as in the K producer.
-        const uint64_t pol_stream = policy_evict_first();
-        int it = 0;
-        bool ok = true;
-        while (ok && walk.next(lane)) {
-          const int32_t* bt_row = table_row(p, walk.r0 + walk.n - 1);
-          int32_t lane_blk = -1;
-          int pg_base = -32;
-          for (int j = walk.j0; j < walk.j1; ++j, ++it) {
-            if (2 * j >= pg_base + 32) {
-              pg_base = 2 * j;
-              const int pg = pg_base + lane;
-              lane_blk = -1;
-              if (pg < walk.npages) {
-                int32_t b = (pg < p.bt_stride) ? __ldg(bt_row + pg) : -1;
-                lane_blk = (b < 0 || b >= p.num_pages) ? 0 : b;  // reported by the K producer
-              }
-            }
-            const int32_t blk0 = __shfl_sync(0xffffffffu, lane_blk, 2 * j - pg_base);
-            const int32_t blk1 = __shfl_sync(0xffffffffu, lane_blk, 2 * j + 1 - pg_base);
-            if (lane == 0) {
-              const int ss = it % kScaleStages;
-              ok = wait_or_abort(bars.sce(ss), ((it / kScaleStages) & 1) ^ 1, abort_flag, p.status);
-              if (ok) {
-                const int npg = (blk0 >= 0 ? 1 : 0) + (blk1 >= 0 ? 1 : 0);
-                mbar_arrive_expect_tx(bars.scf(ss), static_cast<uint32_t>(npg * kPageTokens * 4));
-                if (blk0 >= 0)
-                  bulk_load(s_scale + ss * kScaleStageFloats * 4,
-                            p.kv_cache + static_cast<int64_t>(blk0) * p.page_stride + kPageValBytesFp8,
-                            kPageTokens * 4, bars.scf(ss), pol_stream);
-                if (blk1 >= 0)
-                  bulk_load(s_scale + (ss * kScaleStageFloats + kPageTokens) * 4,
-                            p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride + kPageValBytesFp8,
-                            kPageTokens * 4, bars.scf(ss), pol_stream);
-              }
-            }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) break;
-          }
-        }
-        if (lane == 0)
-          for (int i = max(0, it - kScaleStages); i < it; ++i)
-            wait_drain(bars.scf(i % kScaleStages), (i / kScaleStages) & 1);
+        // FP8: no role (the K producer brings each tile's key scales with its
+        // values); the warp waits at the final barrier.
       } else {
         // =================================================== per group: weights and causal limits
         // A separate producer: the epilogue may hold a group's weights until TMEM
@@ -680,7 +677,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         const uint64_t pol_keep = policy_evict_last();
         int nw = 0;
         bool ok = true;
-        while (ok && walk.next(lane)) {
+        while (ok && walk.next(sched, S, T, p.ctx, walk_ranges, lane)) {
           const int r0 = walk.r0, n = walk.n;
           const int wb = nw & 1;
           ok = warp_wait(bars.we(wb), ((nw >> 1) & 1) ^ 1, abort_flag, p.status);
@@ -725,7 +722,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     const uint64_t pol_keep = policy_evict_last();  // q
     uint32_t it = 0, gi = 0, pos = 0, nq = 0;  // tiles, groups, pairs, Q loads issued
     bool ok = true;
-    while (ok && walk.next(lane)) {
+    while (ok && walk.next(sched, S, T, p.ctx, walk_ranges, lane)) {
       const uint32_t n = static_cast<uint32_t>(walk.n);
       if constexpr (!kDq) {
         // Q buffer free once the previous group's MMAs have completed
@@ -764,10 +761,13 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
           left -= len;
           pos += len;
           b_lo += len * kQRowLo;
-          for (uint32_t i = 0; i < len; ++i) mma_commit_if(issue, bars.tf(c + i));
         } while (left != 0);
         if (!ok) break;
+        // one commit per tile: the K stage is free and every pair of the tile
+        // is in TMEM once it fires (each commit costs the issuing thread about
+        // as much as a small MMA)
         mma_commit_if(issue, bars.kve(st));
+        if constexpr (kDq) mma_commit_if(issue, bars.tr(it, true));
       }
       if (!ok) break;
       mma_commit_if(issue, bars.q_empty);
@@ -790,9 +790,10 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     //   sum_h w_h relu(x_h) = (sum_h w_h x_h + sum_h w_h |x_h|) / 2
     // so the head reduction is 64 packed FMAs (the |x| is an operand
     // modifier) instead of 64 max plus 32 packed FMAs.  The 64 columns come
-    // in pieces of kPiece (register budget); the slot is released after the
-    // last piece is read.
-    constexpr int kPiece = kPieceCols<kFmt>;
+    // in pieces of kPiece (register budget: one 64-column load for FP8, two
+    // 32-column loads for the formats with more warps); the slot is released
+    // after the last piece is read.
+    constexpr int kPiece = kFmt == DSA_KV_FP8 ? 64 : 32;
     const uint32_t wg = static_cast<uint32_t>(warp - 4) >> 2;
     const int quarter = warp & 3;    // TMEM lanes this warp may read
     const int tok = quarter * 32 + lane;
@@ -800,7 +801,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     OutT* const out = static_cast<OutT*>(p.logits);
     uint32_t it = 0, gi = 0, pos = 0;  // tiles, groups, pairs seen
     bool ok = true;
-    while (ok && walk.next(lane)) {
+    while (ok && walk.next(sched, S, T, p.ctx, walk_ranges, lane)) {
       const int n = walk.n;
       const uint32_t wb = gi & 1;
       ok = warp_wait(bars.wf(wb), (gi >> 1) & 1, abort_flag, p.status);
@@ -811,20 +812,22 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       const float* rowf_grp = reinterpret_cast<const float*>(smem + L::kOffRowF) + wb * kGroupMaxRows;
       OutT* const out_grp = out + static_cast<int64_t>(walk.r0) * p.logits_stride;
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
-        const uint32_t ss = it & (kScaleStages - 1);
-        ok = warp_wait(bars.scf(ss), (it / kScaleStages) & 1, abort_flag, p.status);
+        const uint32_t r_first = (wg - pos) & (kEpiWg - 1);
+        if (r_first >= static_cast<uint32_t>(n)) {  // no pair of this warp in the tile
+          pos += static_cast<uint32_t>(n);
+          continue;
+        }
+        // the tile's MMAs are done, so its key scales (loaded with its K
+        // values, a ring of kScaleStages tiles) are in shared memory too
+        ok = warp_wait(bars.tr(it, kDq), (it / kTileRing) & 1, abort_flag, p.status);
         if (!ok) break;
-        const float kscale = scale_sm[ss * kScaleStageFloats + tok];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.sce(ss));
+        tc_fence_after();
+        const float kscale = scale_sm[(it & (kScaleStages - 1)) * kScaleStageFloats + tok];
         const int scol = j * kTileTokens + tok;
         const bool in_span = scol < lim;
-        for (uint32_t r = (wg - pos) & (kEpiWg - 1); r < static_cast<uint32_t>(n); r += kEpiWg) {
+        for (uint32_t r = r_first; r < static_cast<uint32_t>(n); r += kEpiWg) {
           const uint32_t pp = pos + r;
           const uint32_t sl = pp & (kSlots - 1);
-          ok = warp_wait(bars.tf(sl), (pp / kSlots) & 1, abort_flag, p.status);
-          if (!ok) break;
-          tc_fence_after();
           const float4* wr = reinterpret_cast<const float4*>(w_grp + r * kHeads);
           float2 cx = make_float2(0.f, 0.f), ca = cx;
 #pragma unroll

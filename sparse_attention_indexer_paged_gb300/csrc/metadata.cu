@@ -3,17 +3,33 @@
 // Changes: get_paged_mqa_logits_metadata(seq_lens, block_kv, num_sms,
 // indices) -> SM schedule; rows with equal consecutive request ids belong to
 // one request, PR 56811 "Fix fp8_fp4_paged_mqa_logits MQA kpool varlen path
-// for speculative decode", Purpose).
+// for speculative decode", Purpose).  The pages fix the call's inputs and its
+// purpose, balancing (request, K-block) work over the SMs; the split rule is
+// this library's own.
 //
-// One CTA of 1024 threads walks the rows and groups in chunks of 1024 with
-// block-wide scans:
-//   pass 1  group starts: a row starts a group when it starts a run of equal
-//           request ids, or when kGroupMaxRows rows of its run precede it in
-//           the current group;
-//   pass 2  tiles per group = ceil(max L_t / 128) and their prefix sums;
-//   pass 3  prefix weights (tile weight = kTileWeight + kRowWeight * rows) and, for every
-//           SM i, the first tile u with P(u) * num_sms >= i * W (exact
-//           integer arithmetic).
+// A unit is one 128-key tile of one group (up to 8 adjacent rows of one
+// request).  It costs its SM one K tile from HBM, the same for every unit,
+// plus one (tile, row) pair of MMA columns and epilogue work per row of the
+// group.  The rule gives every SM the same number of units (within one) and,
+// as nearly as the groups allow, the same number of pairs:
+//   1. groups: runs of equal request ids, each cut into pieces of at most
+//      kGroupMaxRows rows;
+//   2. the groups are ordered by row count (stable) and their units laid end
+//      to end in that order: sorted position k starts at unit sus[k], and
+//      spp[k] pairs precede it;
+//   3. boundary i (0 <= i <= S) has consumed x_i = floor(i U / S) units,
+//      lambda_i from the light (left) end of that sequence and
+//      x_i - lambda_i from the heavy (right) end; SM i owns the units between
+//      boundaries i and i + 1 at both ends;
+//   4. a_i = the fewest left units such that the pairs consumed, times S,
+//      do not exceed i P (P = all pairs), and lambda_i is a_i moved as little
+//      as needed to keep both ends monotone: lambda_i = max(lambda_{i-1},
+//      min(a_i, lambda_{i-1} + x_i - x_{i-1})).
+//
+// One CTA of 1024 threads: chunked block scans for the groups, the stable
+// counting sort by row count and the prefix sums; one thread per boundary for
+// a_i (bisection; the pairs consumed fall as more units come from the left);
+// thread 0 for the monotone pass.
 #include "common.cuh"
 
 namespace dsa {
@@ -74,40 +90,83 @@ __device__ int block_inclusive_max(int v, int* buf) {
   return r;
 }
 
-struct GroupInfo {
-  int32_t tiles;
-  int32_t weight;
-};
+// Rows up to which the working arrays (group starts, sorted positions, unit
+// starts, pair prefixes) live in dynamic shared memory; the kernel copies them
+// to the schedule at the end.  Larger batches work on the schedule words in
+// global memory directly (the block's own global writes are visible to it
+// after __syncthreads).
+constexpr int kSmemRows = 8192;
+constexpr int kSchedArrays = 5;  // grs, pos, sus, spp_lo, spp_hi
 
-__device__ __forceinline__ GroupInfo group_info(const int32_t* ctx, const int32_t* grs, int g,
-                                                int G, int T) {
-  const int r0 = grs[g];
-  const int r1 = (g + 1 < G) ? grs[g + 1] : T;
-  int lmax = 0;
-  for (int t = r0; t < r1; ++t) lmax = max(lmax, ctx[t]);
-  GroupInfo gi;
-  gi.tiles = (lmax + kTileTokens - 1) / kTileTokens;
-  gi.weight = kTileWeight + kRowWeight * (r1 - r0);
-  return gi;
-}
+// A coarse map from units to sorted positions for the boundary search:
+// entry c is the largest position k with sus[k] <= c * 2^shift, so the
+// position holding unit u lies in [coarse[u >> shift], coarse[(u >> shift) + 1]].
+constexpr int kCoarse = 2048;
+
+struct SortedUnits {
+  const int32_t* pos;
+  const int32_t* sus;
+  const int32_t* spp_lo;
+  const int32_t* spp_hi;
+  const int32_t* coarse;
+  int shift;
+  int G;
+  int64_t P;
+
+  // Pairs of the first u units of the sorted sequence.
+  __device__ __forceinline__ int64_t pairs_before(int64_t u) const {
+    const int64_t c = u >> shift;
+    int lo = coarse[c], hi = min(coarse[c + 1], G);  // largest k in [lo, hi] with sus[k] <= u
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (sus[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    if (lo >= G) return P;
+    const int64_t before = static_cast<int64_t>(static_cast<uint32_t>(spp_lo[lo])) |
+                           (static_cast<int64_t>(spp_hi[lo]) << 32);
+    return before + (u - sus[lo]) * static_cast<int64_t>(static_cast<uint32_t>(pos[lo]) >> kPosRowsShift);
+  }
+
+  // The fewest left units lam in [0, x] with (pairs consumed) * S <= target,
+  // x if none: the pairs consumed, pairs_before(lam) + P - pairs_before(U - x
+  // + lam), do not increase with lam.
+  __device__ __forceinline__ int32_t fewest_left(int64_t x, int64_t U, int64_t S, int64_t target) const {
+    int64_t lo = 0, hi = x;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      const int64_t f = pairs_before(mid) + P - pairs_before(U - x + mid);
+      if (f * S <= target) hi = mid; else lo = mid + 1;
+    }
+    return static_cast<int32_t>(lo);
+  }
+};
 
 __global__ void __launch_bounds__(kThreads, 1)
     metadata_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ ind, int32_t T,
                     int32_t S, int32_t* __restrict__ sched) {
+  extern __shared__ int32_t dyn[];
   __shared__ int32_t buf32[kWarps];
   __shared__ int64_t buf64[kWarps];
-  __shared__ int64_t s_key[kThreads];
-  __shared__ int64_t s_gw[kThreads];
-  __shared__ int32_t s_us[kThreads];
-  __shared__ int32_t s_w[kThreads];
+  __shared__ uint64_t bufu[kWarps];
   __shared__ int32_t s_carry;
+  __shared__ int32_t s_base[kGroupMaxRows + 1];   // first sorted position of each row count
+  __shared__ int32_t s_taken[kGroupMaxRows + 1];  // positions of each row count handed out so far
+  __shared__ int32_t s_a[kThreads];
+  __shared__ int32_t s_x[kThreads];
+  __shared__ int32_t s_lambda[kThreads];
+  __shared__ int32_t s_coarse[kCoarse + 2];
 
   const int tid = threadIdx.x;
-  int32_t* sm_start = sched + kScheduleHeaderWords;
-  int32_t* grs = sm_start + S + 1;
-  int32_t* gus = grs + T + 1;
-
-  // ---- pass 1: group starts
+  const SchedLayout L(S, T);
+  const bool in_smem = T <= kSmemRows;
+  const int64_t n1 = static_cast<int64_t>(T) + 1;
+  int32_t* grs = in_smem ? dyn : sched + L.grs;
+  int32_t* pos = in_smem ? dyn + n1 : sched + L.pos;
+  int32_t* sus = in_smem ? dyn + 2 * n1 : sched + L.sus;
+  int32_t* spp_lo = in_smem ? dyn + 3 * n1 : sched + L.spp_lo;
+  int32_t* spp_hi = in_smem ? dyn + 4 * n1 : sched + L.spp_hi;
+  // ---- groups: a row starts one when it starts a run of equal request ids,
+  // or when kGroupMaxRows rows of its run precede it in the current group
   int carry_run = 0;  // run start of the previous chunk's last row
   int G = 0;
   for (int base = 0; base < T; base += kThreads) {
@@ -127,69 +186,141 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   }
   for (int g = G + tid; g <= T; g += kThreads) grs[g] = T;
-  __syncthreads();
-
-  // ---- pass 2: tiles per group and their prefix sums
-  int U = 0;
-  int64_t W = 0;
-  for (int base = 0; base < G; base += kThreads) {
-    const int g = base + tid;
-    GroupInfo gi{0, 0};
-    if (g < G) gi = group_info(ctx, grs, g, G, T);
-    int32_t tot;
-    const int32_t ex = block_exclusive_sum<int32_t>(gi.tiles, buf32, &tot);
-    int64_t totw;
-    block_exclusive_sum<int64_t>(static_cast<int64_t>(gi.tiles) * gi.weight, buf64, &totw);
-    if (g < G) gus[g] = U + ex;
-    U += tot;
-    W += totw;
+  if (tid <= kGroupMaxRows) {
+    s_base[tid] = 0;
+    s_taken[tid] = 0;
   }
-  for (int g = G + tid; g <= T; g += kThreads) gus[g] = U;
   __syncthreads();
 
-  // ---- pass 3: SM boundaries.  Thread i owns boundary i (i <= S).
-  const int64_t target = static_cast<int64_t>(tid) * W;  // compare P(u) * S >= target
-  bool resolved = tid > S;
-  int32_t answer = U;
-  int unit_carry = 0;
-  int64_t weight_carry = 0;
+  // ---- stable counting sort of the groups by row count (1 .. kGroupMaxRows)
+  for (int g = tid; g < G; g += kThreads) atomicAdd(&s_base[grs[g + 1] - grs[g]], 1);
+  __syncthreads();
+  if (tid == 0) {
+    int b = 0;
+    for (int n = 1; n <= kGroupMaxRows; ++n) {
+      const int c = s_base[n];
+      s_base[n] = b;
+      b += c;
+    }
+  }
+  __syncthreads();
+  // ranks within a row count: one-hot counters, 16 bits each, four counts per
+  // 64-bit scan (a chunk holds at most 1024 groups)
+  static_assert(kGroupMaxRows == 8 && kThreads < 65536, "packed rank counters");
   for (int base = 0; base < G; base += kThreads) {
     const int g = base + tid;
-    GroupInfo gi{0, 0};
-    if (g < G) gi = group_info(ctx, grs, g, G, T);
-    int32_t tot;
-    const int32_t ex = block_exclusive_sum<int32_t>(gi.tiles, buf32, &tot);
-    int64_t totw;
-    const int64_t exw =
-        block_exclusive_sum<int64_t>(static_cast<int64_t>(gi.tiles) * gi.weight, buf64, &totw);
-    const int64_t gw = weight_carry + exw;
-    // key = weight before the group's last tile (empty group: gw - 1), so keys
-    // never decrease along the groups; padding entries are +inf.
-    s_key[tid] = (g < G) ? (gi.tiles > 0 ? gw + static_cast<int64_t>(gi.tiles - 1) * gi.weight
-                                         : gw - 1)
-                         : INT64_MAX;
-    s_gw[tid] = gw;
-    s_us[tid] = unit_carry + ex;
-    s_w[tid] = gi.weight;
-    __syncthreads();
-    const int n_in = min(kThreads, G - base);
-    if (!resolved && s_key[n_in - 1] * S >= target) {
-      int lo = 0, hi = n_in - 1;  // first index with key * S >= target
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (s_key[mid] * S >= target) hi = mid; else lo = mid + 1;
-      }
-      const int64_t num = target - s_gw[lo] * S;
-      const int64_t den = static_cast<int64_t>(s_w[lo]) * S;
-      const int64_t add = num > 0 ? (num + den - 1) / den : 0;
-      answer = s_us[lo] + static_cast<int32_t>(add);
-      resolved = true;
+    const bool valid = g < G;
+    const int n = valid ? grs[g + 1] - grs[g] : 0;
+    const uint64_t one_lo = (valid && n <= 4) ? (1ull << (16 * (n - 1))) : 0ull;
+    const uint64_t one_hi = (valid && n > 4) ? (1ull << (16 * (n - 5))) : 0ull;
+    uint64_t tot_lo, tot_hi;
+    const uint64_t ex_lo = block_exclusive_sum<uint64_t>(one_lo, bufu, &tot_lo);
+    const uint64_t ex_hi = block_exclusive_sum<uint64_t>(one_hi, bufu, &tot_hi);
+    if (valid) {
+      const int rank = static_cast<int>(n <= 4 ? (ex_lo >> (16 * (n - 1))) & 0xffffu : (ex_hi >> (16 * (n - 5))) & 0xffffu);
+      pos[s_base[n] + s_taken[n] + rank] = grs[g] | (n << kPosRowsShift);
     }
     __syncthreads();
-    unit_carry += tot;
-    weight_carry += totw;
+    if (tid < kGroupMaxRows) {
+      const int cls = tid + 1;
+      s_taken[cls] += static_cast<int>(cls <= 4 ? (tot_lo >> (16 * (cls - 1))) & 0xffffu : (tot_hi >> (16 * (cls - 5))) & 0xffffu);
+    }
+    __syncthreads();
   }
-  if (tid <= S) sm_start[tid] = (W == 0) ? 0 : answer;
+
+  // ---- units and pairs along the sorted order
+  int32_t U = 0;
+  int64_t P = 0;
+  for (int base = 0; base < G; base += kThreads) {
+    const int k = base + tid;
+    int32_t tiles = 0;
+    int64_t pairs = 0;
+    if (k < G) {
+      const int32_t w = pos[k];
+      const int r0 = w & kPosRowMask, n = static_cast<int>(static_cast<uint32_t>(w) >> kPosRowsShift);
+      int lmax = 0;
+      for (int t = r0; t < r0 + n; ++t) lmax = max(lmax, ctx[t]);
+      tiles = (lmax + kTileTokens - 1) / kTileTokens;
+      pairs = static_cast<int64_t>(tiles) * n;
+    }
+    int32_t tot;
+    const int32_t ex = block_exclusive_sum<int32_t>(tiles, buf32, &tot);
+    int64_t totp;
+    const int64_t exp = block_exclusive_sum<int64_t>(pairs, buf64, &totp);
+    if (k < G) {
+      sus[k] = U + ex;
+      const int64_t pp = P + exp;
+      spp_lo[k] = static_cast<int32_t>(pp & 0xffffffff);
+      spp_hi[k] = static_cast<int32_t>(pp >> 32);
+    }
+    U += tot;
+    P += totp;
+  }
+
+  for (int k = G + tid; k <= T; k += kThreads) {
+    pos[k] = T;  // past the last group
+    sus[k] = U;
+    spp_lo[k] = static_cast<int32_t>(P & 0xffffffff);
+    spp_hi[k] = static_cast<int32_t>(P >> 32);
+  }
+  __syncthreads();
+
+  // ---- coarse unit -> position map (entries past the last unit hold G)
+  int shift = 0;
+  while ((static_cast<int64_t>(U) >> shift) >= kCoarse) ++shift;
+  for (int c = tid; c <= kCoarse + 1; c += kThreads) {
+    const int64_t u = static_cast<int64_t>(c) << shift;
+    int lo = 0, hi = G;  // largest k in [0, G] with sus[k] <= u
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (sus[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    s_coarse[c] = lo;
+  }
+  __syncthreads();
+
+  // ---- a_i: the fewest left units with (pairs consumed) * S <= i * P
+  if (tid <= S) {
+    const int64_t x = static_cast<int64_t>(tid) * U / S;
+    s_x[tid] = static_cast<int32_t>(x);
+    const int64_t target = static_cast<int64_t>(tid) * P;
+    // the arrays named from their own shared or global base, so that the
+    // loads use the matching state space
+    s_a[tid] = in_smem ? SortedUnits{dyn + n1, dyn + 2 * n1, dyn + 3 * n1, dyn + 4 * n1, s_coarse, shift, G, P}
+                             .fewest_left(x, U, S, target)
+                       : SortedUnits{sched + L.pos, sched + L.sus, sched + L.spp_lo, sched + L.spp_hi, s_coarse, shift,
+                                     G, P}.fewest_left(x, U, S, target);
+  }
+  __syncthreads();
+
+  // ---- monotone path: lambda_i = max(lambda_{i-1}, min(a_i, lambda_{i-1} +
+  // x_i - x_{i-1})).  Where no step of the running maximum of a exceeds its
+  // x step, that running maximum is the path (one block-wide max scan);
+  // otherwise thread 0 walks the recurrence.
+  {
+    const int a = tid <= S ? s_a[tid] : 0;
+    const int run = block_inclusive_max(a, buf32);
+    if (tid <= S) s_lambda[tid] = run;
+    __syncthreads();
+    const bool bad = tid >= 1 && tid <= S && s_lambda[tid] - s_lambda[tid - 1] > s_x[tid] - s_x[tid - 1];
+    const int any_bad = __syncthreads_or(bad ? 1 : 0);
+    if (any_bad && tid == 0) {
+      int32_t lam = 0;
+      s_lambda[0] = 0;
+      for (int i = 1; i <= S; ++i) {
+        lam = max(lam, min(s_a[i], lam + (s_x[i] - s_x[i - 1])));
+        s_lambda[i] = lam;
+      }
+    }
+    __syncthreads();
+  }
+  if (tid <= S) {
+    sched[L.left + tid] = s_lambda[tid];
+    sched[L.right + tid] = U - (s_x[tid] - s_lambda[tid]);
+  }
+  if (in_smem) {  // the working arrays to the schedule
+    for (int64_t i = tid; i < kSchedArrays * n1; i += kThreads) sched[L.grs + i] = dyn[i];
+  }
   if (tid == 0) {
     sched[0] = kScheduleMagic;
     sched[1] = T;
@@ -206,7 +337,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_metadata(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
                             int32_t num_sms, int32_t* schedule, cudaStream_t stream) {
-  metadata_kernel<<<1, kThreads, 0, stream>>>(context_lens, indices, num_rows, num_sms, schedule);
+  static_assert(kSchedArrays * (kSmemRows + 1) * 4 <= 200 * 1024, "metadata shared memory");
+  const size_t smem = num_rows <= kSmemRows ? kSchedArrays * (static_cast<size_t>(num_rows) + 1) * 4 : 0;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kSchedArrays * (kSmemRows + 1) * 4);
+    if (e != cudaSuccess) return e;
+  }
+  metadata_kernel<<<1, kThreads, smem, stream>>>(context_lens, indices, num_rows, num_sms, schedule);
   return cudaGetLastError();
 }
 

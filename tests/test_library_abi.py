@@ -55,7 +55,7 @@ def test_status_strings(lib):
 
 
 def test_schedule_words(lib):
-    assert lib.dsa_schedule_words(148, 134) == 8 + 149 + 2 * 135
+    assert lib.dsa_schedule_words(148, 134) == 8 + 2 * 149 + 5 * 135
     assert lib.dsa_schedule_words(0, 5) == -1
 
 

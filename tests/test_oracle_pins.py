@@ -13,7 +13,7 @@
   (B, max_n), and plain decode (indices = None) against indices = arange(B);
 * top-k against a brute-force Python sort on random, tie-heavy, bf16-rounded,
   -inf and NaN rows;
-* the schedule rule's properties;
+* argument validation (grouping, causal limits, block table);
 * planted mistakes: each deliberate error switched on inside the oracle makes
   at least one of the pins above fail.
 """
@@ -459,11 +459,6 @@ def test_fp4_unit_keys_closed_form():
 def test_plain_equals_arange():
     wl = W.config("tiny")
     B = wl.num_rows
-    s_none = oracle.schedule(wl.context_lens, None, 16)
-    s_ar = oracle.schedule(wl.context_lens, torch.arange(B, dtype=torch.int32), 16)
-    assert s_none[2] == 0 and s_ar[2] == 1
-    s_none[2] = 1
-    assert np.array_equal(s_none, s_ar)
     assert oracle.validate(wl.context_lens, None, wl.block_table, wl.num_pages,
                            wl.logits_stride) == 0
     assert oracle.validate(wl.context_lens, torch.arange(B, dtype=torch.int32), wl.block_table,
@@ -481,61 +476,6 @@ def test_topk_short_rows_pad():
     x = np.arange(10, dtype=np.float64)[None, :]
     assert list(oracle.top_k_per_row(x, [4], 6)[0]) == [0, 1, 2, 3, -1, -1]
     assert list(oracle.top_k_per_row(x, [0], 3)[0]) == [-1, -1, -1]
-
-
-def _schedule_props(lens, ids, S):
-    T = len(lens)
-    words = oracle.schedule(np.array(lens, np.int32), None if ids is None else np.array(ids, np.int32), S)
-    assert len(words) == oracle.schedule_words(S, T)
-    hdr, sm, grs, gus = oracle.parse_schedule(words, S, T)
-    G, U = int(hdr[4]), int(hdr[5])
-    assert hdr[0] == 0x44534131 and hdr[1] == T and hdr[3] == S and hdr[6] == 128 and hdr[7] == 8
-    # groups: cover every row, no longer than 8 rows, one request id each,
-    # a run continues into the next group only when the group is full
-    assert grs[0] == 0 and grs[G] == T and np.all(np.diff(grs[: G + 1]) > 0)
-    assert np.all(np.diff(grs[: G + 1]) <= 8)
-    for g in range(G):
-        rows = range(grs[g], grs[g + 1])
-        if ids is not None:
-            assert len({ids[t] for t in rows}) == 1
-        else:
-            assert len(rows) == 1
-        if g + 1 < G and ids is not None and ids[grs[g + 1]] == ids[grs[g + 1] - 1]:
-            assert grs[g + 1] - grs[g] == 8
-        lmax = max(max(lens[t] for t in rows), 0)
-        assert gus[g + 1] - gus[g] == (lmax + 127) // 128
-    assert gus[0] == 0 and gus[G] == U
-    # SM split: monotone, complete, balanced within one unit's weight
-    assert sm[0] == 0 and sm[S] == U and np.all(np.diff(sm) >= 0)
-    unit_w = []
-    for g in range(G):
-        unit_w += [oracle.TILE_WEIGHT + oracle.ROW_WEIGHT * (grs[g + 1] - grs[g])] * int(gus[g + 1] - gus[g])
-    unit_w = np.array(unit_w, dtype=np.int64)
-    Wt = int(unit_w.sum())
-    if U:
-        mx = int(unit_w.max())
-        for i in range(S):
-            work = int(unit_w[sm[i]: sm[i + 1]].sum())
-            assert work <= Wt / S + mx and work >= Wt / S - mx
-    return words
-
-
-def test_schedule_properties():
-    rng = np.random.default_rng(0)
-    _schedule_props([300, 517], [0, 1], 8)
-    _schedule_props([300, 517], None, 148)
-    _schedule_props([], None, 4)
-    _schedule_props([0, 0, 5], [0, 1, 1], 3)
-    for trial in range(20):
-        B = int(rng.integers(1, 30))
-        n = rng.integers(1, 12, B)
-        ids, lens = [], []
-        for r in range(B):
-            L = int(rng.integers(0, 5000))
-            for j in range(n[r]):
-                ids.append(r)
-                lens.append(max(0, L - n[r] + 1 + j))
-        _schedule_props(lens, ids, int(rng.integers(1, 200)))
 
 
 def test_validate_errors():
