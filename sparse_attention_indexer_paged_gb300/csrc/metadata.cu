@@ -141,6 +141,11 @@ struct SortedUnits {
   }
 };
 
+// kInSmem: the working arrays live in dynamic shared memory (T <= kSmemRows)
+// and every pointer to them is derived from that array, so that their loads
+// and stores are shared-memory accesses; otherwise they are the schedule's
+// own words in global memory.
+template <bool kInSmem>
 __global__ void __launch_bounds__(kThreads, 1)
     metadata_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ ind, int32_t T,
                     int32_t S, int32_t* __restrict__ sched) {
@@ -158,13 +163,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x;
   const SchedLayout L(S, T);
-  const bool in_smem = T <= kSmemRows;
   const int64_t n1 = static_cast<int64_t>(T) + 1;
-  int32_t* grs = in_smem ? dyn : sched + L.grs;
-  int32_t* pos = in_smem ? dyn + n1 : sched + L.pos;
-  int32_t* sus = in_smem ? dyn + 2 * n1 : sched + L.sus;
-  int32_t* spp_lo = in_smem ? dyn + 3 * n1 : sched + L.spp_lo;
-  int32_t* spp_hi = in_smem ? dyn + 4 * n1 : sched + L.spp_hi;
+  int32_t* const base = kInSmem ? dyn : sched + L.grs;  // the five arrays, end to end, in both places
+  int32_t* grs = base;
+  int32_t* pos = base + n1;
+  int32_t* sus = base + 2 * n1;
+  int32_t* spp_lo = base + 3 * n1;
+  int32_t* spp_hi = base + 4 * n1;
   // ---- groups: a row starts one when it starts a run of equal request ids,
   // or when kGroupMaxRows rows of its run precede it in the current group
   int carry_run = 0;  // run start of the previous chunk's last row
@@ -286,10 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t target = static_cast<int64_t>(tid) * P;
     // the arrays named from their own shared or global base, so that the
     // loads use the matching state space
-    s_a[tid] = in_smem ? SortedUnits{dyn + n1, dyn + 2 * n1, dyn + 3 * n1, dyn + 4 * n1, s_coarse, shift, G, P}
-                             .fewest_left(x, U, S, target)
-                       : SortedUnits{sched + L.pos, sched + L.sus, sched + L.spp_lo, sched + L.spp_hi, s_coarse, shift,
-                                     G, P}.fewest_left(x, U, S, target);
+    s_a[tid] = SortedUnits{pos, sus, spp_lo, spp_hi, s_coarse, shift, G, P}.fewest_left(x, U, S, target);
   }
   __syncthreads();
 
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sched[L.left + tid] = s_lambda[tid];
     sched[L.right + tid] = U - (s_x[tid] - s_lambda[tid]);
   }
-  if (in_smem) {  // the working arrays to the schedule
+  if (kInSmem) {  // the working arrays to the schedule
     for (int64_t i = tid; i < kSchedArrays * n1; i += kThreads) sched[L.grs + i] = dyn[i];
   }
   if (tid == 0) {
@@ -338,13 +340,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_metadata(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
                             int32_t num_sms, int32_t* schedule, cudaStream_t stream) {
   static_assert(kSchedArrays * (kSmemRows + 1) * 4 <= 200 * 1024, "metadata shared memory");
-  const size_t smem = num_rows <= kSmemRows ? kSchedArrays * (static_cast<size_t>(num_rows) + 1) * 4 : 0;
+  if (num_rows > kSmemRows) {
+    metadata_kernel<false><<<1, kThreads, 0, stream>>>(context_lens, indices, num_rows, num_sms, schedule);
+    return cudaGetLastError();
+  }
+  const size_t smem = kSchedArrays * (static_cast<size_t>(num_rows) + 1) * 4;
   if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(metadata_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                kSchedArrays * (kSmemRows + 1) * 4);
     if (e != cudaSuccess) return e;
   }
-  metadata_kernel<<<1, kThreads, smem, stream>>>(context_lens, indices, num_rows, num_sms, schedule);
+  metadata_kernel<true><<<1, kThreads, smem, stream>>>(context_lens, indices, num_rows, num_sms, schedule);
   return cudaGetLastError();
 }
 
