@@ -2,9 +2,10 @@
 C ABI (binding -> libdsa_indexer.so), on seeded synthetic inputs.
 
 Small cases run the oracle on every row (several tiles, ragged tails, groups
-longer than 8 rows, empty rows); the full-size decode workloads compare
-sampled rows element by element and every row's top-k against the oracle's
-top-k of the GPU logits."""
+longer than 8 rows, empty rows); the full-size decode workloads compare every
+row's logits element by element with the oracle, every row's top-k bit for
+bit with the oracle's top-k of the GPU logits, and every row's top-k with the
+oracle's top-k of the oracle logits up to the tie band."""
 import numpy as np
 import pytest
 import torch
@@ -12,8 +13,7 @@ import torch
 import oracle
 import sparse_attention_indexer_paged_gb300 as dsa
 import workloads as W
-from gpu_helpers import (check_logits, check_topk_exact, check_topk_tie_band, run_path,
-                         sample_rows)
+from gpu_helpers import check_logits, check_topk_exact, check_topk_tie_band, run_path
 from schedule_check import check_schedule
 
 pytestmark = pytest.mark.gpu
@@ -272,18 +272,24 @@ def test_topk_short_rows(C, dtype):
         assert np.array_equal(got, oracle.top_k_per_row(x.float().cpu().double().numpy(), ends, k)), k
 
 
-# ---------------------------------------------------------------- full-size workloads, sampled
+# ---------------------------------------------------------------- full-size workloads, every row
 
-@pytest.mark.parametrize("name", ["plain", "mtp", "varlen"])
-def test_full_size_sampled(name):
+def _full_size_every_row(name):
+    """The configuration's whole step in the launch configuration bench.py
+    times (every SM, the schedule from the metadata call): all rows, all
+    columns of the logits against the oracle, then both top-k checks."""
     wl = W.config(name, device="cuda")
     out = run_path(wl)
     assert int(out["status"].item()) == 0, dsa.status_string(int(out["status"].item()))
     host = wl.to("cpu")
-    rows = sample_rows(wl.num_rows, 4, seed=len(name))
-    ref, bound, _ = check_logits(host, out["logits"], rows=rows)
+    ref, bound, _ = check_logits(host, out["logits"])
     check_topk_exact(out["logits"], out["idx"], host.context_lens, wl.topk)
-    check_topk_tie_band(out["idx"], ref, bound, host.context_lens, wl.topk, rows)
+    check_topk_tie_band(out["idx"], ref, bound, host.context_lens, wl.topk, list(range(wl.num_rows)))
+
+
+@pytest.mark.parametrize("name", ["plain", "mtp", "varlen"])
+def test_full_size_every_row(name):
+    _full_size_every_row(name)
 
 
 def test_topk_long_row_general_path():
@@ -376,15 +382,8 @@ def test_fp4_padded_page_stride():
                         kv_format=W.KV_FP4, page_stride=4864 + 16 * 9, seed=15))
 
 
-def test_fp4_full_size_sampled():
-    wl = W.config("fp4_varlen", device="cuda")
-    out = run_path(wl)
-    assert int(out["status"].item()) == 0, dsa.status_string(int(out["status"].item()))
-    host = wl.to("cpu")
-    rows = sample_rows(wl.num_rows, 4, seed=5)
-    ref, bound, _ = check_logits(host, out["logits"], rows=rows)
-    check_topk_exact(out["logits"], out["idx"], host.context_lens, wl.topk)
-    check_topk_tie_band(out["idx"], ref, bound, host.context_lens, wl.topk, rows)
+def test_fp4_full_size_every_row():
+    _full_size_every_row("fp4_varlen")
 
 
 # ---------------------------------------------------------------- MXFP4 keys and q
@@ -419,15 +418,8 @@ def test_mxfp4_block_scales_far_below_the_largest():
     _full_check(wl)
 
 
-def test_mxfp4_full_size_sampled():
-    wl = W.config("mxfp4_varlen", device="cuda")
-    out = run_path(wl)
-    assert int(out["status"].item()) == 0, dsa.status_string(int(out["status"].item()))
-    host = wl.to("cpu")
-    rows = sample_rows(wl.num_rows, 4, seed=6)
-    ref, bound, _ = check_logits(host, out["logits"], rows=rows)
-    check_topk_exact(out["logits"], out["idx"], host.context_lens, wl.topk)
-    check_topk_tie_band(out["idx"], ref, bound, host.context_lens, wl.topk, rows)
+def test_mxfp4_full_size_every_row():
+    _full_size_every_row("mxfp4_varlen")
 
 
 # ---------------------------------------------------------------- CUDA graphs
