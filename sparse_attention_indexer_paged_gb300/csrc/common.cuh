@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 #include "dsa_indexer.h"
 
@@ -64,6 +65,27 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s
 constexpr uint64_t kDrainTimeoutNs = 200000000ull;   // 0.2 s
 // Longest a waiting thread sleeps inside one try_wait before it re-checks
 // the abort flag and the clock (it wakes earlier when the phase completes).
+
+// Launch `kernel` so that it may start while the kernel before it on the
+// stream is still running (programmatic dependent launch): its blocks set up
+// (barriers, TMEM) and then wait at grid_dep_wait() until that kernel has
+// finished and its writes are visible.  The earlier kernel lets it start with
+// grid_dep_launch(); without one it starts at that kernel's end.
+template <typename... P, typename... A>
+cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 
 // ----------------------------------------------------------------- launchers
 // (defined in the kernel translation units, called by api.cu after the

@@ -136,6 +136,7 @@ template <int kFmt> struct Smem : Lay<kFmt> {
   static_assert(kBytes <= 232448, "over the per-CTA shared memory limit");
 };
 static_assert(kSlots * kPairCols == kTmemCols, "TMEM slots");
+static_assert(kGroupMaxRows <= kSlots, "a tile's pairs take distinct TMEM slots");
 static_assert(Lay<DSA_KV_FP8>::kKStages == kTileRing, "FP8 tiles signal their pairs on the K stage's own barrier");
 static_assert(kFp4AHalfLo == (kTileTokens * 128) >> 4, "f16 K operand halves as laid out by the dequantising warps");
 static_assert(kPassRowsOf<DSA_KV_FP4> <= kMaxPassRows && kPassRowsOf<DSA_KV_MXFP4> <= kMaxPassRows &&
@@ -326,6 +327,11 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // The schedule (and everything else an earlier kernel on the stream wrote)
+  // is read only once that kernel has finished; the kernel after this one
+  // (the top-k) may be scheduled as this one's CTAs leave their SMs.
+  grid_dep_wait();
+  grid_dep_launch();
   // ---- the schedule must be the one built for these rows, mode and SM count
   const int32_t* sched = p.schedule;
   const int S = p.num_sms;
@@ -740,19 +746,34 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       if (!ok) break;
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
         const uint32_t st = it & (kStages - 1);
-        ok = warp_wait(bars.kvf(st), (it / kStages) & 1, abort_flag, p.status);
+        // A wait that finds its phase complete still costs a few hundred
+        // cycles.  With FP8 keys the K stage and most slots are ready when
+        // the MMA warp comes to them (the K stream runs ahead), so each
+        // barrier is first tested without blocking; the dequantising formats
+        // wait at once (their stages and slots are mostly still pending, and
+        // a test first only delays the wake-up).  The warp votes once per
+        // wait group.
+        {
+          const uint32_t kvp = (it / kStages) & 1;
+          ok = __all_sync(0xffffffffu, (!kDq && mbar_test(bars.kvf(st), kvp)) ||
+                                           wait_or_abort(bars.kvf(st), kvp, abort_flag, p.status));
+        }
         if (!ok) break;
-        tc_fence_after();
         const uint32_t a_lo = a_lo0 + st * kStageLo;
         uint32_t b_lo = q_lo0;
         uint32_t left = n;
         do {  // the tile's rows, cut where a TMEM buffer ends
           const uint32_t c = pos & (kSlots - 1);
           const uint32_t len = min(min(left, kSlots - c), 4u);  // contiguous slots, N <= 256
-          // pair pos + i goes to slot (b, c + i), whose previous use (by the
-          // pair 8 positions earlier) its warpgroup must have read
-          for (uint32_t i = 0; i < len && ok; ++i)
-            ok = warp_wait(bars.te(c + i), (((pos + i) / kSlots) & 1) ^ 1, abort_flag, p.status);
+          // pair pos + i goes to slot c + i, free once the pair 8 positions
+          // earlier has been read by its warpgroup (a tile's n <= 8 pairs
+          // take n distinct slots); each chunk waits only for its own slots
+          bool mine = true;
+          for (uint32_t i = 0; i < len && mine; ++i) {
+            const uint32_t b = bars.te(c + i), pr = (((pos + i) / kSlots) & 1) ^ 1;
+            mine = (!kDq && mbar_test(b, pr)) || wait_or_abort(b, pr, abort_flag, p.status);
+          }
+          ok = __all_sync(0xffffffffu, mine);
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem + c * kPairCols;
@@ -762,6 +783,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
           pos += len;
           b_lo += len * kQRowLo;
         } while (left != 0);
+        if (!ok) break;
         if (!ok) break;
         // one commit per tile: the K stage is free and every pair of the tile
         // is in TMEM once it fires (each commit costs the issuing thread about
@@ -866,6 +888,13 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     }
   }
 
+  // After an abort (a wait that timed out), let any copy still in flight
+  // land before the CTA's shared memory and TMEM are given up.
+  if (*abort_flag) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < kDrainTimeoutNs) {
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -907,8 +936,8 @@ cudaError_t launch_as(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const P
   constexpr int kBytes = Smem<kFmt>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(logits_kernel<kFmt, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
   if (e != cudaSuccess) return e;
-  logits_kernel<kFmt, OutT><<<grid, kThreadsOf<kFmt>, kBytes, stream>>>(tm_q, tm_kv, p);
-  return cudaGetLastError();
+  return launch_dependent(logits_kernel<kFmt, OutT>, dim3(grid), dim3(kThreadsOf<kFmt>), kBytes, stream, tm_q,
+                          tm_kv, p);
 }
 
 template <int kFmt>

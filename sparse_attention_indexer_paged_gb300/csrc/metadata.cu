@@ -31,6 +31,7 @@
 // a_i (bisection; the pairs consumed fall as more units come from the left);
 // thread 0 for the monotone pass.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace dsa {
 namespace {
@@ -149,6 +150,8 @@ template <bool kInSmem>
 __global__ void __launch_bounds__(kThreads, 1)
     metadata_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ ind, int32_t T,
                     int32_t S, int32_t* __restrict__ sched) {
+  // the logits kernel launched after this one may start its set-up now
+  grid_dep_launch();
   extern __shared__ int32_t dyn[];
   __shared__ int32_t buf32[kWarps];
   __shared__ int64_t buf64[kWarps];

@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
     topk_kernel(const LT* __restrict__ logits, int64_t stride, const int32_t* __restrict__ starts,
                 const int32_t* __restrict__ ends, int32_t k, int32_t* __restrict__ out,
                 int64_t out_stride, int32_t* status) {
+  grid_dep_wait();  // the logits come from the kernel before this one
   constexpr int kThreads = C::kThreads, kWarps = C::kWarps;
   constexpr int kFastMaxCols = C::kFastMaxCols, kCandCap = C::kCandCap;
   constexpr int kOffHist = C::kOffHist, kOffSel = C::kOffSel, kOffTie = C::kOffTie;
@@ -666,6 +667,7 @@ __global__ void __launch_bounds__(kShortThreads, kCols <= 8192 ? 4 : 3)
     topk_short_kernel(const LT* __restrict__ logits, int64_t stride, const int32_t* __restrict__ starts,
                       const int32_t* __restrict__ ends, int32_t k, int32_t* __restrict__ out,
                       int64_t out_stride) {
+  grid_dep_wait();  // the logits come from the kernel before this one
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);  // [kCols], column a + i at i
   uint32_t* hist = keys + kCols;                       // [kBins]
@@ -839,9 +841,8 @@ cudaError_t launch_long(const void* logits, int64_t stride, const int32_t* start
   const cudaError_t e =
       cudaFuncSetAttribute(topk_kernel<LT, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  topk_kernel<LT, C><<<num_rows, C::kThreads, C::kSmemBytes, stream>>>(static_cast<const LT*>(logits), stride,
-                                                                       starts, ends, k, out, out_stride, status);
-  return cudaGetLastError();
+  return launch_dependent(topk_kernel<LT, C>, dim3(num_rows), dim3(C::kThreads), C::kSmemBytes, stream,
+                          static_cast<const LT*>(logits), stride, starts, ends, k, out, out_stride, status);
 }
 
 template <typename LT, int kCols>
@@ -850,9 +851,8 @@ cudaError_t launch_short(const void* logits, int64_t stride, const int32_t* star
   const cudaError_t e = cudaFuncSetAttribute(topk_short_kernel<LT, kCols>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kShortSmem<kCols>);
   if (e != cudaSuccess) return e;
-  topk_short_kernel<LT, kCols><<<num_rows, kShortThreads, kShortSmem<kCols>, stream>>>(
-      static_cast<const LT*>(logits), stride, starts, ends, k, out, out_stride);
-  return cudaGetLastError();
+  return launch_dependent(topk_short_kernel<LT, kCols>, dim3(num_rows), dim3(kShortThreads), kShortSmem<kCols>,
+                          stream, static_cast<const LT*>(logits), stride, starts, ends, k, out, out_stride);
 }
 
 }  // namespace
