@@ -29,7 +29,10 @@
 // One CTA of 1024 threads: chunked block scans for the groups, the stable
 // counting sort by row count and the prefix sums; one thread per boundary for
 // a_i (bisection; the pairs consumed fall as more units come from the left);
-// thread 0 for the monotone pass.
+// thread 0 for the monotone pass.  The groups of one row count n are adjacent
+// in the sorted order and each of their units carries n pairs, so the pairs
+// before unit u are piecewise linear in u with one piece per row count: the
+// bisection evaluates them from the 8 pieces' starts, held in registers.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -79,6 +82,31 @@ __device__ T block_exclusive_sum(T v, T* buf, T* total) {
   return before + inc - v;
 }
 
+// Two exclusive prefix sums over the block with the barriers of one.
+template <typename A, typename B>
+__device__ void block_exclusive_sum2(A va, B vb, A* bufa, B* bufb, A& exa, B& exb, A& tota, B& totb) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const A ia = warp_inclusive_sum(va);
+  const B ib = warp_inclusive_sum(vb);
+  if (lane == 31) {
+    bufa[warp] = ia;
+    bufb[warp] = ib;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const A sa = warp_inclusive_sum(bufa[lane]);
+    const B sb = warp_inclusive_sum(bufb[lane]);
+    bufa[lane] = sa;
+    bufb[lane] = sb;
+  }
+  __syncthreads();
+  exa = (warp ? bufa[warp - 1] : A(0)) + ia - va;
+  exb = (warp ? bufb[warp - 1] : B(0)) + ib - vb;
+  tota = bufa[kWarps - 1];
+  totb = bufb[kWarps - 1];
+  __syncthreads();
+}
+
 __device__ int block_inclusive_max(int v, int* buf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int inc = warp_inclusive_max(v);
@@ -99,46 +127,35 @@ __device__ int block_inclusive_max(int v, int* buf) {
 constexpr int kSmemRows = 8192;
 constexpr int kSchedArrays = 5;  // grs, pos, sus, spp_lo, spp_hi
 
-// A coarse map from units to sorted positions for the boundary search:
-// entry c is the largest position k with sus[k] <= c * 2^shift, so the
-// position holding unit u lies in [coarse[u >> shift], coarse[(u >> shift) + 1]].
-constexpr int kCoarse = 2048;
+// The sorted unit sequence as one linear piece per row count n = 1 ..
+// kGroupMaxRows: units [u0[n], u0[n + 1]) carry n pairs each, p0[n] pairs
+// before the first of them (u0 non-decreasing, u0[1] = 0; an empty piece
+// starts where the next one does).
+struct ClassPieces {
+  int32_t u0[kGroupMaxRows + 1];  // in registers: the thresholds
+  const int32_t* su0;             // shared copies, indexed by row count
+  const int64_t* sp0;
 
-struct SortedUnits {
-  const int32_t* pos;
-  const int32_t* sus;
-  const int32_t* spp_lo;
-  const int32_t* spp_hi;
-  const int32_t* coarse;
-  int shift;
-  int G;
-  int64_t P;
-
-  // Pairs of the first u units of the sorted sequence.
-  __device__ __forceinline__ int64_t pairs_before(int64_t u) const {
-    const int64_t c = u >> shift;
-    int lo = coarse[c], hi = min(coarse[c + 1], G);  // largest k in [lo, hi] with sus[k] <= u
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (sus[mid] <= u) lo = mid; else hi = mid - 1;
-    }
-    if (lo >= G) return P;
-    const int64_t before = static_cast<int64_t>(static_cast<uint32_t>(spp_lo[lo])) |
-                           (static_cast<int64_t>(spp_hi[lo]) << 32);
-    return before + (u - sus[lo]) * static_cast<int64_t>(static_cast<uint32_t>(pos[lo]) >> kPosRowsShift);
+  // Pairs of the first u units (0 <= u <= U): the piece holding unit u is the
+  // last one starting at or before u, i.e. the number of pieces that do.
+  __device__ __forceinline__ int64_t pairs_before(int32_t u) const {
+    int n = 0;
+#pragma unroll
+    for (int c = 1; c <= kGroupMaxRows; ++c) n += u >= u0[c] ? 1 : 0;
+    return sp0[n] + static_cast<int64_t>(u - su0[n]) * n;
   }
 
-  // The fewest left units lam in [0, x] with (pairs consumed) * S <= target,
-  // x if none: the pairs consumed, pairs_before(lam) + P - pairs_before(U - x
-  // + lam), do not increase with lam.
-  __device__ __forceinline__ int32_t fewest_left(int64_t x, int64_t U, int64_t S, int64_t target) const {
-    int64_t lo = 0, hi = x;
+  // The fewest left units lam in [0, x] with pairs consumed <= cap, x if
+  // none: the pairs consumed, pairs_before(lam) + P - pairs_before(U - x +
+  // lam), do not increase with lam.
+  __device__ __forceinline__ int32_t fewest_left(int32_t x, int32_t U, int64_t P, int64_t cap) const {
+    int32_t lo = 0, hi = x;
     while (lo < hi) {
-      const int64_t mid = (lo + hi) >> 1;
+      const int32_t mid = (lo + hi) >> 1;
       const int64_t f = pairs_before(mid) + P - pairs_before(U - x + mid);
-      if (f * S <= target) hi = mid; else lo = mid + 1;
+      if (f <= cap) hi = mid; else lo = mid + 1;
     }
-    return static_cast<int32_t>(lo);
+    return lo;
   }
 };
 
@@ -156,13 +173,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int32_t buf32[kWarps];
   __shared__ int64_t buf64[kWarps];
   __shared__ uint64_t bufu[kWarps];
+  __shared__ uint64_t bufu2[kWarps];
   __shared__ int32_t s_carry;
   __shared__ int32_t s_base[kGroupMaxRows + 1];   // first sorted position of each row count
   __shared__ int32_t s_taken[kGroupMaxRows + 1];  // positions of each row count handed out so far
   __shared__ int32_t s_a[kThreads];
   __shared__ int32_t s_x[kThreads];
   __shared__ int32_t s_lambda[kThreads];
-  __shared__ int32_t s_coarse[kCoarse + 2];
+  __shared__ int32_t s_u0[kGroupMaxRows + 1];  // first unit of each row count's piece
+  __shared__ int64_t s_p0[kGroupMaxRows + 1];  // pairs before it
+  __shared__ int64_t s_pq, s_pr;                // P = s_pq * S + s_pr
 
   const int tid = threadIdx.x;
   const SchedLayout L(S, T);
@@ -221,9 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = valid ? grs[g + 1] - grs[g] : 0;
     const uint64_t one_lo = (valid && n <= 4) ? (1ull << (16 * (n - 1))) : 0ull;
     const uint64_t one_hi = (valid && n > 4) ? (1ull << (16 * (n - 5))) : 0ull;
-    uint64_t tot_lo, tot_hi;
-    const uint64_t ex_lo = block_exclusive_sum<uint64_t>(one_lo, bufu, &tot_lo);
-    const uint64_t ex_hi = block_exclusive_sum<uint64_t>(one_hi, bufu, &tot_hi);
+    uint64_t tot_lo, tot_hi, ex_lo, ex_hi;
+    block_exclusive_sum2<uint64_t, uint64_t>(one_lo, one_hi, bufu, bufu2, ex_lo, ex_hi, tot_lo, tot_hi);
     if (valid) {
       const int rank = static_cast<int>(n <= 4 ? (ex_lo >> (16 * (n - 1))) & 0xffffu : (ex_hi >> (16 * (n - 5))) & 0xffffu);
       pos[s_base[n] + s_taken[n] + rank] = grs[g] | (n << kPosRowsShift);
@@ -251,10 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tiles = (lmax + kTileTokens - 1) / kTileTokens;
       pairs = static_cast<int64_t>(tiles) * n;
     }
-    int32_t tot;
-    const int32_t ex = block_exclusive_sum<int32_t>(tiles, buf32, &tot);
-    int64_t totp;
-    const int64_t exp = block_exclusive_sum<int64_t>(pairs, buf64, &totp);
+    int32_t tot, ex;
+    int64_t totp, exp;
+    block_exclusive_sum2<int32_t, int64_t>(tiles, pairs, buf32, buf64, ex, exp, tot, totp);
     if (k < G) {
       sus[k] = U + ex;
       const int64_t pp = P + exp;
@@ -273,28 +291,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  // ---- coarse unit -> position map (entries past the last unit hold G)
-  int shift = 0;
-  while ((static_cast<int64_t>(U) >> shift) >= kCoarse) ++shift;
-  for (int c = tid; c <= kCoarse + 1; c += kThreads) {
-    const int64_t u = static_cast<int64_t>(c) << shift;
-    int lo = 0, hi = G;  // largest k in [0, G] with sus[k] <= u
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (sus[mid] <= u) lo = mid; else hi = mid - 1;
-    }
-    s_coarse[c] = lo;
+  // ---- the pieces: row count n starts at sorted position s_base[n]
+  if (tid >= 1 && tid <= kGroupMaxRows) {
+    const int k = s_base[tid];
+    s_u0[tid] = sus[k];
+    s_p0[tid] = static_cast<int64_t>(static_cast<uint32_t>(spp_lo[k])) | (static_cast<int64_t>(spp_hi[k]) << 32);
+  }
+  if (tid == 0) {
+    s_u0[0] = 0;
+    s_p0[0] = 0;
+    s_pq = P / S;
+    s_pr = P % S;
   }
   __syncthreads();
 
   // ---- a_i: the fewest left units with (pairs consumed) * S <= i * P
   if (tid <= S) {
-    const int64_t x = static_cast<int64_t>(tid) * U / S;
-    s_x[tid] = static_cast<int32_t>(x);
-    const int64_t target = static_cast<int64_t>(tid) * P;
-    // the arrays named from their own shared or global base, so that the
-    // loads use the matching state space
-    s_a[tid] = SortedUnits{pos, sus, spp_lo, spp_hi, s_coarse, shift, G, P}.fewest_left(x, U, S, target);
+    // x = floor(i U / S) and cap = floor(i P / S) without a wide division:
+    // U = q S + r gives i U / S = i q + (i r) / S with i r < 2^20
+    const int32_t uq = U / S, ur = U - uq * S;
+    const int32_t x = tid * uq + (tid * ur) / S;
+    s_x[tid] = x;
+    const int64_t cap = static_cast<int64_t>(tid) * s_pq + static_cast<int64_t>(tid) * s_pr / S;
+    ClassPieces cp;
+#pragma unroll
+    for (int n = 1; n <= kGroupMaxRows; ++n) cp.u0[n] = s_u0[n];
+    cp.su0 = s_u0;
+    cp.sp0 = s_p0;
+    s_a[tid] = cp.fewest_left(x, U, P, cap);
   }
   __syncthreads();
 
