@@ -71,6 +71,8 @@ def parse():
     ap.add_argument("--cpu-budget-s", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config block (the other decode workloads, timed the same way)")
     ap.add_argument("--dcp-world", type=int, default=0,
                     help="time the decode-context-parallel step instead: the workload's keys split "
                          "over this many ranks, every rank emulated in turn on this GPU")
@@ -223,6 +225,123 @@ class ClockSampler:
         sm.sort()
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def measure_fp8_peak(dev):
+    """Dense e4m3 tensor throughput on this GPU, TFLOP/s: a cuBLASLt FP8 GEMM
+    (torch._scaled_mm, 8192^3, bf16 out) timed as a burst after warm-up, the
+    way the bf16 peak beside it was measured.  None if the GEMM is unavailable."""
+    import torch
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.tensor(1.0, device=dev)
+        f = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)  # noqa: E731
+        for _ in range(5):
+            f()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        e0.record()
+        for _ in range(reps):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        sec = e0.elapsed_time(e1) * 1e-3 / reps
+        del a, b
+        return round(2 * n ** 3 / sec / 1e12, 1)
+    except Exception:
+        return None
+
+
+def fp8_peak_tflops(dev, bf16_tf):
+    """(TFLOP/s, how it was obtained) of the dense FP8 tensor rate."""
+    m = measure_fp8_peak(dev)
+    if m is not None:
+        return m, "measured in this run: cuBLASLt e4m3 GEMM 8192^3 (torch._scaled_mm), burst"
+    return bf16_tf * FP8_PEAK_RATIO, f"bf16 peak x {FP8_PEAK_RATIO} (nominal fp8:bf16 ratio; the FP8 GEMM was unavailable)"
+
+
+def measure_config(name, dev, K=200, KB=100, fp8_tf=None, hbm_gbs=None):
+    """One decode workload timed as the headline is: the three-kernel step
+    replayed from a CUDA graph (K replays), then a per-kernel event loop (KB
+    steps); the logits kernel's achieved GB/s against the bytes it must move."""
+    import torch
+    import sparse_attention_indexer_paged_gb300 as dsa
+    import workloads as W
+    wl = W.config(name, device=dev)
+    T, S = wl.num_rows, dsa.device_num_sms()
+    sched = torch.empty(dsa.schedule_words(S, T), dtype=torch.int32, device=dev)
+    ldt = torch.float32 if wl.logits_dtype == W.LOGITS_F32 else torch.bfloat16
+    logits = torch.empty((T, wl.logits_stride), dtype=ldt, device=dev)
+    idx = torch.empty((T, wl.topk), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    gs = torch.cuda.Stream(device=dev)
+
+    def run(ev=None):
+        # the binding launches on the current stream: gs
+        with torch.cuda.stream(gs):
+            if ev is not None:
+                ev[0].record(gs)
+            dsa.paged_mqa_logits_metadata(wl.context_lens, wl.indices, S, out=sched)
+            if ev is not None:
+                ev[1].record(gs)
+            dsa.fp8_fp4_paged_mqa_logits(wl.q, wl.kv_cache, wl.weights, wl.context_lens, wl.block_table, sched,
+                                         indices=wl.indices, kv_format=wl.kv_format, logits_dtype=wl.logits_dtype,
+                                         logits_stride=wl.logits_stride, num_sms=S, status=status, out=logits,
+                                         q_scale=wl.q_scale)
+            if ev is not None:
+                ev[2].record(gs)
+            dsa.top_k_per_row(logits, None, wl.context_lens, wl.topk, out=idx, status=status)
+            if ev is not None:
+                ev[3].record(gs)
+
+    gs.wait_stream(torch.cuda.current_stream(dev))
+    for _ in range(3):
+        run()
+    gs.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=gs, capture_error_mode="relaxed"):
+        run()
+    with torch.cuda.stream(gs):
+        for _ in range(5):
+            g.replay()
+        gs.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(gs)
+        for _ in range(K):
+            g.replay()
+        t1.record(gs)
+    gs.synchronize()
+    step_us = t0.elapsed_time(t1) * 1e3 / K
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KB)]
+    for i in range(KB):
+        run(evs[i])
+    gs.synchronize()
+    kus = [sum(e[j].elapsed_time(e[j + 1]) for e in evs) * 1e3 / KB for j in range(3)]
+    assert int(status.item()) == 0, dsa.status_string(int(status.item()))
+    key_b, logit_b, small_b, flops = algorithmic_bytes(wl)
+    alg = key_b + logit_b + small_b
+    t_mem = alg / (hbm_gbs * 1e9)
+    t_tc = flops / (fp8_tf * 1e12)
+    achieved = alg / (kus[1] * 1e-6) / 1e9
+    res = {
+        "workload": workload_desc(name, wl),
+        "step_us": round(step_us, 3),
+        "kernels_us": {"metadata": round(kus[0], 3), "logits": round(kus[1], 3), "top_k": round(kus[2], 3)},
+        "logits_algorithmic_bytes": alg,
+        "logits_achieved_gbs": round(achieved, 1),
+        "logits_roofline_frac": round(achieved / hbm_gbs, 4),
+        "logits_bound": "hbm" if t_mem >= t_tc else "tensor",
+        "bound_us": round(max(t_mem, t_tc) * 1e6, 2),
+        "logits_frac_of_bound": round(max(t_mem, t_tc) / (kus[1] * 1e-6), 4),
+        "step_roofline_frac": round(max(t_mem, t_tc) / (step_us * 1e-6), 4),
+        "steps": K,
+    }
+    del wl, logits, idx, sched, g
+    torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -465,7 +584,7 @@ def run_ours(args, rank, world, local):
     key_b, logit_b, small_b, flops = algorithmic_bytes(wl)
     alg_bytes = key_b + logit_b + small_b
     achieved = alg_bytes / (logit_ms * 1e-3) / 1e9
-    fp8_tf = bf16_tf * FP8_PEAK_RATIO
+    fp8_tf, fp8_src = fp8_peak_tflops(dev, bf16_tf)
     t_mem = alg_bytes / (hbm_gbs * 1e9)
     t_tc = flops / (fp8_tf * 1e12)
     traffic = profile_traffic("logits.cu", f"logits_{args.workload}_ncu.md")
@@ -510,6 +629,7 @@ def run_ours(args, rank, world, local):
                            else "fallback 6.8 TB/s",
             "tensor_frac_of_fp8_peak": round(flops / (logit_ms * 1e-3) / 1e12 / fp8_tf, 4),
             "fp8_peak_tflops": fp8_tf,
+            "fp8_peak_source": fp8_src,
             "bound_us": round(max(t_mem, t_tc) * 1e6, 2),
             "step_roofline_frac": round(max(t_mem, t_tc) / (ms_step * 1e-3), 4),
         },
@@ -522,6 +642,11 @@ def run_ours(args, rank, world, local):
         "clocks": clk,
         "context": PAGES_CONTEXT,
     }
+    if rank == 0 and not args.no_per_config:
+        # the other decode configurations, each timed the same way (graph
+        # replays, per-kernel events) with its own roofline
+        others = [c for c in ("plain", "mtp", "varlen", "fp4_varlen", "mxfp4_varlen") if c != args.workload]
+        result["per_config"] = {c: measure_config(c, dev, fp8_tf=fp8_tf, hbm_gbs=hbm_gbs) for c in others}
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl.to("cpu"), args.cpu_budget_s)
     if world > 1:
