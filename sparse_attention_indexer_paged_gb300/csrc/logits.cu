@@ -18,33 +18,36 @@
 // are 32 consecutive columns.
 //
 // The CTA's (tile, row) pairs form one stream: pair p goes to TMEM slot
-// (buffer (p / 4) mod 2, column block p mod 4) and is drained by epilogue
-// warpgroup p mod 4, so each warpgroup owns two 64-column slots and uses them
-// alternately.  Every slot has its own full/empty barrier pair: the MMA
-// waits only for the warpgroup whose slot it is about to overwrite, and one
-// slow warpgroup does not hold up the others.  A tile's consecutive pairs
-// within a buffer still go out as one MMA of N = 64 x pairs, followed by one
-// commit per slot.
+// p mod 8 (64 columns each) and is drained by epilogue warpgroup p mod 4.  A
+// tile's consecutive pairs go out as few MMAs of N = 64 x pairs as the slot
+// ring allows (N <= 256, cut where the ring wraps); each chunk waits only for
+// its own slots, released by the warpgroups that read their previous pairs,
+// and one commit per tile tells the epilogue that all its pairs are in TMEM.
 //
-// Rings: K values (kStages tiles, released by the MMA commit) and key scales
-// (kScaleStages tiles, released by the epilogue, loaded by their own warp)
-// are separate, so the HBM prefetch depth does not depend on how far behind
-// the epilogue runs.
+// Rings: K tiles (kStages, released by the tile's MMA commit) and, for FP8,
+// the tiles' key scales, which the K producer copies beside the values on the
+// same barrier into a ring of kScaleStages tiles that the epilogue reads once
+// the tile's commit has fired.
 //
-// Warp roles (640 threads):
+// Warp roles (FP8: 640 threads):
 //   warp 0      K producer: per tile the two K pages (3-D tensor map over the
-//               pool, page id from the block table); runs ahead across groups.
+//               pool, page id from the block table) and their key scales;
+//               runs ahead across groups.
 //   warp 1      MMA issuer and TMEM owner (512 columns): the whole warp walks
 //               the work with warp-uniform values; one elected lane issues.
 //               For FP8 keys it also loads each group's Q rows once the
 //               previous group's MMAs have completed.
 //   warp 2      per group: head weights and causal limits (double buffered).
-//   warp 3      key scales, up to kScaleStages tiles ahead.
+//   warp 3      FP8: no role.  FP4 / MXFP4: one of six dequantising warps
+//               (2, 3, 20-23) that turn raw pages into f16 K tiles.
 //   warps 4-19  four epilogue warpgroups: tcgen05.ld of a pair, relu,
 //               packed-fp32 FMA with the head weights, key scale, causal
-//               mask, store.  Each warp visits only its own pairs and waits
-//               on the mbarriers itself (all lanes, so every lane's reads
-//               are ordered after the completed phase).
+//               mask, store.  Each warp visits only its own pairs.
+//
+// A wait on an mbarrier that has already completed still costs the waiting
+// warp a few hundred cycles; with FP8 keys most of the MMA warp's waits find
+// their phase complete, so it tests each barrier without blocking first.
+// Every wait is bounded (a CTA abort flag and DSA_ERR_TIMEOUT after 2 s).
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
