@@ -412,6 +412,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
       sel[i] = 0;
       tie[i] = 0;
     }
+    if (tid < kWarps) s_wcount[tid] = 0;
     const int ns = 4 * nsq;
     const int64_t want = sv == 1 ? k : (3 * static_cast<int64_t>(k)) / (2 * sv) + 16;
     uint32_t t = 0;  // stays 0 if the sample is not larger than want: every non-NaN score qualifies
@@ -439,16 +440,17 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
     // are compared with t's float form; only candidates are turned into keys.
     // t >= 1 leaves out NaN scores (key 0): if fewer than k keys then reach
     // t, the exact passes below run.  Each warp appends to its own slice of
-    // the candidate arrays, its count held in a register (a ballot per key
-    // position places the lanes' candidates, no shared atomics); the slices
-    // are packed afterwards.
+    // the candidate arrays; about 1.5 k of the row's scores reach t, so a
+    // 4-score vector is tested by its maximum first and a candidate takes its
+    // slot with one shared atomic on the warp's counter (the counter keeps
+    // counting past the slice, which marks an overflow); the slices are
+    // packed afterwards.
     t = max(t, 1u);
     const float tf = key_floor(t);
     constexpr int kWarpCap = kCandCap / kWarps;
     uint32_t* wkey = cand_key + warp * kWarpCap;  // this warp's slice, packed later
     int32_t* wcol = reinterpret_cast<int32_t*>(smem + kOffStage) + warp * kWarpCap;
-    const uint32_t lanes_below = (1u << lane) - 1u;
-    uint32_t wcount = 0;  // candidates this warp has seen (the same in every lane)
+    uint32_t* wcnt = s_wcount + warp;
     constexpr int64_t kStep = 4 * static_cast<int64_t>(kThreads) * kLoadsInFlight;
     for (int64_t base = a4; base < b; base += kStep) {
       typename Vec4<LT>::T v[kLoadsInFlight];
@@ -467,22 +469,21 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
 #pragma unroll
           for (int e = 0; e < 4; ++e) xq[e] = (i + e >= a && i + e < b) ? load_score<LT>(rp, i + e) : __int_as_float(0x7fffffff);
         }
+        // fmaxf ignores a NaN operand; an all-NaN vector has no candidate
+        if (fmaxf(fmaxf(xq[0], xq[1]), fmaxf(xq[2], xq[3])) >= tf) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const bool c = xq[e] >= tf;
-          const uint32_t m = __ballot_sync(0xffffffffu, c);
-          if (c) {
-            const uint32_t slot = wcount + __popc(m & lanes_below);
-            if (slot < static_cast<uint32_t>(kWarpCap)) {
-              wkey[slot] = order_key(xq[e]);
-              wcol[slot] = static_cast<int32_t>(i + e);
+          for (int e = 0; e < 4; ++e) {
+            if (xq[e] >= tf) {
+              const uint32_t slot = atomicAdd(wcnt, 1u);
+              if (slot < static_cast<uint32_t>(kWarpCap)) {
+                wkey[slot] = order_key(xq[e]);
+                wcol[slot] = static_cast<int32_t>(i + e);
+              }
             }
           }
-          wcount += __popc(m);
         }
       }
     }
-    if (lane == 0) s_wcount[warp] = wcount;
     __syncthreads();
     // pack the slices: cand_key in place (slices only move down), columns
     // from the ring area into cand_col
