@@ -451,23 +451,29 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
     uint32_t* wkey = cand_key + warp * kWarpCap;  // this warp's slice, packed later
     int32_t* wcol = reinterpret_cast<int32_t*>(smem + kOffStage) + warp * kWarpCap;
     uint32_t* wcnt = s_wcount + warp;
-    constexpr int64_t kStep = 4 * static_cast<int64_t>(kThreads) * kLoadsInFlight;
-    for (int64_t base = a4; base < b; base += kStep) {
-      typename Vec4<LT>::T v[kLoadsInFlight];
+    // columns as 32-bit offsets from a4 (rows are far below 2^31 columns),
+    // eight 16-byte loads a thread in flight
+    constexpr int kPassLoads = 8;
+    constexpr int32_t kStep = 4 * kThreads * kPassLoads;
+    const LT* rq = rp + a4;
+    const int32_t na = static_cast<int32_t>(a - a4), nb = static_cast<int32_t>(b - a4);
+    const int32_t col0 = static_cast<int32_t>(a4);
+    for (int32_t base = 0; base < nb; base += kStep) {
+      typename Vec4<LT>::T v[kPassLoads];
 #pragma unroll
-      for (int u = 0; u < kLoadsInFlight; ++u) {
-        const int64_t i = base + 4 * (tid + static_cast<int64_t>(u) * kThreads);
-        if (i + 3 < b && i >= a) v[u] = Vec4<LT>::load(rp, i);
+      for (int u = 0; u < kPassLoads; ++u) {
+        const int32_t i = base + 4 * (tid + u * kThreads);
+        if (i + 3 < nb && i >= na) v[u] = Vec4<LT>::load(rq, i);
       }
 #pragma unroll
-      for (int u = 0; u < kLoadsInFlight; ++u) {
-        const int64_t i = base + 4 * (tid + static_cast<int64_t>(u) * kThreads);
+      for (int u = 0; u < kPassLoads; ++u) {
+        const int32_t i = base + 4 * (tid + u * kThreads);
         float xq[4];
-        if (i + 3 < b && i >= a) {
+        if (i + 3 < nb && i >= na) {
           Vec4<LT>::vals(v[u], xq);
         } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) xq[e] = (i + e >= a && i + e < b) ? load_score<LT>(rp, i + e) : __int_as_float(0x7fffffff);
+          for (int e = 0; e < 4; ++e) xq[e] = (i + e >= na && i + e < nb) ? load_score<LT>(rq, i + e) : __int_as_float(0x7fffffff);
         }
         // fmaxf ignores a NaN operand; an all-NaN vector has no candidate
         if (fmaxf(fmaxf(xq[0], xq[1]), fmaxf(xq[2], xq[3])) >= tf) {
@@ -477,7 +483,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
               const uint32_t slot = atomicAdd(wcnt, 1u);
               if (slot < static_cast<uint32_t>(kWarpCap)) {
                 wkey[slot] = order_key(xq[e]);
-                wcol[slot] = static_cast<int32_t>(i + e);
+                wcol[slot] = col0 + i + e;
               }
             }
           }
