@@ -28,11 +28,12 @@
 //
 // One CTA of 1024 threads: chunked block scans for the groups, the stable
 // counting sort by row count and the prefix sums; one thread per boundary for
-// a_i (bisection; the pairs consumed fall as more units come from the left);
-// thread 0 for the monotone pass.  The groups of one row count n are adjacent
-// in the sorted order and each of their units carries n pairs, so the pairs
-// before unit u are piecewise linear in u with one piece per row count: the
-// bisection evaluates them from the 8 pieces' starts, held in registers.
+// a_i; thread 0 for the monotone pass.  The groups of one row count n are
+// adjacent in the sorted order and each of their units carries n pairs, so
+// the pairs before unit u are piecewise linear in u with one piece per row
+// count, and so are the pairs consumed at boundary i as a function of the
+// left units: a_i is solved exactly from their values where either end
+// enters a new piece (ClassPieces::fewest_left).
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -146,16 +147,53 @@ struct ClassPieces {
   }
 
   // The fewest left units lam in [0, x] with pairs consumed <= cap, x if
-  // none: the pairs consumed, pairs_before(lam) + P - pairs_before(U - x +
-  // lam), do not increase with lam.
+  // none.  The pairs consumed, f(lam) = pairs_before(lam) + P -
+  // pairs_before(U - x + lam), do not increase with lam and are linear
+  // between the points where either end enters a new piece: lam = u0[c]
+  // (there pairs_before(lam) = p0[c]) and lam = u0[c] - (U - x) (there the
+  // right term is p0[c]).  f at those points (independent evaluations) gives
+  // the last point above cap and the first at or below it; between the two f
+  // falls by a whole number of pairs per unit, which gives lam exactly.
   __device__ __forceinline__ int32_t fewest_left(int32_t x, int32_t U, int64_t P, int64_t cap) const {
-    int32_t lo = 0, hi = x;
-    while (lo < hi) {
-      const int32_t mid = (lo + hi) >> 1;
-      const int64_t f = pairs_before(mid) + P - pairs_before(U - x + mid);
-      if (f <= cap) hi = mid; else lo = mid + 1;
+    const int32_t off = U - x;  // the right end is off + lam
+    const int64_t f0 = P - pairs_before(off);
+    if (f0 <= cap) return 0;
+    const int64_t fx = pairs_before(x);  // + P - pairs_before(U)
+    if (fx > cap) return x;
+    int32_t blo = 0, bhi = x;  // last point above cap, first at or below
+    int64_t flo = f0, fhi = fx;
+#pragma unroll
+    for (int c = 2; c <= kGroupMaxRows; ++c) {
+      const int32_t bl = u0[c], br = u0[c] - off;
+      const bool inl = bl > 0 && bl < x, inr = br > 0 && br < x;
+      const int64_t fl = sp0[c] + P - pairs_before(inl ? off + bl : 0);
+      const int64_t fr = pairs_before(inr ? br : 0) + P - sp0[c];
+      if (inl) {
+        if (fl > cap) {
+          if (bl > blo) { blo = bl; flo = fl; }
+        } else if (bl < bhi) {
+          bhi = bl;
+          fhi = fl;
+        }
+      }
+      if (inr) {
+        if (fr > cap) {
+          if (br > blo) { blo = br; flo = fr; }
+        } else if (br < bhi) {
+          bhi = br;
+          fhi = fr;
+        }
+      }
     }
-    return lo;
+    // f falls by d = (row count at the right end) - (row count at the left
+    // end) pairs a unit, 1 <= d <= 7; both divisions in 32 bits when the
+    // operands fit (a 64-bit division costs ~1.5K cycles)
+    const uint64_t num = static_cast<uint64_t>(flo - fhi), den = static_cast<uint64_t>(bhi - blo);
+    const uint32_t d = (num >> 32) == 0 ? static_cast<uint32_t>(num) / static_cast<uint32_t>(den)
+                                        : static_cast<uint32_t>(num / den);
+    const uint64_t q = static_cast<uint64_t>(flo - cap) + d - 1;
+    const uint64_t steps = (q >> 32) == 0 ? static_cast<uint32_t>(q) / d : q / d;
+    return blo + static_cast<int32_t>(steps);
   }
 };
 
