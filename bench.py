@@ -284,7 +284,7 @@ def measure_config(name, dev, K=200, KB=100, fp8_tf=None, hbm_gbs=None):
         with torch.cuda.stream(gs):
             if ev is not None:
                 ev[0].record(gs)
-            dsa.paged_mqa_logits_metadata(wl.context_lens, wl.indices, S, out=sched)
+            dsa.paged_mqa_logits_metadata(wl.context_lens, wl.indices, S, out=sched, kv_format=wl.kv_format)
             if ev is not None:
                 ev[1].record(gs)
             dsa.fp8_fp4_paged_mqa_logits(wl.q, wl.kv_cache, wl.weights, wl.context_lens, wl.block_table, sched,
@@ -377,7 +377,7 @@ def run_ours(args, rank, world, local):
 
     def make_calls(q, w, ctx, ind, bt, out_idx, qs=None, strm=None):
         sp_ = sp if strm is None else strm
-        meta = (P(ctx), P(ind), T, 64, S, P(sched), sp_)
+        meta = (P(ctx), P(ind), T, 64, S, wl.kv_format, P(sched), sp_)  # groups sized for the key format
         # MXFP4 keys: the MXFP4 entry point with the q scales; else the key format
         head = (P(q), P(qs), P(wl.kv_cache), wl.page_stride, wl.num_pages) if mx else \
                (P(q), P(wl.kv_cache), wl.page_stride, wl.num_pages, wl.kv_format)
@@ -392,7 +392,7 @@ def run_ours(args, rank, world, local):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        r1 = L.dsa_paged_mqa_logits_metadata(*meta)
+        r1 = L.dsa_paged_mqa_logits_metadata_for_keys(*meta)
         if ev is not None:
             ev[1].record(stream)
         r2 = logits_fn(*lg)
@@ -416,7 +416,7 @@ def run_ours(args, rank, world, local):
     meta_g, lg_g, tk_g = meta[:-1] + (gsp,), lg[:-1] + (gsp,), tk[:-1] + (gsp,)
 
     def gstep():
-        return L.dsa_paged_mqa_logits_metadata(*meta_g) | logits_fn(*lg_g) | L.dsa_top_k_per_row(*tk_g)
+        return L.dsa_paged_mqa_logits_metadata_for_keys(*meta_g) | logits_fn(*lg_g) | L.dsa_top_k_per_row(*tk_g)
 
     gstream.wait_stream(stream)
     with torch.cuda.stream(gstream):
@@ -510,11 +510,11 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         m, lgc, tkc = calls
         with torch.cuda.stream(s_cmp):
-            assert (L.dsa_paged_mqa_logits_metadata(*m) | logits_fn(*lgc) | L.dsa_top_k_per_row(*tkc)) == 0
+            assert (L.dsa_paged_mqa_logits_metadata_for_keys(*m) | logits_fn(*lgc) | L.dsa_top_k_per_row(*tkc)) == 0
         s_cmp.synchronize()
         graph_set = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_set, stream=s_cmp, capture_error_mode="relaxed"):
-            assert (L.dsa_paged_mqa_logits_metadata(*m) | logits_fn(*lgc) | L.dsa_top_k_per_row(*tkc)) == 0
+            assert (L.dsa_paged_mqa_logits_metadata_for_keys(*m) | logits_fn(*lgc) | L.dsa_top_k_per_row(*tkc)) == 0
         sets.append(dict(dblob=dblob, didx=didx, graph=graph_set))
     h2d_bytes = blob_bytes
     d2h_bytes = hidx[0].numel() * hidx[0].element_size()
@@ -683,7 +683,7 @@ def run_dcp(args, local):
         logits = torch.empty((T, wl.logits_stride), dtype=ldt, device=dev)
         idx = torch.empty((T, k), dtype=torch.int32, device=dev)
         packed = torch.empty((T, k, 2), dtype=torch.float32, device=dev)
-        meta = (P(wl.context_lens), P(wl.indices), T, 64, S, P(sched), sp)
+        meta = (P(wl.context_lens), P(wl.indices), T, 64, S, wl.kv_format, P(sched), sp)
         lg = (P(wl.q), P(wl.kv_cache), wl.page_stride, wl.num_pages, wl.kv_format, P(wl.weights),
               P(wl.context_lens), P(wl.block_table), wl.block_table.stride(0), P(wl.indices), P(sched), S,
               P(logits), wl.logits_dtype, wl.logits_stride, T, 64, 128, 64, P(status), sp)
@@ -704,7 +704,7 @@ def run_dcp(args, local):
         for r, c in enumerate(ranks):
             if ev is not None:
                 ev[r][0].record(stream)
-            rc |= L.dsa_paged_mqa_logits_metadata(*c["meta"])
+            rc |= L.dsa_paged_mqa_logits_metadata_for_keys(*c["meta"])
             if ev is not None:
                 ev[r][1].record(stream)
             rc |= L.dsa_fp8_fp4_paged_mqa_logits(*c["lg"])
@@ -726,7 +726,7 @@ def run_dcp(args, local):
         return rc
 
     # the unsharded step, for the exactness check
-    assert (L.dsa_paged_mqa_logits_metadata(*ref["meta"]) | L.dsa_fp8_fp4_paged_mqa_logits(*ref["lg"])
+    assert (L.dsa_paged_mqa_logits_metadata_for_keys(*ref["meta"]) | L.dsa_fp8_fp4_paged_mqa_logits(*ref["lg"])
             | L.dsa_top_k_per_row(*ref["tk"])) == 0
     for _ in range(max(args.warmup, 3)):
         assert step() == 0
@@ -812,7 +812,7 @@ def run_prefill(args, local):
     logits = torch.empty((T, pf.logits_stride), dtype=ldt, device=dev)
     idx = torch.empty((T, k), dtype=torch.int32, device=dev)
     rows_a = (P(pf.cu_seqlen_ks), P(pf.cu_seqlen_ke), T, P(pf.local_cu_seq_lens), B, P(ctx), P(req), P(status), sp)
-    meta_a = (P(ctx), P(req), T, 64, S, P(sched), sp)
+    meta_a = (P(ctx), P(req), T, 64, S, pf.kv_format, P(sched), sp)
     lg_a = (P(pf.q), P(pf.q_scale), P(pf.kv_cache), pf.page_stride, int(pf.kv_cache.shape[0]), pf.kv_format, P(pf.weights),
             P(ctx), P(req), P(pf.block_table), pf.block_table.stride(0), B, P(sched), S, P(logits),
             pf.logits_dtype, pf.logits_stride, T, 64, 128, 64, P(status), sp)
@@ -820,7 +820,7 @@ def run_prefill(args, local):
 
     def step(ev=None):
         rc = 0
-        calls = ((L.dsa_prefill_rows, rows_a), (L.dsa_paged_mqa_logits_metadata, meta_a),
+        calls = ((L.dsa_prefill_rows, rows_a), (L.dsa_paged_mqa_logits_metadata_for_keys, meta_a),
                  (L.dsa_prefill_mqa_logits, lg_a), (L.dsa_top_k_per_row, tk_a))
         for i, (fn, a) in enumerate(calls):
             if ev is not None:

@@ -115,7 +115,8 @@ int32_t dsa_device_num_sms(void);
  *   schedule     (device) int32 [dsa_schedule_words(num_sms, num_rows)], out.
  *
  * Rule (the pages fix the purpose, not the split; this is the library's):
- * runs of equal ids are cut into groups of at most 8 rows; a unit is one
+ * runs of equal ids are cut into groups of at most 8 rows (this call; see
+ * dsa_paged_mqa_logits_metadata_for_keys for other sizes); a unit is one
  * 128-key tile of a group (ceil(max L_t / 128) units per group) and costs its
  * SM one K tile from HBM plus one (tile, row) pair of MMA and epilogue work
  * per row.  The groups are ordered by row count (stable) and their units laid
@@ -123,7 +124,7 @@ int32_t dsa_device_num_sms(void);
  * SM owns floor or ceil of units / num_sms units and, as nearly as the group
  * sizes allow, the same number of (tile, row) pairs.  Layout:
  * header[8] = {0x44534132, num_rows, varlen flag, num_sms, num_groups,
- * num_units, 128, 8}, left[num_sms + 1], right[num_sms + 1] (SM i owns sorted
+ * num_units, 128, group rows (8 here)}, left[num_sms + 1], right[num_sms + 1] (SM i owns sorted
  * units [left[i], left[i+1]) and [right[i+1], right[i])),
  * group_row_start[num_rows + 1], position[num_rows + 1] (first row of the
  * group at sorted position k | its rows << 24), unit_start[num_rows + 1],
@@ -133,6 +134,25 @@ int32_t dsa_device_num_sms(void);
 int dsa_paged_mqa_logits_metadata(const int32_t* context_lens, const int32_t* indices,
                                   int32_t num_rows, int32_t block_kv, int32_t num_sms,
                                   int32_t* schedule, dsa_stream_t stream);
+
+/*
+ * dsa_paged_mqa_logits_metadata_for_keys - the same schedule, with groups cut
+ * at the rows one pass of the logits call serves for that key format:
+ * DSA_KV_FP8 8 (= dsa_paged_mqa_logits_metadata), DSA_KV_MXFP4 6, DSA_KV_FP4 4
+ * (the dequantising formats convert q into a pass-sized buffer, so a larger
+ * group costs one pass per 4 or 6 rows while the split counts it as one unit).
+ * No counterpart in the pages, whose metadata call takes no key format; the
+ * extra argument only sizes the groups (header word 7 records it).  Any
+ * format's logits call accepts a schedule of any group size from 1 to 8;
+ * this one balances the FP4 and MXFP4 calls better.
+ *
+ *   kv_format    DSA_KV_FP8, DSA_KV_FP4 or DSA_KV_MXFP4 (else
+ *                DSA_ERR_INVALID_ARG); the other arguments and the layout are
+ *                those of dsa_paged_mqa_logits_metadata.
+ */
+int dsa_paged_mqa_logits_metadata_for_keys(const int32_t* context_lens, const int32_t* indices,
+                                           int32_t num_rows, int32_t block_kv, int32_t num_sms,
+                                           int32_t kv_format, int32_t* schedule, dsa_stream_t stream);
 
 /*
  * dsa_fp8_fp4_paged_mqa_logits - varlen paged MQA logits.

@@ -82,6 +82,7 @@ _SIGS = {
     "dsa_schedule_words": ([_I32, _I32], _I64),
     "dsa_device_num_sms": ([], _I32),
     "dsa_paged_mqa_logits_metadata": ([_P, _P, _I32, _I32, _I32, _P, _P], ctypes.c_int),
+    "dsa_paged_mqa_logits_metadata_for_keys": ([_P, _P, _I32, _I32, _I32, _I32, _P, _P], ctypes.c_int),
     "dsa_fp8_fp4_paged_mqa_logits": ([_P, _P, _I64, _I64, _I32, _P, _P, _P, _I64, _P, _P, _I32,
                                       _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P],
                                      ctypes.c_int),
@@ -168,8 +169,12 @@ def schedule_words(num_sms: int, num_rows: int) -> int:
 
 
 def paged_mqa_logits_metadata(context_lens, indices=None, num_sms=None, block_kv=BLOCK_KV,
-                              out=None):
-    """Per-SM work schedule (int32 device tensor) for the logits call."""
+                              out=None, kv_format=None):
+    """Per-SM work schedule (int32 device tensor) for the logits call.
+
+    kv_format None: groups of up to 8 rows (dsa_paged_mqa_logits_metadata);
+    KV_FP8 / KV_FP4 / KV_MXFP4: groups sized for that key format's logits
+    call (dsa_paged_mqa_logits_metadata_for_keys)."""
     ctx = context_lens
     device = ctx.device
     T = int(ctx.shape[0])
@@ -181,9 +186,15 @@ def paged_mqa_logits_metadata(context_lens, indices=None, num_sms=None, block_kv
     assert out.dtype == torch.int32 and out.is_contiguous() and out.numel() >= words
     ctx = _dev_i32(ctx, device)
     ind = _dev_i32(indices, device)
-    _check(lib().dsa_paged_mqa_logits_metadata(_ptr(ctx), _ptr(ind), T, int(block_kv),
-                                               int(num_sms), _ptr(out), _stream(device)),
-           "paged_mqa_logits_metadata")
+    if kv_format is None:
+        _check(lib().dsa_paged_mqa_logits_metadata(_ptr(ctx), _ptr(ind), T, int(block_kv),
+                                                   int(num_sms), _ptr(out), _stream(device)),
+               "paged_mqa_logits_metadata")
+    else:
+        _check(lib().dsa_paged_mqa_logits_metadata_for_keys(_ptr(ctx), _ptr(ind), T, int(block_kv),
+                                                            int(num_sms), int(kv_format), _ptr(out),
+                                                            _stream(device)),
+               "paged_mqa_logits_metadata_for_keys")
     return out
 
 

@@ -114,14 +114,22 @@ int32_t dsa_device_num_sms(void) {
 int dsa_paged_mqa_logits_metadata(const int32_t* context_lens, const int32_t* indices,
                                   int32_t num_rows, int32_t block_kv, int32_t num_sms,
                                   int32_t* schedule, dsa_stream_t stream) {
+  return dsa_paged_mqa_logits_metadata_for_keys(context_lens, indices, num_rows, block_kv, num_sms, DSA_KV_FP8,
+                                                schedule, stream);
+}
+
+int dsa_paged_mqa_logits_metadata_for_keys(const int32_t* context_lens, const int32_t* indices,
+                                           int32_t num_rows, int32_t block_kv, int32_t num_sms,
+                                           int32_t kv_format, int32_t* schedule, dsa_stream_t stream) {
   if (num_rows < 0 || num_sms < 1 || schedule == nullptr) return DSA_ERR_INVALID_ARG;
+  if (kv_format != DSA_KV_FP8 && kv_format != DSA_KV_FP4 && kv_format != DSA_KV_MXFP4) return DSA_ERR_INVALID_ARG;
   if (num_rows > 0 && context_lens == nullptr) return DSA_ERR_INVALID_ARG;
   if (num_sms > 1023 || num_rows > kMaxScheduleRows) return DSA_ERR_UNSUPPORTED;
   if (block_kv != kPageTokens) return DSA_ERR_UNSUPPORTED;
   const int dev = check_device();
   if (dev != DSA_OK) return dev;
-  return launch_status(launch_metadata(context_lens, indices, num_rows, num_sms, schedule,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+  return launch_status(launch_metadata(context_lens, indices, num_rows, num_sms, group_rows_for(kv_format),
+                                       schedule, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

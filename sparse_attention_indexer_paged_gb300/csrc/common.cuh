@@ -32,6 +32,14 @@ constexpr int kPageTokens = DSA_BLOCK_KV;   // 64 tokens per page
 //   spp_lo[T + 1], spp_hi[T + 1]  (tile, row) pairs before position k
 constexpr int kTileTokens = 128;
 constexpr int kGroupMaxRows = 8;
+// Rows a group holds for each key format: what one pass of that format's
+// logits kernel over a tile serves (FP8 all 8; the dequantising formats
+// convert q into a pass-sized buffer: MXFP4 6 rows, FP4 4), so that a unit
+// costs one pass.  The logits call takes a schedule of any group size up to
+// kGroupMaxRows.
+__host__ __device__ constexpr int group_rows_for(int kv_format) {
+  return kv_format == DSA_KV_FP4 ? 4 : (kv_format == DSA_KV_MXFP4 ? 6 : kGroupMaxRows);
+}
 constexpr int32_t kScheduleMagic = 0x44534132;
 constexpr int kScheduleHeaderWords = 8;
 constexpr int kPosRowsShift = 24;
@@ -92,7 +100,7 @@ cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, size_t
 // arguments have been checked)
 
 cudaError_t launch_metadata(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
-                            int32_t num_sms, int32_t* schedule, cudaStream_t stream);
+                            int32_t num_sms, int32_t group_rows, int32_t* schedule, cudaStream_t stream);
 
 struct LogitsArgs {
   const uint8_t* q;

@@ -120,7 +120,7 @@ int dsa_indexer_decode_topk(const void* q, const void* q_scale, const void* kv_c
     const int32_t rows = static_cast<int32_t>(e - s);
     const int32_t* ctx = context_lens + s;
     const int32_t* ind = indices ? indices + s : nullptr;
-    st = dsa_paged_mqa_logits_metadata(ctx, ind, rows, block_kv, num_sms, schedule, stream);
+    st = dsa_paged_mqa_logits_metadata_for_keys(ctx, ind, rows, block_kv, num_sms, kv_format, schedule, stream);
     if (st != DSA_OK) return st;
     if (kv_format == DSA_KV_MXFP4) {  // q: packed e2m1 with ue8m0 scales
       st = dsa_mxfp4_paged_mqa_logits(qb + s * int64_t{kHeads} * (kHeadDim / 2),

@@ -140,6 +140,9 @@ template <int kFmt> struct Smem : Lay<kFmt> {
 };
 static_assert(kSlots * kPairCols == kTmemCols, "TMEM slots");
 static_assert(kGroupMaxRows <= kSlots, "a tile's pairs take distinct TMEM slots");
+static_assert(group_rows_for(DSA_KV_FP4) == kPassRowsOf<DSA_KV_FP4> &&
+                  group_rows_for(DSA_KV_MXFP4) == kPassRowsOf<DSA_KV_MXFP4>,
+              "a dequantising format's schedule groups are one row pass each");
 static_assert(Lay<DSA_KV_FP8>::kKStages == kTileRing, "FP8 tiles signal their pairs on the K stage's own barrier");
 static_assert(kFp4AHalfLo == (kTileTokens * 128) >> 4, "f16 K operand halves as laid out by the dequantising warps");
 static_assert(kPassRowsOf<DSA_KV_FP4> <= kMaxPassRows && kPassRowsOf<DSA_KV_MXFP4> <= kMaxPassRows &&
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   const int S = p.num_sms;
   const int T = p.num_rows;
   if (sched[0] != kScheduleMagic || sched[1] != T || sched[2] != (p.indices != nullptr ? 1 : 0) ||
-      sched[3] != S || sched[6] != kTileTokens || sched[7] != kGroupMaxRows ||
+      sched[3] != S || sched[6] != kTileTokens || sched[7] < 1 || sched[7] > kGroupMaxRows ||
       static_cast<int>(gridDim.x) != S || sched[4] < 0 || sched[4] > T || sched[5] < 0) {
     if (threadIdx.x == 0 && blockIdx.x == 0) report(p.status, kErrScheduleMismatch);
     return;

@@ -204,7 +204,7 @@ struct ClassPieces {
 template <bool kInSmem>
 __global__ void __launch_bounds__(kThreads, 1)
     metadata_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ ind, int32_t T,
-                    int32_t S, int32_t* __restrict__ sched) {
+                    int32_t S, int32_t cap, int32_t* __restrict__ sched) {
   // the logits kernel launched after this one may start its set-up now
   grid_dep_launch();
   extern __shared__ int32_t dyn[];
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* spp_lo = base + 3 * n1;
   int32_t* spp_hi = base + 4 * n1;
   // ---- groups: a row starts one when it starts a run of equal request ids,
-  // or when kGroupMaxRows rows of its run precede it in the current group
+  // or when cap (<= kGroupMaxRows) rows of its run precede it in the current group
   int carry_run = 0;  // run start of the previous chunk's last row
   int G = 0;
   for (int base = 0; base < T; base += kThreads) {
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool run_start = valid && (t == 0 || ind == nullptr || ind[t] != ind[t - 1]);
     int rs = block_inclusive_max(run_start ? t : -1, buf32);
     rs = max(rs, carry_run);
-    const bool gstart = valid && ((t - rs) % kGroupMaxRows == 0);
+    const bool gstart = valid && ((t - rs) % cap == 0);
     int32_t total;
     const int32_t idx = block_exclusive_sum<int32_t>(gstart ? 1 : 0, buf32, &total);
     if (gstart) grs[G + idx] = t;
@@ -396,17 +396,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     sched[4] = G;
     sched[5] = U;
     sched[6] = kTileTokens;
-    sched[7] = kGroupMaxRows;
+    sched[7] = cap;
   }
 }
 
 }  // namespace
 
 cudaError_t launch_metadata(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
-                            int32_t num_sms, int32_t* schedule, cudaStream_t stream) {
+                            int32_t num_sms, int32_t group_rows, int32_t* schedule, cudaStream_t stream) {
   static_assert(kSchedArrays * (kSmemRows + 1) * 4 <= 200 * 1024, "metadata shared memory");
   if (num_rows > kSmemRows) {
-    metadata_kernel<false><<<1, kThreads, 0, stream>>>(context_lens, indices, num_rows, num_sms, schedule);
+    metadata_kernel<false><<<1, kThreads, 0, stream>>>(context_lens, indices, num_rows, num_sms, group_rows,
+                                                        schedule);
     return cudaGetLastError();
   }
   const size_t smem = kSchedArrays * (static_cast<size_t>(num_rows) + 1) * 4;
@@ -415,7 +416,8 @@ cudaError_t launch_metadata(const int32_t* context_lens, const int32_t* indices,
                                                kSchedArrays * (kSmemRows + 1) * 4);
     if (e != cudaSuccess) return e;
   }
-  metadata_kernel<true><<<1, kThreads, smem, stream>>>(context_lens, indices, num_rows, num_sms, schedule);
+  metadata_kernel<true><<<1, kThreads, smem, stream>>>(context_lens, indices, num_rows, num_sms, group_rows,
+                                                       schedule);
   return cudaGetLastError();
 }
 

@@ -22,15 +22,19 @@ REL_TOL = 1e-3
 ABS_TOL = 1e-6
 
 
-def run_path(wl, num_sms=None, use_indices=True, logits_out=None):
-    """metadata -> logits -> top-k on cuda:0; returns a dict of device tensors."""
+def run_path(wl, num_sms=None, use_indices=True, logits_out=None, groups_for_keys=True):
+    """metadata -> logits -> top-k on cuda:0; returns a dict of device tensors.
+
+    groups_for_keys: the schedule's groups sized for the workload's key
+    format (else the 8-row groups of the plain metadata call)."""
     dev = torch.device("cuda")
     g = wl if wl.q.is_cuda else wl.to(dev)
     ind = g.indices if use_indices else None
     if num_sms is None:
         num_sms = dsa.device_num_sms()
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    sched = dsa.paged_mqa_logits_metadata(g.context_lens, ind, num_sms)
+    sched = dsa.paged_mqa_logits_metadata(g.context_lens, ind, num_sms,
+                                          kv_format=g.kv_format if groups_for_keys else None)
     logits = dsa.fp8_fp4_paged_mqa_logits(
         g.q, g.kv_cache, g.weights, g.context_lens, g.block_table, sched, indices=ind,
         kv_format=g.kv_format, logits_dtype=g.logits_dtype, logits_stride=g.logits_stride,

@@ -29,8 +29,8 @@ def _lib():
     dsa.lib()
 
 
-def _full_check(wl, num_sms=None, use_indices=True):
-    out = run_path(wl, num_sms=num_sms, use_indices=use_indices)
+def _full_check(wl, num_sms=None, use_indices=True, groups_for_keys=True):
+    out = run_path(wl, num_sms=num_sms, use_indices=use_indices, groups_for_keys=groups_for_keys)
     assert int(out["status"].item()) == 0, dsa.status_string(int(out["status"].item()))
     ref, bound, worst = check_logits(wl, out["logits"])
     check_topk_exact(out["logits"], out["idx"], wl.context_lens, wl.topk)
@@ -58,6 +58,19 @@ def test_metadata_ragged_groups():
     for S in (1, 3, 5, 64, 152):
         got = dsa.paged_mqa_logits_metadata(wl.context_lens.cuda(), wl.indices.cuda(), S)
         check_schedule(got.cpu().numpy(), wl.context_lens.numpy(), wl.indices.numpy(), S)
+
+
+@pytest.mark.parametrize("kv_format,cap", [(W.KV_FP8, 8), (W.KV_FP4, 4), (W.KV_MXFP4, 6)])
+def test_metadata_groups_for_keys(kv_format, cap):
+    """Groups sized for the key format's row pass: the header records the
+    size, and every group is at most that size and cut only where full."""
+    wl = W.build("mixed", **MIXED, topk=64)
+    ctx, ids = wl.context_lens.numpy(), wl.indices.numpy()
+    for S in (1, 5, 152):
+        got = dsa.paged_mqa_logits_metadata(wl.context_lens.cuda(), wl.indices.cuda(), S,
+                                            kv_format=kv_format).cpu().numpy()
+        assert got[7] == cap
+        check_schedule(got, ctx, ids, S)
 
 
 @pytest.mark.parametrize("requests", [450, 900])
@@ -371,6 +384,12 @@ def test_fp4_mixed_ragged(logits_dtype):
                         seed=13))
 
 
+def test_fp4_with_8_row_groups():
+    """The FP4 call on a schedule built for 8-row groups (several row passes
+    a group) gives the oracle's logits too."""
+    _full_check(W.build("fp4", **MIXED, topk=64, kv_format=W.KV_FP4, seed=13), groups_for_keys=False)
+
+
 @pytest.mark.parametrize("S", [1, 7])
 def test_fp4_any_sm_split(S):
     _full_check(W.build("fp4s", request_lens=[700, 129, 1500], rows_per_request=[3, 8, 5], topk=128,
@@ -392,6 +411,11 @@ def test_fp4_full_size_every_row():
 def test_mxfp4_mixed_ragged(logits_dtype):
     _full_check(W.build("mxfp4", **MIXED, topk=64, kv_format=W.KV_MXFP4, logits_dtype=logits_dtype,
                         seed=41))
+
+
+def test_mxfp4_with_8_row_groups():
+    """The MXFP4 call on a schedule built for 8-row groups gives the oracle's logits too."""
+    _full_check(W.build("mxfp4", **MIXED, topk=64, kv_format=W.KV_MXFP4, seed=41), groups_for_keys=False)
 
 
 @pytest.mark.parametrize("S", [1, 7])

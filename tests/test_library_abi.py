@@ -98,6 +98,10 @@ def test_host_checks_metadata_and_topk(lib):
         dsa.DSA_ERR_INVALID_ARG
     assert lib.dsa_paged_mqa_logits_metadata(P(16), None, 4, 64, 8, None, None) == \
         dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_paged_mqa_logits_metadata_for_keys(P(16), None, 4, 64, 8, 3, P(16), None) == \
+        dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_paged_mqa_logits_metadata_for_keys(P(16), None, 4, 32, 8, dsa.KV_FP4, P(16), None) == \
+        dsa.DSA_ERR_UNSUPPORTED
     assert lib.dsa_top_k_per_row(P(16), 0, 64, None, P(16), 2, 0, P(16), 8, None, None) == \
         dsa.DSA_ERR_UNSUPPORTED
     assert lib.dsa_top_k_per_row(P(16), 0, 64, None, P(16), 2, 4096, P(16), 4096, None, None) == \
