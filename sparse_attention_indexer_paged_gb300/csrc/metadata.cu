@@ -26,10 +26,11 @@
 //      as needed to keep both ends monotone: lambda_i = max(lambda_{i-1},
 //      min(a_i, lambda_{i-1} + x_i - x_{i-1})).
 //
-// One CTA of 1024 threads: chunked block scans for the groups, the stable
-// counting sort by row count and the prefix sums; one thread per boundary for
-// a_i; thread 0 for the monotone pass.  The groups of one row count n are
-// adjacent in the sorted order and each of their units carries n pairs, so
+// One CTA (256 threads, or 1024 for 256 SMs or more): chunked block scans
+// for the groups, the stable counting sort by row count and the prefix sums;
+// one thread per boundary for a_i; thread 0 for the monotone pass.  The
+// groups of one row count n are adjacent in the sorted order and each of
+// their units carries n pairs, so
 // the pairs before unit u are piecewise linear in u with one piece per row
 // count, and so are the pairs consumed at boundary i as a function of the
 // left units: a_i is solved exactly from their values where either end
@@ -40,8 +41,10 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
+// Block sizes: 256 threads (8 warps: shorter barriers and scans) when there
+// are fewer than 256 SMs to split over, else 1024; a boundary takes one thread.
+constexpr int kThreadsSmall = 256;
+constexpr int kThreadsLarge = 1024;
 
 template <typename T>
 __device__ __forceinline__ T warp_inclusive_sum(T x) {
@@ -64,27 +67,27 @@ __device__ __forceinline__ int warp_inclusive_max(int x) {
   return x;
 }
 
-// Exclusive prefix sum over the block; *total receives the block sum.
-template <typename T>
+// Exclusive prefix sum over a block of kW warps; *total receives the block sum.
+template <int kW, typename T>
 __device__ T block_exclusive_sum(T v, T* buf, T* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const T inc = warp_inclusive_sum(v);
   if (lane == 31) buf[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    T s = buf[lane];
+    T s = lane < kW ? buf[lane] : T(0);
     s = warp_inclusive_sum(s);
-    buf[lane] = s;
+    if (lane < kW) buf[lane] = s;
   }
   __syncthreads();
   const T before = warp ? buf[warp - 1] : T(0);
-  *total = buf[kWarps - 1];
+  *total = buf[kW - 1];
   __syncthreads();
   return before + inc - v;
 }
 
 // Two exclusive prefix sums over the block with the barriers of one.
-template <typename A, typename B>
+template <int kW, typename A, typename B>
 __device__ void block_exclusive_sum2(A va, B vb, A* bufa, B* bufb, A& exa, B& exb, A& tota, B& totb) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const A ia = warp_inclusive_sum(va);
@@ -95,25 +98,31 @@ __device__ void block_exclusive_sum2(A va, B vb, A* bufa, B* bufb, A& exa, B& ex
   }
   __syncthreads();
   if (warp == 0) {
-    const A sa = warp_inclusive_sum(bufa[lane]);
-    const B sb = warp_inclusive_sum(bufb[lane]);
-    bufa[lane] = sa;
-    bufb[lane] = sb;
+    const A sa = warp_inclusive_sum(lane < kW ? bufa[lane] : A(0));
+    const B sb = warp_inclusive_sum(lane < kW ? bufb[lane] : B(0));
+    if (lane < kW) {
+      bufa[lane] = sa;
+      bufb[lane] = sb;
+    }
   }
   __syncthreads();
   exa = (warp ? bufa[warp - 1] : A(0)) + ia - va;
   exb = (warp ? bufb[warp - 1] : B(0)) + ib - vb;
-  tota = bufa[kWarps - 1];
-  totb = bufb[kWarps - 1];
+  tota = bufa[kW - 1];
+  totb = bufb[kW - 1];
   __syncthreads();
 }
 
+template <int kW>
 __device__ int block_inclusive_max(int v, int* buf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int inc = warp_inclusive_max(v);
   if (lane == 31) buf[warp] = inc;
   __syncthreads();
-  if (warp == 0) buf[lane] = warp_inclusive_max(buf[lane]);
+  if (warp == 0) {
+    const int m = warp_inclusive_max(lane < kW ? buf[lane] : INT_MIN);
+    if (lane < kW) buf[lane] = m;
+  }
   __syncthreads();
   const int r = warp ? max(inc, buf[warp - 1]) : inc;
   __syncthreads();
@@ -201,12 +210,13 @@ struct ClassPieces {
 // and every pointer to them is derived from that array, so that their loads
 // and stores are shared-memory accesses; otherwise they are the schedule's
 // own words in global memory.
-template <bool kInSmem>
+template <bool kInSmem, int kThreads>
 __global__ void __launch_bounds__(kThreads, 1)
     metadata_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ ind, int32_t T,
                     int32_t S, int32_t cap, int32_t* __restrict__ sched) {
   // the logits kernel launched after this one may start its set-up now
   grid_dep_launch();
+  constexpr int kWarps = kThreads / 32;
   extern __shared__ int32_t dyn[];
   __shared__ int32_t buf32[kWarps];
   __shared__ int64_t buf64[kWarps];
@@ -239,11 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = base + tid;
     const bool valid = t < T;
     const bool run_start = valid && (t == 0 || ind == nullptr || ind[t] != ind[t - 1]);
-    int rs = block_inclusive_max(run_start ? t : -1, buf32);
+    int rs = block_inclusive_max<kWarps>(run_start ? t : -1, buf32);
     rs = max(rs, carry_run);
     const bool gstart = valid && ((t - rs) % cap == 0);
     int32_t total;
-    const int32_t idx = block_exclusive_sum<int32_t>(gstart ? 1 : 0, buf32, &total);
+    const int32_t idx = block_exclusive_sum<kWarps, int32_t>(gstart ? 1 : 0, buf32, &total);
     if (gstart) grs[G + idx] = t;
     G += total;
     if (tid == kThreads - 1) s_carry = rs;
@@ -280,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t one_lo = (valid && n <= 4) ? (1ull << (16 * (n - 1))) : 0ull;
     const uint64_t one_hi = (valid && n > 4) ? (1ull << (16 * (n - 5))) : 0ull;
     uint64_t tot_lo, tot_hi, ex_lo, ex_hi;
-    block_exclusive_sum2<uint64_t, uint64_t>(one_lo, one_hi, bufu, bufu2, ex_lo, ex_hi, tot_lo, tot_hi);
+    block_exclusive_sum2<kWarps, uint64_t, uint64_t>(one_lo, one_hi, bufu, bufu2, ex_lo, ex_hi, tot_lo, tot_hi);
     if (valid) {
       const int rank = static_cast<int>(n <= 4 ? (ex_lo >> (16 * (n - 1))) & 0xffffu : (ex_hi >> (16 * (n - 5))) & 0xffffu);
       pos[s_base[n] + s_taken[n] + rank] = grs[g] | (n << kPosRowsShift);
@@ -310,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int32_t tot, ex;
     int64_t totp, exp;
-    block_exclusive_sum2<int32_t, int64_t>(tiles, pairs, buf32, buf64, ex, exp, tot, totp);
+    block_exclusive_sum2<kWarps, int32_t, int64_t>(tiles, pairs, buf32, buf64, ex, exp, tot, totp);
     if (k < G) {
       sus[k] = U + ex;
       const int64_t pp = P + exp;
@@ -366,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // otherwise thread 0 walks the recurrence.
   {
     const int a = tid <= S ? s_a[tid] : 0;
-    const int run = block_inclusive_max(a, buf32);
+    const int run = block_inclusive_max<kWarps>(a, buf32);
     if (tid <= S) s_lambda[tid] = run;
     __syncthreads();
     const bool bad = tid >= 1 && tid <= S && s_lambda[tid] - s_lambda[tid - 1] > s_x[tid] - s_x[tid - 1];
@@ -402,23 +412,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_metadata(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
-                            int32_t num_sms, int32_t group_rows, int32_t* schedule, cudaStream_t stream) {
-  static_assert(kSchedArrays * (kSmemRows + 1) * 4 <= 200 * 1024, "metadata shared memory");
+namespace {
+
+template <int kThreads>
+cudaError_t launch_metadata_as(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
+                               int32_t num_sms, int32_t group_rows, int32_t* schedule, cudaStream_t stream) {
   if (num_rows > kSmemRows) {
-    metadata_kernel<false><<<1, kThreads, 0, stream>>>(context_lens, indices, num_rows, num_sms, group_rows,
-                                                        schedule);
+    metadata_kernel<false, kThreads><<<1, kThreads, 0, stream>>>(context_lens, indices, num_rows, num_sms,
+                                                                  group_rows, schedule);
     return cudaGetLastError();
   }
   const size_t smem = kSchedArrays * (static_cast<size_t>(num_rows) + 1) * 4;
   if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(metadata_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(metadata_kernel<true, kThreads>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                kSchedArrays * (kSmemRows + 1) * 4);
     if (e != cudaSuccess) return e;
   }
-  metadata_kernel<true><<<1, kThreads, smem, stream>>>(context_lens, indices, num_rows, num_sms, group_rows,
-                                                       schedule);
+  metadata_kernel<true, kThreads><<<1, kThreads, smem, stream>>>(context_lens, indices, num_rows, num_sms,
+                                                                 group_rows, schedule);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_metadata(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
+                            int32_t num_sms, int32_t group_rows, int32_t* schedule, cudaStream_t stream) {
+  static_assert(kSchedArrays * (kSmemRows + 1) * 4 <= 200 * 1024, "metadata shared memory");
+  // one thread per boundary 0 .. num_sms
+  if (num_sms < kThreadsSmall)
+    return launch_metadata_as<kThreadsSmall>(context_lens, indices, num_rows, num_sms, group_rows, schedule, stream);
+  return launch_metadata_as<kThreadsLarge>(context_lens, indices, num_rows, num_sms, group_rows, schedule, stream);
 }
 
 }  // namespace dsa
