@@ -790,7 +790,6 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
           b_lo += len * kQRowLo;
         } while (left != 0);
         if (!ok) break;
-        if (!ok) break;
         // one commit per tile: the K stage is free and every pair of the tile
         // is in TMEM once it fires (each commit costs the issuing thread about
         // as much as a small MMA)
