@@ -852,7 +852,7 @@ def run_prefill(args, local):
     names = ("prefill_rows", "metadata", "logits", "top_k")
     us = {n: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / K * 1e3 for i, n in enumerate(names)}
     hbm_gbs, bf16_tf, peak_src = peaks()
-    fp8_tf = bf16_tf * FP8_PEAK_RATIO
+    fp8_tf, fp8_src = fp8_peak_tflops(dev, bf16_tf)
     lens = ctx.cpu().to(torch.int64)
     flops = int(lens.sum()) * 64 * 128 * 2
     achieved = flops / (us["logits"] * 1e-6) / 1e12
@@ -873,7 +873,7 @@ def run_prefill(args, local):
         "roofline": {"kernel": "logits", "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": fp8_tf, "unit": "TFLOP/s", "frac": round(achieved / fp8_tf, 4),
                      "flops": flops, "traffic": profile_traffic("logits.cu", "logits_prefill_ncu.md"),
-                     "peak_source": f"{peak_src} bf16 x {FP8_PEAK_RATIO} (nominal fp8:bf16 ratio)"},
+                     "peak_source": fp8_src},
         "gpu_launches": 4 * K,
         "clocks": clk,
     }

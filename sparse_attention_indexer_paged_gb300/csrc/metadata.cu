@@ -26,15 +26,15 @@
 //      as needed to keep both ends monotone: lambda_i = max(lambda_{i-1},
 //      min(a_i, lambda_{i-1} + x_i - x_{i-1})).
 //
-// One CTA (256 threads, or 1024 for 256 SMs or more): chunked block scans
-// for the groups, the stable counting sort by row count and the prefix sums;
-// one thread per boundary for a_i; thread 0 for the monotone pass.  The
-// groups of one row count n are adjacent in the sorted order and each of
-// their units carries n pairs, so
-// the pairs before unit u are piecewise linear in u with one piece per row
-// count, and so are the pairs consumed at boundary i as a function of the
-// left units: a_i is solved exactly from their values where either end
-// enters a new piece (ClassPieces::fewest_left).
+// One CTA (256 threads; 1024 for 256 SMs or more, or more than 1024 rows):
+// chunked block scans for the groups, the stable counting sort by row count
+// and the prefix sums; one thread per boundary for a_i; thread 0 for the
+// monotone pass.  The groups of one row count n are adjacent in the sorted
+// order and each of their units carries n pairs, so the pairs before unit u
+// are piecewise linear in u with one piece per row count, and so are the
+// pairs consumed at boundary i as a function of the left units: a_i is
+// solved exactly from their values where either end enters a new piece
+// (ClassPieces::fewest_left).
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -42,7 +42,8 @@ namespace dsa {
 namespace {
 
 // Block sizes: 256 threads (8 warps: shorter barriers and scans) when there
-// are fewer than 256 SMs to split over, else 1024; a boundary takes one thread.
+// are fewer than 256 SMs to split over and at most 1024 rows, else 1024; a
+// boundary takes one thread.
 constexpr int kThreadsSmall = 256;
 constexpr int kThreadsLarge = 1024;
 
@@ -439,8 +440,9 @@ cudaError_t launch_metadata_as(const int32_t* context_lens, const int32_t* indic
 cudaError_t launch_metadata(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
                             int32_t num_sms, int32_t group_rows, int32_t* schedule, cudaStream_t stream) {
   static_assert(kSchedArrays * (kSmemRows + 1) * 4 <= 200 * 1024, "metadata shared memory");
-  // one thread per boundary 0 .. num_sms
-  if (num_sms < kThreadsSmall)
+  // one thread per boundary 0 .. num_sms; many rows (prefill chunks) take the
+  // large block, whose scans cover 1024 rows a pass
+  if (num_sms < kThreadsSmall && num_rows <= kThreadsLarge)
     return launch_metadata_as<kThreadsSmall>(context_lens, indices, num_rows, num_sms, group_rows, schedule, stream);
   return launch_metadata_as<kThreadsLarge>(context_lens, indices, num_rows, num_sms, group_rows, schedule, stream);
 }
