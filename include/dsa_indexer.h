@@ -118,18 +118,22 @@ int32_t dsa_device_num_sms(void);
  * runs of equal ids are cut into groups of at most 8 rows (this call; see
  * dsa_paged_mqa_logits_metadata_for_keys for other sizes); a unit is one
  * 128-key tile of a group (ceil(max L_t / 128) units per group) and costs its
- * SM one K tile from HBM plus one (tile, row) pair of MMA and epilogue work
- * per row.  The groups are ordered by row count (stable) and their units laid
- * end to end; SM i takes units from both ends of that sequence, so that every
- * SM owns floor or ceil of units / num_sms units and, as nearly as the group
- * sizes allow, the same number of (tile, row) pairs.  Layout:
+ * SM one K tile from HBM plus MMA and epilogue work that grows with the
+ * group's rows n: the unit weighs 4n + n^2 here (FP8 keys; a tile's cost
+ * grows faster than its rows) and n for the FP4 and MXFP4 schedules of
+ * dsa_paged_mqa_logits_metadata_for_keys.  The groups are ordered by row
+ * count (stable) and their units laid end to end; SM i takes units from both
+ * ends of that sequence, so that every SM owns floor or ceil of
+ * units / num_sms units and, as nearly as the group sizes allow, the same
+ * weight.  Layout:
  * header[8] = {0x44534132, num_rows, varlen flag, num_sms, num_groups,
  * num_units, 128, group rows (8 here)}, left[num_sms + 1], right[num_sms + 1] (SM i owns sorted
  * units [left[i], left[i+1]) and [right[i+1], right[i])),
  * group_row_start[num_rows + 1], position[num_rows + 1] (first row of the
  * group at sorted position k | its rows << 24), unit_start[num_rows + 1],
- * pairs_before low and high words [num_rows + 1] each; entries past the last
- * group hold num_rows, num_rows, num_units and the pair total.
+ * weight_before low and high words [num_rows + 1] each (the weight of the
+ * units before position k); entries past the last group hold num_rows,
+ * num_rows, num_units and the weight total.
  */
 int dsa_paged_mqa_logits_metadata(const int32_t* context_lens, const int32_t* indices,
                                   int32_t num_rows, int32_t block_kv, int32_t num_sms,

@@ -128,7 +128,7 @@ int dsa_paged_mqa_logits_metadata_for_keys(const int32_t* context_lens, const in
   if (block_kv != kPageTokens) return DSA_ERR_UNSUPPORTED;
   const int dev = check_device();
   if (dev != DSA_OK) return dev;
-  return launch_status(launch_metadata(context_lens, indices, num_rows, num_sms, group_rows_for(kv_format),
+  return launch_status(launch_metadata(context_lens, indices, num_rows, num_sms, kv_format,
                                        schedule, reinterpret_cast<cudaStream_t>(stream)));
 }
 

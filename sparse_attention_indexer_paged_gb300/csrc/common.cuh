@@ -29,7 +29,7 @@ constexpr int kPageTokens = DSA_BLOCK_KV;   // 64 tokens per page
 //   pos[T + 1]    sorted position k: first row of its group | rows << 24;
 //                 entries past G hold T
 //   sus[T + 1]    first unit of sorted position k; entries past G hold U
-//   spp_lo[T + 1], spp_hi[T + 1]  (tile, row) pairs before position k
+//   spp_lo[T + 1], spp_hi[T + 1]  weight (unit_weight) before position k
 constexpr int kTileTokens = 128;
 constexpr int kGroupMaxRows = 8;
 // Rows a group holds for each key format: what one pass of that format's
@@ -39,6 +39,15 @@ constexpr int kGroupMaxRows = 8;
 // kGroupMaxRows.
 __host__ __device__ constexpr int group_rows_for(int kv_format) {
   return kv_format == DSA_KV_FP4 ? 4 : (kv_format == DSA_KV_MXFP4 ? 6 : kGroupMaxRows);
+}
+// What one unit (tile) of a group of `rows` rows weighs in the schedule's
+// second balanced quantity (the first is the units themselves).  FP8: 4n +
+// n^2, since a tile's cost grows faster than its rows (a tile of 6 rows fills
+// 6 of the 8 TMEM slots, so tiles no longer overlap; measured microseconds
+// per tile by rows 0.49, 0.56, 0.65, 0.82, 1.01, 1.17); the dequantising
+// formats: n, their groups being one row pass each.
+__host__ __device__ constexpr int64_t unit_weight(int kv_format, int rows) {
+  return kv_format == DSA_KV_FP8 ? 4 * rows + rows * rows : rows;
 }
 constexpr int32_t kScheduleMagic = 0x44534132;
 constexpr int kScheduleHeaderWords = 8;
@@ -100,7 +109,7 @@ cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, size_t
 // arguments have been checked)
 
 cudaError_t launch_metadata(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
-                            int32_t num_sms, int32_t group_rows, int32_t* schedule, cudaStream_t stream);
+                            int32_t num_sms, int32_t kv_format, int32_t* schedule, cudaStream_t stream);
 
 struct LogitsArgs {
   const uint8_t* q;

@@ -9,32 +9,34 @@
 //
 // A unit is one 128-key tile of one group (up to 8 adjacent rows of one
 // request).  It costs its SM one K tile from HBM, the same for every unit,
-// plus one (tile, row) pair of MMA columns and epilogue work per row of the
-// group.  The rule gives every SM the same number of units (within one) and,
-// as nearly as the groups allow, the same number of pairs:
+// plus MMA columns and epilogue work that grow with the group's rows: a unit
+// of n rows weighs unit_weight(format, n) (n for the dequantising formats,
+// 4n + n^2 for FP8, whose tiles cost more than linearly in their rows).  The
+// rule gives every SM the same number of units (within one) and, as nearly
+// as the groups allow, the same weight:
 //   1. groups: runs of equal request ids, each cut into pieces of at most
-//      kGroupMaxRows rows;
+//      group_rows_for(format) rows;
 //   2. the groups are ordered by row count (stable) and their units laid end
 //      to end in that order: sorted position k starts at unit sus[k], and
-//      spp[k] pairs precede it;
+//      spp[k] weight precedes it;
 //   3. boundary i (0 <= i <= S) has consumed x_i = floor(i U / S) units,
 //      lambda_i from the light (left) end of that sequence and
 //      x_i - lambda_i from the heavy (right) end; SM i owns the units between
 //      boundaries i and i + 1 at both ends;
-//   4. a_i = the fewest left units such that the pairs consumed, times S,
-//      do not exceed i P (P = all pairs), and lambda_i is a_i moved as little
-//      as needed to keep both ends monotone: lambda_i = max(lambda_{i-1},
-//      min(a_i, lambda_{i-1} + x_i - x_{i-1})).
+//   4. a_i = the fewest left units such that the weight consumed, times S,
+//      does not exceed i P (P = all weight), and lambda_i is a_i moved as
+//      little as needed to keep both ends monotone: lambda_i =
+//      max(lambda_{i-1}, min(a_i, lambda_{i-1} + x_i - x_{i-1})).
 //
 // One CTA (256 threads; 1024 for 256 SMs or more, or more than 1024 rows):
 // chunked block scans for the groups, the stable counting sort by row count
 // and the prefix sums; one thread per boundary for a_i; thread 0 for the
 // monotone pass.  The groups of one row count n are adjacent in the sorted
-// order and each of their units carries n pairs, so the pairs before unit u
-// are piecewise linear in u with one piece per row count, and so are the
-// pairs consumed at boundary i as a function of the left units: a_i is
-// solved exactly from their values where either end enters a new piece
-// (ClassPieces::fewest_left).
+// order and their units weigh the same, so the weight before unit u is
+// piecewise linear in u with one piece per row count, and so is the weight
+// consumed at boundary i as a function of the left units: a_i is solved
+// exactly from its values where either end enters a new piece
+// (ClassPieces::fewest_left).  ("pairs" in the code below is that weight.)
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -139,13 +141,14 @@ constexpr int kSmemRows = 8192;
 constexpr int kSchedArrays = 5;  // grs, pos, sus, spp_lo, spp_hi
 
 // The sorted unit sequence as one linear piece per row count n = 1 ..
-// kGroupMaxRows: units [u0[n], u0[n + 1]) carry n pairs each, p0[n] pairs
-// before the first of them (u0 non-decreasing, u0[1] = 0; an empty piece
+// kGroupMaxRows: units [u0[n], u0[n + 1]) weigh wt[n] each, p0[n] before the
+// first of them (u0 non-decreasing, u0[1] = 0; an empty piece
 // starts where the next one does).
 struct ClassPieces {
   int32_t u0[kGroupMaxRows + 1];  // in registers: the thresholds
   const int32_t* su0;             // shared copies, indexed by row count
   const int64_t* sp0;
+  const int64_t* swt;             // weight of one unit of each piece
 
   // Pairs of the first u units (0 <= u <= U): the piece holding unit u is the
   // last one starting at or before u, i.e. the number of pieces that do.
@@ -153,7 +156,7 @@ struct ClassPieces {
     int n = 0;
 #pragma unroll
     for (int c = 1; c <= kGroupMaxRows; ++c) n += u >= u0[c] ? 1 : 0;
-    return sp0[n] + static_cast<int64_t>(u - su0[n]) * n;
+    return sp0[n] + static_cast<int64_t>(u - su0[n]) * swt[n];
   }
 
   // The fewest left units lam in [0, x] with pairs consumed <= cap, x if
@@ -195,9 +198,9 @@ struct ClassPieces {
         }
       }
     }
-    // f falls by d = (row count at the right end) - (row count at the left
-    // end) pairs a unit, 1 <= d <= 7; both divisions in 32 bits when the
-    // operands fit (a 64-bit division costs ~1.5K cycles)
+    // f falls by d = (unit weight at the right end) - (unit weight at the
+    // left end) a unit, d >= 1; both divisions in 32 bits when the operands
+    // fit (a 64-bit division costs ~1.5K cycles)
     const uint64_t num = static_cast<uint64_t>(flo - fhi), den = static_cast<uint64_t>(bhi - blo);
     const uint32_t d = (num >> 32) == 0 ? static_cast<uint32_t>(num) / static_cast<uint32_t>(den)
                                         : static_cast<uint32_t>(num / den);
@@ -214,7 +217,7 @@ struct ClassPieces {
 template <bool kInSmem, int kThreads>
 __global__ void __launch_bounds__(kThreads, 1)
     metadata_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ ind, int32_t T,
-                    int32_t S, int32_t cap, int32_t* __restrict__ sched) {
+                    int32_t S, int32_t kv_format, int32_t* __restrict__ sched) {
   // the logits kernel launched after this one may start its set-up now
   grid_dep_launch();
   constexpr int kWarps = kThreads / 32;
@@ -230,11 +233,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int32_t s_x[kThreads];
   __shared__ int32_t s_lambda[kThreads];
   __shared__ int32_t s_u0[kGroupMaxRows + 1];  // first unit of each row count's piece
-  __shared__ int64_t s_p0[kGroupMaxRows + 1];  // pairs before it
+  __shared__ int64_t s_p0[kGroupMaxRows + 1];  // weight before it
+  __shared__ int64_t s_wt[kGroupMaxRows + 1];  // weight of one unit of the piece
   __shared__ int64_t s_pq, s_pr;                // P = s_pq * S + s_pr
 
   const int tid = threadIdx.x;
   const SchedLayout L(S, T);
+  const int group_rows = group_rows_for(kv_format);
   const int64_t n1 = static_cast<int64_t>(T) + 1;
   int32_t* const base = kInSmem ? dyn : sched + L.grs;  // the five arrays, end to end, in both places
   int32_t* grs = base;
@@ -243,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* spp_lo = base + 3 * n1;
   int32_t* spp_hi = base + 4 * n1;
   // ---- groups: a row starts one when it starts a run of equal request ids,
-  // or when cap (<= kGroupMaxRows) rows of its run precede it in the current group
+  // or when group_rows (<= kGroupMaxRows) rows of its run precede it in the current group
   int carry_run = 0;  // run start of the previous chunk's last row
   int G = 0;
   for (int base = 0; base < T; base += kThreads) {
@@ -252,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool run_start = valid && (t == 0 || ind == nullptr || ind[t] != ind[t - 1]);
     int rs = block_inclusive_max<kWarps>(run_start ? t : -1, buf32);
     rs = max(rs, carry_run);
-    const bool gstart = valid && ((t - rs) % cap == 0);
+    const bool gstart = valid && ((t - rs) % group_rows == 0);
     int32_t total;
     const int32_t idx = block_exclusive_sum<kWarps, int32_t>(gstart ? 1 : 0, buf32, &total);
     if (gstart) grs[G + idx] = t;
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int lmax = 0;
       for (int t = r0; t < r0 + n; ++t) lmax = max(lmax, ctx[t]);
       tiles = (lmax + kTileTokens - 1) / kTileTokens;
-      pairs = static_cast<int64_t>(tiles) * n;
+      pairs = static_cast<int64_t>(tiles) * unit_weight(kv_format, n);
     }
     int32_t tot, ex;
     int64_t totp, exp;
@@ -342,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- the pieces: row count n starts at sorted position s_base[n]
   if (tid >= 1 && tid <= kGroupMaxRows) {
+    s_wt[tid] = unit_weight(kv_format, tid);
     const int k = s_base[tid];
     s_u0[tid] = sus[k];
     s_p0[tid] = static_cast<int64_t>(static_cast<uint32_t>(spp_lo[k])) | (static_cast<int64_t>(spp_hi[k]) << 32);
@@ -349,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     s_u0[0] = 0;
     s_p0[0] = 0;
+    s_wt[0] = 0;
     s_pq = P / S;
     s_pr = P % S;
   }
@@ -367,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = 1; n <= kGroupMaxRows; ++n) cp.u0[n] = s_u0[n];
     cp.su0 = s_u0;
     cp.sp0 = s_p0;
+    cp.swt = s_wt;
     s_a[tid] = cp.fewest_left(x, U, P, cap);
   }
   __syncthreads();
@@ -407,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sched[4] = G;
     sched[5] = U;
     sched[6] = kTileTokens;
-    sched[7] = cap;
+    sched[7] = group_rows;
   }
 }
 
@@ -417,10 +425,10 @@ namespace {
 
 template <int kThreads>
 cudaError_t launch_metadata_as(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
-                               int32_t num_sms, int32_t group_rows, int32_t* schedule, cudaStream_t stream) {
+                               int32_t num_sms, int32_t kv_format, int32_t* schedule, cudaStream_t stream) {
   if (num_rows > kSmemRows) {
     metadata_kernel<false, kThreads><<<1, kThreads, 0, stream>>>(context_lens, indices, num_rows, num_sms,
-                                                                  group_rows, schedule);
+                                                                  kv_format, schedule);
     return cudaGetLastError();
   }
   const size_t smem = kSchedArrays * (static_cast<size_t>(num_rows) + 1) * 4;
@@ -431,20 +439,20 @@ cudaError_t launch_metadata_as(const int32_t* context_lens, const int32_t* indic
     if (e != cudaSuccess) return e;
   }
   metadata_kernel<true, kThreads><<<1, kThreads, smem, stream>>>(context_lens, indices, num_rows, num_sms,
-                                                                 group_rows, schedule);
+                                                                 kv_format, schedule);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_metadata(const int32_t* context_lens, const int32_t* indices, int32_t num_rows,
-                            int32_t num_sms, int32_t group_rows, int32_t* schedule, cudaStream_t stream) {
+                            int32_t num_sms, int32_t kv_format, int32_t* schedule, cudaStream_t stream) {
   static_assert(kSchedArrays * (kSmemRows + 1) * 4 <= 200 * 1024, "metadata shared memory");
   // one thread per boundary 0 .. num_sms; many rows (prefill chunks) take the
   // large block, whose scans cover 1024 rows a pass
   if (num_sms < kThreadsSmall && num_rows <= kThreadsLarge)
-    return launch_metadata_as<kThreadsSmall>(context_lens, indices, num_rows, num_sms, group_rows, schedule, stream);
-  return launch_metadata_as<kThreadsLarge>(context_lens, indices, num_rows, num_sms, group_rows, schedule, stream);
+    return launch_metadata_as<kThreadsSmall>(context_lens, indices, num_rows, num_sms, kv_format, schedule, stream);
+  return launch_metadata_as<kThreadsLarge>(context_lens, indices, num_rows, num_sms, kv_format, schedule, stream);
 }
 
 }  // namespace dsa

@@ -15,11 +15,16 @@ balanced in the two quantities the logits kernel pays for:
 * sorted positions: a permutation of the groups, in non-decreasing row count
   (equal counts in row order), each with its own row count;
 * unit starts: each group holds ceil(max causal limit / tile) units, laid end
-  to end in position order; the pair prefix counts units x rows;
+  to end in position order;
+* weights: the prefix words after the unit starts carry the weight before
+  each position; every unit of a group of n rows weighs the same w(n) >= 1,
+  one value per row count, not decreasing with n (w(n) = n counts (tile,
+  row) pairs; the schedule may weigh rows more than linearly, and this
+  checker reads the weights from the words, not from the library);
 * ownership: the SMs' left ranges tile [0, m) and their right ranges tile
   [m, U), so every unit belongs to exactly one SM;
-* balance: every SM owns floor or ceil of U / S units, and its (unit, row)
-  pairs lie within twice the largest group's rows of P / S.
+* balance: every SM owns floor or ceil of U / S units, and its weight lies
+  within twice the largest unit weight of the total over S.
 
 The real proof that any such schedule gives the right logits is the logits
 parity against the oracle at several SM counts.
@@ -43,7 +48,7 @@ def layout(S, T):
 
 
 def check_schedule(words, context_lens, indices, S, balance=True):
-    """Assert that `words` is a valid, balanced schedule; return per-SM (units, pairs)."""
+    """Assert that `words` is a valid, balanced schedule; return per-SM (units, weight)."""
     w = np.asarray(words).astype(np.int64)
     ctx = np.asarray(context_lens).astype(np.int64)
     ids = None if indices is None else np.asarray(indices).astype(np.int64)
@@ -96,9 +101,19 @@ def check_schedule(words, context_lens, indices, S, balance=True):
     assert sus[0] == 0 and np.array_equal(np.diff(sus[: G + 1]), tiles) and sus[G] == U
     assert np.all(sus[G:] == U)
     spp = (sec["spp_lo"] & 0xFFFFFFFF) | (sec["spp_hi"] << 32)
-    pp = np.concatenate([[0], np.cumsum(tiles * nr)])
-    assert np.array_equal(spp[: G + 1], pp)
-    P = int(pp[-1])
+    assert spp[0] == 0 and np.all(np.diff(spp[: G + 1]) >= 0)
+    wt = {}  # unit weight of each row count, read from the words
+    for k in range(G):
+        dw = int(spp[k + 1] - spp[k])
+        if tiles[k] == 0:
+            assert dw == 0, f"position {k}: weight without units"
+            continue
+        assert dw % int(tiles[k]) == 0, f"position {k}: weight not a whole number per unit"
+        w = dw // int(tiles[k])
+        assert w >= 1 and wt.setdefault(int(nr[k]), w) == w, f"position {k}: {w} per unit for {nr[k]} rows"
+    ws = [wt[n] for n in sorted(wt)]
+    assert all(a <= b for a, b in zip(ws, ws[1:])), f"unit weight decreases with rows: {wt}"
+    P = int(spp[G])
     assert np.all(spp[G:] == P)
 
     # ownership
@@ -107,7 +122,7 @@ def check_schedule(words, context_lens, indices, S, balance=True):
     assert np.all(np.diff(left) >= 0) and np.all(np.diff(right) <= 0)
     assert left[S] == right[S] and 0 <= left[S] <= U
 
-    dens = np.repeat(nr, tiles)
+    dens = np.repeat([wt.get(int(n), 0) for n in nr], tiles)
 
     def pairs(a, b):
         return int(dens[a:b].sum())
@@ -117,6 +132,6 @@ def check_schedule(words, context_lens, indices, S, balance=True):
     assert units.sum() == U and prs.sum() == P
     if balance and U:
         assert np.all(units >= U // S) and np.all(units <= -(-U // S)), (units.min(), units.max(), U / S)
-        band = 2 * cap
+        band = 2 * max(ws)
         assert np.all(np.abs(prs - P / S) <= band), (prs.min(), prs.max(), P / S)
     return units, prs

@@ -69,3 +69,35 @@ def test_rejects_a_group_cut_before_it_is_full():
                  sus=[0, 1] + [2] * 8, spp=[0, 4] + [9] * 8)
     with pytest.raises(AssertionError):
         check_schedule(bad, ctx, ids, S)
+
+
+def _rows_sorted(spp):
+    ctx, ids, S = [130, 131, 132, 256], [0, 0, 0, 1], 1
+    words = _words(hdr=[MAGIC, 4, 1, 1, 2, 4, 128, 8], left=[0, 1], right=[4, 1], grs=[0, 3, 4, 4, 4],
+                   pos=[3 | 1 << 24, 0 | 3 << 24, 4, 4, 4], sus=[0, 2, 4, 4, 4], spp=spp)
+    return words, ctx, ids, S
+
+
+def test_accepts_weights_growing_faster_than_rows():
+    # the same two groups with a unit of n rows weighing 4n + n^2 (5 and 21)
+    words, ctx, ids, S = _rows_sorted([0, 10, 52, 52, 52])
+    units, weight = check_schedule(words, ctx, ids, S)
+    assert list(units) == [4] and list(weight) == [52]
+
+
+@pytest.mark.parametrize("spp", [
+    [0, 10, 18, 18, 18],   # a 3-row unit weighs less (4) than a 1-row unit (5)
+    [0, 10, 51, 51, 51],   # 41 over 2 units: not a whole weight per unit
+])
+def test_rejects_bad_unit_weights(spp):
+    words, ctx, ids, S = _rows_sorted(spp)
+    with pytest.raises(AssertionError):
+        check_schedule(words, ctx, ids, S)
+
+
+def test_rejects_two_weights_for_one_row_count():
+    # both groups have 1 row; the prefix weighs the first one's units 1 and the second's 2
+    ctx, ids, S, kw = _two_requests()
+    kw["spp"] = [0, 3, 13]
+    with pytest.raises(AssertionError):
+        check_schedule(_words(**kw), ctx, ids, S)
