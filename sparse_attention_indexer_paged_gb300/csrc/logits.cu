@@ -56,10 +56,11 @@ namespace dsa {
 namespace {
 
 // Warps 0-3 have the producer, MMA and loader roles; warps 4-19 are four
-// epilogue warpgroups.  FP8: 20 warps, 96 registers a thread, a pair read
-// from TMEM in one 64-column load.  FP4: plus warps 20-23 so that six warps
-// (3, 2, 20-23) share the dequantisation; 24 warps leave 80 registers, so
-// the pair is read in two 32-column pieces.
+// epilogue warpgroups.  FP8: 20 warps; FP4 and MXFP4: plus warps 20-23 so
+// that six warps (3, 2, 20-23) share the dequantisation.  Every format reads
+// a pair from TMEM in two 32-column pieces (one 64-column load measured the
+// same on varlen and 2 us slower on MTP; five or six epilogue warpgroups, so
+// that a 6-row tile's pairs are read at once, measured slower).
 template <int kFmt> constexpr int kEpiWgOf = 4;
 template <int kFmt> constexpr int kThreadsOf = kFmt == DSA_KV_FP8 ? 640 : 768;
 constexpr int kFp4Converters = 6;
@@ -821,10 +822,9 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     //   sum_h w_h relu(x_h) = (sum_h w_h x_h + sum_h w_h |x_h|) / 2
     // so the head reduction is 64 packed FMAs (the |x| is an operand
     // modifier) instead of 64 max plus 32 packed FMAs.  The 64 columns come
-    // in pieces of kPiece (register budget: one 64-column load for FP8, two
-    // 32-column loads for the formats with more warps); the slot is released
-    // after the last piece is read.
-    constexpr int kPiece = kFmt == DSA_KV_FP8 ? 64 : 32;
+    // in two pieces of kPiece; the slot is released after the last piece is
+    // read.
+    constexpr int kPiece = 32;
     const uint32_t wg = static_cast<uint32_t>(warp - 4) >> 2;
     const int quarter = warp & 3;    // TMEM lanes this warp may read
     const int tok = quarter * 32 + lane;
