@@ -52,7 +52,8 @@ int launch_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CU
 }  // namespace
 
 bool encode_tensor_map_u8(void* tmap_out, int rank, void* base, const uint64_t* dims,
-                          const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128) {
+                          const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes) {
+  if (swizzle_bytes != 0 && swizzle_bytes != 64 && swizzle_bytes != 128) return false;
   std::call_once(g_encode_once, resolve_encode);
   if (g_encode == nullptr) return false;
   cuuint64_t gd[5];
@@ -68,7 +69,9 @@ bool encode_tensor_map_u8(void* tmap_out, int rank, void* base, const uint64_t* 
   const CUresult r = g_encode(static_cast<CUtensorMap*>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_UINT8,
                               static_cast<cuuint32_t>(rank), base, gd, gs, bx, es,
                               CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                              : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                    : CU_TENSOR_MAP_SWIZZLE_NONE,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

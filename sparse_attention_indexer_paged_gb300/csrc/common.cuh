@@ -155,7 +155,8 @@ cudaError_t launch_dcp_merge(const float* gathered, int32_t world, int32_t num_r
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, int32_t* status, cudaStream_t stream);
 
 // Tensor-map encoding through the driver entry point (no libcuda link).
+// swizzle_bytes: 0 (none), 64 or 128 (the inner box is that many bytes).
 bool encode_tensor_map_u8(void* tmap_out, int rank, void* base, const uint64_t* dims,
-                          const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);
+                          const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes);
 
 }  // namespace dsa

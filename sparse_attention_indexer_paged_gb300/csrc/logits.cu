@@ -62,9 +62,16 @@ namespace {
 // same on varlen and 2 us slower on MTP; five or six epilogue warpgroups, so
 // that a 6-row tile's pairs are read at once, measured slower).
 template <int kFmt> constexpr int kEpiWgOf = 4;
-template <int kFmt> constexpr int kThreadsOf = kFmt == DSA_KV_FP8 ? 640 : 768;
+template <int kFmt> constexpr int kThreadsOf = kFmt == DSA_KV_FP4 ? 768 : 640;
 constexpr int kFp4Converters = 6;
-constexpr int kSlots = 8;  // 64-column TMEM slots; pair p of the CTA's stream uses slot p mod 8
+// 64-column TMEM slots; pair p of the CTA's stream uses slot p mod kSlots.
+// MXFP4 keeps the last 64 of the 512 columns for its scale factors: the key
+// scales of K stage s at columns 448 + 4 s, the q scales of pass row r at
+// 480 + 2 r (two rows per 4-column block).
+template <int kFmt> constexpr int kSlotsOf = kFmt == DSA_KV_MXFP4 ? 7 : 8;
+constexpr int kMaxSlots = 8;
+constexpr uint32_t kMxSfaCol = 448;
+constexpr uint32_t kMxSfbCol = 480;
 constexpr int kTileRing = 8;  // tiles whose "pairs in TMEM" barrier phases are tracked at once
 constexpr int kScaleStages = 16;   // key scale ring
 constexpr int kTmemCols = 512;
@@ -73,26 +80,25 @@ constexpr int kWBufFloats = kGroupMaxRows * kHeads;       // 512
 constexpr int kPageValBytesFp8 = kPageTokens * kHeadDim;  // 8192
 constexpr int kFp4PageBytes = DSA_FP4_PAGE_BYTES;         // 4864: values, block scales, token scales
 constexpr int kFp4GScaleOffset = kPageTokens * (kHeadDim / 2 + kHeadDim / 16);  // 4608
-constexpr int kMxPageBytes = DSA_MXFP4_PAGE_BYTES;         // 4352: values, ue8m0 block scales
-constexpr int kMxScaleOffset = kPageTokens * (kHeadDim / 2);  // 4096
-// whole pages copied raw and dequantised by the converter warps
-template <int kFmt> constexpr int kDqPageBytes = kFmt == DSA_KV_MXFP4 ? kMxPageBytes : kFp4PageBytes;
-constexpr int kScaleStageFloats = kTileTokens;            // 128 key scales per tile
+constexpr int kMxPageValBytes = kPageTokens * (kHeadDim / 2);  // 4096: packed e2m1 values, then 4 ue8m0 scales a token
+constexpr int kScaleStageFloats = kTileTokens;            // 128 key scales (or scale words) per tile
 constexpr int kMaxKStages = 8;
 constexpr int kMaxRawStages = 8;
-// q rows per MMA pass over a tile (dequantising formats): the f16 q of a
-// pass and the raw page ring share shared memory, so MXFP4's smaller pages
-// leave room for 6-row passes (every varlen group of up to 6 rows converts
-// each tile once) where FP4 keeps 4 rows and a deeper page ring.
+constexpr int kFp4RawStages = 8;
+// q rows per MMA pass over a tile.  FP4: the f16 q of a pass and the raw
+// page ring share shared memory (4 rows).  MXFP4: a tile's pairs take
+// distinct TMEM slots (7 of them), so groups are walked in passes of 6 rows.
 template <int kFmt> constexpr int kPassRowsOf = kFmt == DSA_KV_MXFP4 ? 6 : 4;
-template <int kFmt> constexpr int kRawStagesOf = kFmt == DSA_KV_MXFP4 ? 6 : 8;
-constexpr int kMaxPassRows = 6;
 
 // Shared memory layouts (offsets from a 1024-aligned base).
-//   FP8: K ring of e4m3 tiles [128 tokens][128 B] filled by TMA, Q rows e4m3.
-//   FP4: raw page pairs (bulk copies of whole pages), dequantised f16 K tiles
-//        [2 k-halves][128 tokens][128 B], Q rows in f16 [2 k-halves][pass rows x 64 heads][128 B];
-//        all MMA operands K-major with the 128-byte swizzle.
+//   FP8:   K ring of e4m3 tiles [128 tokens][128 B] filled by TMA, Q rows e4m3;
+//          K-major with the 128-byte swizzle.
+//   MXFP4: K ring of packed e2m1 tiles [128 tokens][64 B] filled by TMA, Q
+//          rows packed e2m1 [64 heads][64 B]; K-major with the 64-byte
+//          swizzle; the pass's q scales in the TMEM copy layout (512 B a row pair).
+//   FP4:   raw page pairs (bulk copies of whole pages), dequantised f16 K tiles
+//          [2 k-halves][128 tokens][128 B], Q rows in f16 [2 k-halves][pass rows x 64 heads][128 B];
+//          K-major with the 128-byte swizzle.
 template <int kFmt> struct Lay;
 template <> struct Lay<DSA_KV_FP8> {
   static constexpr int kKStages = 8;
@@ -102,32 +108,39 @@ template <> struct Lay<DSA_KV_FP8> {
   static constexpr int kQRowBytes = kHeads * kHeadDim;        // 8192
   static constexpr int kOffKv = 0;
   static constexpr int kOffQ = kOffKv + kKStages * kKStageBytes;
-  static constexpr int kOffRaw = kOffQ + kGroupMaxRows * kQRowBytes;
+  static constexpr int kOffQsf = kOffQ + kGroupMaxRows * kQRowBytes;  // (unused)
+  static constexpr int kOffRaw = kOffQsf;
 };
-template <int kPageBytes, int kRows, int kRaw> struct LayDq {
+template <> struct Lay<DSA_KV_MXFP4> {
+  static constexpr int kKStages = 8;
+  static constexpr int kKStageBytes = 2 * kMxPageValBytes;   // 8192
+  static constexpr int kRawStages = 0;
+  static constexpr int kRawStageBytes = 0;
+  static constexpr int kQRowBytes = kHeads * (kHeadDim / 2);  // 4096
+  static constexpr int kOffKv = 0;
+  static constexpr int kOffQ = kOffKv + kKStages * kKStageBytes;
+  static constexpr int kOffQsf = kOffQ + kPassRowsOf<DSA_KV_MXFP4> * kQRowBytes;
+  static constexpr int kOffRaw = kOffQsf + (kPassRowsOf<DSA_KV_MXFP4> + 1) / 2 * 512;
+};
+template <> struct Lay<DSA_KV_FP4> {
   static constexpr int kKStages = 2;
   static constexpr int kKStageBytes = 2 * kTileTokens * 128;  // 32768
-  static constexpr int kRawStages = kRaw;
-  static constexpr int kRawStageBytes = 2 * kPageBytes;       // 9728 (FP4), 8704 (MXFP4)
-  static constexpr int kQHalfBytes = kRows * kHeads * 128;    // one k-half of the pass's f16 q
+  static constexpr int kRawStages = kFp4RawStages;
+  static constexpr int kRawStageBytes = 2 * kFp4PageBytes;    // 9728
+  static constexpr int kQHalfBytes = kPassRowsOf<DSA_KV_FP4> * kHeads * 128;  // one k-half of the pass's f16 q
   static constexpr int kOffQ = 0;
   static constexpr int kOffKv = kOffQ + 2 * kQHalfBytes;
   static constexpr int kOffRaw = kOffKv + kKStages * kKStageBytes;
 };
-template <> struct Lay<DSA_KV_FP4>
-    : LayDq<kFp4PageBytes, kPassRowsOf<DSA_KV_FP4>, kRawStagesOf<DSA_KV_FP4>> {};
-template <> struct Lay<DSA_KV_MXFP4>
-    : LayDq<kMxPageBytes, kPassRowsOf<DSA_KV_MXFP4>, kRawStagesOf<DSA_KV_MXFP4>> {};
 template <int kFmt> struct Smem : Lay<kFmt> {
   using B = Lay<kFmt>;
   static constexpr int kOffScale = B::kOffRaw + B::kRawStages * B::kRawStageBytes;
   static constexpr int kOffW = kOffScale + kScaleStages * kScaleStageFloats * 4;
   static constexpr int kOffCtx = kOffW + 2 * kWBufFloats * 4;  // causal limits of the group's rows
-  static constexpr int kOffRowF = kOffCtx + 2 * kGroupMaxRows * 4;  // MXFP4: q scale factor of each row
-  static constexpr int kOffBar = kOffRowF + 2 * kGroupMaxRows * 4;
+  static constexpr int kOffBar = kOffCtx + 2 * kGroupMaxRows * 4;
   // barriers: kv_full[8], kv_empty[8], raw_full[2], raw_empty[2], q_full, q_empty,
   // w_full[2], w_empty[2], tm_empty[8], mma_done, tile_ready[8]
-  static constexpr int kNumBars = 2 * kMaxKStages + 2 * kMaxRawStages + 2 + 4 + 8 + 1 + kTileRing;
+  static constexpr int kNumBars = 2 * kMaxKStages + 2 * kMaxRawStages + 2 + 4 + kMaxSlots + 1 + kTileRing;
   static constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemAddr + 4;
   static constexpr int kOffWalk = kOffAbort + 4;  // WalkRanges
@@ -136,19 +149,27 @@ template <int kFmt> struct Smem : Lay<kFmt> {
                 "MMA tiles need 1024-byte alignment");
   static_assert(B::kOffRaw % 16 == 0 && B::kRawStageBytes % 16 == 0, "bulk copies need 16 bytes");
   static_assert((B::kKStages & (B::kKStages - 1)) == 0 && B::kKStages <= kMaxKStages, "K ring");
+  static_assert(kOffScale % 512 == 0, "scale blocks are copied to TMEM from 16-byte rows");
   static_assert(kOffBar % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(kBytes <= 232448, "over the per-CTA shared memory limit");
 };
-static_assert(kSlots * kPairCols == kTmemCols, "TMEM slots");
-static_assert(kGroupMaxRows <= kSlots, "a tile's pairs take distinct TMEM slots");
+static_assert(kSlotsOf<DSA_KV_FP8> * kPairCols == kTmemCols && kSlotsOf<DSA_KV_FP4> * kPairCols == kTmemCols &&
+                  kSlotsOf<DSA_KV_MXFP4> * kPairCols == kMxSfaCol &&
+                  kMxSfaCol + 4 * Lay<DSA_KV_MXFP4>::kKStages <= kMxSfbCol &&
+                  kMxSfbCol + 4 * ((kPassRowsOf<DSA_KV_MXFP4> + 1) / 2) <= kTmemCols,
+              "TMEM slots and the MXFP4 scale columns");
+static_assert(kGroupMaxRows <= kSlotsOf<DSA_KV_FP8> && kPassRowsOf<DSA_KV_MXFP4> <= kSlotsOf<DSA_KV_MXFP4> &&
+                  kPassRowsOf<DSA_KV_FP4> <= kSlotsOf<DSA_KV_FP4> && kSlotsOf<DSA_KV_FP8> <= kMaxSlots,
+              "a tile's pairs take distinct TMEM slots");
 static_assert(group_rows_for(DSA_KV_FP4) == kPassRowsOf<DSA_KV_FP4> &&
                   group_rows_for(DSA_KV_MXFP4) == kPassRowsOf<DSA_KV_MXFP4>,
-              "a dequantising format's schedule groups are one row pass each");
-static_assert(Lay<DSA_KV_FP8>::kKStages == kTileRing, "FP8 tiles signal their pairs on the K stage's own barrier");
+              "the schedule's groups of the FP4 formats are one row pass each");
+static_assert(Lay<DSA_KV_FP8>::kKStages == kTileRing && Lay<DSA_KV_MXFP4>::kKStages == kTileRing,
+              "FP8 and MXFP4 tiles signal their pairs on the K stage's own barrier");
+static_assert(Lay<DSA_KV_MXFP4>::kKStages <= kMaxRawStages, "MXFP4 scale barriers reuse the raw ring's");
+static_assert(kScaleStageFloats * 4 == 512, "a tile's key scales are one 512-byte TMEM copy block (MXFP4)");
 static_assert(kFp4AHalfLo == (kTileTokens * 128) >> 4, "f16 K operand halves as laid out by the dequantising warps");
-static_assert(kPassRowsOf<DSA_KV_FP4> <= kMaxPassRows && kPassRowsOf<DSA_KV_MXFP4> <= kMaxPassRows &&
-                  kRawStagesOf<DSA_KV_FP4> <= kMaxRawStages && kRawStagesOf<DSA_KV_MXFP4> <= kMaxRawStages,
-              "pass rows and raw stages");
+static_assert(kFp4RawStages <= kMaxRawStages, "raw stages");
 
 struct Params {
   const uint8_t* q;
@@ -193,6 +214,8 @@ struct Bars {
   __device__ uint32_t kve(int s) const { return kv_empty + 8 * s; }
   __device__ uint32_t rwf(int s) const { return raw_full + 8 * s; }
   __device__ uint32_t rwe(int s) const { return raw_empty + 8 * s; }
+  // MXFP4 (no raw ring): K stage s's key scales are in the TMEM copy layout
+  __device__ uint32_t sfr(int s) const { return raw_full + 8 * s; }
   __device__ uint32_t wf(int b) const { return w_full + 8 * b; }
   __device__ uint32_t we(int b) const { return w_empty + 8 * b; }
   // TMEM slot s: drained by the warpgroup of the pair in it
@@ -323,8 +346,9 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                   const Params p) {
   using L = Smem<kFmt>;
-  constexpr bool kDq = kFmt != DSA_KV_FP8;   // dequantising pipeline: FP4 and MXFP4 keys
-  constexpr bool kMx = kFmt == DSA_KV_MXFP4;
+  constexpr bool kDq = kFmt == DSA_KV_FP4;    // dequantising pipeline: FP4 keys
+  constexpr bool kMx = kFmt == DSA_KV_MXFP4;  // block-scaled e2m1 MMA: MXFP4 keys and q
+  constexpr int kSlots = kSlotsOf<kFmt>;
   constexpr int kEpiWg = kEpiWgOf<kFmt>;
   constexpr int kEpiWarps = 4 * kEpiWg;
   constexpr int kStages = L::kKStages;
@@ -366,21 +390,25 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   bars.w_full = bars.q_empty + 8;
   bars.w_empty = bars.w_full + 16;
   bars.tm_empty = bars.w_empty + 16;
-  bars.mma_done = bars.tm_empty + 8 * kSlots;
+  bars.mma_done = bars.tm_empty + 8 * kMaxSlots;
   bars.tile_ready = bars.mma_done + 8;
   uint32_t* tmem_addr_smem = reinterpret_cast<uint32_t*>(smem + L::kOffTmemAddr);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kOffAbort);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bars.kvf(s), kDq ? kFp4Converters : 1);  // TMA (FP8) or the dequantising warps (FP4, MXFP4)
+      mbar_init(bars.kvf(s), kDq ? kFp4Converters : 1);  // TMA (FP8, MXFP4) or the dequantising warps (FP4)
       mbar_init(bars.kve(s), 1);  // the MMA commit of the tile: stage free, the tile's pairs in TMEM
     }
     for (int s = 0; s < L::kRawStages; ++s) {
       mbar_init(bars.rwf(s), 1);
       mbar_init(bars.rwe(s), kFp4Converters);  // the dequantising warps
     }
-    mbar_init(bars.q_full, kDq ? kFp4Converters : 1);  // the MMA warp's TMA (FP8) or the converting warps (FP4, MXFP4)
+    if (kMx)
+      for (int s = 0; s < kStages; ++s) mbar_init(bars.sfr(s), 1);  // the scale warp
+    // the MMA warp's TMA (FP8), plus the scale warp's q scales (MXFP4), or
+    // the converting warps (FP4)
+    mbar_init(bars.q_full, kDq ? kFp4Converters : (kMx ? 2 : 1));
     mbar_init(bars.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.wf(b), 1);
@@ -422,7 +450,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   const float* w_sm = reinterpret_cast<const float*>(smem + L::kOffW);
   int32_t* ctx_sm = reinterpret_cast<int32_t*>(smem + L::kOffCtx);
 
-  Walk<kDq ? kPassRowsOf<kFmt> : kGroupMaxRows> walk;
+  Walk<kFmt == DSA_KV_FP8 ? kGroupMaxRows : kPassRowsOf<kFmt>> walk;
   walk.start(sched, walk_ranges);
 
   // =================================================== FP4 dequantisation (warps 3, 2, 20-23)
@@ -434,18 +462,10 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   // conversion of every pass's q rows (e4m3 -> f16, exact) into the swizzled
   // B-operand layout.  Warp 2 first loads the pass's head weights and causal
   // limits (double buffered).
-  //
-  // MXFP4 keys and q (ue8m0 scale e_b per 32 elements): a token's pieces are
-  // scaled by 2^(e_b - e_max) in f16, e_max the token's largest block
-  // exponent, and 2^(e_max - 127) goes to the token-scale ring; q rows the
-  // same way with the row's largest exponent, whose factor the epilogue
-  // applies.  Every product stays exact unless a block lies more than 2^14
-  // below its token's (or row's) largest, where f16 keeps fewer bits of it.
   auto fp4_worker = [&]() {
-    using LF = Lay<kFmt == DSA_KV_FP8 ? DSA_KV_FP4 : kFmt>;  // (compiled, never run, for FP8)
-    constexpr int kPg = kDqPageBytes<kFmt>;
+    using LF = Lay<DSA_KV_FP4>;  // (compiled, never run, for the other formats)
+    constexpr int kPg = kFp4PageBytes;
     constexpr int kStride = 32 * kFp4Converters;
-    float* rowf_sm = reinterpret_cast<float*>(smem + L::kOffRowF);
     const int part = warp == 3 ? 0 : (warp == 2 ? 1 : warp - (4 + kEpiWarps) + 2);
     const uint64_t pol_keep = policy_evict_last();
     const uint32_t q_half = static_cast<uint32_t>(LF::kQHalfBytes);
@@ -453,24 +473,11 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     bool ok = true;
     while (ok && walk.next(sched, S, T, p.ctx, walk_ranges, lane)) {
       const int r0 = walk.r0, n = walk.n;
-      // MXFP4: largest q scale exponent of each row of the pass (lane r holds row r's)
-      uint32_t row_emax = 0;
-      if constexpr (kMx) {
-        for (int r = 0; r < n; ++r) {
-          const uint2 e8 = __ldg(reinterpret_cast<const uint2*>(p.q_scale + static_cast<int64_t>(r0 + r) * kHeads *
-                                                                              (kHeadDim / 32)) + lane);
-          uint32_t m = max_byte4(__vmaxu4(e8.x, e8.y));
-#pragma unroll
-          for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-          if (lane == r) row_emax = m;
-        }
-      }
       if (part == 1) {
         const int wb = nw & 1;
         ok = warp_wait(bars.we(wb), ((nw >> 1) & 1) ^ 1, abort_flag, p.status);
         if (!ok) break;
         if (lane < n) ctx_sm[wb * kGroupMaxRows + lane] = walk.lane_ctx;
-        if (kMx && lane < n) rowf_sm[wb * kGroupMaxRows + lane] = ue8m0_to_f32(row_emax);
         __threadfence_block();
         __syncwarp();
         if (lane == 0) {
@@ -483,53 +490,23 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       // q rows of the pass, once the previous pass's MMAs have completed
       ok = warp_wait(bars.q_empty, (nq & 1) ^ 1, abort_flag, p.status);
       if (!ok) break;
-      if constexpr (kMx) {
-        // 8 e2m1 codes (4 bytes) per step with their block's relative scale
-        const uint32_t* qsrc = reinterpret_cast<const uint32_t*>(p.q + static_cast<int64_t>(r0) * kHeads * (kHeadDim / 2));
-        const uint8_t* qsc = p.q_scale + static_cast<int64_t>(r0) * kHeads * (kHeadDim / 32);
-        const int nchunks = n * kHeads * (kHeadDim / 8);
-        // every lane gets all rows' exponents before the loop, whose trip
-        // count differs between lanes
-        int em[kMaxPassRows];
-#pragma unroll
-        for (int r = 0; r < kMaxPassRows; ++r) em[r] = static_cast<int>(__shfl_sync(0xffffffffu, row_emax, r));
-        for (int i = part * 32 + lane; i < nchunks; i += kStride) {
-          const uint32_t c = __ldg(qsrc + i);
-          const int R = i >> 4;      // q row (row * 64 + head) within the pass
-          const int c16 = i & 15;    // 8-element chunk along d
-          const int rr = R >> 6;
-          int emax = em[0];
-#pragma unroll
-          for (int r = 1; r < kMaxPassRows; ++r) emax = rr == r ? em[r] : emax;
-          const uint32_t f = pow2_f16x2(static_cast<int>(__ldg(qsc + R * (kHeadDim / 32) + (c16 >> 2))) - emax);
-          uint32_t h[4];
-          e2m1x8_to_f16x2(c, h);
-          uint4 o;
-          o.x = hmul2_u32(h[0], f);
-          o.y = hmul2_u32(h[1], f);
-          o.z = hmul2_u32(h[2], f);
-          o.w = hmul2_u32(h[3], f);
-          const uint32_t off = static_cast<uint32_t>(c16 >> 3) * q_half + static_cast<uint32_t>(R >> 3) * 1024u +
-                               static_cast<uint32_t>(R & 7) * 128u + (static_cast<uint32_t>((c16 & 7) ^ (R & 7)) << 4);
-          *reinterpret_cast<uint4*>(smem + LF::kOffQ + off) = o;
-        }
-      } else {
-        // 8 e4m3 codes per step; the warps take interleaved 32-chunk blocks
-        const uint2* qsrc = reinterpret_cast<const uint2*>(p.q + static_cast<int64_t>(r0) * kHeads * kHeadDim);
-        const int nchunks = n * kHeads * (kHeadDim / 8);
-        for (int i = part * 32 + lane; i < nchunks; i += kStride) {
-          const uint2 c = __ldg(qsrc + i);
-          const int R = i >> 4;      // q row (row * 64 + head) within the pass
-          const int c16 = i & 15;    // 8-element chunk along d
-          uint4 o;
-          o.x = e4m3x2_to_f16x2(c.x & 0xffffu);
-          o.y = e4m3x2_to_f16x2(c.x >> 16);
-          o.z = e4m3x2_to_f16x2(c.y & 0xffffu);
-          o.w = e4m3x2_to_f16x2(c.y >> 16);
-          const uint32_t off = static_cast<uint32_t>(c16 >> 3) * q_half + static_cast<uint32_t>(R >> 3) * 1024u +
-                               static_cast<uint32_t>(R & 7) * 128u + (static_cast<uint32_t>((c16 & 7) ^ (R & 7)) << 4);
-          *reinterpret_cast<uint4*>(smem + LF::kOffQ + off) = o;
-        }
+      {
+      // 8 e4m3 codes per step; the warps take interleaved 32-chunk blocks
+      const uint2* qsrc = reinterpret_cast<const uint2*>(p.q + static_cast<int64_t>(r0) * kHeads * kHeadDim);
+      const int nchunks = n * kHeads * (kHeadDim / 8);
+      for (int i = part * 32 + lane; i < nchunks; i += kStride) {
+        const uint2 c = __ldg(qsrc + i);
+        const int R = i >> 4;      // q row (row * 64 + head) within the pass
+        const int c16 = i & 15;    // 8-element chunk along d
+        uint4 o;
+        o.x = e4m3x2_to_f16x2(c.x & 0xffffu);
+        o.y = e4m3x2_to_f16x2(c.x >> 16);
+        o.z = e4m3x2_to_f16x2(c.y & 0xffffu);
+        o.w = e4m3x2_to_f16x2(c.y >> 16);
+        const uint32_t off = static_cast<uint32_t>(c16 >> 3) * q_half + static_cast<uint32_t>(R >> 3) * 1024u +
+                             static_cast<uint32_t>(R & 7) * 128u + (static_cast<uint32_t>((c16 & 7) ^ (R & 7)) << 4);
+        *reinterpret_cast<uint4*>(smem + LF::kOffQ + off) = o;
+      }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -543,14 +520,9 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
              warp_wait(bars.kve(st), ((it / LF::kKStages) & 1) ^ 1, abort_flag, p.status);
         if (!ok) break;
         const uint8_t* raw = smem + LF::kOffRaw + rs * LF::kRawStageBytes;
-        for (int t = part * 32 + lane; t < kTileTokens; t += kStride) {  // token scales -> scale ring
-          if constexpr (kMx)
-            scale_sm[ss * kScaleStageFloats + t] = ue8m0_to_f32(
-                max_byte4(*reinterpret_cast<const uint32_t*>(raw + (t >> 6) * kPg + kMxScaleOffset + (t & 63) * 4)));
-          else
-            scale_sm[ss * kScaleStageFloats + t] =
-                *reinterpret_cast<const float*>(raw + (t >> 6) * kPg + kFp4GScaleOffset + (t & 63) * 4);
-        }
+        for (int t = part * 32 + lane; t < kTileTokens; t += kStride)  // token scales -> scale ring
+          scale_sm[ss * kScaleStageFloats + t] =
+              *reinterpret_cast<const float*>(raw + (t >> 6) * kPg + kFp4GScaleOffset + (t & 63) * 4);
         uint8_t* tile = smem + LF::kOffKv + st * LF::kKStageBytes;
 #pragma unroll 1
         for (int k = part * 32 + lane; k < kTileTokens * 4; k += kStride) {
@@ -558,18 +530,12 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
           const uint8_t* tokp = raw + (tk >> 6) * kPg;
           const int slot = tk & 63;
           const uint4 pv = *reinterpret_cast<const uint4*>(tokp + slot * (kHeadDim / 2) + q4 * 16);
+          // block scales of the piece's two 16-element blocks
           uint32_t sb[2];
-          if constexpr (kMx) {
-            // the piece is one 32-element block: 2^(e_b - e_max of the token)
-            const uint32_t e4 = *reinterpret_cast<const uint32_t*>(tokp + kMxScaleOffset + slot * 4);
-            sb[0] = sb[1] = pow2_f16x2(static_cast<int>((e4 >> (8 * q4)) & 0xffu) - static_cast<int>(max_byte4(e4)));
-          } else {
-            // block scales of the piece's two 16-element blocks
-            const uint32_t s2 = e4m3x2_to_f16x2(
-                *reinterpret_cast<const uint16_t*>(tokp + kPageTokens * (kHeadDim / 2) + slot * 8 + q4 * 2));
-            sb[0] = __byte_perm(s2, 0, 0x1010);
-            sb[1] = __byte_perm(s2, 0, 0x3232);
-          }
+          const uint32_t s2 = e4m3x2_to_f16x2(
+              *reinterpret_cast<const uint16_t*>(tokp + kPageTokens * (kHeadDim / 2) + slot * 8 + q4 * 2));
+          sb[0] = __byte_perm(s2, 0, 0x1010);
+          sb[1] = __byte_perm(s2, 0, 0x3232);
           const uint32_t words[4] = {pv.x, pv.y, pv.z, pv.w};
           const uint32_t row = static_cast<uint32_t>(tk >> 3) * 1024u + static_cast<uint32_t>(tk & 7) * 128u;
 #pragma unroll
@@ -642,7 +608,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
             const int npg = (blk0 >= 0 ? 1 : 0) + (blk1 >= 0 ? 1 : 0);
             if constexpr (kDq) {
               // whole pages: packed values and their scales
-              constexpr int kPg = kDqPageBytes<kFmt>;
+              constexpr int kPg = kFp4PageBytes;
               mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(npg * kPg));
               const uint32_t dst = sbase + L::kOffRaw + st * L::kRawStageBytes;
               if (blk0 >= 0)
@@ -653,20 +619,22 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
                           pol_stream);
             } else {
               // the two pages' values (tensor map, swizzled) and their key
-              // scales (plain copies into the scale ring), one barrier
+              // scales (plain copies into the scale ring), one barrier: FP8
+              // pages hold 8192 value bytes then an fp32 scale a token, MXFP4
+              // pages 4096 packed e2m1 bytes then 4 ue8m0 block scales a token
+              constexpr uint32_t kVal = kMx ? kMxPageValBytes : kPageValBytesFp8;
+              constexpr uint32_t kSc = kPageTokens * 4;
               const uint32_t sc_dst = s_scale + (it % kScaleStages) * kScaleStageFloats * 4;
-              mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(npg * (kPageValBytesFp8 + kPageTokens * 4)));
+              mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(npg) * (kVal + kSc));
               if (blk0 >= 0) {
                 tma_load_3d(s_kv + st * L::kKStageBytes, &tm_kv, 0, 0, blk0, full_bar, pol_stream);
-                bulk_load(sc_dst, p.kv_cache + static_cast<int64_t>(blk0) * p.page_stride + kPageValBytesFp8,
-                          kPageTokens * 4, full_bar, pol_stream);
+                bulk_load(sc_dst, p.kv_cache + static_cast<int64_t>(blk0) * p.page_stride + kVal, kSc, full_bar,
+                          pol_stream);
               }
               if (blk1 >= 0) {
-                tma_load_3d(s_kv + st * L::kKStageBytes + kPageValBytesFp8, &tm_kv, 0, 0, blk1,
-                            full_bar, pol_stream);
-                bulk_load(sc_dst + kPageTokens * 4,
-                          p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride + kPageValBytesFp8,
-                          kPageTokens * 4, full_bar, pol_stream);
+                tma_load_3d(s_kv + st * L::kKStageBytes + kVal, &tm_kv, 0, 0, blk1, full_bar, pol_stream);
+                bulk_load(sc_dst + kSc, p.kv_cache + static_cast<int64_t>(blk1) * p.page_stride + kVal, kSc,
+                          full_bar, pol_stream);
               }
             }
           }
@@ -686,6 +654,55 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       if (warp == 3) {
         // FP8: no role (the K producer brings each tile's key scales with its
         // values); the warp waits at the final barrier.
+        if constexpr (kMx) {
+          // =================================================== MXFP4: scales into the TMEM copy layout
+          // A 128-row scale block goes to TMEM as one copy that gives lane l,
+          // column c the source word 4 l + c, and row x's scales must land in
+          // lane x mod 32, column x / 32: so row x's word moves from position x
+          // to 4 (x mod 32) + x / 32, a 4 x 32 transpose (lane l gathers rows
+          // l, 32 + l, 64 + l, 96 + l and stores them as one 16-byte row).
+          //   q: per pass, two rows (128 B-operand rows) per block, straight
+          //      from global memory, once the previous pass's MMAs (and the
+          //      copies before them) have completed; then one arrival on q_full.
+          //   keys: per tile, in place in the scale ring once the tile has
+          //      landed; then the stage's sfr barrier.
+          const uint32_t* qsc = reinterpret_cast<const uint32_t*>(p.q_scale);
+          uint8_t* qsf = smem + L::kOffQsf;
+          uint32_t it = 0, gi = 0;
+          bool ok = true;
+          while (ok && walk.next(sched, S, T, p.ctx, walk_ranges, lane)) {
+            const int r0 = walk.r0, n = walk.n;
+            ok = warp_wait(bars.q_empty, (gi & 1) ^ 1, abort_flag, p.status);
+            if (!ok) break;
+            for (int b = 0; 2 * b < n; ++b) {
+              uint32_t w[4];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const int r = 2 * b + (c >> 1);  // row of the pass; heads 32 (c & 1) + lane
+                w[c] = r < n ? __ldg(qsc + static_cast<int64_t>(r0 + r) * kHeads + 32 * (c & 1) + lane)
+                             : 0x7f7f7f7fu;
+              }
+              *reinterpret_cast<uint4*>(qsf + b * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.q_full);
+            ++gi;
+            for (int j = walk.j0; j < walk.j1; ++j, ++it) {
+              const uint32_t st = it & (kStages - 1);
+              ok = warp_wait(bars.kvf(st), (it / kStages) & 1, abort_flag, p.status);
+              if (!ok) break;
+              uint32_t* blk = reinterpret_cast<uint32_t*>(smem + L::kOffScale) +
+                              (it & (kScaleStages - 1)) * kScaleStageFloats;
+              const uint4 v = make_uint4(blk[lane], blk[32 + lane], blk[64 + lane], blk[96 + lane]);
+              __syncwarp();
+              *reinterpret_cast<uint4*>(blk + 4 * lane) = v;
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bars.sfr(st));
+            }
+          }
+        }
       } else {
         // =================================================== per group: weights and causal limits
         // A separate producer: the epilogue may hold a group's weights until TMEM
@@ -725,12 +742,15 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     // instruction descriptor for N = 64 * len: the N field (N >> 3 at bit
     // 17) grows by len << 20; format code 0 is e4m3 for kind::f8f6f4 and f16
     // for kind::f16
-    const uint32_t id_base = idesc(0, 0, 128, 0);
+    const uint32_t id_base = kMx ? idesc_mxf4(128, 0) : idesc(0, 0, 128, 0);
+    constexpr uint32_t kHi = kMx ? kSdescHiSw64 : kSdescHi;
     const uint32_t a_lo0 = sdesc_lo(s_kv), q_lo0 = sdesc_lo(s_q);
     constexpr uint32_t kStageLo = L::kKStageBytes >> 4;
-    constexpr uint32_t kQRowLo = (kDq ? kHeads * 128 : kHeads * kHeadDim) >> 4;  // one q row (64 heads) of B
+    // one q row (64 heads) of B: 8192 bytes of e4m3 (FP8), 64 f16 rows of
+    // 128 bytes in each k-half (FP4), 4096 bytes of packed e2m1 (MXFP4)
+    constexpr uint32_t kQRowLo = (kMx ? kHeads * (kHeadDim / 2) : kHeads * 128) >> 4;
     // dequantising formats: the B operand's second k-half follows the pass's first
-    constexpr uint32_t kQHalfLo = Lay<kFmt == DSA_KV_FP8 ? DSA_KV_FP4 : kFmt>::kQHalfBytes >> 4;
+    constexpr uint32_t kQHalfLo = Lay<DSA_KV_FP4>::kQHalfBytes >> 4;
     const uint32_t issue = elect_one() ? 1u : 0u;
     const bool leader = issue != 0;
     if constexpr (!kDq) {
@@ -755,6 +775,13 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       }
       ok = warp_wait(bars.q_full, gi & 1, abort_flag, p.status);
       if (!ok) break;
+      if constexpr (kMx) {
+        // the pass's q scales to TMEM: rows 2b, 2b + 1 at columns kMxSfbCol + 4b
+        tc_fence_after();
+        const uint32_t s_qsf = sbase + L::kOffQsf;
+        for (uint32_t b = 0; 2 * b < n; ++b)
+          tmem_cp_scales(issue, tmem + kMxSfbCol + 4 * b, sdesc_lo_plain(s_qsf + 512 * b), kSdescHiPlain);
+      }
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
         const uint32_t st = it & (kStages - 1);
         // A wait that finds its phase complete still costs a few hundred
@@ -765,20 +792,29 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         // a test first only delays the wake-up).  The warp votes once per
         // wait group.
         {
+          // MXFP4: the stage's scales are in the copy layout too (the scale
+          // warp saw the stage land first)
           const uint32_t kvp = (it / kStages) & 1;
-          ok = __all_sync(0xffffffffu, (!kDq && mbar_test(bars.kvf(st), kvp)) ||
-                                           wait_or_abort(bars.kvf(st), kvp, abort_flag, p.status));
+          const uint32_t kb = kMx ? bars.sfr(st) : bars.kvf(st);
+          ok = __all_sync(0xffffffffu,
+                          (!kDq && mbar_test(kb, kvp)) || wait_or_abort(kb, kvp, abort_flag, p.status));
         }
         if (!ok) break;
+        if constexpr (kMx) {
+          tc_fence_after();
+          tmem_cp_scales(issue, tmem + kMxSfaCol + 4 * st,
+                         sdesc_lo_plain(s_scale + (it & (kScaleStages - 1)) * kScaleStageFloats * 4), kSdescHiPlain);
+        }
         const uint32_t a_lo = a_lo0 + st * kStageLo;
         uint32_t b_lo = q_lo0;
         uint32_t left = n;
         do {  // the tile's rows, cut where a TMEM buffer ends
-          const uint32_t c = pos & (kSlots - 1);
+          const uint32_t c = pos % kSlots;
           const uint32_t len = min(min(left, kSlots - c), 4u);  // contiguous slots, N <= 256
-          // pair pos + i goes to slot c + i, free once the pair 8 positions
-          // earlier has been read by its warpgroup (a tile's n <= 8 pairs
-          // take n distinct slots); each chunk waits only for its own slots
+          // pair pos + i goes to slot c + i, free once the pair kSlots
+          // positions earlier has been read by its warpgroup (a tile's
+          // n <= kSlots pairs take n distinct slots); each chunk waits only
+          // for its own slots
           bool mine = true;
           for (uint32_t i = 0; i < len && mine; ++i) {
             const uint32_t b = bars.te(c + i), pr = (((pos + i) / kSlots) & 1) ^ 1;
@@ -788,8 +824,13 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem + c * kPairCols;
-          if constexpr (!kDq) mma_fp8_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20));
-          else mma_f16_k128(issue, d_tmem, a_lo, b_lo, kSdescHi, id_base + (len << 20), kQHalfLo);
+          if constexpr (kMx)
+            mma_mxf4_k128(issue, d_tmem, a_lo, b_lo, kHi, id_base + (len << 20), tmem + kMxSfaCol + 4 * st,
+                          tmem + kMxSfbCol + 2 * (n - left));
+          else if constexpr (!kDq)
+            mma_fp8_k128(issue, d_tmem, a_lo, b_lo, kHi, id_base + (len << 20));
+          else
+            mma_f16_k128(issue, d_tmem, a_lo, b_lo, kHi, id_base + (len << 20), kQHalfLo);
           left -= len;
           pos += len;
           b_lo += len * kQRowLo;
@@ -840,7 +881,6 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       const int lim = static_cast<int>(min(static_cast<int64_t>(walk.npages) * kPageTokens, p.logits_stride));
       const float* w_grp = w_sm + wb * kWBufFloats;
       const int32_t* ctx_grp = ctx_sm + wb * kGroupMaxRows;
-      const float* rowf_grp = reinterpret_cast<const float*>(smem + L::kOffRowF) + wb * kGroupMaxRows;
       OutT* const out_grp = out + static_cast<int64_t>(walk.r0) * p.logits_stride;
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
         const uint32_t r_first = (wg - pos) & (kEpiWg - 1);
@@ -853,12 +893,13 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         ok = warp_wait(bars.tr(it, kDq), (it / kTileRing) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        const float kscale = scale_sm[(it & (kScaleStages - 1)) * kScaleStageFloats + tok];
+        // (MXFP4: every scale is applied inside the MMA)
+        const float kscale = kMx ? 1.f : scale_sm[(it & (kScaleStages - 1)) * kScaleStageFloats + tok];
         const int scol = j * kTileTokens + tok;
         const bool in_span = scol < lim;
         for (uint32_t r = r_first; r < static_cast<uint32_t>(n); r += kEpiWg) {
           const uint32_t pp = pos + r;
-          const uint32_t sl = pp & (kSlots - 1);
+          const uint32_t sl = pp % kSlots;
           const float4* wr = reinterpret_cast<const float4*>(w_grp + r * kHeads);
           float2 cx = make_float2(0.f, 0.f), ca = cx;
 #pragma unroll
@@ -883,7 +924,6 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
             }
           }
           float acc = 0.5f * ((cx.x + cx.y) + (ca.x + ca.y));
-          if constexpr (kMx) acc *= rowf_grp[r];  // the row's q scale factor, a power of two
           const float logit = (scol < ctx_grp[r]) ? kscale * acc : -INFINITY;
           if (in_span) store_logit(out_grp + static_cast<int64_t>(r) * p.logits_stride + scol, logit);
         }
@@ -964,13 +1004,13 @@ cudaError_t launch_logits_fp8(const LogitsArgs& a, cudaStream_t stream) {
                              static_cast<uint64_t>(a.num_rows) * kHeads};
   const uint64_t qstrides[1] = {static_cast<uint64_t>(kHeadDim)};
   const uint32_t qbox[2] = {static_cast<uint32_t>(kHeadDim), static_cast<uint32_t>(kHeads)};
-  if (!encode_tensor_map_u8(&tm_q, 2, const_cast<uint8_t*>(a.q), qdims, qstrides, qbox, true))
+  if (!encode_tensor_map_u8(&tm_q, 2, const_cast<uint8_t*>(a.q), qdims, qstrides, qbox, 128))
     return cudaErrorInvalidValue;
   const uint64_t kdims[3] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(kPageTokens),
                              static_cast<uint64_t>(a.num_pages)};
   const uint64_t kstrides[2] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(a.page_stride)};
   const uint32_t kbox[3] = {static_cast<uint32_t>(kHeadDim), static_cast<uint32_t>(kPageTokens), 1};
-  if (!encode_tensor_map_u8(&tm_kv, 3, const_cast<uint8_t*>(a.kv_cache), kdims, kstrides, kbox, true))
+  if (!encode_tensor_map_u8(&tm_kv, 3, const_cast<uint8_t*>(a.kv_cache), kdims, kstrides, kbox, 128))
     return cudaErrorInvalidValue;
   const Params p = make_params(a);
   return launch<DSA_KV_FP8>(a, tm_q, tm_kv, p, stream);
@@ -985,10 +1025,22 @@ cudaError_t launch_logits_fp4(const LogitsArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_logits_mxfp4(const LogitsArgs& a, cudaStream_t stream) {
-  // as FP4: plain bulk copies of whole pages, q converted by the kernel
-  alignas(64) CUtensorMap unused{};
+  // packed e2m1 q rows and key pages by TMA with the 64-byte swizzle (rows of
+  // 64 bytes: 128 elements)
+  alignas(64) CUtensorMap tm_q, tm_kv;
+  constexpr uint32_t kRowBytes = kHeadDim / 2;
+  const uint64_t qdims[2] = {kRowBytes, static_cast<uint64_t>(a.num_rows) * kHeads};
+  const uint64_t qstrides[1] = {kRowBytes};
+  const uint32_t qbox[2] = {kRowBytes, static_cast<uint32_t>(kHeads)};
+  if (!encode_tensor_map_u8(&tm_q, 2, const_cast<uint8_t*>(a.q), qdims, qstrides, qbox, 64))
+    return cudaErrorInvalidValue;
+  const uint64_t kdims[3] = {kRowBytes, static_cast<uint64_t>(kPageTokens), static_cast<uint64_t>(a.num_pages)};
+  const uint64_t kstrides[2] = {kRowBytes, static_cast<uint64_t>(a.page_stride)};
+  const uint32_t kbox[3] = {kRowBytes, static_cast<uint32_t>(kPageTokens), 1};
+  if (!encode_tensor_map_u8(&tm_kv, 3, const_cast<uint8_t*>(a.kv_cache), kdims, kstrides, kbox, 64))
+    return cudaErrorInvalidValue;
   const Params p = make_params(a);
-  return launch<DSA_KV_MXFP4>(a, unused, unused, p, stream);
+  return launch<DSA_KV_MXFP4>(a, tm_q, tm_kv, p, stream);
 }
 
 }  // namespace dsa

@@ -342,6 +342,72 @@ __device__ __forceinline__ void mma_f16_k128(uint32_t issue, uint32_t d_tmem, ui
       : "memory");
 }
 
+// ---------------------------------------------------------------- block-scaled e2m1 (kind::mxf4)
+// Packed e2m1 operands (two elements a byte, K-major, 64-byte rows) stored
+// with the 64-byte swizzle: 8-row groups of 512 bytes (stride byte offset),
+// layout code 4.  High word of the shared-memory descriptor:
+constexpr uint32_t kSdescHiSw64 = (512 >> 4) | (1u << 14) | (4u << 29);
+
+// Instruction descriptor of kind::mxf4 (scale_vec::2X, ue8m0 scales): A and
+// B e2m1 (format code 1 at bits 7-9 and 10-12), D always f32, bit 23 = ue8m0
+// scale format, N >> 3 at bits 17-22, M >> 4 at bits 24-28; the scale-factor
+// ids (which byte of each 32-bit scale word the instruction starts at) sit at
+// bits 29-30 (A) and 4-5 (B).
+__host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+
+// Scale factors in TMEM for kind::mxf4: the scales of operand row x (a key
+// token of A, a column of B) are the 32-bit word at lane x mod 32 -- the
+// same in every lane quarter -- and column base + x / 32; byte i of the word
+// scales K block i (32 elements) of the row.  One 128-row block is 32 lanes x
+// 4 columns, filled from 512 bytes of shared memory by one copy that
+// replicates to the four lane quarters: TMEM lane l, column c <- the 32-bit
+// word 4 l + c of the source.  So the source holds row x's word at
+// 4 (x mod 32) + x / 32.
+//
+// Shared-memory descriptor of that source (no swizzle: 8-row x 16-byte core
+// matrices of 128 contiguous bytes, both strides 128 bytes):
+__device__ __forceinline__ uint32_t sdesc_lo_plain(uint32_t saddr) {
+  return ((saddr >> 4) & 0x3FFFu) | ((128u >> 4) << 16);
+}
+constexpr uint32_t kSdescHiPlain = (128 >> 4) | (1u << 14);
+
+// tcgen05.cp of one 512-byte scale block to TMEM (32 lanes x 128 bits, to
+// all four lane quarters), by the threads with `issue` set.  It runs in issue
+// order with the same thread's MMAs, and a later commit covers it.
+__device__ __forceinline__ void tmem_cp_scales(uint32_t issue, uint32_t taddr, uint32_t s_lo, uint32_t s_hi) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 d;\n\t"
+      "setp.ne.b32 p, %0, 0;\n\t"
+      "mov.b64 d, {%2, %3};\n\t"
+      "@p tcgen05.cp.cta_group::1.32x128b.warpx4 [%1], d;\n\t}" ::"r"(issue),
+      "r"(taddr), "r"(s_lo), "r"(s_hi)
+      : "memory");
+}
+
+// A 128-deep block-scaled e2m1 contraction into d_tmem: two K = 64 steps,
+// each 32 bytes into the operands' 64-byte rows (+2 in the descriptor's
+// address field); the first takes scale bytes 0-1 (K blocks 0 and 1) and
+// overwrites, the second takes bytes 2-3 (scale-factor id 2 for A and B)
+// and accumulates.  sfa / sfb: TMEM addresses of the two operands' scales.
+__device__ __forceinline__ void mma_mxf4_k128(uint32_t issue, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                              uint32_t hi, uint32_t idesc_v, uint32_t sfa, uint32_t sfb) {
+  asm volatile(
+      "{\n\t.reg .pred p, f, t;\n\t.reg .b64 da, db;\n\t.reg .b32 al, bl, id2;\n\t"
+      "setp.ne.b32 p, %0, 0;\n\t"
+      "setp.ne.b32 f, %4, %4;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "mov.b64 da, {%2, %4};\n\tmov.b64 db, {%3, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%1], da, db, %5, [%6], [%7], f;\n\t"
+      "add.u32 al, %2, 2;\n\tadd.u32 bl, %3, 2;\n\t"
+      "or.b32 id2, %5, 0x40000020;\n\t"
+      "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%1], da, db, id2, [%6], [%7], t;\n\t}" ::"r"(issue),
+      "r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc_v), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+
 // tcgen05.commit by the threads with `issue` set.
 __device__ __forceinline__ void mma_commit_if(uint32_t issue, uint32_t bar) {
   asm volatile(
