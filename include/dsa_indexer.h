@@ -119,8 +119,8 @@ int32_t dsa_device_num_sms(void);
  * dsa_paged_mqa_logits_metadata_for_keys for other sizes); a unit is one
  * 128-key tile of a group (ceil(max L_t / 128) units per group) and costs its
  * SM one K tile from HBM plus MMA and epilogue work that grows with the
- * group's rows n: the unit weighs 4n + n^2 here (FP8 keys; a tile's cost
- * grows faster than its rows) and n for the FP4 and MXFP4 schedules of
+ * group's rows n: the unit weighs 4n + n^2 here and for MXFP4 keys (a tile's
+ * cost grows faster than its rows), and n for the FP4 schedule of
  * dsa_paged_mqa_logits_metadata_for_keys.  The groups are ordered by row
  * count (stable) and their units laid end to end; SM i takes units from both
  * ends of that sequence, so that every SM owns floor or ceil of
@@ -143,8 +143,9 @@ int dsa_paged_mqa_logits_metadata(const int32_t* context_lens, const int32_t* in
  * dsa_paged_mqa_logits_metadata_for_keys - the same schedule, with groups cut
  * at the rows one pass of the logits call serves for that key format:
  * DSA_KV_FP8 8 (= dsa_paged_mqa_logits_metadata), DSA_KV_MXFP4 6, DSA_KV_FP4 4
- * (the dequantising formats convert q into a pass-sized buffer, so a larger
- * group costs one pass per 4 or 6 rows while the split counts it as one unit).
+ * (an MXFP4 tile's pairs have 7 TMEM slots, and FP4 converts q into a
+ * pass-sized buffer, so a larger group costs one pass per 6 or 4 rows while
+ * the split counts it as one unit).
  * No counterpart in the pages, whose metadata call takes no key format; the
  * extra argument only sizes the groups (header word 7 records it).  Any
  * format's logits call accepts a schedule of any group size from 1 to 8;

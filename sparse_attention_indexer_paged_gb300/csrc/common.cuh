@@ -33,21 +33,22 @@ constexpr int kPageTokens = DSA_BLOCK_KV;   // 64 tokens per page
 constexpr int kTileTokens = 128;
 constexpr int kGroupMaxRows = 8;
 // Rows a group holds for each key format: what one pass of that format's
-// logits kernel over a tile serves (FP8 all 8; the dequantising formats
-// convert q into a pass-sized buffer: MXFP4 6 rows, FP4 4), so that a unit
-// costs one pass.  The logits call takes a schedule of any group size up to
-// kGroupMaxRows.
+// logits kernel over a tile serves (FP8 all 8; MXFP4 6, its last TMEM
+// columns holding scale factors; FP4 4, converting q into a pass-sized
+// buffer), so that a unit costs one pass.  The logits call takes a schedule
+// of any group size up to kGroupMaxRows.
 __host__ __device__ constexpr int group_rows_for(int kv_format) {
   return kv_format == DSA_KV_FP4 ? 4 : (kv_format == DSA_KV_MXFP4 ? 6 : kGroupMaxRows);
 }
 // What one unit (tile) of a group of `rows` rows weighs in the schedule's
-// second balanced quantity (the first is the units themselves).  FP8: 4n +
-// n^2, since a tile's cost grows faster than its rows (a tile of 6 rows fills
-// 6 of the 8 TMEM slots, so tiles no longer overlap; measured microseconds
-// per tile by rows 0.49, 0.56, 0.65, 0.82, 1.01, 1.17); the dequantising
-// formats: n, their groups being one row pass each.
+// second balanced quantity (the first is the units themselves).  FP8 and
+// MXFP4: 4n + n^2, since a tile's cost grows faster than its rows (a tile of
+// 6 rows fills 6 of the 8 TMEM slots, so tiles no longer overlap; measured
+// microseconds per FP8 tile by rows 0.49, 0.56, 0.65, 0.82, 1.01, 1.17; the
+// MXFP4 kernel has the same pipeline and measured 9 us faster with this
+// weight than with n); FP4: n, its tiles' cost being the conversion.
 __host__ __device__ constexpr int64_t unit_weight(int kv_format, int rows) {
-  return kv_format == DSA_KV_FP8 ? 4 * rows + rows * rows : rows;
+  return kv_format != DSA_KV_FP4 ? 4 * rows + rows * rows : rows;
 }
 constexpr int32_t kScheduleMagic = 0x44534132;
 constexpr int kScheduleHeaderWords = 8;

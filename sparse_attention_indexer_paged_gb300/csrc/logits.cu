@@ -12,41 +12,52 @@
 //
 // The contraction is laid out with the keys as M: for a tile and one row r
 // of the group, D[token, h] = sum_d K[token, d] * Q[r, h, d] is a 128 x 64
-// tcgen05 MMA (A = the K tile, B = Q row r, K = 128 in four steps).  TMEM
+// tcgen05 MMA (A = the K tile, B = Q row r, K = 128 in steps).  TMEM
 // lane = token, so the head-weighted ReLU reduction of a (tile, row) pair
 // runs inside one thread with no cross-lane traffic, and a warp's 32 logits
-// are 32 consecutive columns.
+// are 32 consecutive columns.  Per key format:
+//   FP8    e4m3 x e4m3, kind::f8f6f4, four K = 32 steps; the fp32 key scale
+//          in the epilogue.
+//   MXFP4  packed e2m1 x e2m1 with ue8m0 scales per 32 elements on both
+//          sides, kind::mxf4 block-scaled, two K = 64 steps; the scales go
+//          to TMEM (tcgen05.cp) and the tensor core applies them.
+//   FP4    e2m1 keys (e4m3 scales per 16, fp32 per token) against e4m3 q:
+//          dequantised to f16 tiles by six warps, kind::f16, eight K = 16 steps.
 //
 // The CTA's (tile, row) pairs form one stream: pair p goes to TMEM slot
-// p mod 8 (64 columns each) and is drained by epilogue warpgroup p mod 4.  A
+// p mod kSlots (64 columns each; 8 slots, 7 for MXFP4) and is drained by
+// epilogue warpgroup p mod 4.  A
 // tile's consecutive pairs go out as few MMAs of N = 64 x pairs as the slot
 // ring allows (N <= 256, cut where the ring wraps); each chunk waits only for
 // its own slots, released by the warpgroups that read their previous pairs,
 // and one commit per tile tells the epilogue that all its pairs are in TMEM.
 //
-// Rings: K tiles (kStages, released by the tile's MMA commit) and, for FP8,
-// the tiles' key scales, which the K producer copies beside the values on the
-// same barrier into a ring of kScaleStages tiles that the epilogue reads once
-// the tile's commit has fired.
+// Rings: K tiles (kStages, released by the tile's MMA commit) and, for FP8
+// and MXFP4, the tiles' key scales, which the K producer copies beside the
+// values on the same barrier into a ring of kScaleStages tiles (FP8: read by
+// the epilogue once the tile's commit has fired; MXFP4: copied to TMEM
+// before the tile's MMAs).
 //
-// Warp roles (FP8: 640 threads):
+// Warp roles (FP8 and MXFP4: 640 threads; FP4: 768):
 //   warp 0      K producer: per tile the two K pages (3-D tensor map over the
-//               pool, page id from the block table) and their key scales;
-//               runs ahead across groups.
+//               pool, page id from the block table) and their key scales
+//               (FP4: whole pages by bulk copy); runs ahead across groups.
 //   warp 1      MMA issuer and TMEM owner (512 columns): the whole warp walks
 //               the work with warp-uniform values; one elected lane issues.
-//               For FP8 keys it also loads each group's Q rows once the
-//               previous group's MMAs have completed.
+//               For FP8 and MXFP4 keys it also loads each pass's Q rows once
+//               the previous pass's MMAs have completed.
 //   warp 2      per group: head weights and causal limits (double buffered).
-//   warp 3      FP8: no role.  FP4 / MXFP4: one of six dequantising warps
+//   warp 3      FP8: no role.  MXFP4: puts the q and key scales in the layout
+//               the TMEM copy wants.  FP4: one of six dequantising warps
 //               (2, 3, 20-23) that turn raw pages into f16 K tiles.
 //   warps 4-19  four epilogue warpgroups: tcgen05.ld of a pair, relu,
 //               packed-fp32 FMA with the head weights, key scale, causal
 //               mask, store.  Each warp visits only its own pairs.
 //
 // A wait on an mbarrier that has already completed still costs the waiting
-// warp a few hundred cycles; with FP8 keys most of the MMA warp's waits find
-// their phase complete, so it tests each barrier without blocking first.
+// warp a few hundred cycles; with FP8 and MXFP4 keys most of the MMA warp's
+// waits find their phase complete, so it tests each barrier without
+// blocking first.
 // Every wait is bounded (a CTA abort flag and DSA_ERR_TIMEOUT after 2 s).
 #include <cuda_bf16.h>
 
@@ -56,7 +67,7 @@ namespace dsa {
 namespace {
 
 // Warps 0-3 have the producer, MMA and loader roles; warps 4-19 are four
-// epilogue warpgroups.  FP8: 20 warps; FP4 and MXFP4: plus warps 20-23 so
+// epilogue warpgroups.  FP8 and MXFP4: 20 warps; FP4: plus warps 20-23 so
 // that six warps (3, 2, 20-23) share the dequantisation.  Every format reads
 // a pair from TMEM in two 32-column pieces (one 64-column load measured the
 // same on varlen and 2 us slower on MTP; five or six epilogue warpgroups, so
@@ -220,9 +231,9 @@ struct Bars {
   __device__ uint32_t we(int b) const { return w_empty + 8 * b; }
   // TMEM slot s: drained by the warpgroup of the pair in it
   // Tile i's pairs are in TMEM: one MMA commit per tile.  With 8 K stages
-  // (FP8) this is the stage's kv_empty barrier; the dequantising formats have
-  // 2 stages and a ring of their own, so that a warp waiting for tile i never
-  // finds the barrier already two phases on.
+  // (FP8, MXFP4) this is the stage's kv_empty barrier; FP4 has 2 stages and a
+  // ring of its own, so that a warp waiting for tile i never finds the
+  // barrier already two phases on.
   __device__ uint32_t tr(uint32_t i, bool own_ring) const {
     return own_ring ? tile_ready + 8 * (i & (kTileRing - 1)) : kv_empty + 8 * (i & (kTileRing - 1));
   }
@@ -749,7 +760,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     // one q row (64 heads) of B: 8192 bytes of e4m3 (FP8), 64 f16 rows of
     // 128 bytes in each k-half (FP4), 4096 bytes of packed e2m1 (MXFP4)
     constexpr uint32_t kQRowLo = (kMx ? kHeads * (kHeadDim / 2) : kHeads * 128) >> 4;
-    // dequantising formats: the B operand's second k-half follows the pass's first
+    // FP4: the B operand's second k-half follows the pass's first
     constexpr uint32_t kQHalfLo = Lay<DSA_KV_FP4>::kQHalfBytes >> 4;
     const uint32_t issue = elect_one() ? 1u : 0u;
     const bool leader = issue != 0;
@@ -785,12 +796,11 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
         const uint32_t st = it & (kStages - 1);
         // A wait that finds its phase complete still costs a few hundred
-        // cycles.  With FP8 keys the K stage and most slots are ready when
-        // the MMA warp comes to them (the K stream runs ahead), so each
-        // barrier is first tested without blocking; the dequantising formats
-        // wait at once (their stages and slots are mostly still pending, and
-        // a test first only delays the wake-up).  The warp votes once per
-        // wait group.
+        // cycles.  With FP8 and MXFP4 keys the K stage and most slots are
+        // ready when the MMA warp comes to them (the K stream runs ahead), so
+        // each barrier is first tested without blocking; FP4 waits at once
+        // (its stages and slots are mostly still pending, and a test first
+        // only delays the wake-up).  The warp votes once per wait group.
         {
           // MXFP4: the stage's scales are in the copy layout too (the scale
           // warp saw the stage land first)

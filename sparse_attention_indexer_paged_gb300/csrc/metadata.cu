@@ -10,8 +10,8 @@
 // A unit is one 128-key tile of one group (up to 8 adjacent rows of one
 // request).  It costs its SM one K tile from HBM, the same for every unit,
 // plus MMA columns and epilogue work that grow with the group's rows: a unit
-// of n rows weighs unit_weight(format, n) (n for the dequantising formats,
-// 4n + n^2 for FP8, whose tiles cost more than linearly in their rows).  The
+// of n rows weighs unit_weight(format, n) (n for FP4 keys, 4n + n^2 for FP8
+// and MXFP4, whose tiles cost more than linearly in their rows).  The
 // rule gives every SM the same number of units (within one) and, as nearly
 // as the groups allow, the same weight:
 //   1. groups: runs of equal request ids, each cut into pieces of at most

@@ -449,31 +449,6 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return r;
 }
 
-// 2^d (d <= 0) as an f16 in both halves, built from the f16 bit layout
-// (exponent bias 15, 10 fraction bits): normal down to 2^-14, subnormal down
-// to 2^-24, zero below.
-__device__ __forceinline__ uint32_t pow2_f16x2(int d) {
-  uint32_t b = 0;
-  if (d >= -14)
-    b = static_cast<uint32_t>(d + 15) << 10;
-  else if (d >= -24)
-    b = 1u << (d + 24);
-  return b | (b << 16);
-}
-
-// The OCP MX E8M0 scale 2^(e - 127) as fp32 from its bit layout: exponent
-// field e for e in 1..254, the subnormal 2^-127 for e = 0, NaN for 255.
-__device__ __forceinline__ float ue8m0_to_f32(uint32_t e) {
-  if (e == 0) return __uint_as_float(0x00400000u);
-  if (e >= 255) return __uint_as_float(0x7fc00000u);
-  return __uint_as_float(e << 23);
-}
-
-// Largest of the four bytes of x.
-__device__ __forceinline__ uint32_t max_byte4(uint32_t x) {
-  return max(max(x & 0xffu, (x >> 8) & 0xffu), max((x >> 16) & 0xffu, x >> 24));
-}
-
 // High and low 32-bit words of sdesc_k_sw128(saddr).
 constexpr uint32_t kSdescHi = (1024 >> 4) | (1u << 14) | (2u << 29);
 __device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr) { return ((saddr >> 4) & 0x3FFFu) | (1u << 16); }
