@@ -57,6 +57,7 @@ PAGES_CONTEXT = ("pages: sm100_paged_mqa_logits 214.304 us -> 51.808 us (varlen)
                  "GLM-5.3-Flash, 120K context, batch 40, 5 speculative steps (nsys); "
                  "another machine and kernel-only")
 FP8_PEAK_RATIO = 2.0  # nominal dense fp8 : bf16 tensor rate
+FP4_PER_FP8 = 3.0     # nominal dense fp4 : fp8 tensor rate of the part (13.5 : 4.5 PFLOP/s)
 
 
 def parse():
@@ -263,7 +264,21 @@ def fp8_peak_tflops(dev, bf16_tf):
     return bf16_tf * FP8_PEAK_RATIO, f"bf16 peak x {FP8_PEAK_RATIO} (nominal fp8:bf16 ratio; the FP8 GEMM was unavailable)"
 
 
-def measure_config(name, dev, K=200, KB=100, fp8_tf=None, hbm_gbs=None):
+def tensor_peak(kv_format, fp8_tf, fp8_src, bf16_tf):
+    """(TFLOP/s, how it was obtained) of the tensor rate the logits
+    contraction runs at for this key format: FP8 keys (kind::f8f6f4) the FP8
+    GEMM figure; FP4 keys (dequantised to f16 tiles, kind::f16) the measured
+    bf16 GEMM (f16 and bf16 share a rate); MXFP4 (block-scaled kind::mxf4)
+    the FP8 figure times the nominal fp4:fp8 ratio."""
+    import workloads as W
+    if kv_format == W.KV_FP4:
+        return bf16_tf, "bf16 GEMM peak (MEASURED_PEAKS.json bf16_tflops): the FP4 kernel's MMAs are kind::f16"
+    if kv_format == W.KV_MXFP4:
+        return round(fp8_tf * FP4_PER_FP8, 1), f"FP8 peak x {FP4_PER_FP8} (nominal fp4:fp8 ratio; kind::mxf4 MMAs)"
+    return fp8_tf, fp8_src
+
+
+def measure_config(name, dev, K=200, KB=100, fp8_tf=None, fp8_src="", bf16_tf=None, hbm_gbs=None):
     """One decode workload timed as the headline is: the three-kernel step
     replayed from a CUDA graph (K replays), then a per-kernel event loop (KB
     steps); the logits kernel's achieved GB/s against the bytes it must move."""
@@ -324,7 +339,8 @@ def measure_config(name, dev, K=200, KB=100, fp8_tf=None, hbm_gbs=None):
     key_b, logit_b, small_b, flops = algorithmic_bytes(wl)
     alg = key_b + logit_b + small_b
     t_mem = alg / (hbm_gbs * 1e9)
-    t_tc = flops / (fp8_tf * 1e12)
+    tc_tf, tc_src = tensor_peak(wl.kv_format, fp8_tf, fp8_src, bf16_tf)
+    t_tc = flops / (tc_tf * 1e12)
     achieved = alg / (kus[1] * 1e-6) / 1e9
     res = {
         "workload": workload_desc(name, wl),
@@ -334,6 +350,9 @@ def measure_config(name, dev, K=200, KB=100, fp8_tf=None, hbm_gbs=None):
         "logits_achieved_gbs": round(achieved, 1),
         "logits_roofline_frac": round(achieved / hbm_gbs, 4),
         "logits_bound": "hbm" if t_mem >= t_tc else "tensor",
+        "tensor_peak_tflops": tc_tf,
+        "tensor_peak_source": tc_src,
+        "tensor_frac": round(flops / (kus[1] * 1e-6) / 1e12 / tc_tf, 4),
         "bound_us": round(max(t_mem, t_tc) * 1e6, 2),
         "logits_frac_of_bound": round(max(t_mem, t_tc) / (kus[1] * 1e-6), 4),
         "step_roofline_frac": round(max(t_mem, t_tc) / (step_us * 1e-6), 4),
@@ -585,8 +604,9 @@ def run_ours(args, rank, world, local):
     alg_bytes = key_b + logit_b + small_b
     achieved = alg_bytes / (logit_ms * 1e-3) / 1e9
     fp8_tf, fp8_src = fp8_peak_tflops(dev, bf16_tf)
+    tc_tf, tc_src = tensor_peak(wl.kv_format, fp8_tf, fp8_src, bf16_tf)
     t_mem = alg_bytes / (hbm_gbs * 1e9)
-    t_tc = flops / (fp8_tf * 1e12)
+    t_tc = flops / (tc_tf * 1e12)
     traffic = profile_traffic("logits.cu", f"logits_{args.workload}_ncu.md")
     step_bytes = alg_bytes + logit_b + T * wl.topk * 4   # + top-k re-read of logits and index write
     result = {
@@ -630,6 +650,9 @@ def run_ours(args, rank, world, local):
             "tensor_frac_of_fp8_peak": round(flops / (logit_ms * 1e-3) / 1e12 / fp8_tf, 4),
             "fp8_peak_tflops": fp8_tf,
             "fp8_peak_source": fp8_src,
+            "tensor_peak_tflops": tc_tf,
+            "tensor_peak_source": tc_src,
+            "tensor_frac": round(flops / (logit_ms * 1e-3) / 1e12 / tc_tf, 4),
             "bound_us": round(max(t_mem, t_tc) * 1e6, 2),
             "step_roofline_frac": round(max(t_mem, t_tc) / (ms_step * 1e-3), 4),
         },
@@ -646,7 +669,8 @@ def run_ours(args, rank, world, local):
         # the other decode configurations, each timed the same way (graph
         # replays, per-kernel events) with its own roofline
         others = [c for c in ("plain", "mtp", "varlen", "fp4_varlen", "mxfp4_varlen") if c != args.workload]
-        result["per_config"] = {c: measure_config(c, dev, fp8_tf=fp8_tf, hbm_gbs=hbm_gbs) for c in others}
+        result["per_config"] = {c: measure_config(c, dev, fp8_tf=fp8_tf, fp8_src=fp8_src, bf16_tf=bf16_tf,
+                                                  hbm_gbs=hbm_gbs) for c in others}
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl.to("cpu"), args.cpu_budget_s)
     if world > 1:
