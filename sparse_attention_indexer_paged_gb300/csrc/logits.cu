@@ -68,10 +68,14 @@ namespace {
 
 // Warps 0-3 have the producer, MMA and loader roles; warps 4-19 are four
 // epilogue warpgroups.  FP8 and MXFP4: 20 warps; FP4: plus warps 20-23 so
-// that six warps (3, 2, 20-23) share the dequantisation.  Every format reads
-// a pair from TMEM in two 32-column pieces (one 64-column load measured the
-// same on varlen and 2 us slower on MTP; five or six epilogue warpgroups, so
-// that a 6-row tile's pairs are read at once, measured slower).
+// that six warps (3, 2, 20-23) share the dequantisation.  The epilogue reads
+// a pair from TMEM in pieces of kPieceCols columns: two of 32 for decode
+// batches (a 64-column load measured 1.3 us slower on varlen and 2.7 us on
+// MTP), one of 64 for FP8 calls whose groups are full 8-row groups (rows
+// mapped onto fewer table rows, 8 or more each, as prefill's: 34 us faster on
+// 8192 prefill rows).  Both sizes in one kernel, chosen per tile, cost the
+// decode batches 4-8 us (more registers); five or six epilogue warpgroups,
+// so that a 6-row tile's pairs are read at once, measured slower.
 template <int kFmt> constexpr int kEpiWgOf = 4;
 template <int kFmt> constexpr int kThreadsOf = kFmt == DSA_KV_FP4 ? 768 : 640;
 constexpr int kFp4Converters = 6;
@@ -352,7 +356,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 __device__ __forceinline__ void store_logit(float* dst, float v) { *dst = v; }
 __device__ __forceinline__ void store_logit(__nv_bfloat16* dst, float v) { *dst = __float2bfloat16_rn(v); }
 
-template <int kFmt, typename OutT>
+template <int kFmt, typename OutT, int kPieceCols>
 __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                   const Params p) {
@@ -873,9 +877,10 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     //   sum_h w_h relu(x_h) = (sum_h w_h x_h + sum_h w_h |x_h|) / 2
     // so the head reduction is 64 packed FMAs (the |x| is an operand
     // modifier) instead of 64 max plus 32 packed FMAs.  The 64 columns come
-    // in two pieces of kPiece; the slot is released after the last piece is
+    // in pieces of kPiece; the slot is released after the last piece is
     // read.
-    constexpr int kPiece = 32;
+    constexpr int kPiece = kPieceCols;
+    static_assert(kPiece == 32 || kPiece == 64, "TMEM pieces of 32 or 64 columns");
     const uint32_t wg = static_cast<uint32_t>(warp - 4) >> 2;
     const int quarter = warp & 3;    // TMEM lanes this warp may read
     const int tok = quarter * 32 + lane;
@@ -989,21 +994,35 @@ Params make_params(const LogitsArgs& a) {
   return p;
 }
 
-template <int kFmt, typename OutT>
+template <int kFmt, typename OutT, int kPieceCols>
 cudaError_t launch_as(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const Params& p, int grid,
                       cudaStream_t stream) {
   constexpr int kBytes = Smem<kFmt>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(logits_kernel<kFmt, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
+  auto* kernel = logits_kernel<kFmt, OutT, kPieceCols>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
   if (e != cudaSuccess) return e;
-  return launch_dependent(logits_kernel<kFmt, OutT>, dim3(grid), dim3(kThreadsOf<kFmt>), kBytes, stream, tm_q,
-                          tm_kv, p);
+  return launch_dependent(kernel, dim3(grid), dim3(kThreadsOf<kFmt>), kBytes, stream, tm_q, tm_kv, p);
+}
+
+// FP8 calls whose rows map onto table rows 8 or more at a time (prefill
+// rows reading their request's pages) are walked in full 8-row groups and
+// read each pair from TMEM in one 64-column piece; everything else in two of 32.
+template <int kFmt, typename OutT>
+cudaError_t launch_pieces(const LogitsArgs& a, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const Params& p,
+                          cudaStream_t stream) {
+  if constexpr (kFmt == DSA_KV_FP8) {
+    if (a.bt_rows != nullptr && a.bt_num_rows > 0 &&
+        static_cast<int64_t>(a.num_rows) >= static_cast<int64_t>(kGroupMaxRows) * a.bt_num_rows)
+      return launch_as<kFmt, OutT, 64>(tm_q, tm_kv, p, a.num_sms, stream);
+  }
+  return launch_as<kFmt, OutT, 32>(tm_q, tm_kv, p, a.num_sms, stream);
 }
 
 template <int kFmt>
 cudaError_t launch(const LogitsArgs& a, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const Params& p,
                    cudaStream_t stream) {
-  if (a.logits_dtype == DSA_LOGITS_BF16) return launch_as<kFmt, __nv_bfloat16>(tm_q, tm_kv, p, a.num_sms, stream);
-  return launch_as<kFmt, float>(tm_q, tm_kv, p, a.num_sms, stream);
+  if (a.logits_dtype == DSA_LOGITS_BF16) return launch_pieces<kFmt, __nv_bfloat16>(a, tm_q, tm_kv, p, stream);
+  return launch_pieces<kFmt, float>(a, tm_q, tm_kv, p, stream);
 }
 
 }  // namespace
