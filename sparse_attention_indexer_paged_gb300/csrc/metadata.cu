@@ -236,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int64_t s_p0[kGroupMaxRows + 1];  // weight before it
   __shared__ int64_t s_wt[kGroupMaxRows + 1];  // weight of one unit of the piece
   __shared__ int64_t s_pq, s_pr;                // P = s_pq * S + s_pr
+  __shared__ int32_t s_ctx[kThreads];           // causal limits when T <= kThreads
 
   const int tid = threadIdx.x;
   const SchedLayout L(S, T);
@@ -249,6 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* spp_hi = base + 4 * n1;
   // ---- groups: a row starts one when it starts a run of equal request ids,
   // or when group_rows (<= kGroupMaxRows) rows of its run precede it in the current group
+  // When the rows fit one pass of the block, each thread's causal limit is
+  // loaded now (in flight during the groups phase) and kept in shared memory
+  // for the units phase, which would otherwise wait on a second global load.
+  const bool one_chunk = T <= kThreads;
+  const int32_t my_ctx = (one_chunk && tid < T) ? __ldg(ctx + tid) : 0;
   int carry_run = 0;  // run start of the previous chunk's last row
   int G = 0;
   for (int base = 0; base < T; base += kThreads) {
@@ -268,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   }
   for (int g = G + tid; g <= T; g += kThreads) grs[g] = T;
+  if (one_chunk) s_ctx[tid] = my_ctx;
   if (tid <= kGroupMaxRows) {
     s_base[tid] = 0;
     s_taken[tid] = 0;
@@ -319,8 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (k < G) {
       const int32_t w = pos[k];
       const int r0 = w & kPosRowMask, n = static_cast<int>(static_cast<uint32_t>(w) >> kPosRowsShift);
+      // the group's largest causal limit: all its loads in flight at once
       int lmax = 0;
-      for (int t = r0; t < r0 + n; ++t) lmax = max(lmax, ctx[t]);
+#pragma unroll
+      for (int j = 0; j < kGroupMaxRows; ++j)
+        if (j < n) lmax = max(lmax, one_chunk ? s_ctx[r0 + j] : __ldg(ctx + r0 + j));
       tiles = (lmax + kTileTokens - 1) / kTileTokens;
       pairs = static_cast<int64_t>(tiles) * unit_weight(kv_format, n);
     }
@@ -356,8 +366,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_u0[0] = 0;
     s_p0[0] = 0;
     s_wt[0] = 0;
-    s_pq = P / S;
-    s_pr = P % S;
+    // (a 64-bit division costs ~1.5K cycles: 32 bits when P fits)
+    if ((static_cast<uint64_t>(P) >> 32) == 0) {
+      const uint32_t p32 = static_cast<uint32_t>(P), s32 = static_cast<uint32_t>(S);
+      s_pq = p32 / s32;
+      s_pr = p32 - (p32 / s32) * s32;
+    } else {
+      s_pq = P / S;
+      s_pr = P % S;
+    }
   }
   __syncthreads();
 
@@ -368,7 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t uq = U / S, ur = U - uq * S;
     const int32_t x = tid * uq + (tid * ur) / S;
     s_x[tid] = x;
-    const int64_t cap = static_cast<int64_t>(tid) * s_pq + static_cast<int64_t>(tid) * s_pr / S;
+    // i (P mod S) < S^2 < 2^20: a 32-bit division
+    const int64_t cap = static_cast<int64_t>(tid) * s_pq +
+                        static_cast<int64_t>(static_cast<uint32_t>(tid * static_cast<int32_t>(s_pr)) /
+                                             static_cast<uint32_t>(S));
     ClassPieces cp;
 #pragma unroll
     for (int n = 1; n <= kGroupMaxRows; ++n) cp.u0[n] = s_u0[n];
