@@ -231,11 +231,11 @@ int dsa_fp8_fp4_paged_mqa_logits(const void* q, const void* kv_cache, int64_t pa
  *   kv_cache pages of DSA_MXFP4_PAGE_BYTES: packed e2m1 [64][64], then
  *            ue8m0 [64][4].
  * The other arguments, the -inf tail and the status word are those of
- * dsa_fp8_fp4_paged_mqa_logits.  The products are formed exactly (f16
- * operands scaled by 2^(e - e_max) of their token or row, that factor
- * applied to the fp32 result) unless a block's scale lies more than 2^14
- * below its token's or row's largest, when f16 keeps fewer of its bits; a
- * scale code 255 (NaN) gives a non-finite logit.
+ * dsa_fp8_fp4_paged_mqa_logits.  The tensor core takes the packed e2m1
+ * values and both operands' ue8m0 scales directly (block-scaled MMA,
+ * kind::mxf4): every 32-element block product is formed exactly and scaled
+ * by its two powers of two, the sum accumulated in fp32; a scale code 255
+ * (NaN) on a block makes the logits that block enters non-finite.
  */
 int dsa_mxfp4_paged_mqa_logits(const void* q, const void* q_scale, const void* kv_cache, int64_t page_stride_bytes,
                                int64_t num_pages, const float* weights, const int32_t* context_lens,

@@ -13,7 +13,7 @@ import torch
 import oracle
 import sparse_attention_indexer_paged_gb300 as dsa
 import workloads as W
-from gpu_helpers import check_logits, check_topk_exact, check_topk_tie_band, run_path
+from gpu_helpers import check_logits, check_topk_exact, check_topk_tie_band, logits_tolerance, run_path
 from schedule_check import check_schedule
 
 pytestmark = pytest.mark.gpu
@@ -429,8 +429,8 @@ def test_mxfp4_padded_page_stride():
 
 
 def test_mxfp4_block_scales_far_below_the_largest():
-    """Blocks 2^12 below their token's or row's largest scale (still exact in
-    the f16 operands) and 2^20 below (fewer bits kept; within tolerance)."""
+    """Blocks 2^12 and 2^20 below their token's or row's largest scale: the
+    block-scaled MMA applies each block's powers of two exactly."""
     wl = W.build("mxfp4", [300, 517], [2, 3], topk=64, kv_format=W.KV_MXFP4, seed=44)
     es = W._page_views(wl.kv_cache, W.KV_MXFP4)["bscale"]          # [pages, 64, 4] ue8m0
     ok = es != W.UE8M0_NAN
@@ -440,6 +440,35 @@ def test_mxfp4_block_scales_far_below_the_largest():
     wl.q_scale[:, ::3, 2] = (wl.q_scale[:, ::3, 2].int() - 12).clamp(min=0).to(torch.uint8)
     wl.q_scale[:, 1::5, 0] = (wl.q_scale[:, 1::5, 0].int() - 20).clamp(min=0).to(torch.uint8)
     _full_check(wl)
+
+
+def test_mxfp4_nan_scale_gives_non_finite_logit():
+    """A NaN block scale (ue8m0 code 255, OCP MX) on a live key block or on one
+    head's q block makes exactly the logits whose dot product it enters
+    non-finite, as in the oracle (whose ReLU keeps the NaN); every other logit
+    matches the oracle."""
+    wl = W.build("mxfp4", [300, 517], [2, 3], topk=64, kv_format=W.KV_MXFP4, seed=45)
+    es = W._page_views(wl.kv_cache, W.KV_MXFP4)["bscale"]   # [pages, 64, 4] ue8m0
+    # key token 70 of row 0's table (its second page, slot 6), block 2
+    es[int(wl.block_table[0, 1]), 6, 2] = W.UE8M0_NAN
+    # q of row 3 (the second request), head 5, block 0
+    wl.q_scale[3, 5, 0] = W.UE8M0_NAN
+    out = run_path(wl)
+    assert int(out["status"].item()) == 0, dsa.status_string(int(out["status"].item()))
+    ref, bound = oracle.workload_logits(wl)
+    g = out["logits"].float().cpu().double().numpy()
+    ctx = wl.context_lens.cpu().numpy()
+    planted = 0
+    for t in range(wl.num_rows):
+        L = int(ctx[t])
+        bad_ref = ~np.isfinite(ref[t, :L])
+        assert np.array_equal(~np.isfinite(g[t, :L]), bad_ref), f"row {t}: non-finite columns differ"
+        planted += int(bad_ref.sum())
+        ok = np.nonzero(~bad_ref)[0]
+        tol = logits_tolerance(bound[t, ok], ref[t, ok], out["logits"].dtype == torch.bfloat16)
+        assert np.all(np.abs(g[t, ok] - ref[t, ok]) <= tol), f"row {t}: finite logits off"
+    # row 3's every column, and column 70 of the two rows of request 0
+    assert planted >= int(ctx[3]) + 2, planted
 
 
 def test_mxfp4_full_size_every_row():
