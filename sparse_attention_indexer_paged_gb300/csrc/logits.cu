@@ -31,6 +31,10 @@
 // ring allows (N <= 256, cut where the ring wraps); each chunk waits only for
 // its own slots, released by the warpgroups that read their previous pairs,
 // and one commit per tile tells the epilogue that all its pairs are in TMEM.
+// FP8 calls with full 8-row groups (prefill rows on their request's table),
+// whose tiles fill every slot, also commit each earlier chunk of a tile, so
+// that its pairs are read while the tile's last chunk waits for slots (on
+// decode batches that bookkeeping costs more than it gains).
 //
 // Rings: K tiles (kStages, released by the tile's MMA commit) and, for FP8
 // and MXFP4, the tiles' key scales, which the K producer copies beside the
@@ -68,14 +72,10 @@ namespace {
 
 // Warps 0-3 have the producer, MMA and loader roles; warps 4-19 are four
 // epilogue warpgroups.  FP8 and MXFP4: 20 warps; FP4: plus warps 20-23 so
-// that six warps (3, 2, 20-23) share the dequantisation.  The epilogue reads
-// a pair from TMEM in pieces of kPieceCols columns: two of 32 for decode
-// batches (a 64-column load measured 1.3 us slower on varlen and 2.7 us on
-// MTP), one of 64 for FP8 calls whose groups are full 8-row groups (rows
-// mapped onto fewer table rows, 8 or more each, as prefill's: 34 us faster on
-// 8192 prefill rows).  Both sizes in one kernel, chosen per tile, cost the
-// decode batches 4-8 us (more registers); five or six epilogue warpgroups,
-// so that a 6-row tile's pairs are read at once, measured slower.
+// that six warps (3, 2, 20-23) share the dequantisation.  Every format reads
+// a pair from TMEM in two 32-column pieces (one 64-column load measured 1.3
+// us slower on varlen and 2.7 us on MTP; five or six epilogue warpgroups, so
+// that a 6-row tile's pairs are read at once, measured slower).
 template <int kFmt> constexpr int kEpiWgOf = 4;
 template <int kFmt> constexpr int kThreadsOf = kFmt == DSA_KV_FP4 ? 768 : 640;
 constexpr int kFp4Converters = 6;
@@ -88,6 +88,10 @@ constexpr int kMaxSlots = 8;
 constexpr uint32_t kMxSfaCol = 448;
 constexpr uint32_t kMxSfbCol = 480;
 constexpr int kTileRing = 8;  // tiles whose "pairs in TMEM" barrier phases are tracked at once
+// FP8 and MXFP4: every chunk of a tile but its last signals its pairs on a
+// ring of chunk barriers (a chunk's MMAs wait for slots that pairs at most
+// kSlots positions earlier held, so fewer than 16 chunks are ever pending)
+constexpr int kChunkRing = 16;
 constexpr int kScaleStages = 16;   // key scale ring
 constexpr int kTmemCols = 512;
 constexpr int kPairCols = 64;      // 64 heads of one pair
@@ -154,8 +158,8 @@ template <int kFmt> struct Smem : Lay<kFmt> {
   static constexpr int kOffCtx = kOffW + 2 * kWBufFloats * 4;  // causal limits of the group's rows
   static constexpr int kOffBar = kOffCtx + 2 * kGroupMaxRows * 4;
   // barriers: kv_full[8], kv_empty[8], raw_full[2], raw_empty[2], q_full, q_empty,
-  // w_full[2], w_empty[2], tm_empty[8], mma_done, tile_ready[8]
-  static constexpr int kNumBars = 2 * kMaxKStages + 2 * kMaxRawStages + 2 + 4 + kMaxSlots + 1 + kTileRing;
+  // w_full[2], w_empty[2], tm_empty[8], mma_done, tile_ready[8], chunk_ready[16]
+  static constexpr int kNumBars = 2 * kMaxKStages + 2 * kMaxRawStages + 2 + 4 + kMaxSlots + 1 + kTileRing + kChunkRing;
   static constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemAddr + 4;
   static constexpr int kOffWalk = kOffAbort + 4;  // WalkRanges
@@ -224,7 +228,7 @@ __device__ __forceinline__ const int32_t* table_row(const Params& p, int row) {
 
 struct Bars {
   uint32_t kv_full, kv_empty, raw_full, raw_empty, q_full, q_empty, w_full,
-      w_empty, tm_empty, mma_done, tile_ready;
+      w_empty, tm_empty, mma_done, tile_ready, chunk_ready;
   __device__ uint32_t kvf(int s) const { return kv_full + 8 * s; }
   __device__ uint32_t kve(int s) const { return kv_empty + 8 * s; }
   __device__ uint32_t rwf(int s) const { return raw_full + 8 * s; }
@@ -242,6 +246,9 @@ struct Bars {
     return own_ring ? tile_ready + 8 * (i & (kTileRing - 1)) : kv_empty + 8 * (i & (kTileRing - 1));
   }
   __device__ uint32_t te(uint32_t s) const { return tm_empty + 8 * s; }
+  // chunk c of the CTA's early chunks (all but each tile's last) has its
+  // pairs in TMEM
+  __device__ uint32_t ch(uint32_t c) const { return chunk_ready + 8 * (c & (kChunkRing - 1)); }
 };
 
 // The CTA's walk over its units: two ranges of the schedule's sorted unit
@@ -353,10 +360,19 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag, status));
 }
 
+// The chunk of a tile's pairs that starts at stream position pos with
+// `left` pairs to go: contiguous TMEM slots (cut where the slot ring wraps),
+// at most 4 pairs (N <= 256).  The MMA warp issues, and the epilogue waits
+// for, the same chunks.
+template <int kSlots>
+__device__ __forceinline__ uint32_t chunk_len(uint32_t pos, uint32_t left) {
+  return min(min(left, static_cast<uint32_t>(kSlots) - pos % kSlots), 4u);
+}
+
 __device__ __forceinline__ void store_logit(float* dst, float v) { *dst = v; }
 __device__ __forceinline__ void store_logit(__nv_bfloat16* dst, float v) { *dst = __float2bfloat16_rn(v); }
 
-template <int kFmt, typename OutT, int kPieceCols>
+template <int kFmt, typename OutT, bool kChunkCommits>
 __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                   const Params p) {
@@ -407,6 +423,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   bars.tm_empty = bars.w_empty + 16;
   bars.mma_done = bars.tm_empty + 8 * kMaxSlots;
   bars.tile_ready = bars.mma_done + 8;
+  bars.chunk_ready = bars.tile_ready + 8 * kTileRing;
   uint32_t* tmem_addr_smem = reinterpret_cast<uint32_t*>(smem + L::kOffTmemAddr);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kOffAbort);
 
@@ -433,6 +450,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       mbar_init(bars.te(sl), 4);  // the four warps of the pair's warpgroup have read it
     mbar_init(bars.mma_done, 1);
     for (int i = 0; i < kTileRing; ++i) mbar_init(bars.tile_ready + 8 * i, 1);  // the tile's MMA commit
+    for (int i = 0; i < kChunkRing; ++i) mbar_init(bars.chunk_ready + 8 * i, 1);  // a chunk's MMA commit
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -505,7 +523,6 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       // q rows of the pass, once the previous pass's MMAs have completed
       ok = warp_wait(bars.q_empty, (nq & 1) ^ 1, abort_flag, p.status);
       if (!ok) break;
-      {
       // 8 e4m3 codes per step; the warps take interleaved 32-chunk blocks
       const uint2* qsrc = reinterpret_cast<const uint2*>(p.q + static_cast<int64_t>(r0) * kHeads * kHeadDim);
       const int nchunks = n * kHeads * (kHeadDim / 8);
@@ -521,7 +538,6 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         const uint32_t off = static_cast<uint32_t>(c16 >> 3) * q_half + static_cast<uint32_t>(R >> 3) * 1024u +
                              static_cast<uint32_t>(R & 7) * 128u + (static_cast<uint32_t>((c16 & 7) ^ (R & 7)) << 4);
         *reinterpret_cast<uint4*>(smem + LF::kOffQ + off) = o;
-      }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -772,7 +788,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       if (leader) prefetch_tensormap(&tm_q);
     }
     const uint64_t pol_keep = policy_evict_last();  // q
-    uint32_t it = 0, gi = 0, pos = 0, nq = 0;  // tiles, groups, pairs, Q loads issued
+    uint32_t it = 0, gi = 0, pos = 0, nq = 0, ce = 0;  // tiles, groups, pairs, Q loads, early chunks issued
     bool ok = true;
     while (ok && walk.next(sched, S, T, p.ctx, walk_ranges, lane)) {
       const uint32_t n = static_cast<uint32_t>(walk.n);
@@ -824,7 +840,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         uint32_t left = n;
         do {  // the tile's rows, cut where a TMEM buffer ends
           const uint32_t c = pos % kSlots;
-          const uint32_t len = min(min(left, kSlots - c), 4u);  // contiguous slots, N <= 256
+          const uint32_t len = chunk_len<kSlots>(pos, left);
           // pair pos + i goes to slot c + i, free once the pair kSlots
           // positions earlier has been read by its warpgroup (a tile's
           // n <= kSlots pairs take n distinct slots); each chunk waits only
@@ -848,6 +864,13 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
           left -= len;
           pos += len;
           b_lo += len * kQRowLo;
+          // FP8, MXFP4: a chunk before the tile's last tells the epilogue
+          // that its pairs are in TMEM, so that they are read while the rest
+          // of the tile waits for slots
+          if (kChunkCommits && left != 0) {
+            mma_commit_if(issue, bars.ch(ce));
+            ++ce;
+          }
         } while (left != 0);
         if (!ok) break;
         // one commit per tile: the K stage is free and every pair of the tile
@@ -879,14 +902,13 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
     // modifier) instead of 64 max plus 32 packed FMAs.  The 64 columns come
     // in pieces of kPiece; the slot is released after the last piece is
     // read.
-    constexpr int kPiece = kPieceCols;
-    static_assert(kPiece == 32 || kPiece == 64, "TMEM pieces of 32 or 64 columns");
+    constexpr int kPiece = 32;
     const uint32_t wg = static_cast<uint32_t>(warp - 4) >> 2;
     const int quarter = warp & 3;    // TMEM lanes this warp may read
     const int tok = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     OutT* const out = static_cast<OutT*>(p.logits);
-    uint32_t it = 0, gi = 0, pos = 0;  // tiles, groups, pairs seen
+    uint32_t it = 0, gi = 0, pos = 0, ce = 0;  // tiles, groups, pairs, early chunks seen
     bool ok = true;
     while (ok && walk.next(sched, S, T, p.ctx, walk_ranges, lane)) {
       const int n = walk.n;
@@ -899,20 +921,53 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       OutT* const out_grp = out + static_cast<int64_t>(walk.r0) * p.logits_stride;
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
         const uint32_t r_first = (wg - pos) & (kEpiWg - 1);
+        // the tile's chunks as the MMA warp forms them (FP8, MXFP4): pairs
+        // [0, e0), [e0, e1), [e1, n); chunks before the last signal on the
+        // chunk ring from ce on, the last one with the tile's commit.  A tile
+        // of n <= kSlots rows has at most three chunks (one cut where the
+        // slot ring wraps, the others at 4 pairs).
+        const uint32_t nu = static_cast<uint32_t>(n);
+        uint32_t e0 = nu, e1 = nu, nch = 1;
+        if constexpr (kChunkCommits) {
+          e0 = chunk_len<kSlots>(pos, nu);
+          if (e0 < nu) {
+            e1 = e0 + chunk_len<kSlots>(pos + e0, nu - e0);
+            nch = e1 < nu ? 3 : 2;
+          }
+        }
         if (r_first >= static_cast<uint32_t>(n)) {  // no pair of this warp in the tile
           pos += static_cast<uint32_t>(n);
+          ce += nch - 1;
           continue;
         }
-        // the tile's MMAs are done, so its key scales (loaded with its K
-        // values, a ring of kScaleStages tiles) are in shared memory too
-        ok = warp_wait(bars.tr(it, kDq), (it / kTileRing) & 1, abort_flag, p.status);
-        if (!ok) break;
-        tc_fence_after();
-        // (MXFP4: every scale is applied inside the MMA)
-        const float kscale = kMx ? 1.f : scale_sm[(it & (kScaleStages - 1)) * kScaleStageFloats + tok];
         const int scol = j * kTileTokens + tok;
         const bool in_span = scol < lim;
+        float kscale = 1.f;  // (MXFP4: every scale is applied inside the MMA)
+        int waited = -1;     // the chunk this warp last waited for
+        if constexpr (!kChunkCommits) {
+          // the tile's MMAs are done, so its key scales (loaded with its K
+          // values, a ring of kScaleStages tiles) are in shared memory too
+          ok = warp_wait(bars.tr(it, kDq), (it / kTileRing) & 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          if (!kMx) kscale = scale_sm[(it & (kScaleStages - 1)) * kScaleStageFloats + tok];
+        }
         for (uint32_t r = r_first; r < static_cast<uint32_t>(n); r += kEpiWg) {
+          if constexpr (kChunkCommits) {
+            const int k = (r >= e0 ? 1 : 0) + (r >= e1 ? 1 : 0);
+            if (k != waited) {
+              // the chunk's (or the tile's) MMAs are done, and with them the
+              // tile's key scales have landed
+              if (k + 1 == static_cast<int>(nch))
+                ok = warp_wait(bars.tr(it, kDq), (it / kTileRing) & 1, abort_flag, p.status);
+              else
+                ok = warp_wait(bars.ch(ce + k), ((ce + k) / kChunkRing) & 1, abort_flag, p.status);
+              if (!ok) break;
+              tc_fence_after();
+              if (!kMx && waited < 0) kscale = scale_sm[(it & (kScaleStages - 1)) * kScaleStageFloats + tok];
+              waited = k;
+            }
+          }
           const uint32_t pp = pos + r;
           const uint32_t sl = pp % kSlots;
           const float4* wr = reinterpret_cast<const float4*>(w_grp + r * kHeads);
@@ -944,6 +999,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
         }
         if (!ok) break;
         pos += static_cast<uint32_t>(n);
+        ce += nch - 1;
       }
       if (!ok) break;
       __syncwarp();
@@ -994,35 +1050,37 @@ Params make_params(const LogitsArgs& a) {
   return p;
 }
 
-template <int kFmt, typename OutT, int kPieceCols>
+template <int kFmt, typename OutT, bool kChunkCommits>
 cudaError_t launch_as(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const Params& p, int grid,
                       cudaStream_t stream) {
   constexpr int kBytes = Smem<kFmt>::kBytes;
-  auto* kernel = logits_kernel<kFmt, OutT, kPieceCols>;
+  auto* kernel = logits_kernel<kFmt, OutT, kChunkCommits>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
   if (e != cudaSuccess) return e;
   return launch_dependent(kernel, dim3(grid), dim3(kThreadsOf<kFmt>), kBytes, stream, tm_q, tm_kv, p);
 }
 
 // FP8 calls whose rows map onto table rows 8 or more at a time (prefill
-// rows reading their request's pages) are walked in full 8-row groups and
-// read each pair from TMEM in one 64-column piece; everything else in two of 32.
+// rows reading their request's pages) are walked in full 8-row groups, whose
+// tiles fill all 8 TMEM slots: their kernel commits each chunk of a tile's
+// MMAs, so that the epilogue reads a tile's first pairs while the rest wait
+// for slots.  Decode batches (1-6 rows a group) commit once per tile.
 template <int kFmt, typename OutT>
-cudaError_t launch_pieces(const LogitsArgs& a, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const Params& p,
+cudaError_t launch_mode(const LogitsArgs& a, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const Params& p,
                           cudaStream_t stream) {
   if constexpr (kFmt == DSA_KV_FP8) {
     if (a.bt_rows != nullptr && a.bt_num_rows > 0 &&
         static_cast<int64_t>(a.num_rows) >= static_cast<int64_t>(kGroupMaxRows) * a.bt_num_rows)
-      return launch_as<kFmt, OutT, 64>(tm_q, tm_kv, p, a.num_sms, stream);
+      return launch_as<kFmt, OutT, true>(tm_q, tm_kv, p, a.num_sms, stream);
   }
-  return launch_as<kFmt, OutT, 32>(tm_q, tm_kv, p, a.num_sms, stream);
+  return launch_as<kFmt, OutT, false>(tm_q, tm_kv, p, a.num_sms, stream);
 }
 
 template <int kFmt>
 cudaError_t launch(const LogitsArgs& a, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const Params& p,
                    cudaStream_t stream) {
-  if (a.logits_dtype == DSA_LOGITS_BF16) return launch_pieces<kFmt, __nv_bfloat16>(a, tm_q, tm_kv, p, stream);
-  return launch_pieces<kFmt, float>(a, tm_q, tm_kv, p, stream);
+  if (a.logits_dtype == DSA_LOGITS_BF16) return launch_mode<kFmt, __nv_bfloat16>(a, tm_q, tm_kv, p, stream);
+  return launch_mode<kFmt, float>(a, tm_q, tm_kv, p, stream);
 }
 
 }  // namespace
