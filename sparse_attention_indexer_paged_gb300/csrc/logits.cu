@@ -88,9 +88,10 @@ constexpr int kMaxSlots = 8;
 constexpr uint32_t kMxSfaCol = 448;
 constexpr uint32_t kMxSfbCol = 480;
 constexpr int kTileRing = 8;  // tiles whose "pairs in TMEM" barrier phases are tracked at once
-// FP8 and MXFP4: every chunk of a tile but its last signals its pairs on a
-// ring of chunk barriers (a chunk's MMAs wait for slots that pairs at most
-// kSlots positions earlier held, so fewer than 16 chunks are ever pending)
+// Full-group FP8 calls (kChunkCommits): every chunk of a tile but its last
+// signals its pairs on a ring of chunk barriers (a chunk's MMAs wait for
+// slots that pairs at most kSlots positions earlier held, so fewer than 16
+// chunks are ever pending)
 constexpr int kChunkRing = 16;
 constexpr int kScaleStages = 16;   // key scale ring
 constexpr int kTmemCols = 512;
@@ -864,9 +865,9 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
           left -= len;
           pos += len;
           b_lo += len * kQRowLo;
-          // FP8, MXFP4: a chunk before the tile's last tells the epilogue
-          // that its pairs are in TMEM, so that they are read while the rest
-          // of the tile waits for slots
+          // (kChunkCommits) a chunk before the tile's last tells the
+          // epilogue that its pairs are in TMEM, so that they are read while
+          // the rest of the tile waits for slots
           if (kChunkCommits && left != 0) {
             mma_commit_if(issue, bars.ch(ce));
             ++ce;
@@ -894,9 +895,9 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
   } else if (warp >= 4 && warp < 4 + kEpiWarps) {
     // =================================================== epilogue
     // Pair p of the CTA's stream (tile's first pair position pos, row r:
-    // p = pos + r) sits in TMEM slot p mod 8 and belongs to warpgroup
+    // p = pos + r) sits in TMEM slot p mod kSlots and belongs to warpgroup
     // p mod kEpiWg, so this warp visits r = (wg - pos) mod kEpiWg, + kEpiWg,
-    // ... of each tile; the slot's fill index is p / 8.
+    // ... of each tile; the slot's fill index is p / kSlots.
     //   sum_h w_h relu(x_h) = (sum_h w_h x_h + sum_h w_h |x_h|) / 2
     // so the head reduction is 64 packed FMAs (the |x| is an operand
     // modifier) instead of 64 max plus 32 packed FMAs.  The 64 columns come
@@ -921,7 +922,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFmt>, 1)
       OutT* const out_grp = out + static_cast<int64_t>(walk.r0) * p.logits_stride;
       for (int j = walk.j0; j < walk.j1; ++j, ++it) {
         const uint32_t r_first = (wg - pos) & (kEpiWg - 1);
-        // the tile's chunks as the MMA warp forms them (FP8, MXFP4): pairs
+        // the tile's chunks as the MMA warp forms them (kChunkCommits): pairs
         // [0, e0), [e0, e1), [e1, n); chunks before the last signal on the
         // chunk ring from ce on, the last one with the tile's commit.  A tile
         // of n <= kSlots rows has at most three chunks (one cut where the
